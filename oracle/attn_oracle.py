@@ -1,0 +1,195 @@
+"""fp64 CPU oracle for the fused attention backward pass.
+
+TEST INFRASTRUCTURE ONLY.  Nothing on the product path imports this module:
+only ``tests/``, ``__graft_entry__.smoke()`` and the ``cpu_baseline`` /
+``--impl reference`` legs of ``bench.py`` may use it.  It shares no code with
+the CUDA path; its inputs come from ``attention_backward_bwd_gb300.synth``
+(random numbers only).
+
+What it computes is the plain definition of softmax attention and of its
+gradient, written out step by step in float64 with a library matmul as the
+only primitive.  No tiling, no online softmax, no recomputation tricks.
+
+Sources (page title, section):
+  * test_tilelang_kernel_mha_bwd.py (TileLang), ``ref_program``: scores =
+    Q K^T / sqrt(D), lower-triangular causal mask filled with -inf, softmax
+    over keys, output = P V; gradients by differentiation.
+  * same page, ``flashattn_bwd``: the backward steps P = softmax(S),
+    dV = P^T dO, dP = dO V^T, dS = P * (dP - Delta), dK = dS^T Q, dQ = dS K,
+    all times the softmax scale; ``flashattn_bwd_preprocess``: Delta =
+    rowsum(O * dO).
+  * flash-attention csrc/flash_attn_ck/mha_bwd.cpp, ``mha_bwd``: query head h
+    reads key/value head h // (H / H_k), and dK, dV are summed over the
+    H / H_k query heads of a group (the ``sum_out`` over the group dim);
+    causal is a window (left, 0) in bottom-right alignment; seqlen_q == 0
+    gives zero dK, dV.
+  * flash-attention hopper/flash_bwd_launch_template.h, ``run_flash_bwd``:
+    varlen tensors are packed [total, H, D] with per-sequence offsets from
+    cu_seqlens; LSE is natural-log (the preprocess makes the log2 copy).
+
+Readings where the pages leave a point open:
+  * causal with Sq != Sk: key j is allowed for query i iff j <= i + (Sk - Sq).
+  * a query row with no allowed key: O = 0, LSE = +inf, dQ = 0, and it adds
+    nothing to dK or dV.
+  * scale defaults to 1/sqrt(D).
+
+Every function here is pinned by ``tests/test_oracle_pins.py`` (finite
+differences, algebraic identities, closed forms, an independent fp64 torch
+autograd run and planted-mistake checks).
+"""
+from __future__ import annotations
+
+import numpy as np
+
+
+def allowed_mask(sq: int, sk: int, causal: bool) -> np.ndarray:
+    """Boolean [sq, sk]: True where query i may attend key j."""
+    if not causal:
+        return np.ones((sq, sk), dtype=bool)
+    i = np.arange(sq)[:, None]
+    j = np.arange(sk)[None, :]
+    return j <= i + (sk - sq)
+
+
+def head_forward(q: np.ndarray, k: np.ndarray, v: np.ndarray, scale: float, causal: bool):
+    """Forward of one head.  q [Sq, D], k and v [Sk, D], float64.
+
+    Returns (O [Sq, D], LSE [Sq] natural log, P [Sq, Sk]).
+    """
+    sq, sk = q.shape[0], k.shape[0]
+    s = scale * (q @ k.T)
+    allowed = allowed_mask(sq, sk, causal)
+    s = np.where(allowed, s, -np.inf)
+    any_key = allowed.any(axis=1) if sk > 0 else np.zeros(sq, dtype=bool)
+    m = np.where(any_key, s.max(axis=1, initial=-np.inf), 0.0)
+    e = np.where(allowed, np.exp(s - m[:, None]), 0.0)
+    ell = e.sum(axis=1)
+    lse = np.where(any_key, m + np.log(np.where(any_key, ell, 1.0)), np.inf)
+    p = np.where(allowed, np.exp(s - np.where(any_key, lse, 0.0)[:, None]), 0.0)
+    o = p @ v
+    return o, lse, p
+
+
+def head_backward(q, k, v, do, scale: float, causal: bool):
+    """Gradient of one head, by the definition.  All arrays float64.
+
+    Returns a dict with O, LSE, P, dP, Delta (= rowsum(P * dP)), dS, dQ, dK, dV.
+    """
+    o, lse, p = head_forward(q, k, v, scale, causal)
+    dv = p.T @ do
+    dp = do @ v.T
+    delta = (p * dp).sum(axis=1)
+    ds = p * (dp - delta[:, None])
+    dq = scale * (ds @ k)
+    dk = scale * (ds.T @ q)
+    return {"O": o, "LSE": lse, "P": p, "dP": dp, "Delta": delta, "dS": ds,
+            "dQ": dq, "dK": dk, "dV": dv}
+
+
+def delta_from_output(o: np.ndarray, do: np.ndarray) -> np.ndarray:
+    """Delta_i = sum_d O_id * dO_id (the backward preprocess), over the last axis."""
+    return (np.asarray(o, dtype=np.float64) * np.asarray(do, dtype=np.float64)).sum(axis=-1)
+
+
+def _f64(x):
+    if hasattr(x, "detach"):
+        x = x.detach().cpu().double().numpy()
+    return np.asarray(x, dtype=np.float64)
+
+
+def _sequences(q, k, cu_q, cu_k):
+    """Yield (b, q_rows, k_rows) slices for padded [B,S,H,D] or packed [total,H,D]."""
+    if cu_q is None:
+        for b in range(q.shape[0]):
+            yield b, (b, slice(None)), (b, slice(None))
+    else:
+        cq = [int(x) for x in _f64(cu_q)]
+        ck = [int(x) for x in _f64(cu_k)]
+        for b in range(len(cq) - 1):
+            yield b, (slice(cq[b], cq[b + 1]),), (slice(ck[b], ck[b + 1]),)
+
+
+def _take(x, sel, h):
+    if len(sel) == 2:
+        return x[sel[0], sel[1], h, :]
+    return x[sel[0], h, :]
+
+
+def _put(x, sel, h, val, add=False):
+    if len(sel) == 2:
+        if add:
+            x[sel[0], sel[1], h, :] += val
+        else:
+            x[sel[0], sel[1], h, :] = val
+    else:
+        if add:
+            x[sel[0], h, :] += val
+        else:
+            x[sel[0], h, :] = val
+
+
+def mha_forward(q, k, v, scale=None, causal=False, cu_seqlens_q=None, cu_seqlens_k=None,
+                heads=None):
+    """Multi-head forward.  q [B,Sq,H,D] (or packed [total,H,D]), k/v with H_k heads.
+
+    Returns (O like q, LSE [B,H,Sq] or [H,total_q]).  ``heads`` restricts the
+    query heads computed (others are left zero).
+    """
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    hq, hk, d = q.shape[-2], k.shape[-2], q.shape[-1]
+    scale = d ** -0.5 if scale is None else scale
+    g = hq // hk
+    o = np.zeros_like(q)
+    if cu_seqlens_q is None:
+        lse = np.zeros((q.shape[0], hq, q.shape[1]))
+    else:
+        lse = np.zeros((hq, q.shape[0]))
+    hs = range(hq) if heads is None else heads
+    for b, qs, ks in _sequences(q, k, cu_seqlens_q, cu_seqlens_k):
+        for h in hs:
+            oh, lh, _ = head_forward(_take(q, qs, h), _take(k, ks, h // g), _take(v, ks, h // g),
+                                     scale, causal)
+            _put(o, qs, h, oh)
+            if cu_seqlens_q is None:
+                lse[b, h, :] = lh
+            else:
+                lse[h, qs[0]] = lh
+    return o, lse
+
+
+def mha_backward(q, k, v, do, scale=None, causal=False, cu_seqlens_q=None, cu_seqlens_k=None,
+                 kv_heads=None):
+    """Multi-head backward by the definition, with GQA group sums.
+
+    Returns dict(dQ, dK, dV, O, LSE, Delta) in the input layouts (LSE/Delta as
+    [B,H,Sq] or [H,total_q]).  ``kv_heads`` restricts the computation to the
+    query heads of those key/value heads (others stay zero).
+    """
+    q, k, v, do = _f64(q), _f64(k), _f64(v), _f64(do)
+    hq, hk, d = q.shape[-2], k.shape[-2], q.shape[-1]
+    scale = d ** -0.5 if scale is None else scale
+    g = hq // hk
+    dq, dk, dv, o = np.zeros_like(q), np.zeros_like(k), np.zeros_like(v), np.zeros_like(q)
+    if cu_seqlens_q is None:
+        lse = np.zeros((q.shape[0], hq, q.shape[1]))
+    else:
+        lse = np.zeros((hq, q.shape[0]))
+    delta = np.zeros_like(lse)
+    kvs = range(hk) if kv_heads is None else kv_heads
+    for b, qs, ks in _sequences(q, k, cu_seqlens_q, cu_seqlens_k):
+        for hkv in kvs:
+            for h in range(hkv * g, hkv * g + g):
+                r = head_backward(_take(q, qs, h), _take(k, ks, hkv), _take(v, ks, hkv),
+                                  _take(do, qs, h), scale, causal)
+                _put(dq, qs, h, r["dQ"])
+                _put(o, qs, h, r["O"])
+                _put(dk, ks, hkv, r["dK"], add=True)
+                _put(dv, ks, hkv, r["dV"], add=True)
+                if cu_seqlens_q is None:
+                    lse[b, h, :] = r["LSE"]
+                    delta[b, h, :] = r["Delta"]
+                else:
+                    lse[h, qs[0]] = r["LSE"]
+                    delta[h, qs[0]] = r["Delta"]
+    return {"dQ": dq, "dK": dk, "dV": dv, "O": o, "LSE": lse, "Delta": delta}
+
