@@ -1,0 +1,242 @@
+"""ctypes binding of libattn_gb300.so (include/attn_bwd.h, include/attn_diag.h).
+
+Argument marshalling only: torch tensors are turned into pointers and element
+strides, outputs and workspace are allocated with torch (device memory), and
+every step of the computation runs in the library's CUDA kernels.  There is no
+CPU or PyTorch fallback: if the library is missing or a call fails, an
+exception is raised.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+from typing import Optional, Tuple
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libattn_gb300.so")
+
+ATTN_FP16, ATTN_BF16 = 0, 1
+STATUS = {0: "ATTN_OK", -1: "ATTN_ERR_DTYPE", -2: "ATTN_ERR_SHAPE", -3: "ATTN_ERR_STRIDE",
+          -4: "ATTN_ERR_ALIGN", -5: "ATTN_ERR_NULL", -6: "ATTN_ERR_WORKSPACE",
+          -7: "ATTN_ERR_CUDA", -8: "ATTN_ERR_DEVICE_TIMEOUT", -9: "ATTN_ERR_ARG"}
+
+
+class AttnError(RuntimeError):
+    def __init__(self, code: int, msg: str):
+        super().__init__(f"{STATUS.get(code, code)}: {msg}")
+        self.code = code
+
+
+class AttnTensor(ctypes.Structure):
+    _fields_ = [("ptr", ctypes.c_void_p), ("stride_b", ctypes.c_int64),
+                ("stride_s", ctypes.c_int64), ("stride_h", ctypes.c_int64)]
+
+
+_T = ctypes.POINTER(AttnTensor)
+_P = ctypes.c_void_p
+_I = ctypes.c_int
+_BWD_ARGS = [_T, _T, _T, _T, _P, _T, _T, _T, _T, _I, _I, _I, _I, _I, _I, _I, ctypes.c_float, _I,
+             _P, _P, _I, _I, _I, _P, ctypes.c_size_t, _P]
+
+_lib = None
+_lock = threading.Lock()
+
+EXPORTS = ("attn_fwd", "attn_bwd", "attn_bwd_preprocess", "attn_bwd_main", "attn_bwd_postprocess",
+           "attn_bwd_workspace_size", "attn_bwd_workspace_layout", "attn_check_device_status",
+           "attn_set_wait_timeout_ns", "attn_last_error", "attn_version", "attn_diag_mma",
+           "attn_diag_wait_timeout")
+
+
+def lib() -> ctypes.CDLL:
+    """Load the library (once).  Raises if it has not been built."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(LIB_PATH):
+            raise ImportError(
+                f"{LIB_PATH} is missing: build it with `python -c 'import __graft_entry__ as g; "
+                f"g.build()'` (nvcc, sm_103a).  There is no fallback implementation.")
+        L = ctypes.CDLL(LIB_PATH)
+        L.attn_fwd.argtypes = [_T, _T, _T, _T, _P, _I, _I, _I, _I, _I, _I, _I, ctypes.c_float, _I,
+                               _P, _P, _I, _I, _P]
+        L.attn_fwd.restype = _I
+        for name in ("attn_bwd", "attn_bwd_preprocess", "attn_bwd_main", "attn_bwd_postprocess"):
+            f = getattr(L, name)
+            f.argtypes = _BWD_ARGS
+            f.restype = _I
+        L.attn_bwd_workspace_size.argtypes = [_I, _I, _I, _I, _I, _I]
+        L.attn_bwd_workspace_size.restype = ctypes.c_size_t
+        L.attn_bwd_workspace_layout.argtypes = [_I, _I, _I, _I, _I,
+                                                ctypes.POINTER(ctypes.c_size_t),
+                                                ctypes.POINTER(ctypes.c_int64)]
+        L.attn_bwd_workspace_layout.restype = _I
+        L.attn_check_device_status.argtypes = [_P]
+        L.attn_check_device_status.restype = _I
+        L.attn_set_wait_timeout_ns.argtypes = [ctypes.c_int64]
+        L.attn_set_wait_timeout_ns.restype = None
+        L.attn_last_error.argtypes = []
+        L.attn_last_error.restype = ctypes.c_char_p
+        L.attn_version.argtypes = []
+        L.attn_version.restype = ctypes.c_char_p
+        L.attn_diag_mma.argtypes = [_I, _I, _I, _P, _P, _P, _P]
+        L.attn_diag_mma.restype = _I
+        L.attn_diag_wait_timeout.argtypes = [ctypes.c_int64, _P]
+        L.attn_diag_wait_timeout.restype = _I
+        _lib = L
+        return L
+
+
+def _check(rc: int):
+    if rc != 0:
+        raise AttnError(rc, lib().attn_last_error().decode())
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.float16:
+        return ATTN_FP16
+    if t.dtype == torch.bfloat16:
+        return ATTN_BF16
+    return 99  # rejected by the library with ATTN_ERR_DTYPE
+
+
+def _desc(t: Optional[torch.Tensor]) -> AttnTensor:
+    if t is None:
+        return AttnTensor(None, 0, 0, 0)
+    if t.dim() == 4:
+        return AttnTensor(t.data_ptr(), t.stride(0), t.stride(1), t.stride(2))
+    if t.dim() == 3:  # packed varlen [total, H, D]
+        return AttnTensor(t.data_ptr(), 0, t.stride(0), t.stride(1))
+    raise ValueError("attention tensors are [B, S, H, D] or packed [total, H, D]")
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else t.data_ptr()
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _dims(q: torch.Tensor, k: torch.Tensor, cu_q, cu_k, max_q, max_k):
+    if cu_q is not None:
+        if q.dim() != 3 or k.dim() != 3:
+            raise ValueError("varlen tensors must be packed [total, H, D]")
+        batch = int(cu_q.numel()) - 1
+        sq, sk = q.shape[0], k.shape[0]
+        hq, d, hk = q.shape[1], q.shape[2], k.shape[1]
+        if max_q is None or max_k is None:
+            raise ValueError("varlen calls need max_seqlen_q and max_seqlen_k")
+        return batch, sq, sk, hq, hk, d, int(max_q), int(max_k)
+    if q.dim() != 4 or k.dim() != 4:
+        raise ValueError("tensors must be [B, S, H, D]")
+    return q.shape[0], q.shape[1], k.shape[1], q.shape[2], k.shape[2], q.shape[3], q.shape[1], k.shape[1]
+
+
+def version() -> str:
+    return lib().attn_version().decode()
+
+
+def attn_fwd(q, k, v, causal: bool = False, scale: Optional[float] = None, cu_seqlens_q=None,
+             cu_seqlens_k=None, max_seqlen_q=None, max_seqlen_k=None, out=None, lse=None,
+             stream=None) -> Tuple[torch.Tensor, torch.Tensor]:
+    """Forward pass: returns (O like q, LSE fp32 [B,H,Sq] or [H,total_q], natural log)."""
+    L = lib()
+    b, sq, sk, hq, hk, d, mq, mk = _dims(q, k, cu_seqlens_q, cu_seqlens_k, max_seqlen_q,
+                                         max_seqlen_k)
+    scale = d ** -0.5 if scale is None else float(scale)
+    o = torch.empty_like(q) if out is None else out
+    if lse is None:
+        shape = (hq, sq) if cu_seqlens_q is not None else (b, hq, sq)
+        lse = torch.empty(shape, dtype=torch.float32, device=q.device)
+    dq_, dk_, dv_, do_ = _desc(q), _desc(k), _desc(v), _desc(o)
+    rc = L.attn_fwd(ctypes.byref(dq_), ctypes.byref(dk_), ctypes.byref(dv_), ctypes.byref(do_),
+                    _ptr(lse), _dtype_code(q), b, sq, sk, hq, hk, d, scale, int(bool(causal)),
+                    _ptr(cu_seqlens_q), _ptr(cu_seqlens_k), mq, mk, _stream(stream))
+    _check(rc)
+    return o, lse
+
+
+def workspace_size(batch: int, seqlen_q: int, h_q: int, head_dim: int, deterministic: bool = False,
+                   varlen: bool = False) -> int:
+    return int(lib().attn_bwd_workspace_size(batch, seqlen_q, h_q, head_dim, int(deterministic),
+                                             int(varlen)))
+
+
+def workspace_layout(batch: int, seqlen_q: int, h_q: int, head_dim: int, varlen: bool = False):
+    """Returns (offsets dict in bytes, rows)."""
+    offs = (ctypes.c_size_t * 4)()
+    rows = ctypes.c_int64()
+    _check(lib().attn_bwd_workspace_layout(batch, seqlen_q, h_q, head_dim, int(varlen), offs,
+                                           ctypes.byref(rows)))
+    return {"lse2": offs[0], "delta": offs[1], "dqaccum": offs[2], "sem": offs[3]}, rows.value
+
+
+def alloc_workspace(q, cu_seqlens_q=None, deterministic=False) -> torch.Tensor:
+    if cu_seqlens_q is not None:
+        b, sq, hq, d = int(cu_seqlens_q.numel()) - 1, q.shape[0], q.shape[1], q.shape[2]
+    else:
+        b, sq, hq, d = q.shape[0], q.shape[1], q.shape[2], q.shape[3]
+    n = workspace_size(b, sq, hq, d, deterministic, cu_seqlens_q is not None)
+    return torch.empty(max(n, 256), dtype=torch.uint8, device=q.device)
+
+
+_STAGE_FN = {"all": "attn_bwd", "pre": "attn_bwd_preprocess", "main": "attn_bwd_main",
+             "post": "attn_bwd_postprocess"}
+
+
+def attn_bwd(q, k, v, o, lse, do, causal: bool = False, scale: Optional[float] = None,
+             cu_seqlens_q=None, cu_seqlens_k=None, max_seqlen_q=None, max_seqlen_k=None,
+             deterministic: bool = False, workspace: Optional[torch.Tensor] = None, dq=None,
+             dk=None, dv=None, stream=None, stage: str = "all"):
+    """Backward pass: returns (dQ, dK, dV), each like its input.
+
+    ``stage`` selects one of the three kernels ("pre", "main", "post") or all
+    of them in order ("all"); the stages must share the workspace.
+    """
+    L = lib()
+    b, sq, sk, hq, hk, d, mq, mk = _dims(q, k, cu_seqlens_q, cu_seqlens_k, max_seqlen_q,
+                                         max_seqlen_k)
+    scale = d ** -0.5 if scale is None else float(scale)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    if workspace is None:
+        workspace = alloc_workspace(q, cu_seqlens_q, deterministic)
+    descs = [_desc(t) for t in (q, k, v, o)]
+    d_do, d_dq, d_dk, d_dv = _desc(do), _desc(dq), _desc(dk), _desc(dv)
+    fn = getattr(L, _STAGE_FN[stage])
+    rc = fn(*(ctypes.byref(x) for x in descs), _ptr(lse), ctypes.byref(d_do), ctypes.byref(d_dq),
+            ctypes.byref(d_dk), ctypes.byref(d_dv), _dtype_code(q), b, sq, sk, hq, hk, d, scale,
+            int(bool(causal)), _ptr(cu_seqlens_q), _ptr(cu_seqlens_k), mq, mk,
+            int(bool(deterministic)), workspace.data_ptr(), workspace.numel(), _stream(stream))
+    _check(rc)
+    return dq, dk, dv
+
+
+def check_device_status(stream=None):
+    """Synchronise the stream and raise if a kernel reported a device-side error."""
+    _check(lib().attn_check_device_status(_stream(stream)))
+
+
+def set_wait_timeout_ns(ns: int):
+    lib().attn_set_wait_timeout_ns(int(ns))
+
+
+def diag_mma(mode: int, a: torch.Tensor, b: torch.Tensor) -> torch.Tensor:
+    """Single-tile tensor-core check (see include/attn_diag.h); returns fp32 C."""
+    d = b.shape[1]
+    rows_c, cols_c = (128, 128) if mode == 0 else (128, d)
+    c = torch.empty(rows_c, cols_c, dtype=torch.float32, device=a.device)
+    _check(lib().attn_diag_mma(mode, _dtype_code(a), d, a.data_ptr(), b.data_ptr(), c.data_ptr(),
+                               _stream(None)))
+    return c
+
+
+def diag_wait_timeout(ns: int):
+    _check(lib().attn_diag_wait_timeout(int(ns), _stream(None)))

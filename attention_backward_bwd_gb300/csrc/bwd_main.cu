@@ -1,0 +1,574 @@
+// Main attention-backward kernel for sm_103a: tcgen05 MMAs with TMEM
+// accumulators, TMA tile loads, warp-specialised, persistent over work units.
+//
+// Algorithm (TileLang test_tilelang_kernel_mha_bwd.py, flashattn_bwd): KV
+// stationary.  One work unit = (KV tile n of BN=128 keys, kv head g, sequence
+// b).  K_n and V_n are loaded once; for each of the G query heads of the
+// group and each query tile m of BM=128 rows in the causal range:
+//   S^T  = K_n Q_m^T                        (TMEM, fp32)
+//   P^T  = exp2(S^T * scale * log2 e - LSE2[query]), masked  (bf16/fp16, TMEM)
+//   dP^T = V_n dO_m^T                       (TMEM, fp32)
+//   dV  += P^T dO_m                         (TMEM accumulator, A operand from TMEM)
+//   dS^T = P^T * (dP^T - Delta[query])      (TMEM and smem, bf16/fp16)
+//   dK  += dS^T Q_m                         (TMEM accumulator, A operand from TMEM)
+//   dQ_m = dS K_n -> reduced into the fp32 dQaccum in global memory
+// dK (times scale) and dV are written once per unit; dK/dV of a GQA group are
+// summed in TMEM over the group's query heads (the group sum of
+// flash-attention csrc/flash_attn_ck/mha_bwd.cpp, done without extra memory).
+// dQaccum is reduced with fp32 vector atomics, or, in deterministic mode, in
+// ascending KV-tile order behind a per-(head, query tile) semaphore (the
+// dq_semaphore of flash-attention hopper/flash_bwd_launch_template.h).
+//
+// Warp roles (384 threads): warp 0 TMA producer, warp 1 MMA issuer (one
+// thread), warp 2 TMEM allocator, warps 4-7 softmax / dS / dK-dV epilogue
+// (thread = key row = TMEM lane), warps 8-11 dQ drain (thread = query row).
+//
+// TMEM columns (512 allocated, 128 lanes):
+//   [  0,128) S^T fp32; its first 64 columns are then reused for packed P^T
+//   [128,256) dP^T fp32; its first 64 columns are then reused for packed dS^T
+//   [ 64,128) dQ columns 0..63 and [192,256) dQ columns 64..127 (free halves)
+//   [256,256+D) dK, [384,384+D) dV
+// Every mbarrier wait is bounded (see WaitCtl): on timeout the kernel records
+// the site in the status word and unwinds.
+#include "common.cuh"
+
+namespace attn {
+
+namespace {
+
+constexpr int BM = 128;  // query tile
+constexpr int BN = 128;  // key tile
+constexpr int kThreads = 384;
+constexpr int kStages = 2;
+constexpr uint32_t kChunk = 128 * 128;  // one 64-column (128-byte) slice of a 128-row tile
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t TM_S = 0, TM_P = 0, TM_DP = 128, TM_DS = 128;
+constexpr uint32_t TM_DQ0 = 64, TM_DQ1 = 192, TM_DK = 256, TM_DV = 384;
+
+enum Bar : uint32_t {
+  B_FULLQ = 0,
+  B_FULLDO = B_FULLQ + kStages,
+  B_EMPTY = B_FULLDO + kStages,
+  B_KVFULL = B_EMPTY + kStages,
+  B_KVEMPTY,
+  B_SFULL,
+  B_DPFULL,
+  B_PREADY,
+  B_DSREADY,
+  B_DQFULL0,
+  B_DQFULL1,
+  B_DQFREE0,
+  B_DQFREE1,
+  B_DKDVFULL,
+  B_DKDVFREE,
+  B_FINAL,
+  B_COUNT
+};
+
+template <int D>
+struct Smem {
+  static constexpr uint32_t kTile = (D / 64) * kChunk;
+  static constexpr uint32_t kK = 0;
+  static constexpr uint32_t kV = kK + kTile;
+  static constexpr uint32_t kQ = kV + kTile;
+  static constexpr uint32_t kDO = kQ + kStages * kTile;
+  static constexpr uint32_t kDS = kDO + kStages * kTile;  // dS^T [BN keys][BM queries], 2 chunks
+  static constexpr uint32_t kLSE = kDS + 2 * kChunk;
+  static constexpr uint32_t kDelta = kLSE + kStages * BM * 4;
+  static constexpr uint32_t kBar = kDelta + kStages * BM * 4;
+  static constexpr uint32_t kTmemSlot = kBar + B_COUNT * 8;
+  static constexpr uint32_t kAbort = kTmemSlot + 4;
+  static constexpr uint32_t kTotal = kAbort + 4;
+};
+static_assert(Smem<128>::kTotal <= 232448, "shared memory budget");
+
+struct Unit {
+  int n, g, b;
+  SeqInfo si;
+  int m_start, m_count, n_iters;
+  bool has_keys;
+};
+
+__device__ __forceinline__ Unit get_unit(const BwdParams& p, int u, int G) {
+  Unit r;
+  const int per_n = p.seq.batch * p.h_k;
+  r.n = u / per_n;
+  const int rem = u - r.n * per_n;
+  r.b = rem / p.h_k;
+  r.g = rem - r.b * p.h_k;
+  r.si = seq_info(p.seq, r.b);
+  r.has_keys = r.n * BN < r.si.sk;
+  const int m_end = ceil_div(r.si.sq, BM);
+  int m_start = 0;
+  if (p.causal) {
+    const int lo = r.n * BN - (r.si.sk - r.si.sq);  // first query that sees key n*BN
+    m_start = lo > 0 ? lo / BM : 0;
+  }
+  r.m_start = m_start;
+  r.m_count = m_end > m_start ? m_end - m_start : 0;
+  r.n_iters = r.has_keys ? G * r.m_count : 0;
+  return r;
+}
+
+template <typename T, int D>
+__global__ void __launch_bounds__(kThreads, 1)
+    bwd_main_kernel(const BwdParams p, const __grid_constant__ CUtensorMap tmQ,
+                    const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+                    const __grid_constant__ CUtensorMap tmDO) {
+  using L = Smem<D>;
+  extern __shared__ __align__(1024) unsigned char smem[];
+  if (p.input_bad != nullptr && *p.input_bad) return;
+  const uint32_t sb = smem_u32(smem);
+  if (sb & 1023u) {  // 128-byte swizzled tiles need a 1024-byte aligned base
+    if (threadIdx.x == 0) atomicCAS(p.status, 0u, 0xA1100000u);
+    return;
+  }
+  auto bar = [&](uint32_t i) -> uint32_t { return sb + L::kBar + i * 8; };
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kAbort);
+  const WaitCtl ctl{abort_flag, p.status, p.timeout_ns};
+
+  const uint32_t warp = warp_id();
+  const uint32_t lane = lane_id();
+  const int G = p.h_q / p.h_k;
+  const bool varlen = p.seq.cu_q != nullptr;
+  const int n_tiles = ceil_div(p.max_seqlen_k, BN);
+  const int num_units = n_tiles * p.seq.batch * p.h_k;
+  constexpr int kIsBf16 = Pack<T>::kIsBf16;
+
+  if (threadIdx.x == 0) {
+    *abort_flag = 0;
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(bar(B_FULLQ + s), 1);
+      mbar_init(bar(B_FULLDO + s), 1);
+      mbar_init(bar(B_EMPTY + s), 1 + 4);  // MMA commit + 4 softmax warps
+    }
+    mbar_init(bar(B_KVFULL), 1);
+    mbar_init(bar(B_KVEMPTY), 1);
+    mbar_init(bar(B_SFULL), 1);
+    mbar_init(bar(B_DPFULL), 1);
+    mbar_init(bar(B_PREADY), 4);
+    mbar_init(bar(B_DSREADY), 4);
+    mbar_init(bar(B_DQFULL0), 1);
+    mbar_init(bar(B_DQFULL1), 1);
+    mbar_init(bar(B_DQFREE0), 4);
+    mbar_init(bar(B_DQFREE1), 4);
+    mbar_init(bar(B_DKDVFULL), 1);
+    mbar_init(bar(B_DKDVFREE), 4);
+    mbar_init(bar(B_FINAL), 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    fence_proxy_async_smem();
+  }
+  if (warp == 2) {
+    tmem_alloc(sb + L::kTmemSlot, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + L::kTmemSlot);
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      prefetch_tmap(&tmQ);
+      prefetch_tmap(&tmK);
+      prefetch_tmap(&tmV);
+      prefetch_tmap(&tmDO);
+      uint32_t it = 0, uc = 0;  // iterations and units whose loads were issued
+      for (int u = blockIdx.x; u < num_units; u += gridDim.x) {
+        const Unit un = get_unit(p, u, G);
+        if (un.n_iters == 0) continue;
+        if (uc > 0 && !wait1(bar(B_KVEMPTY), (uc - 1) & 1, ctl, 0xA0000001u)) break;
+        ++uc;
+        {
+          const int krow = un.si.k_start + un.n * BN;
+          const int bk = varlen ? 0 : un.b;
+          mbar_expect_tx(bar(B_KVFULL), 2 * L::kTile);
+#pragma unroll
+          for (int c = 0; c < D / 64; ++c) {
+            tma_load_4d(sb + L::kK + c * kChunk, &tmK, bar(B_KVFULL), c * 64, krow, un.g, bk);
+            tma_load_4d(sb + L::kV + c * kChunk, &tmV, bar(B_KVFULL), c * 64, krow, un.g, bk);
+          }
+        }
+        for (int j = 0; j < un.n_iters; ++j, ++it) {
+          const uint32_t s = it % kStages;
+          const uint32_t use = it / kStages;
+          if (use > 0 && !wait1(bar(B_EMPTY + s), (use - 1) & 1, ctl, 0xA0000002u)) break;
+          const int h = un.g * G + j / un.m_count;
+          const int m = un.m_start + j % un.m_count;
+          const int qrow = un.si.q_start + m * BM;
+          const int bq = varlen ? 0 : un.b;
+          const int64_t ws = static_cast<int64_t>(h) * p.ws_rows + un.si.ws_row0 + m * BM;
+          mbar_expect_tx(bar(B_FULLQ + s), L::kTile + BM * 4);
+#pragma unroll
+          for (int c = 0; c < D / 64; ++c)
+            tma_load_4d(sb + L::kQ + s * L::kTile + c * kChunk, &tmQ, bar(B_FULLQ + s), c * 64,
+                        qrow, h, bq);
+          bulk_load(sb + L::kLSE + s * BM * 4, p.lse2 + ws, BM * 4, bar(B_FULLQ + s));
+          mbar_expect_tx(bar(B_FULLDO + s), L::kTile + BM * 4);
+#pragma unroll
+          for (int c = 0; c < D / 64; ++c)
+            tma_load_4d(sb + L::kDO + s * L::kTile + c * kChunk, &tmDO, bar(B_FULLDO + s), c * 64,
+                        qrow, h, bq);
+          bulk_load(sb + L::kDelta + s * BM * 4, p.delta + ws, BM * 4, bar(B_FULLDO + s));
+        }
+        if (*abort_flag) break;
+      }
+      // Before exit, wait (bounded, ignoring the abort flag) until every copy this
+      // thread issued has landed, so no TMA write targets a finished CTA.
+      if (uc > 0) wait1(bar(B_KVFULL), (uc - 1) & 1, ctl, 0xA0000003u, false);
+      for (uint32_t s = 0; s < kStages && s < it; ++s) {
+        const uint32_t last = (it - 1 - s) / kStages;  // uses of stage (it-1-s) % kStages
+        const uint32_t st = (it - 1 - s) % kStages;
+        wait1(bar(B_FULLQ + st), last & 1, ctl, 0xA0000004u, false);
+        wait1(bar(B_FULLDO + st), last & 1, ctl, 0xA0000005u, false);
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t kIdS = idesc_f16(kIsBf16, 0, 0, BN, BM);
+      constexpr uint32_t kIdKV = idesc_f16(kIsBf16, 0, 1, BN, D);
+      constexpr uint32_t kIdDQ = idesc_f16(kIsBf16, 1, 1, BM, 64);
+      uint32_t it = 0, uc = 0;
+      for (int u = blockIdx.x; u < num_units; u += gridDim.x) {
+        const Unit un = get_unit(p, u, G);
+        if (un.n_iters == 0) continue;
+        if (!wait1(bar(B_KVFULL), uc & 1, ctl, 0xA0000011u)) goto mma_exit;
+        tc_fence_after();
+        for (int j = 0; j < un.n_iters; ++j, ++it) {
+          const uint32_t s = it % kStages;
+          const uint32_t ph = (it / kStages) & 1;
+          const uint32_t sQ = sb + L::kQ + s * L::kTile;
+          const uint32_t sDO = sb + L::kDO + s * L::kTile;
+          if (!wait1(bar(B_FULLQ + s), ph, ctl, 0xA0000013u)) goto mma_exit;
+          if (it > 0 && !wait1(bar(B_DQFREE0), (it - 1) & 1, ctl, 0xA0000014u)) goto mma_exit;
+          tc_fence_after();
+          // S^T = K Q^T   (M = keys, N = queries, K = head dim; both K-major)
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t koff = (kk >> 2) * kChunk + (kk & 3) * 32;
+            mma_ss(tmem + TM_S, sdesc_sw128(sb + L::kK + koff, 16, 1024),
+                   sdesc_sw128(sQ + koff, 16, 1024), kIdS, kk > 0);
+          }
+          tc_commit(bar(B_SFULL));
+          if (!wait1(bar(B_FULLDO + s), ph, ctl, 0xA0000015u)) goto mma_exit;
+          if (D == 128 && it > 0 && !wait1(bar(B_DQFREE1), (it - 1) & 1, ctl, 0xA0000016u))
+            goto mma_exit;
+          tc_fence_after();
+          // dP^T = V dO^T
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t koff = (kk >> 2) * kChunk + (kk & 3) * 32;
+            mma_ss(tmem + TM_DP, sdesc_sw128(sb + L::kV + koff, 16, 1024),
+                   sdesc_sw128(sDO + koff, 16, 1024), kIdS, kk > 0);
+          }
+          tc_commit(bar(B_DPFULL));
+          // dV += P^T dO   (A = P^T from TMEM, B = dO MN-major, K = queries)
+          if (!wait1(bar(B_PREADY), it & 1, ctl, 0xA0000017u)) goto mma_exit;
+          // the previous unit's epilogue must have read dK/dV before they restart
+          if (j == 0 && uc > 0 && !wait1(bar(B_DKDVFREE), (uc - 1) & 1, ctl, 0xA0000012u))
+            goto mma_exit;
+          tc_fence_after();
+#pragma unroll
+          for (int kk = 0; kk < BM / 16; ++kk)
+            mma_ts(tmem + TM_DV, tmem + TM_P + kk * 8, sdesc_sw128(sDO + kk * 2048, kChunk, 1024),
+                   kIdKV, (j > 0 || kk > 0) ? 1u : 0u);
+          if (!wait1(bar(B_DSREADY), it & 1, ctl, 0xA0000018u)) goto mma_exit;
+          tc_fence_after();
+          if (D == 128) {
+            // dQ[:, 0:64] = dS K[:, 0:64]  (A = dS MN-major from the dS^T tile, B = K MN-major)
+#pragma unroll
+            for (int kk = 0; kk < BN / 16; ++kk)
+              mma_ss(tmem + TM_DQ0, sdesc_sw128(sb + L::kDS + kk * 2048, kChunk, 1024),
+                     sdesc_sw128(sb + L::kK + kk * 2048, kChunk, 1024), kIdDQ, kk > 0);
+            tc_commit(bar(B_DQFULL0));
+            // dK += dS^T Q
+#pragma unroll
+            for (int kk = 0; kk < BM / 16; ++kk)
+              mma_ts(tmem + TM_DK, tmem + TM_DS + kk * 8, sdesc_sw128(sQ + kk * 2048, kChunk, 1024),
+                     kIdKV, (j > 0 || kk > 0) ? 1u : 0u);
+            // dQ[:, 64:128] = dS K[:, 64:128]
+#pragma unroll
+            for (int kk = 0; kk < BN / 16; ++kk)
+              mma_ss(tmem + TM_DQ1, sdesc_sw128(sb + L::kDS + kk * 2048, kChunk, 1024),
+                     sdesc_sw128(sb + L::kK + kChunk + kk * 2048, kChunk, 1024), kIdDQ, kk > 0);
+            tc_commit(bar(B_DQFULL1));
+          } else {
+#pragma unroll
+            for (int kk = 0; kk < BM / 16; ++kk)
+              mma_ts(tmem + TM_DK, tmem + TM_DS + kk * 8, sdesc_sw128(sQ + kk * 2048, kChunk, 1024),
+                     kIdKV, (j > 0 || kk > 0) ? 1u : 0u);
+#pragma unroll
+            for (int kk = 0; kk < BN / 16; ++kk)
+              mma_ss(tmem + TM_DQ0, sdesc_sw128(sb + L::kDS + kk * 2048, kChunk, 1024),
+                     sdesc_sw128(sb + L::kK + kk * 2048, kChunk, 1024), kIdDQ, kk > 0);
+            tc_commit(bar(B_DQFULL0));
+          }
+          tc_commit(bar(B_EMPTY + s));
+        }
+        tc_commit(bar(B_DKDVFULL));
+        tc_commit(bar(B_KVEMPTY));
+        ++uc;
+      }
+    mma_exit:
+      // make sure no MMA is still running before TMEM is released
+      tc_commit(bar(B_FINAL));
+      wait1(bar(B_FINAL), 0, ctl, 0xA000001Fu, false);
+    }
+  } else if (warp >= 4 && warp < 8) {
+    // ------------------------------------------------- softmax / dS / epilogue
+    const uint32_t quad = warp & 3;
+    const int jl = static_cast<int>(quad * 32 + lane);  // key row within the tile
+    const uint32_t tl = tmem + ((quad * 32) << 16);    // this warp's TMEM lanes
+    const float sl2 = p.scale_log2;
+    uint32_t it = 0, uc = 0;
+    for (int u = blockIdx.x; u < num_units; u += gridDim.x) {
+      const Unit un = get_unit(p, u, G);
+      if (!un.has_keys) continue;
+      const int key = un.n * BN + jl;
+      const bool key_ok = key < un.si.sk;
+      T* dk_row = static_cast<T*>(const_cast<void*>(p.dk.ptr)) + (varlen ? 0 : un.b * p.dk.sb) +
+                  static_cast<int64_t>(un.si.k_start + key) * p.dk.ss +
+                  static_cast<int64_t>(un.g) * p.dk.sh;
+      T* dv_row = static_cast<T*>(const_cast<void*>(p.dv.ptr)) + (varlen ? 0 : un.b * p.dv.sb) +
+                  static_cast<int64_t>(un.si.k_start + key) * p.dv.ss +
+                  static_cast<int64_t>(un.g) * p.dv.sh;
+      if (un.n_iters == 0) {  // keys but no queries: dK = dV = 0
+        if (key_ok) {
+#pragma unroll
+          for (int c = 0; c < D / 8; ++c) {
+            reinterpret_cast<uint4*>(dk_row)[c] = make_uint4(0, 0, 0, 0);
+            reinterpret_cast<uint4*>(dv_row)[c] = make_uint4(0, 0, 0, 0);
+          }
+        }
+        continue;
+      }
+      const int off = un.si.sk - un.si.sq;
+      for (int j = 0; j < un.n_iters; ++j, ++it) {
+        const uint32_t s = it % kStages;
+        const uint32_t ph = (it / kStages) & 1;
+        const int m = un.m_start + j % un.m_count;
+        const int q0 = m * BM;
+        const bool need_mask = (q0 + BM > un.si.sq) || (un.n * BN + BN > un.si.sk) ||
+                               (p.causal && un.n * BN + BN - 1 > q0 + off);
+        const float* lse2 = reinterpret_cast<const float*>(smem + L::kLSE + s * BM * 4);
+        const float* dlt = reinterpret_cast<const float*>(smem + L::kDelta + s * BM * 4);
+        if (!wait_warp(bar(B_FULLQ + s), ph, ctl, 0xA0000021u)) goto done;
+        if (!wait_warp(bar(B_SFULL), it & 1, ctl, 0xA0000022u)) goto done;
+        tc_fence_after();
+        // P^T row `jl`: 4 chunks of 32 queries; packed P overwrites the S columns already read.
+#pragma unroll 1
+        for (int c = 0; c < BM / 32; ++c) {
+          uint32_t sv[32];
+          tmem_ld32(tl + TM_S + c * 32, sv);
+          tmem_wait_ld();
+          uint32_t pk[16];
+#pragma unroll
+          for (int e = 0; e < 32; e += 2) {
+            float x0 = ex2(fmaf(__uint_as_float(sv[e]), sl2, -lse2[c * 32 + e]));
+            float x1 = ex2(fmaf(__uint_as_float(sv[e + 1]), sl2, -lse2[c * 32 + e + 1]));
+            if (need_mask) {
+              const int i0 = q0 + c * 32 + e;
+              const bool ok0 = key_ok && i0 < un.si.sq && (!p.causal || key <= i0 + off);
+              const bool ok1 = key_ok && i0 + 1 < un.si.sq && (!p.causal || key <= i0 + 1 + off);
+              x0 = ok0 ? x0 : 0.f;
+              x1 = ok1 ? x1 : 0.f;
+            }
+            pk[e / 2] = Pack<T>::two(x0, x1);
+          }
+          tmem_st16(tl + TM_P + c * 16, pk);
+        }
+        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(B_PREADY));
+
+        if (!wait_warp(bar(B_FULLDO + s), ph, ctl, 0xA0000023u)) goto done;
+        if (!wait_warp(bar(B_DPFULL), it & 1, ctl, 0xA0000024u)) goto done;
+        tc_fence_after();
+        // dS^T row `jl` = P^T (dP^T - Delta); to TMEM (packed, over dP) and to the smem dS^T tile.
+#pragma unroll 1
+        for (int c = 0; c < BM / 32; ++c) {
+          uint32_t dpv[32], pv[16];
+          tmem_ld32(tl + TM_DP + c * 32, dpv);
+          tmem_ld16(tl + TM_P + c * 16, pv);
+          tmem_wait_ld();
+          uint32_t pk[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            const float2 pp = Pack<T>::unpack(pv[e]);
+            const float d0 = pp.x * (__uint_as_float(dpv[2 * e]) - dlt[c * 32 + 2 * e]);
+            const float d1 = pp.y * (__uint_as_float(dpv[2 * e + 1]) - dlt[c * 32 + 2 * e + 1]);
+            pk[e] = Pack<T>::two(d0, d1);
+          }
+          tmem_st16(tl + TM_DS + c * 16, pk);
+          // smem dS^T tile: chunk c/2 holds queries [64*(c/2), +64); row jl is 128 bytes,
+          // its 16-byte units u are stored at u ^ (jl % 8) (128-byte swizzle).
+          const uint32_t row_base = L::kDS + (c >> 1) * kChunk + jl * 128;
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const uint32_t unit = ((c & 1) * 4 + q) ^ (jl & 7);
+            *reinterpret_cast<uint4*>(smem + row_base + unit * 16) =
+                make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+          }
+        }
+        tmem_wait_st();
+        fence_proxy_async_smem();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(bar(B_DSREADY));
+          mbar_arrive(bar(B_EMPTY + s));
+        }
+      }
+      // ---- epilogue: dK = scale * acc, dV = acc
+      if (!wait_warp(bar(B_DKDVFULL), uc & 1, ctl, 0xA0000025u)) goto done;
+      tc_fence_after();
+#pragma unroll 1
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t a[32], v[32];
+        tmem_ld32(tl + TM_DK + c * 32, a);
+        tmem_ld32(tl + TM_DV + c * 32, v);
+        tmem_wait_ld();
+        if (key_ok) {
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            uint4 ok, ov;
+            ok.x = Pack<T>::two(__uint_as_float(a[8 * q + 0]) * p.scale, __uint_as_float(a[8 * q + 1]) * p.scale);
+            ok.y = Pack<T>::two(__uint_as_float(a[8 * q + 2]) * p.scale, __uint_as_float(a[8 * q + 3]) * p.scale);
+            ok.z = Pack<T>::two(__uint_as_float(a[8 * q + 4]) * p.scale, __uint_as_float(a[8 * q + 5]) * p.scale);
+            ok.w = Pack<T>::two(__uint_as_float(a[8 * q + 6]) * p.scale, __uint_as_float(a[8 * q + 7]) * p.scale);
+            ov.x = Pack<T>::two(__uint_as_float(v[8 * q + 0]), __uint_as_float(v[8 * q + 1]));
+            ov.y = Pack<T>::two(__uint_as_float(v[8 * q + 2]), __uint_as_float(v[8 * q + 3]));
+            ov.z = Pack<T>::two(__uint_as_float(v[8 * q + 4]), __uint_as_float(v[8 * q + 5]));
+            ov.w = Pack<T>::two(__uint_as_float(v[8 * q + 6]), __uint_as_float(v[8 * q + 7]));
+            reinterpret_cast<uint4*>(dk_row + c * 32)[q] = ok;
+            reinterpret_cast<uint4*>(dv_row + c * 32)[q] = ov;
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(B_DKDVFREE));
+      ++uc;
+    }
+  } else if (warp >= 8) {
+    // ------------------------------------------------------------ dQ drain
+    // Thread = query row (TMEM lane); each warp owns 32 rows of the tile, so the
+    // four warps touch disjoint dQaccum rows and synchronise only through the
+    // semaphore in deterministic mode (4 arrivals per KV tile, no CTA barrier).
+    const uint32_t quad = warp & 3;
+    const int il = static_cast<int>(quad * 32 + lane);  // query row within the tile
+    const uint32_t tl = tmem + ((quad * 32) << 16);
+    uint32_t it = 0;
+    for (int u = blockIdx.x; u < num_units; u += gridDim.x) {
+      const Unit un = get_unit(p, u, G);
+      if (un.n_iters == 0) continue;
+      for (int j = 0; j < un.n_iters; ++j, ++it) {
+        const int h = un.g * G + j / un.m_count;
+        const int m = un.m_start + j % un.m_count;
+        const bool row_ok = m * BM + il < un.si.sq;
+        const int64_t wrow = static_cast<int64_t>(h) * p.ws_rows + un.si.ws_row0 + m * BM;
+        float* dst = p.dqacc + (wrow + il) * D;
+        uint32_t a[D];
+        if (!wait_warp(bar(B_DQFULL0), it & 1, ctl, 0xA0000031u)) goto done;
+        tc_fence_after();
+        tmem_ld32p(tl + TM_DQ0, a);
+        tmem_ld32p(tl + TM_DQ0 + 32, a + 32);
+        tmem_wait_ld();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(B_DQFREE0));
+        if (D == 128) {
+          if (!wait_warp(bar(B_DQFULL1), it & 1, ctl, 0xA0000032u)) goto done;
+          tc_fence_after();
+          tmem_ld32p(tl + TM_DQ1, a + (D == 128 ? 64 : 0));
+          tmem_ld32p(tl + TM_DQ1 + 32, a + (D == 128 ? 96 : 0));
+          tmem_wait_ld();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar(B_DQFREE1));
+        }
+        int* sem = p.sem + static_cast<int64_t>(h) * (p.ws_rows / kTileRows) +
+                   un.si.ws_row0 / kTileRows + m;
+        if (p.deterministic) {
+          // KV tiles 0..n-1 have each released 4 arrivals for this query tile
+          int stop = 0;
+          if (lane == 0) {
+            const int want = 4 * un.n;
+            const uint64_t t0 = globaltimer_ns();
+            for (uint32_t spin = 0;; ++spin) {
+              if (ld_acquire(sem) >= want) break;
+              if ((spin & 15) == 15) {
+                if (*abort_flag) { stop = 1; break; }
+                if (globaltimer_ns() - t0 > p.timeout_ns) {
+                  raise_abort(ctl, 0xA0000033u);
+                  stop = 1;
+                  break;
+                }
+              }
+            }
+          }
+          if (__shfl_sync(0xffffffffu, stop, 0)) goto done;
+        }
+        if (row_ok) {
+#pragma unroll
+          for (int d = 0; d < D; d += 4)
+            red_add_v4(dst + d, __uint_as_float(a[d]), __uint_as_float(a[d + 1]),
+                       __uint_as_float(a[d + 2]), __uint_as_float(a[d + 3]));
+        }
+        if (p.deterministic) {
+          __threadfence();
+          __syncwarp();
+          if (lane == 0) red_release_add(sem, 1);
+        }
+      }
+    }
+  }
+
+done:
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 2) tmem_dealloc(tmem, kTmemCols);
+}
+
+template <typename T, int D>
+cudaError_t launch_t(const BwdParams& p, int dtype, cudaStream_t stream) {
+  const bool varlen = p.seq.cu_q != nullptr;
+  const int nb = varlen ? 1 : p.seq.batch;
+  CUtensorMap tq, tk, tv, tdo;
+  if (!encode_tmap_bshd(&tq, p.q, dtype, p.seq.seqlen_q, p.h_q, nb, D, BM) ||
+      !encode_tmap_bshd(&tk, p.k, dtype, p.seq.seqlen_k, p.h_k, nb, D, BN) ||
+      !encode_tmap_bshd(&tv, p.v, dtype, p.seq.seqlen_k, p.h_k, nb, D, BN) ||
+      !encode_tmap_bshd(&tdo, p.dout, dtype, p.seq.seqlen_q, p.h_q, nb, D, BM))
+    return cudaErrorInvalidValue;
+  constexpr uint32_t smem = Smem<D>::kTotal;
+  static bool attr_done = false;
+  if (!attr_done) {
+    cudaError_t e = cudaFuncSetAttribute(bwd_main_kernel<T, D>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    attr_done = true;
+  }
+  const int n_tiles = ceil_div(p.max_seqlen_k, BN);
+  const int units = n_tiles * p.seq.batch * p.h_k;
+  if (units <= 0) return cudaSuccess;
+  const int grid = units < num_sms() ? units : num_sms();
+  bwd_main_kernel<T, D><<<grid, kThreads, smem, stream>>>(p, tq, tk, tv, tdo);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_bwd_main(const BwdParams& p, int dtype, cudaStream_t stream) {
+  if (dtype == 1) {
+    return p.head_dim == 64 ? launch_t<__nv_bfloat16, 64>(p, dtype, stream)
+                            : launch_t<__nv_bfloat16, 128>(p, dtype, stream);
+  }
+  return p.head_dim == 64 ? launch_t<__half, 64>(p, dtype, stream)
+                          : launch_t<__half, 128>(p, dtype, stream);
+}
+
+}  // namespace attn

@@ -1,0 +1,110 @@
+// Internal parameter blocks and launcher declarations shared by the host API
+// (api.cu) and the kernels.  Not part of the public C ABI.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace attn {
+
+// Query/key tile height of the backward kernels; workspace rows are padded to it.
+constexpr int kTileRows = 128;
+
+__host__ __device__ inline int round_up(int x, int m) { return (x + m - 1) / m * m; }
+__host__ __device__ inline int ceil_div(int x, int m) { return (x + m - 1) / m; }
+
+struct SeqParams {
+  const int* cu_q;  // nullptr in padded mode
+  const int* cu_k;
+  int seqlen_q;     // padded: per-sequence length; varlen: total packed rows
+  int seqlen_k;
+  int batch;        // number of sequences
+};
+
+// A [B, S, H, D] (or packed [total, H, D]) tensor: element strides, last dim contiguous.
+struct TensorArg {
+  const void* ptr;
+  int64_t sb, ss, sh;
+};
+
+struct BwdParams {
+  SeqParams seq;
+  TensorArg q, k, v, o, dout, dq, dk, dv;
+  const float* lse;  // natural log, [B, Hq, Sq] or [Hq, total_q]
+  // workspace
+  float* lse2;   // [Hq][ws_rows]
+  float* delta;  // [Hq][ws_rows]
+  float* dqacc;  // [Hq][ws_rows][D]
+  int* sem;      // [Hq][ws_rows / kTileRows]
+  int64_t ws_rows;
+  int h_q, h_k, head_dim;
+  int causal, deterministic;
+  float scale, scale_log2;
+  int max_seqlen_q, max_seqlen_k;
+  unsigned int* status;
+  const unsigned int* input_bad;  // nonzero after cu_seqlens failed validation (varlen)
+  unsigned long long timeout_ns;
+};
+
+struct FwdParams {
+  SeqParams seq;
+  TensorArg q, k, v, o;
+  float* lse;
+  int h_q, h_k, head_dim;
+  int causal;
+  float scale_log2;
+  int max_seqlen_q;
+  const unsigned int* input_bad;
+};
+
+// Workspace layout (byte offsets), identical on host and device.
+struct WsLayout {
+  int64_t rows;
+  size_t off_lse2, off_delta, off_dqacc, off_sem, total;
+};
+
+inline size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+inline WsLayout ws_layout(int batch, int seqlen_q, int h_q, int head_dim, int varlen) {
+  WsLayout w;
+  if (varlen) {
+    w.rows = round_up(seqlen_q + batch * kTileRows, kTileRows);
+  } else {
+    w.rows = static_cast<int64_t>(batch) * round_up(seqlen_q, kTileRows);
+  }
+  const size_t per_row = static_cast<size_t>(h_q) * static_cast<size_t>(w.rows);
+  w.off_lse2 = 0;
+  w.off_delta = align256(w.off_lse2 + per_row * 4);
+  w.off_dqacc = align256(w.off_delta + per_row * 4);
+  w.off_sem = align256(w.off_dqacc + per_row * static_cast<size_t>(head_dim) * 4);
+  w.total = align256(w.off_sem + static_cast<size_t>(h_q) * (w.rows / kTileRows) * 4);
+  return w;
+}
+
+// Launchers (return a cudaError_t from the launch).
+cudaError_t launch_preprocess(const BwdParams& p, int dtype, cudaStream_t stream);
+cudaError_t launch_postprocess(const BwdParams& p, int dtype, cudaStream_t stream);
+cudaError_t launch_bwd_main(const BwdParams& p, int dtype, cudaStream_t stream);
+cudaError_t launch_fwd(const FwdParams& p, int dtype, cudaStream_t stream);
+cudaError_t launch_zero_rows(const TensorArg& t, int dtype, int nseq, int rows_per_seq,
+                             const int* cu, int total_rows, int heads, int head_dim,
+                             cudaStream_t stream);
+
+cudaError_t launch_validate_cu(const int* cu_q, const int* cu_k, int batch, int total_q,
+                               int total_k, int max_q, int max_k, unsigned int* bad,
+                               cudaStream_t stream);
+
+int num_sms();
+
+// Device status words of the current device ([0] waits, [1] input validation).
+unsigned int* status_word();
+
+// 4-D TMA map over a [B, S, H, D] tensor (dims D, S, H, B; element strides from
+// `t`), box {64, box_rows, 1, 1}, 128-byte swizzle, zero fill out of bounds.
+// For packed varlen tensors pass batch = 1 and rows = total rows.
+bool encode_tmap_bshd(CUtensorMap* out, const TensorArg& t, int dtype, int rows, int heads,
+                      int batch, int head_dim, int box_rows);
+
+}  // namespace attn

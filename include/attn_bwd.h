@@ -1,0 +1,189 @@
+/*
+ * attn_bwd.h -- C ABI of the GB300 (sm_103a) fused attention backward library
+ * (libattn_gb300.so).
+ *
+ * Problem (TileLang test_tilelang_kernel_mha_bwd.py, ref_program and
+ * flashattn_bwd; flash-attention csrc/flash_attn_ck/mha_bwd.cpp, mha_bwd):
+ * for every sequence b and query head h, with key/value head g = h / (H_q/H_k)
+ * and scale s,
+ *     S = s Q K^T (causal: key j allowed for query i iff j <= i + Sk - Sq),
+ *     P = softmax(S) = exp(S - LSE),  O = P V,
+ *     dV_g = sum over the group of P^T dO,   dP = dO V^T,
+ *     Delta = rowsum(O * dO),   dS = P * (dP - Delta),
+ *     dQ = s dS K,   dK_g = s * sum over the group of dS^T Q,
+ * computed without materialising S or P in memory.
+ *
+ * Layout.  Q, O, dO, dQ are [B, Sq, H_q, D]; K, V, dK, dV are [B, Sk, H_k, D]
+ * (flash-attention mha_bwd argument comments).  Each tensor is passed as an
+ * attn_tensor: a device pointer plus element strides for the batch, sequence
+ * and head dimensions; the head dimension is contiguous (stride 1).  In varlen
+ * mode (cu_seqlens given) tensors are packed [total, H, D], stride_b is
+ * ignored, and seqlen_q / seqlen_k are the TOTAL packed row counts while
+ * max_seqlen_q / max_seqlen_k bound the per-sequence lengths.
+ * LSE is fp32, natural log: [B, H_q, Sq] contiguous, or [H_q, total_q] in
+ * varlen mode (flash-attention's softmax_lse).
+ *
+ * Supported: dtype fp16 or bf16 (all of Q,K,V,O,dO,dQ,dK,dV share it), D in
+ * {64, 128}, H_q % H_k == 0, base pointers and strides 16-byte aligned
+ * (strides multiples of 8 elements).
+ *
+ * Ownership.  The caller owns every buffer, including the workspace; the
+ * library allocates nothing per call and keeps no state across calls except
+ * one-time kernel attributes and a device status word.  All compute calls
+ * are asynchronous on `stream` (a cudaStream_t; NULL = legacy default stream).
+ *
+ * Errors.  Every call returns ATTN_OK (0) or a negative code and then
+ * attn_last_error() gives a message (thread-local).  Argument errors are
+ * detected on the host before anything is launched (the convention of
+ * mha_bwd's argument checks: a negative return means invalid argument).
+ * Device-side waits are bounded; a wait that gives up records a nonzero
+ * status that attn_check_device_status() reports as ATTN_ERR_DEVICE_TIMEOUT.
+ */
+#ifndef ATTN_BWD_GB300_H
+#define ATTN_BWD_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* attn_stream_t; /* same type as cudaStream_t */
+
+enum attn_dtype { ATTN_FP16 = 0, ATTN_BF16 = 1 };
+
+enum attn_status {
+  ATTN_OK = 0,
+  ATTN_ERR_DTYPE = -1,          /* dtype not fp16/bf16 */
+  ATTN_ERR_SHAPE = -2,          /* bad sizes: B<=0, H_q%H_k, D not 64/128, ... */
+  ATTN_ERR_STRIDE = -3,         /* stride not a multiple of 8 elements or negative */
+  ATTN_ERR_ALIGN = -4,          /* base pointer not 16-byte aligned */
+  ATTN_ERR_NULL = -5,           /* required pointer is NULL */
+  ATTN_ERR_WORKSPACE = -6,      /* workspace missing, misaligned or too small */
+  ATTN_ERR_CUDA = -7,           /* a CUDA launch or runtime call failed */
+  ATTN_ERR_DEVICE_TIMEOUT = -8, /* a bounded device wait gave up */
+  ATTN_ERR_ARG = -9             /* other invalid argument (scale, max_seqlen, ...) */
+};
+
+typedef struct {
+  void* ptr;        /* device pointer to element [0,0,0,0] */
+  int64_t stride_b; /* elements between batches (ignored in varlen mode) */
+  int64_t stride_s; /* elements between sequence positions */
+  int64_t stride_h; /* elements between heads; the D dimension has stride 1 */
+} attn_tensor;
+
+/*
+ * attn_fwd -- forward pass producing O and the natural-log LSE that
+ * attn_bwd consumes (TileLang flashattn_fwd, online softmax).  Supporting
+ * call: the library's subject is the backward.  Rows with no allowed key get
+ * O = 0 and LSE = +inf.  q, k, v are read; o and lse are written.
+ */
+int attn_fwd(const attn_tensor* q, const attn_tensor* k, const attn_tensor* v,
+             const attn_tensor* o, float* lse, int dtype, int batch, int seqlen_q,
+             int seqlen_k, int h_q, int h_k, int head_dim, float scale, int causal,
+             const int* cu_seqlens_q, const int* cu_seqlens_k, int max_seqlen_q,
+             int max_seqlen_k, attn_stream_t stream);
+
+/*
+ * attn_bwd_workspace_size -- bytes of device workspace attn_bwd needs
+ * (flash-attention hopper/flash_bwd_launch_template.h, run_flash_bwd:
+ * softmax_lse_log2, dsoftmax_sum, dq_accum and dq_semaphore).
+ * varlen != 0: seqlen_q is the total packed query rows and batch the number
+ * of sequences.  Workspace rows are padded to 128 per sequence.
+ */
+size_t attn_bwd_workspace_size(int batch, int seqlen_q, int h_q, int head_dim,
+                               int deterministic, int varlen);
+
+/*
+ * attn_bwd_workspace_layout -- where the pieces of the workspace live, for
+ * callers that inspect them.  Writes byte offsets of LSE2 (fp32
+ * [H_q][rows]), Delta (fp32 [H_q][rows]), dQaccum (fp32 [H_q][rows][D]) and
+ * the semaphores (int32 [H_q][rows/128]) into offsets[0..3], and `rows`.
+ * Row of query i of sequence b: padded mode b*round_up(Sq,128) + i; varlen
+ * 128*(cu_seqlens_q[b]/128 + b) + i.  Returns ATTN_OK or ATTN_ERR_NULL.
+ */
+int attn_bwd_workspace_layout(int batch, int seqlen_q, int h_q, int head_dim, int varlen,
+                              size_t offsets[4], int64_t* rows);
+
+/*
+ * attn_bwd -- fused backward: dq, dk, dv from q, k, v, o, lse, dout.
+ * Runs the three stages below on `stream`.  dq, dk, dv are fully overwritten.
+ * deterministic != 0: dQ contributions are added in ascending key-tile order,
+ * so results are bit-identical run to run (in the reference CK wrapper the
+ * same property comes from split dq_accum buffers; here a semaphore orders
+ * the adds).  Sq == 0 gives dk = dv = 0; Sk == 0 gives dq = 0.
+ * workspace: device memory of at least attn_bwd_workspace_size(...) bytes,
+ * 256-byte aligned, owned by the caller, not shared by concurrent calls.
+ */
+int attn_bwd(const attn_tensor* q, const attn_tensor* k, const attn_tensor* v,
+             const attn_tensor* o, const float* lse, const attn_tensor* dout,
+             const attn_tensor* dq, const attn_tensor* dk, const attn_tensor* dv, int dtype,
+             int batch, int seqlen_q, int seqlen_k, int h_q, int h_k, int head_dim,
+             float scale, int causal, const int* cu_seqlens_q, const int* cu_seqlens_k,
+             int max_seqlen_q, int max_seqlen_k, int deterministic, void* workspace,
+             size_t workspace_bytes, attn_stream_t stream);
+
+/*
+ * The three stages of attn_bwd, callable one by one (same arguments, same
+ * checks) so that each kernel can be timed on its own.  They must run in this
+ * order on one stream with the same workspace.
+ *   attn_bwd_preprocess  -- Delta = rowsum(O*dO) (fp32), LSE2 = LSE*log2(e),
+ *                           dQaccum = 0, semaphores = 0
+ *                           (TileLang flashattn_bwd_preprocess; FA3 preprocess
+ *                           with Clear_dQaccum).
+ *   attn_bwd_main        -- dK, dV written; dQ accumulated in fp32 dQaccum
+ *                           (TileLang flashattn_bwd; FA3 CollectiveMainloopBwd).
+ *   attn_bwd_postprocess -- dQ = scale * dQaccum cast to the dtype
+ *                           (mslk flash_bwd_postprocess.py; FA3
+ *                           FlashAttnBwdPostprocessConvertdQ).
+ */
+int attn_bwd_preprocess(const attn_tensor* q, const attn_tensor* k, const attn_tensor* v,
+                        const attn_tensor* o, const float* lse, const attn_tensor* dout,
+                        const attn_tensor* dq, const attn_tensor* dk, const attn_tensor* dv,
+                        int dtype, int batch, int seqlen_q, int seqlen_k, int h_q, int h_k,
+                        int head_dim, float scale, int causal, const int* cu_seqlens_q,
+                        const int* cu_seqlens_k, int max_seqlen_q, int max_seqlen_k,
+                        int deterministic, void* workspace, size_t workspace_bytes,
+                        attn_stream_t stream);
+int attn_bwd_main(const attn_tensor* q, const attn_tensor* k, const attn_tensor* v,
+                  const attn_tensor* o, const float* lse, const attn_tensor* dout,
+                  const attn_tensor* dq, const attn_tensor* dk, const attn_tensor* dv, int dtype,
+                  int batch, int seqlen_q, int seqlen_k, int h_q, int h_k, int head_dim,
+                  float scale, int causal, const int* cu_seqlens_q, const int* cu_seqlens_k,
+                  int max_seqlen_q, int max_seqlen_k, int deterministic, void* workspace,
+                  size_t workspace_bytes, attn_stream_t stream);
+int attn_bwd_postprocess(const attn_tensor* q, const attn_tensor* k, const attn_tensor* v,
+                         const attn_tensor* o, const float* lse, const attn_tensor* dout,
+                         const attn_tensor* dq, const attn_tensor* dk, const attn_tensor* dv,
+                         int dtype, int batch, int seqlen_q, int seqlen_k, int h_q, int h_k,
+                         int head_dim, float scale, int causal, const int* cu_seqlens_q,
+                         const int* cu_seqlens_k, int max_seqlen_q, int max_seqlen_k,
+                         int deterministic, void* workspace, size_t workspace_bytes,
+                         attn_stream_t stream);
+
+/*
+ * attn_check_device_status -- synchronises `stream`, then reads and clears the
+ * device status word.  Returns ATTN_OK, ATTN_ERR_DEVICE_TIMEOUT (a bounded
+ * wait inside a kernel gave up; attn_last_error names the wait site) or
+ * ATTN_ERR_CUDA (the stream reported an error).
+ */
+int attn_check_device_status(attn_stream_t stream);
+
+/*
+ * attn_set_wait_timeout_ns -- limit for every device-side wait of later calls
+ * (default 4e9 ns).  Values <= 0 restore the default.
+ */
+void attn_set_wait_timeout_ns(int64_t ns);
+
+/* Message for the last error on this thread ("" if none). */
+const char* attn_last_error(void);
+
+/* Library version string. */
+const char* attn_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ATTN_BWD_GB300_H */

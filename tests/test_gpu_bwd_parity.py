@@ -1,0 +1,177 @@
+"""GPU backward (attn_bwd through the C ABI) against the fp64 CPU oracle.
+
+Primary check: GPU attn_fwd -> GPU attn_bwd, compared with the all-fp64
+oracle gradients of the same rounded inputs.  Secondary check: the oracle's
+O (rounded to the dtype) and LSE are fed to the GPU backward, isolating the
+backward's own error.  Tolerance: rel-L2 <= 1e-2, max-abs <= 2e-2 * max|ref|.
+"""
+import numpy as np
+import pytest
+import torch
+
+import attention_backward_bwd_gb300 as ab
+from attention_backward_bwd_gb300 import synth
+from oracle import attn_oracle
+from tests.gpu_helpers import assert_close, to_dev
+
+pytestmark = pytest.mark.gpu
+
+DT = {"bf16": torch.bfloat16, "fp16": torch.float16}
+
+
+def run_gpu(w, x, deterministic=False, o=None, lse=None):
+    (q, k, v, do), cu_q, cu_k = to_dev(x)
+    mq = mk = None
+    if cu_q is not None:
+        mq = mk = max(x.lengths) if x.lengths else 0
+    if o is None:
+        o, lse = ab.attn_fwd(q, k, v, causal=w.causal, cu_seqlens_q=cu_q, cu_seqlens_k=cu_k,
+                             max_seqlen_q=mq, max_seqlen_k=mk)
+    dq, dk, dv = ab.attn_bwd(q, k, v, o, lse, do, causal=w.causal, cu_seqlens_q=cu_q,
+                             cu_seqlens_k=cu_k, max_seqlen_q=mq, max_seqlen_k=mk,
+                             deterministic=deterministic or w.deterministic)
+    ab.check_device_status()
+    return dq, dk, dv
+
+
+def oracle_grads(w, x):
+    return attn_oracle.mha_backward(x.q, x.k, x.v, x.do, w.scale, w.causal, x.cu_seqlens_q,
+                                    x.cu_seqlens_k)
+
+
+def check(w, x, deterministic=False):
+    dq, dk, dv = run_gpu(w, x, deterministic)
+    ref = oracle_grads(w, x)
+    out = {}
+    floor = float(np.abs(ref["dV"]).max())
+    for name, got in (("dQ", dq), ("dK", dk), ("dV", dv)):
+        out[name] = assert_close(f"{w.name} {name}", got, ref[name], floor=floor)
+    return out
+
+
+@pytest.mark.parametrize("name", ["mha_b1_h2_s128_d64_fp16", "mha_b4_h16_s1024_d64_fp16_causal"])
+def test_small_workloads_full(name):
+    w = synth.WORKLOADS[name]
+    check(w, synth.make_inputs(w))
+
+
+EDGE = [
+    # B, Hq, Hk, Sq, Sk, D, dtype, causal
+    (1, 1, 1, 1, 1, 64, "bf16", False),
+    (1, 2, 2, 63, 63, 64, "fp16", True),
+    (1, 2, 1, 65, 65, 128, "bf16", True),
+    (2, 2, 2, 129, 129, 128, "fp16", False),
+    (1, 4, 2, 200, 200, 64, "bf16", True),
+    (2, 4, 1, 300, 300, 128, "bf16", True),
+    (1, 2, 2, 256, 256, 128, "bf16", False),
+    (1, 2, 2, 100, 300, 128, "bf16", False),  # Sq < Sk
+    (1, 2, 2, 100, 300, 64, "fp16", True),    # causal, bottom-right alignment
+    (1, 2, 2, 300, 100, 128, "bf16", True),   # causal Sq > Sk: leading rows see no key
+    (1, 8, 2, 384, 384, 128, "bf16", True),   # GQA 4:1, several tiles
+]
+
+
+@pytest.mark.parametrize("case", EDGE, ids=str)
+def test_edge_shapes(case):
+    b, hq, hk, sq, sk, d, dtype, causal = case
+    w = synth.small("edge", b, hq, hk, sq, sk, d, dtype, causal, 50 + sq + sk)
+    check(w, synth.make_inputs(w))
+
+
+@pytest.mark.parametrize("case", EDGE[3:7], ids=str)
+def test_edge_shapes_deterministic(case):
+    b, hq, hk, sq, sk, d, dtype, causal = case
+    w = synth.small("edge_det", b, hq, hk, sq, sk, d, dtype, causal, 60 + sq, deterministic=True)
+    check(w, synth.make_inputs(w), deterministic=True)
+
+
+def test_secondary_oracle_forward_inputs():
+    w = synth.small("sec", 2, 4, 2, 333, 333, 128, "bf16", True, 71)
+    x = synth.make_inputs(w)
+    o_ref, lse_ref = attn_oracle.mha_forward(x.q, x.k, x.v, w.scale, True)
+    o = torch.tensor(o_ref).to(torch.bfloat16).cuda()
+    lse = torch.tensor(lse_ref, dtype=torch.float32).cuda()
+    dq, dk, dv = run_gpu(w, x, o=o, lse=lse)
+    ref = oracle_grads(w, x)
+    for name, got in (("dQ", dq), ("dK", dk), ("dV", dv)):
+        assert_close(name, got, ref[name])
+
+
+def test_varlen_with_empty_sequences():
+    lens = [5, 130, 0, 64, 1, 257, 128]
+    w = synth.Workload("vl", 0, 4, 2, 0, 0, 128, "bf16", True, 81, n_seqs=len(lens), len_lo=0,
+                       len_hi=300)
+    check(w, synth.make_inputs(w, lengths=lens))
+
+
+def test_varlen_deterministic_d64():
+    lens = [300, 17, 129]
+    w = synth.Workload("vl64", 0, 2, 2, 0, 0, 64, "fp16", False, 82, n_seqs=3, len_lo=1,
+                       len_hi=300, deterministic=True)
+    check(w, synth.make_inputs(w, lengths=lens), deterministic=True)
+
+
+def test_deterministic_is_bitwise_repeatable():
+    w = synth.small("det", 1, 8, 2, 1000, 1000, 128, "bf16", True, 91, deterministic=True)
+    x = synth.make_inputs(w)
+    runs = [run_gpu(w, x, deterministic=True) for _ in range(3)]
+    for r in runs[1:]:
+        for a, b in zip(runs[0], r):
+            assert torch.equal(a, b)
+    ref = oracle_grads(w, x)
+    for name, got in zip(("dQ", "dK", "dV"), runs[0]):
+        assert_close(name, got, ref[name])
+
+
+def test_empty_query_and_key_sides():
+    (q, k, v, do) = [torch.randn(1, 0, 2, 64, dtype=torch.bfloat16, device="cuda")
+                     for _ in range(4)]
+    k = torch.randn(1, 50, 2, 64, dtype=torch.bfloat16, device="cuda")
+    v = torch.randn_like(k)
+    o = torch.empty_like(q)
+    lse = torch.empty(1, 2, 0, device="cuda")
+    dk = torch.full_like(k, 7.0)
+    dv = torch.full_like(v, 7.0)
+    ab.attn_bwd(q, k, v, o, lse, do, dk=dk, dv=dv)
+    ab.check_device_status()
+    assert (dk == 0).all() and (dv == 0).all()
+    q = torch.randn(1, 40, 2, 64, dtype=torch.bfloat16, device="cuda")
+    k = torch.randn(1, 0, 2, 64, dtype=torch.bfloat16, device="cuda")
+    dq = torch.full_like(q, 7.0)
+    ab.attn_bwd(q, k, k, q, torch.zeros(1, 2, 40, device="cuda"), q, dq=dq)
+    ab.check_device_status()
+    assert (dq == 0).all()
+
+
+def test_strided_inputs():
+    """Heads taken from a wider tensor: stride_h = D, stride_s = 2*H*D."""
+    w = synth.small("str", 2, 4, 2, 160, 160, 64, "bf16", False, 93)
+    x = synth.make_inputs(w)
+    dev = "cuda"
+
+    def widen(t):
+        big = torch.zeros(t.shape[0], t.shape[1], 2 * t.shape[2], t.shape[3], dtype=t.dtype)
+        big[:, :, 1::2] = t
+        return big.to(dev)[:, :, 1::2]
+
+    q, k, v, do = (widen(t) for t in (x.q, x.k, x.v, x.do))
+    assert q.stride(2) == 2 * 64
+    o, lse = ab.attn_fwd(q, k, v)
+    dq, dk, dv = ab.attn_bwd(q, k, v, o, lse, do)
+    ab.check_device_status()
+    ref = oracle_grads(w, x)
+    for name, got in (("dQ", dq), ("dK", dk), ("dV", dv)):
+        assert_close(name, got, ref[name])
+
+
+def test_full_size_invariants_mha_s1024():
+    """Properties that hold at any size: sum_j dV_j = sum_i dO_i per head
+    (rows of P sum to one) and sum_j dK_j = 0 per kv head (rows of dS sum to 0)."""
+    w = synth.WORKLOADS["mha_b4_h16_s1024_d64_fp16_causal"]
+    x = synth.make_inputs(w)
+    dq, dk, dv = run_gpu(w, x)
+    sdv = dv.double().sum(dim=1).cpu()
+    sdo = x.do.double().sum(dim=1)
+    assert torch.allclose(sdv, sdo, rtol=2e-2, atol=2e-2 * sdo.abs().max().item())
+    sdk = dk.double().sum(dim=1).cpu()
+    assert sdk.abs().max().item() <= 2e-2 * dk.double().abs().sum(dim=1).max().item()
