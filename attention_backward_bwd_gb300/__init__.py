@@ -5,9 +5,9 @@ The computation runs in hand-written sm_103a CUDA kernels inside
 builds and binds it.  PyTorch provides device memory and streams.
 """
 from .binding import (AttnError, alloc_workspace, attn_bwd, attn_fwd, check_device_status,
-                      diag_mma, diag_wait_timeout, lib, set_wait_timeout_ns, version,
+                      diag_exp2, diag_mma, diag_wait_timeout, lib, set_wait_timeout_ns, version,
                       workspace_layout, workspace_size)
 
 __all__ = ["AttnError", "alloc_workspace", "attn_bwd", "attn_fwd", "check_device_status",
-           "diag_mma", "diag_wait_timeout", "lib", "set_wait_timeout_ns", "version",
+           "diag_exp2", "diag_mma", "diag_wait_timeout", "lib", "set_wait_timeout_ns", "version",
            "workspace_layout", "workspace_size"]

@@ -47,7 +47,7 @@ _lock = threading.Lock()
 EXPORTS = ("attn_fwd", "attn_bwd", "attn_bwd_preprocess", "attn_bwd_main", "attn_bwd_postprocess",
            "attn_bwd_workspace_size", "attn_bwd_workspace_layout", "attn_check_device_status",
            "attn_set_wait_timeout_ns", "attn_last_error", "attn_version", "attn_diag_mma",
-           "attn_diag_wait_timeout")
+           "attn_diag_wait_timeout", "attn_diag_exp2")
 
 
 def lib() -> ctypes.CDLL:
@@ -84,6 +84,8 @@ def lib() -> ctypes.CDLL:
         L.attn_version.restype = ctypes.c_char_p
         L.attn_diag_mma.argtypes = [_I, _I, _I, _P, _P, _P, _P]
         L.attn_diag_mma.restype = _I
+        L.attn_diag_exp2.argtypes = [_P, _P, _I, _P]
+        L.attn_diag_exp2.restype = _I
         L.attn_diag_wait_timeout.argtypes = [ctypes.c_int64, _P]
         L.attn_diag_wait_timeout.restype = _I
         _lib = L
@@ -236,6 +238,13 @@ def diag_mma(mode: int, a: torch.Tensor, b: torch.Tensor) -> torch.Tensor:
     _check(lib().attn_diag_mma(mode, _dtype_code(a), d, a.data_ptr(), b.data_ptr(), c.data_ptr(),
                                _stream(None)))
     return c
+
+
+def diag_exp2(x: torch.Tensor) -> torch.Tensor:
+    """The kernel's polynomial 2^x on a device fp32 tensor (see include/attn_diag.h)."""
+    y = torch.empty_like(x)
+    _check(lib().attn_diag_exp2(x.data_ptr(), y.data_ptr(), x.numel(), _stream(None)))
+    return y
 
 
 def diag_wait_timeout(ns: int):

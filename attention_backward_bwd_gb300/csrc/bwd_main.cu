@@ -25,8 +25,9 @@
 //
 // TMEM columns (512 allocated, 128 lanes):
 //   [  0,128) S^T fp32; its first 64 columns are then reused for packed P^T
-//   [128,256) dP^T fp32; its first 64 columns are then reused for packed dS^T
-//   [ 64,128) dQ columns 0..63 and [192,256) dQ columns 64..127 (free halves)
+//   [128,256) dP^T fp32; its last 64 columns are then reused for packed dS^T
+//   [ 64,64+D) dQ (the S and dP columns freed once P^T and dS^T are packed),
+//              one N = D MMA: N = 64 MMAs run at 2/3 rate on this part
 //   [256,256+D) dK, [384,384+D) dV
 // Every mbarrier wait is bounded (see WaitCtl): on timeout the kernel records
 // the site in the status word and unwinds.
@@ -42,8 +43,8 @@ constexpr int kThreads = 384;
 constexpr int kStages = 2;
 constexpr uint32_t kChunk = 128 * 128;  // one 64-column (128-byte) slice of a 128-row tile
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t TM_S = 0, TM_P = 0, TM_DP = 128, TM_DS = 128;
-constexpr uint32_t TM_DQ0 = 64, TM_DQ1 = 192, TM_DK = 256, TM_DV = 384;
+constexpr uint32_t TM_S = 0, TM_P = 0, TM_DP = 128, TM_DS = 192;
+constexpr uint32_t TM_DQ = 64, TM_DK = 256, TM_DV = 384;
 
 enum Bar : uint32_t {
   B_FULLQ = 0,
@@ -55,10 +56,9 @@ enum Bar : uint32_t {
   B_DPFULL,
   B_PREADY,
   B_DSREADY,
-  B_DQFULL0,
-  B_DQFULL1,
-  B_DQFREE0,
-  B_DQFREE1,
+  B_DQFULL,
+  B_DQFREE,
+  B_DKDONE,
   B_DKDVFULL,
   B_DKDVFREE,
   B_FINAL,
@@ -148,10 +148,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(bar(B_DPFULL), 1);
     mbar_init(bar(B_PREADY), 4);
     mbar_init(bar(B_DSREADY), 4);
-    mbar_init(bar(B_DQFULL0), 1);
-    mbar_init(bar(B_DQFULL1), 1);
-    mbar_init(bar(B_DQFREE0), 4);
-    mbar_init(bar(B_DQFREE1), 4);
+    mbar_init(bar(B_DQFULL), 1);
+    mbar_init(bar(B_DQFREE), 4);
+    mbar_init(bar(B_DKDONE), 1);
     mbar_init(bar(B_DKDVFULL), 1);
     mbar_init(bar(B_DKDVFREE), 4);
     mbar_init(bar(B_FINAL), 1);
@@ -229,7 +228,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       constexpr uint32_t kIdS = idesc_f16(kIsBf16, 0, 0, BN, BM);
       constexpr uint32_t kIdKV = idesc_f16(kIsBf16, 0, 1, BN, D);
-      constexpr uint32_t kIdDQ = idesc_f16(kIsBf16, 1, 1, BM, 64);
+      constexpr uint32_t kIdDQ = idesc_f16(kIsBf16, 1, 1, BM, D);
       uint32_t it = 0, uc = 0;
       for (int u = blockIdx.x; u < num_units; u += gridDim.x) {
         const Unit un = get_unit(p, u, G);
@@ -242,7 +241,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t sQ = sb + L::kQ + s * L::kTile;
           const uint32_t sDO = sb + L::kDO + s * L::kTile;
           if (!wait1(bar(B_FULLQ + s), ph, ctl, 0xA0000013u)) goto mma_exit;
-          if (it > 0 && !wait1(bar(B_DQFREE0), (it - 1) & 1, ctl, 0xA0000014u)) goto mma_exit;
+          // S and the dQ columns of the previous iteration must be drained
+          if (it > 0 && !wait1(bar(B_DQFREE), (it - 1) & 1, ctl, 0xA0000014u)) goto mma_exit;
           tc_fence_after();
           // S^T = K Q^T   (M = keys, N = queries, K = head dim; both K-major)
 #pragma unroll
@@ -253,8 +253,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           tc_commit(bar(B_SFULL));
           if (!wait1(bar(B_FULLDO + s), ph, ctl, 0xA0000015u)) goto mma_exit;
-          if (D == 128 && it > 0 && !wait1(bar(B_DQFREE1), (it - 1) & 1, ctl, 0xA0000016u))
-            goto mma_exit;
+          // dP^T overwrites the packed dS^T the previous dK read
+          if (it > 0 && !wait1(bar(B_DKDONE), (it - 1) & 1, ctl, 0xA0000016u)) goto mma_exit;
           tc_fence_after();
           // dP^T = V dO^T
 #pragma unroll
@@ -276,35 +276,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                    kIdKV, (j > 0 || kk > 0) ? 1u : 0u);
           if (!wait1(bar(B_DSREADY), it & 1, ctl, 0xA0000018u)) goto mma_exit;
           tc_fence_after();
-          if (D == 128) {
-            // dQ[:, 0:64] = dS K[:, 0:64]  (A = dS MN-major from the dS^T tile, B = K MN-major)
+          // dQ = dS K   (A = dS MN-major from the dS^T tile, B = K MN-major, N = D)
 #pragma unroll
-            for (int kk = 0; kk < BN / 16; ++kk)
-              mma_ss(tmem + TM_DQ0, sdesc_sw128(sb + L::kDS + kk * 2048, kChunk, 1024),
-                     sdesc_sw128(sb + L::kK + kk * 2048, kChunk, 1024), kIdDQ, kk > 0);
-            tc_commit(bar(B_DQFULL0));
-            // dK += dS^T Q
+          for (int kk = 0; kk < BN / 16; ++kk)
+            mma_ss(tmem + TM_DQ, sdesc_sw128(sb + L::kDS + kk * 2048, kChunk, 1024),
+                   sdesc_sw128(sb + L::kK + kk * 2048, kChunk, 1024), kIdDQ, kk > 0);
+          tc_commit(bar(B_DQFULL));
+          // dK += dS^T Q   (A = dS^T from TMEM, B = Q MN-major)
 #pragma unroll
-            for (int kk = 0; kk < BM / 16; ++kk)
-              mma_ts(tmem + TM_DK, tmem + TM_DS + kk * 8, sdesc_sw128(sQ + kk * 2048, kChunk, 1024),
-                     kIdKV, (j > 0 || kk > 0) ? 1u : 0u);
-            // dQ[:, 64:128] = dS K[:, 64:128]
-#pragma unroll
-            for (int kk = 0; kk < BN / 16; ++kk)
-              mma_ss(tmem + TM_DQ1, sdesc_sw128(sb + L::kDS + kk * 2048, kChunk, 1024),
-                     sdesc_sw128(sb + L::kK + kChunk + kk * 2048, kChunk, 1024), kIdDQ, kk > 0);
-            tc_commit(bar(B_DQFULL1));
-          } else {
-#pragma unroll
-            for (int kk = 0; kk < BM / 16; ++kk)
-              mma_ts(tmem + TM_DK, tmem + TM_DS + kk * 8, sdesc_sw128(sQ + kk * 2048, kChunk, 1024),
-                     kIdKV, (j > 0 || kk > 0) ? 1u : 0u);
-#pragma unroll
-            for (int kk = 0; kk < BN / 16; ++kk)
-              mma_ss(tmem + TM_DQ0, sdesc_sw128(sb + L::kDS + kk * 2048, kChunk, 1024),
-                     sdesc_sw128(sb + L::kK + kk * 2048, kChunk, 1024), kIdDQ, kk > 0);
-            tc_commit(bar(B_DQFULL0));
-          }
+          for (int kk = 0; kk < BM / 16; ++kk)
+            mma_ts(tmem + TM_DK, tmem + TM_DS + kk * 8, sdesc_sw128(sQ + kk * 2048, kChunk, 1024),
+                   kIdKV, (j > 0 || kk > 0) ? 1u : 0u);
+          tc_commit(bar(B_DKDONE));
           tc_commit(bar(B_EMPTY + s));
         }
         tc_commit(bar(B_DKDVFULL));
@@ -355,29 +338,51 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float* lse2 = reinterpret_cast<const float*>(smem + L::kLSE + s * BM * 4);
         const float* dlt = reinterpret_cast<const float*>(smem + L::kDelta + s * BM * 4);
         if (!wait_warp(bar(B_FULLQ + s), ph, ctl, 0xA0000021u)) goto done;
+        // valid queries of this key row, in tile coordinates: lo <= il < hi
+        int lo = 0, hi = key_ok ? min(BM, un.si.sq - q0) : 0;
+        if (p.causal) lo = max(0, key - off - q0);
         if (!wait_warp(bar(B_SFULL), it & 1, ctl, 0xA0000022u)) goto done;
         tc_fence_after();
-        // P^T row `jl`: 4 chunks of 32 queries; packed P overwrites the S columns already read.
-#pragma unroll 1
-        for (int c = 0; c < BM / 32; ++c) {
-          uint32_t sv[32];
-          tmem_ld32(tl + TM_S + c * 32, sv);
-          tmem_wait_ld();
-          uint32_t pk[16];
+        // P^T row `jl`, 4 chunks of 32 queries.  The TMEM load of chunk c+1 is in
+        // flight while chunk c is computed; packed P overwrites S columns already read.
+        {
+          uint32_t sv[2][32];
+          tmem_ld32(tl + TM_S, sv[0]);
 #pragma unroll
-          for (int e = 0; e < 32; e += 2) {
-            float x0 = ex2(fmaf(__uint_as_float(sv[e]), sl2, -lse2[c * 32 + e]));
-            float x1 = ex2(fmaf(__uint_as_float(sv[e + 1]), sl2, -lse2[c * 32 + e + 1]));
-            if (need_mask) {
-              const int i0 = q0 + c * 32 + e;
-              const bool ok0 = key_ok && i0 < un.si.sq && (!p.causal || key <= i0 + off);
-              const bool ok1 = key_ok && i0 + 1 < un.si.sq && (!p.causal || key <= i0 + 1 + off);
-              x0 = ok0 ? x0 : 0.f;
-              x1 = ok1 ? x1 : 0.f;
+          for (int c = 0; c < BM / 32; ++c) {
+            tmem_wait_ld();
+            if (c + 1 < BM / 32) tmem_ld32(tl + TM_S + (c + 1) * 32, sv[(c + 1) & 1]);
+            const float4* l4 = reinterpret_cast<const float4*>(lse2 + c * 32);
+            uint32_t pk[16];
+#pragma unroll
+            for (int e4 = 0; e4 < 8; ++e4) {
+              const float4 l = l4[e4];
+              const uint32_t* v = &sv[c & 1][e4 * 4];
+              // half of the exponentials on MUFU, half as a polynomial on the FMA pipe
+              float x0, x1, x2, x3;
+              if (e4 & 1) {
+                x0 = ex2_poly(fmaf(__uint_as_float(v[0]), sl2, -l.x));
+                x1 = ex2_poly(fmaf(__uint_as_float(v[1]), sl2, -l.y));
+                x2 = ex2_poly(fmaf(__uint_as_float(v[2]), sl2, -l.z));
+                x3 = ex2_poly(fmaf(__uint_as_float(v[3]), sl2, -l.w));
+              } else {
+                x0 = ex2(fmaf(__uint_as_float(v[0]), sl2, -l.x));
+                x1 = ex2(fmaf(__uint_as_float(v[1]), sl2, -l.y));
+                x2 = ex2(fmaf(__uint_as_float(v[2]), sl2, -l.z));
+                x3 = ex2(fmaf(__uint_as_float(v[3]), sl2, -l.w));
+              }
+              if (need_mask) {
+                const int i = c * 32 + e4 * 4;
+                x0 = (i + 0 >= lo && i + 0 < hi) ? x0 : 0.f;
+                x1 = (i + 1 >= lo && i + 1 < hi) ? x1 : 0.f;
+                x2 = (i + 2 >= lo && i + 2 < hi) ? x2 : 0.f;
+                x3 = (i + 3 >= lo && i + 3 < hi) ? x3 : 0.f;
+              }
+              pk[e4 * 2] = Pack<T>::two(x0, x1);
+              pk[e4 * 2 + 1] = Pack<T>::two(x2, x3);
             }
-            pk[e / 2] = Pack<T>::two(x0, x1);
+            tmem_st16(tl + TM_P + c * 16, pk);
           }
-          tmem_st16(tl + TM_P + c * 16, pk);
         }
         tmem_wait_st();
         tc_fence_before();
@@ -387,30 +392,46 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!wait_warp(bar(B_FULLDO + s), ph, ctl, 0xA0000023u)) goto done;
         if (!wait_warp(bar(B_DPFULL), it & 1, ctl, 0xA0000024u)) goto done;
         tc_fence_after();
-        // dS^T row `jl` = P^T (dP^T - Delta); to TMEM (packed, over dP) and to the smem dS^T tile.
-#pragma unroll 1
-        for (int c = 0; c < BM / 32; ++c) {
-          uint32_t dpv[32], pv[16];
-          tmem_ld32(tl + TM_DP + c * 32, dpv);
-          tmem_ld16(tl + TM_P + c * 16, pv);
-          tmem_wait_ld();
-          uint32_t pk[16];
+        // dS^T row `jl` = P^T (dP^T - Delta); to TMEM (packed into the upper dP
+        // columns) and to the smem dS^T tile.  Chunks go from the last to the first
+        // so every packed store lands on dP columns already read; the loads of
+        // chunk c-1 overlap the math of chunk c.
+        {
+          uint32_t dpv[2][32], pv[2][16];
+          constexpr int kC = BM / 32;
+          tmem_ld32(tl + TM_DP + (kC - 1) * 32, dpv[(kC - 1) & 1]);
+          tmem_ld16(tl + TM_P + (kC - 1) * 16, pv[(kC - 1) & 1]);
 #pragma unroll
-          for (int e = 0; e < 16; ++e) {
-            const float2 pp = Pack<T>::unpack(pv[e]);
-            const float d0 = pp.x * (__uint_as_float(dpv[2 * e]) - dlt[c * 32 + 2 * e]);
-            const float d1 = pp.y * (__uint_as_float(dpv[2 * e + 1]) - dlt[c * 32 + 2 * e + 1]);
-            pk[e] = Pack<T>::two(d0, d1);
-          }
-          tmem_st16(tl + TM_DS + c * 16, pk);
-          // smem dS^T tile: chunk c/2 holds queries [64*(c/2), +64); row jl is 128 bytes,
-          // its 16-byte units u are stored at u ^ (jl % 8) (128-byte swizzle).
-          const uint32_t row_base = L::kDS + (c >> 1) * kChunk + jl * 128;
+          for (int cc = 0; cc < kC; ++cc) {
+            const int c = kC - 1 - cc;
+            tmem_wait_ld();
+            if (c > 0) {
+              tmem_ld32(tl + TM_DP + (c - 1) * 32, dpv[(c - 1) & 1]);
+              tmem_ld16(tl + TM_P + (c - 1) * 16, pv[(c - 1) & 1]);
+            }
+            const float4* d4 = reinterpret_cast<const float4*>(dlt + c * 32);
+            uint32_t pk[16];
 #pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            const uint32_t unit = ((c & 1) * 4 + q) ^ (jl & 7);
-            *reinterpret_cast<uint4*>(smem + row_base + unit * 16) =
-                make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+            for (int e4 = 0; e4 < 8; ++e4) {
+              const float4 dl = d4[e4];
+              const float2 p01 = Pack<T>::unpack(pv[c & 1][e4 * 2]);
+              const float2 p23 = Pack<T>::unpack(pv[c & 1][e4 * 2 + 1]);
+              const uint32_t* v = &dpv[c & 1][e4 * 4];
+              pk[e4 * 2] = Pack<T>::two(p01.x * (__uint_as_float(v[0]) - dl.x),
+                                        p01.y * (__uint_as_float(v[1]) - dl.y));
+              pk[e4 * 2 + 1] = Pack<T>::two(p23.x * (__uint_as_float(v[2]) - dl.z),
+                                            p23.y * (__uint_as_float(v[3]) - dl.w));
+            }
+            tmem_st16(tl + TM_DS + c * 16, pk);
+            // smem dS^T tile: chunk c/2 holds queries [64*(c/2), +64); row jl is 128
+            // bytes, its 16-byte unit u is stored at u ^ (jl % 8) (128-byte swizzle).
+            const uint32_t row_base = L::kDS + (c >> 1) * kChunk + jl * 128;
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              const uint32_t unit = ((c & 1) * 4 + q) ^ (jl & 7);
+              *reinterpret_cast<uint4*>(smem + row_base + unit * 16) =
+                  make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+            }
           }
         }
         tmem_wait_st();
@@ -472,24 +493,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int64_t wrow = static_cast<int64_t>(h) * p.ws_rows + un.si.ws_row0 + m * BM;
         float* dst = p.dqacc + (wrow + il) * D;
         uint32_t a[D];
-        if (!wait_warp(bar(B_DQFULL0), it & 1, ctl, 0xA0000031u)) goto done;
+        if (!wait_warp(bar(B_DQFULL), it & 1, ctl, 0xA0000031u)) goto done;
         tc_fence_after();
-        tmem_ld32p(tl + TM_DQ0, a);
-        tmem_ld32p(tl + TM_DQ0 + 32, a + 32);
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) tmem_ld32p(tl + TM_DQ + c * 32, a + c * 32);
         tmem_wait_ld();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(bar(B_DQFREE0));
-        if (D == 128) {
-          if (!wait_warp(bar(B_DQFULL1), it & 1, ctl, 0xA0000032u)) goto done;
-          tc_fence_after();
-          tmem_ld32p(tl + TM_DQ1, a + (D == 128 ? 64 : 0));
-          tmem_ld32p(tl + TM_DQ1 + 32, a + (D == 128 ? 96 : 0));
-          tmem_wait_ld();
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(bar(B_DQFREE1));
-        }
+        if (lane == 0) mbar_arrive(bar(B_DQFREE));
         int* sem = p.sem + static_cast<int64_t>(h) * (p.ws_rows / kTileRows) +
                    un.si.ws_row0 / kTileRows + m;
         if (p.deterministic) {

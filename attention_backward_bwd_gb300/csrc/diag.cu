@@ -105,11 +105,10 @@ __global__ void __launch_bounds__(128, 1)
         for (int kk = 0; kk < 8; ++kk)
           mma_ts(tmem + 128, tmem + kk * 8, sdesc_sw128(sB + kk * 2048, kChunk, 1024), id, kk > 0);
       } else {
-        constexpr uint32_t id = idesc_f16(kBf, 1, 1, 128, 64);
-        for (int hh = 0; hh < D / 64; ++hh)
-          for (int kk = 0; kk < 8; ++kk)
-            mma_ss(tmem + 256 + hh * 64, sdesc_sw128(sA + kk * 2048, kChunk, 1024),
-                   sdesc_sw128(sB + hh * kChunk + kk * 2048, kChunk, 1024), id, kk > 0);
+        constexpr uint32_t id = idesc_f16(kBf, 1, 1, 128, D);
+        for (int kk = 0; kk < 8; ++kk)
+          mma_ss(tmem + 256, sdesc_sw128(sA + kk * 2048, kChunk, 1024),
+                 sdesc_sw128(sB + kk * 2048, kChunk, 1024), id, kk > 0);
       }
     }
     tc_commit(bar_mma);
@@ -145,6 +144,11 @@ __global__ void diag_wait_kernel(unsigned int* status, unsigned long long timeou
   const WaitCtl ctl{&abort_flag, status, timeout_ns};
   wait_warp(smem_u32(&bar), 0, ctl, 0xD1A0000Fu);  // phase 0 never completes
   __syncthreads();
+}
+
+__global__ void diag_exp2_kernel(const float* x, float* y, int n) {
+  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x)
+    y[i] = ex2_poly(x[i]);
 }
 
 template <typename T, int D>
@@ -187,6 +191,13 @@ int attn_diag_mma(int mode, int dtype, int head_dim, const void* a, const void* 
     return head_dim == 64 ? diag_mma_t<__half, 64>(mode, a, b, c, s, st, to)
                           : diag_mma_t<__half, 128>(mode, a, b, c, s, st, to);
   return ATTN_ERR_DTYPE;
+}
+
+int attn_diag_exp2(const float* x, float* y, int n, attn_stream_t stream) {
+  if (x == nullptr || y == nullptr) return ATTN_ERR_NULL;
+  if (n <= 0) return ATTN_ERR_ARG;
+  diag_exp2_kernel<<<64, 256, 0, reinterpret_cast<cudaStream_t>(stream)>>>(x, y, n);
+  return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
 int attn_diag_wait_timeout(int64_t timeout_ns, attn_stream_t stream) {

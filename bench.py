@@ -1,0 +1,387 @@
+"""Benchmark of the fused attention backward on GB300.
+
+Default workload: GQA backward, B=2, H_q=32, H_k=8, Sq=Sk=8192, D=128, bf16,
+causal, non-deterministic dQ reduction, synthetic N(0,1) inputs (seed 3);
+O and LSE come from this library's forward.  One step = one attn_bwd call
+(preprocess + main + postprocess kernels) over that batch.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                  [--workload NAME] [--deterministic]
+
+Metric: backward TFLOPS = 2.5 * 4 * B * H_q * Sq * Sk * D / t, halved for
+causal.  Prints one JSON line (rank 0).  Multi-GPU runs (torchrun) are
+independent replicas, one per GPU; value = total FLOPs of all ranks / the
+slowest rank's time.  `--impl reference` times the fp64 CPU oracle on a
+bounded sample of the same workload on this host's cores.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+from attention_backward_bwd_gb300 import synth  # noqa: E402
+
+DEFAULT_WORKLOAD = "gqa_b2_hq32_hk8_s8192_d128_bf16_causal"
+METRIC = "attention-backward TFLOPS (bf16, 1xGB300) and % of dense tensor-core peak"
+L2_BYTES = 129 * 2 ** 20
+
+
+def bwd_flops(w: synth.Workload, lengths=None) -> float:
+    """2.5 x forward FLOPs (4 B H Sq Sk D), halved when causal; varlen sums sequences."""
+    if w.varlen:
+        f = sum(2.5 * 4.0 * w.h_q * n * n * w.head_dim for n in lengths)
+    else:
+        f = 2.5 * 4.0 * w.batch * w.h_q * w.seqlen_q * w.seqlen_k * w.head_dim
+    return f / 2 if w.causal else f
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return {"hbm_gbs": float(d["hbm_gbs"]), "bf16_tflops": float(d["bf16_tflops"]),
+                "bf16_tflops_sustained": float(d["bf16_tflops_sustained"]), "src": "measured"}
+    except Exception:
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+                "src": "fallback"}
+
+
+def kernel_traffic():
+    """DRAM bytes per launch of the main kernel from the committed ncu summary,
+    valid only while the kernel source still hashes to the profiled version."""
+    src = os.path.join(ROOT, "attention_backward_bwd_gb300", "csrc", "bwd_main.cu")
+    prof = os.path.join(ROOT, "profiles", "bwd_main_traffic.txt")
+    try:
+        h = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+        kv = dict(line.strip().split("=", 1) for line in open(prof) if "=" in line)
+        if kv.get("source_sha256_16") == h:
+            return float(kv["dram_bytes_per_launch"])
+    except Exception:
+        pass
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi sampling (200 ms) of SM clock and throttle reasons."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = os.path.join("/tmp", f"attn_bench_clocks_{os.getpid()}.csv")
+
+    def __enter__(self):
+        try:
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"], stdout=self.f,
+                stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            self.f.close()
+
+    def summary(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        rows = []
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) >= 9:
+                rows.append(parts)
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = set()
+        sm, smax, pw = [], [], []
+        for r in rows:
+            try:
+                sm.append(float(r[1]))
+                smax.append(float(r[2]))
+                pw.append(float(r[3]))
+            except ValueError:
+                pass
+            for i, n in enumerate(names):
+                if r[5 + i].lower().startswith("active"):
+                    reasons.add(n)
+        load = [s for s, p in zip(sm, pw) if p > 200.0] or sm
+        return {"sm_mhz": statistics.median(load) if load else None,
+                "sm_max_mhz": max(smax) if smax else None, "reasons": sorted(reasons),
+                "samples": len(rows), "power_w_max": max(pw) if pw else None}
+
+
+def dist_setup(n_gpus: int):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+        return rank, world, local, dist
+    return 0, 1, 0, None
+
+
+def barrier(dist):
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+
+
+def max_over_ranks(x: float, dist) -> float:
+    if dist is None:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def run_ours(args):
+    import attention_backward_bwd_gb300 as ab
+    rank, world, local, dist = dist_setup(args.gpus)
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    w = synth.WORKLOADS[args.workload]
+    det = bool(args.deterministic or w.deterministic)
+    x = synth.make_inputs(w)
+    mq = mk = max(x.lengths) if w.varlen else None
+    cu_q = x.cu_seqlens_q.to(dev) if w.varlen else None
+    cu_k = x.cu_seqlens_k.to(dev) if w.varlen else None
+    q, k, v, do = (t.to(dev) for t in (x.q, x.k, x.v, x.do))
+    o, lse = ab.attn_fwd(q, k, v, causal=w.causal, cu_seqlens_q=cu_q, cu_seqlens_k=cu_k,
+                         max_seqlen_q=mq, max_seqlen_k=mk)
+    ws = ab.alloc_workspace(q, cu_q, det)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    kw = dict(causal=w.causal, cu_seqlens_q=cu_q, cu_seqlens_k=cu_k, max_seqlen_q=mq,
+              max_seqlen_k=mk, deterministic=det, workspace=ws, dq=dq, dk=dk, dv=dv)
+    stream = torch.cuda.current_stream()
+    flops = bwd_flops(w, x.lengths)
+    in_bytes = sum(t.numel() * t.element_size() for t in (q, k, v, o, do, lse))
+
+    def step():
+        ab.attn_bwd(q, k, v, o, lse, do, stream=stream, **kw)
+
+    for _ in range(args.warmup):
+        step()
+    ab.check_device_status()
+
+    # --- timed region: K steps, device-resident inputs
+    barrier(dist)
+    with ClockSampler(local) as clk:
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.steps):
+            step()
+        e1.record(stream)
+        barrier(dist)
+        # per-kernel times over the same number of steps (events on the launch stream)
+        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+        for i in range(args.steps):
+            ev = evs[i]
+            ev[0].record(stream)
+            ab.attn_bwd(q, k, v, o, lse, do, stream=stream, stage="pre", **kw)
+            ev[1].record(stream)
+            ab.attn_bwd(q, k, v, o, lse, do, stream=stream, stage="main", **kw)
+            ev[2].record(stream)
+            ab.attn_bwd(q, k, v, o, lse, do, stream=stream, stage="post", **kw)
+            ev[3].record(stream)
+        barrier(dist)
+    ab.check_device_status()
+    ms = e0.elapsed_time(e1) / args.steps
+    ms_max = max_over_ranks(ms, dist)
+    t_pre = statistics.mean(e[0].elapsed_time(e[1]) for e in evs)
+    t_main = statistics.mean(e[1].elapsed_time(e[2]) for e in evs)
+    t_post = statistics.mean(e[2].elapsed_time(e[3]) for e in evs)
+
+    # --- end to end: pinned host inputs -> device -> attn_bwd -> host results
+    hq_ = [t.cpu().pin_memory() for t in (q, k, v, o, do, lse)]
+    dev_in = [torch.empty_like(t) for t in (q, k, v, o, do, lse)]
+    host_out = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in (dq, dk, dv)]
+    h2d = sum(t.numel() * t.element_size() for t in hq_)
+    d2h = sum(t.numel() * t.element_size() for t in host_out)
+
+    def e2e_step():
+        for dst, src in zip(dev_in, hq_):
+            dst.copy_(src, non_blocking=True)
+        ab.attn_bwd(dev_in[0], dev_in[1], dev_in[2], dev_in[3], dev_in[5], dev_in[4],
+                    stream=stream, **kw)
+        for dst, src in zip(host_out, (dq, dk, dv)):
+            dst.copy_(src, non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    barrier(dist)
+    n_e2e = max(2, args.steps // 2)
+    a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a0.record(stream)
+    for _ in range(n_e2e):
+        e2e_step()
+    a1.record(stream)
+    barrier(dist)
+    e2e_ms = max_over_ranks(a0.elapsed_time(a1) / n_e2e, dist)
+
+    if rank != 0:
+        if dist is not None:
+            dist.destroy_process_group()
+        return
+    peaks = measured_peaks()
+    achieved = flops / (t_main * 1e-3) / 1e12
+    peak = peaks["bf16_tflops_sustained"]
+    traffic = kernel_traffic()
+    rows_heads = (sum(x.lengths) if w.varlen else w.batch * w.seqlen_q) * w.h_q
+    esz = 2
+    pre_bytes = rows_heads * (2 * w.head_dim * esz + 4 + 8 + 4 * w.head_dim)
+    post_bytes = rows_heads * (4 * w.head_dim + esz * w.head_dim)
+    value = world * flops / (ms_max * 1e-3) / 1e12
+    cfg = {"workload": w.name, "batch": w.batch if not w.varlen else len(x.lengths),
+           "h_q": w.h_q, "h_k": w.h_k, "seqlen": w.seqlen_q if not w.varlen else "varlen",
+           "head_dim": w.head_dim, "causal": w.causal, "deterministic": det,
+           "l2": "inputs larger than L2 (%.0f MB resident per step)" % (in_bytes / 1e6),
+           "parallelism": f"replicas x{world}" if world > 1 else "single GPU"}
+    if w.varlen:
+        cfg["lengths"] = x.lengths
+    out = {
+        "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_max, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": w.dtype,
+        "data": "synthetic N(0,1), seeded; O and LSE from attn_fwd", "config": cfg,
+        "pct_of_peak": round(100.0 * value / world / peak, 2),
+        "roofline": {"bound": "tensor", "kernel": "bwd_main_kernel", "achieved": round(achieved, 2),
+                     "peak": peak, "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
+                     "peak_src": peaks["src"] + " bf16 sustained",
+                     "traffic": traffic},
+        "kernels_ms": {"preprocess": round(t_pre, 4), "main": round(t_main, 4),
+                       "postprocess": round(t_post, 4)},
+        "hbm": {"preprocess_gbs": round(pre_bytes / (t_pre * 1e-3) / 1e9, 1),
+                "postprocess_gbs": round(post_bytes / (t_post * 1e-3) / 1e9, 1),
+                "peak_gbs": peaks["hbm_gbs"]},
+        "e2e": {"value": round(world * flops / (e2e_ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
+                "ms_per_step": round(e2e_ms, 3), "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "gpu_launches": 3 * args.steps,
+        "clocks": clk.summary(),
+    }
+    if not args.no_cpu_baseline:
+        out["cpu_baseline"] = cpu_baseline(w, x, budget_s=args.cpu_budget)
+    print(json.dumps(out))
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+def _cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except Exception:
+        return os.cpu_count() or 1
+
+
+def oracle_sample(w, x, n_heads=1):
+    """A bounded slice of the workload for the CPU oracle: the first n_heads
+    query heads (one GQA group member each) of sequence 0, full length."""
+    from oracle import attn_oracle
+    if w.varlen:
+        n = x.lengths[0]
+        q, k, v, do = x.q[:n], x.k[:n], x.v[:n], x.do[:n]
+        sl = lambda t, h: t[:, h]  # noqa: E731
+        L = n
+    else:
+        q, k, v, do = x.q[0], x.k[0], x.v[0], x.do[0]
+        sl = lambda t, h: t[:, h]  # noqa: E731
+        L = w.seqlen_q
+    g = w.h_q // w.h_k
+
+    def run(h):
+        return attn_oracle.head_backward(sl(q, h).double().numpy(), sl(k, h // g).double().numpy(),
+                                         sl(v, h // g).double().numpy(),
+                                         sl(do, h).double().numpy(), w.scale, w.causal)
+    f_one = 2.5 * 4.0 * L * L * w.head_dim / (2 if w.causal else 1)
+    return run, f_one, L
+
+
+def cpu_baseline(w, x, budget_s=20.0):
+    run, f_one, L = oracle_sample(w, x)
+    t0 = time.perf_counter()
+    n = 0
+    while True:
+        run(n % w.h_q)
+        n += 1
+        if time.perf_counter() - t0 >= budget_s or n >= 8:
+            break
+    dt = time.perf_counter() - t0
+    return {"value": round(n * f_one / dt / 1e12, 6), "unit": "TFLOP/s", "cores": _cores(),
+            "kind": "oracle",
+            "sample": f"{n} query head(s) of sequence 0, length {L}, fp64 numpy oracle, "
+                      f"{dt:.1f} s"}
+
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    w = synth.WORKLOADS[args.workload]
+    x = synth.make_inputs(w)
+    run, f_one, L = oracle_sample(w, x)
+    for i in range(args.warmup):
+        run(i % w.h_q)
+    times = []
+    for i in range(args.steps):
+        t0 = time.perf_counter()
+        run(i % w.h_q)
+        times.append(time.perf_counter() - t0)
+    ms = 1e3 * statistics.mean(times)
+    val = f_one / (ms * 1e-3) / 1e12
+    sample = f"one query head of sequence 0 per step (length {L}), fp64 numpy oracle"
+    out = {"impl": "reference", "metric": METRIC, "value": round(val, 6), "unit": "TFLOP/s",
+           "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+           "ms_per_step": round(ms, 2), "higher_is_better": True, "scaling": "weak",
+           "vs_baseline": None, "dtype": "f64", "data": "synthetic N(0,1), seeded",
+           "config": {"workload": w.name, "sample": sample},
+           "cpu_baseline": {"value": round(val, 6), "unit": "TFLOP/s", "cores": _cores(),
+                            "kind": "oracle", "sample": sample},
+           "e2e": {"value": round(val, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                   "d2h_bytes_per_step": 0}}
+    print(json.dumps(out))
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(synth.WORKLOADS))
+    ap.add_argument("--deterministic", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-budget", type=float, default=20.0)
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -34,6 +34,14 @@ int attn_diag_mma(int mode, int dtype, int head_dim, const void* a, const void* 
                   attn_stream_t stream);
 
 /*
+ * attn_diag_exp2 -- y[i] = 2^x[i] computed with the polynomial (FMA-pipe)
+ * exponential the backward kernel uses for half of its P entries, so its
+ * accuracy can be checked against a reference.  Valid for x in [-125, 1].
+ * x, y: device fp32 arrays of n elements.
+ */
+int attn_diag_exp2(const float* x, float* y, int n, attn_stream_t stream);
+
+/*
  * attn_diag_wait_timeout -- launches a kernel whose only work is a bounded wait
  * on a barrier that nothing completes.  After timeout_ns (1 .. 2e9) the wait
  * gives up, so attn_check_device_status(stream) must then return

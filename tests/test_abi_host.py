@@ -1,0 +1,155 @@
+"""Host-side checks of the C ABI (no GPU needed): the library loads, exports
+every function the headers declare, and rejects bad arguments with the
+documented status codes before launching anything."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    import __graft_entry__ as g
+    g.build()
+    from attention_backward_bwd_gb300 import binding
+    return binding.lib()
+
+
+def declared_functions():
+    names = []
+    for h in ("attn_bwd.h", "attn_diag.h"):
+        text = open(os.path.join(ROOT, "include", h)).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        names += re.findall(r"\b(attn_[a-z0-9_]+)\s*\(", text)
+    return sorted(set(names))
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = declared_functions()
+    assert len(names) >= 13
+    for n in names:
+        assert hasattr(lib, n), f"{n} declared in include/ but not exported"
+
+
+def test_version(lib):
+    assert b"sm_103a" in lib.attn_version()
+
+
+def test_workspace_size_and_layout(lib):
+    from attention_backward_bwd_gb300 import binding
+    offs, rows = binding.workspace_layout(2, 300, 4, 128)
+    assert rows == 2 * 384
+    assert offs["lse2"] == 0 and offs["delta"] >= 4 * rows * 4
+    assert offs["dqaccum"] >= offs["delta"] + 4 * rows * 4
+    assert offs["sem"] >= offs["dqaccum"] + 4 * rows * 128 * 4
+    size = binding.workspace_size(2, 300, 4, 128)
+    assert size >= offs["sem"] + 4 * (rows // 128) * 4 and size % 256 == 0
+    # varlen: total rows + one padding tile per sequence
+    _, vrows = binding.workspace_layout(3, 1000, 4, 64, varlen=True)
+    assert vrows == ((1000 + 3 * 128 + 127) // 128) * 128
+    assert lib.attn_bwd_workspace_size(0, 10, 1, 64, 0, 0) == 0
+
+
+class FakeTensor:
+    """Just enough of a tensor for the marshalling code: no memory behind it."""
+
+    def __init__(self, shape, ptr=1 << 20, dtype="bf16", strides=None):
+        import torch
+        self.shape = shape
+        self._ptr = ptr
+        self.dtype = {"bf16": torch.bfloat16, "fp16": torch.float16, "f32": torch.float32}[dtype]
+        if strides is None:
+            strides, acc = [], 1
+            for n in reversed(shape):
+                strides.insert(0, acc)
+                acc *= n
+        self._strides = strides
+
+    def dim(self):
+        return len(self.shape)
+
+    def stride(self, i):
+        return self._strides[i]
+
+    def data_ptr(self):
+        return self._ptr
+
+    def numel(self):
+        n = 1
+        for s in self.shape:
+            n *= s
+        return n
+
+
+def call_bwd(lib, q, k, v, o, do, ws_bytes=1 << 30, lse_ptr=1 << 21, ws_ptr=1 << 24,
+             dtype=None, causal=0, head_dim=None, cu=None):
+    from attention_backward_bwd_gb300 import binding as bd
+    ds = [bd._desc(t) for t in (q, k, v, o)]
+    d_do, d_dq, d_dk, d_dv = bd._desc(do), bd._desc(q), bd._desc(k), bd._desc(v)
+    b, sq, hq, d = q.shape
+    sk, hk = k.shape[1], k.shape[2]
+    dt = bd._dtype_code(q) if dtype is None else dtype
+    return lib.attn_bwd(*(ctypes.byref(x) for x in ds), lse_ptr, ctypes.byref(d_do),
+                        ctypes.byref(d_dq), ctypes.byref(d_dk), ctypes.byref(d_dv), dt, b, sq, sk,
+                        hq, hk, head_dim or d, 0.125, causal, cu, cu, sq, sk, 0, ws_ptr, ws_bytes,
+                        None)
+
+
+def shapes(b=1, sq=64, sk=64, hq=2, hk=2, d=64, dtype="bf16", ptr=1 << 20):
+    q = FakeTensor((b, sq, hq, d), ptr, dtype)
+    k = FakeTensor((b, sk, hk, d), ptr, dtype)
+    return q, k, FakeTensor((b, sk, hk, d), ptr, dtype), FakeTensor((b, sq, hq, d), ptr, dtype), \
+        FakeTensor((b, sq, hq, d), ptr, dtype)
+
+
+@pytest.mark.parametrize("case,code", [
+    ("dtype", -1), ("head_dim", -2), ("gqa_ratio", -2), ("align", -4), ("stride", -3),
+    ("null", -5), ("workspace_small", -6), ("workspace_align", -6), ("varlen_half", -9),
+])
+def test_argument_errors(lib, case, code):
+    q, k, v, o, do = shapes()
+    kw = {}
+    if case == "dtype":
+        q, k, v, o, do = shapes(dtype="f32")
+    elif case == "head_dim":
+        q, k, v, o, do = shapes(d=96)
+    elif case == "gqa_ratio":
+        q, k, v, o, do = shapes(hq=3, hk=2)
+    elif case == "align":
+        q, k, v, o, do = shapes(ptr=(1 << 20) + 8)
+    elif case == "stride":
+        q = FakeTensor((1, 64, 2, 64), strides=[64 * 2 * 64, 2 * 64 + 4, 64, 1])
+    elif case == "null":
+        q, k, v, o, do = shapes(ptr=0)
+    elif case == "workspace_small":
+        kw["ws_bytes"] = 1024
+    elif case == "workspace_align":
+        kw["ws_ptr"] = (1 << 24) + 64
+    if case == "varlen_half":
+        from attention_backward_bwd_gb300 import binding as bd
+        ds = [bd._desc(t) for t in (q, k, v, o)]
+        rc = lib.attn_bwd(*(ctypes.byref(x) for x in ds), 1 << 21, ctypes.byref(bd._desc(do)),
+                          ctypes.byref(bd._desc(q)), ctypes.byref(bd._desc(k)),
+                          ctypes.byref(bd._desc(v)), 1, 1, 64, 64, 2, 2, 64, 0.125, 0, 1 << 22,
+                          None, 64, 64, 0, 1 << 24, 1 << 30, None)
+    else:
+        rc = call_bwd(lib, q, k, v, o, do, **kw)
+    assert rc == code, (rc, lib.attn_last_error())
+    assert lib.attn_last_error()  # a message is set
+
+
+def test_error_message_names_the_problem(lib):
+    q, k, v, o, do = shapes(hq=3, hk=2)
+    assert call_bwd(lib, q, k, v, o, do) == -2
+    assert b"h_k" in lib.attn_last_error()
+
+
+def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
+    from attention_backward_bwd_gb300 import binding
+    monkeypatch.setattr(binding, "_lib", None)
+    monkeypatch.setattr(binding, "LIB_PATH", str(tmp_path / "missing.so"))
+    with pytest.raises(ImportError):
+        binding.lib()

@@ -36,6 +36,16 @@ def test_diag_mma_tile(mode, d, dtype):
     assert err <= 1e-3 * ref.abs().max().item(), f"mode {mode}: max err {err}"
 
 
+def test_diag_exp2_polynomial_accuracy():
+    """The FMA-pipe 2^x used for half of the P entries: relative error <= 1e-4
+    against float64 over the whole input range the kernel feeds it."""
+    x = torch.cat([torch.linspace(-125.0, 1.0, 1 << 20), torch.tensor([0.0, -0.5, 0.5, -1.0])])
+    y = ab.diag_exp2(x.cuda()).cpu().double()
+    ref = torch.exp2(x.double())
+    rel = ((y - ref).abs() / ref).max().item()
+    assert rel <= 1e-4, rel
+
+
 def test_device_wait_timeout_is_reported():
     ab.diag_wait_timeout(50_000_000)  # 50 ms on a barrier nothing completes
     with pytest.raises(ab.AttnError) as e:
