@@ -110,6 +110,17 @@ __device__ __forceinline__ Unit get_unit(const BwdParams& p, int u, int G) {
   return r;
 }
 
+// Iteration j of a unit -> (query head h, query tile m).  Query tiles run from
+// the last to the first, heads of the group innermost: every CTA working on the
+// same (sequence, kv head) then reads the same Q/dO tile at about the same
+// time (the causal start tile only shortens the tail), so those tiles are
+// served from L2 instead of being streamed from HBM once per key tile.
+__device__ __forceinline__ void iter_hm(const Unit& un, int j, int G, int& h, int& m) {
+  const int jm = j / G;
+  h = un.g * G + (j - jm * G);
+  m = un.m_start + un.m_count - 1 - jm;
+}
+
 template <typename T, int D>
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_main_kernel(const BwdParams p, const __grid_constant__ CUtensorMap tmQ,
@@ -193,8 +204,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t s = it % kStages;
           const uint32_t use = it / kStages;
           if (use > 0 && !wait1(bar(B_EMPTY + s), (use - 1) & 1, ctl, 0xA0000002u)) break;
-          const int h = un.g * G + j / un.m_count;
-          const int m = un.m_start + j % un.m_count;
+          int h, m;
+          iter_hm(un, j, G, h, m);
           const int qrow = un.si.q_start + m * BM;
           const int bq = varlen ? 0 : un.b;
           const int64_t ws = static_cast<int64_t>(h) * p.ws_rows + un.si.ws_row0 + m * BM;
@@ -331,7 +342,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int j = 0; j < un.n_iters; ++j, ++it) {
         const uint32_t s = it % kStages;
         const uint32_t ph = (it / kStages) & 1;
-        const int m = un.m_start + j % un.m_count;
+        int h_unused, m;
+        iter_hm(un, j, G, h_unused, m);
         const int q0 = m * BM;
         const bool need_mask = (q0 + BM > un.si.sq) || (un.n * BN + BN > un.si.sk) ||
                                (p.causal && un.n * BN + BN - 1 > q0 + off);
@@ -358,19 +370,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int e4 = 0; e4 < 8; ++e4) {
               const float4 l = l4[e4];
               const uint32_t* v = &sv[c & 1][e4 * 4];
-              // half of the exponentials on MUFU, half as a polynomial on the FMA pipe
-              float x0, x1, x2, x3;
-              if (e4 & 1) {
-                x0 = ex2_poly(fmaf(__uint_as_float(v[0]), sl2, -l.x));
-                x1 = ex2_poly(fmaf(__uint_as_float(v[1]), sl2, -l.y));
-                x2 = ex2_poly(fmaf(__uint_as_float(v[2]), sl2, -l.z));
-                x3 = ex2_poly(fmaf(__uint_as_float(v[3]), sl2, -l.w));
-              } else {
-                x0 = ex2(fmaf(__uint_as_float(v[0]), sl2, -l.x));
-                x1 = ex2(fmaf(__uint_as_float(v[1]), sl2, -l.y));
-                x2 = ex2(fmaf(__uint_as_float(v[2]), sl2, -l.z));
-                x3 = ex2(fmaf(__uint_as_float(v[3]), sl2, -l.w));
-              }
+              float x0 = ex2(fmaf(__uint_as_float(v[0]), sl2, -l.x));
+              float x1 = ex2(fmaf(__uint_as_float(v[1]), sl2, -l.y));
+              float x2 = ex2(fmaf(__uint_as_float(v[2]), sl2, -l.z));
+              float x3 = ex2(fmaf(__uint_as_float(v[3]), sl2, -l.w));
               if (need_mask) {
                 const int i = c * 32 + e4 * 4;
                 x0 = (i + 0 >= lo && i + 0 < hi) ? x0 : 0.f;
@@ -487,8 +490,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const Unit un = get_unit(p, u, G);
       if (un.n_iters == 0) continue;
       for (int j = 0; j < un.n_iters; ++j, ++it) {
-        const int h = un.g * G + j / un.m_count;
-        const int m = un.m_start + j % un.m_count;
+        int h, m;
+        iter_hm(un, j, G, h, m);
         const bool row_ok = m * BM + il < un.si.sq;
         const int64_t wrow = static_cast<int64_t>(h) * p.ws_rows + un.si.ws_row0 + m * BM;
         float* dst = p.dqacc + (wrow + il) * D;
