@@ -124,6 +124,19 @@ bool encode_tmap_bshd(CUtensorMap* out, const TensorArg& t, int dtype, int rows,
   return r == CUDA_SUCCESS;
 }
 
+bool encode_tmap_f32_2d(CUtensorMap* out, float* base, int64_t rows, int cols) {
+  EncodeTiledFn fn = encode_fn();
+  if (fn == nullptr || rows <= 0 || cols <= 0) return false;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols) * 4};
+  cuuint32_t box[2] = {32, 32};
+  cuuint32_t estr[2] = {1, 1};
+  const CUresult r = fn(out, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, base, dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 namespace {
 
 int check_tensor(const attn_tensor* t, const char* name, bool varlen, bool need) {

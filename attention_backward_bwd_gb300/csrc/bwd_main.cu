@@ -61,6 +61,7 @@ enum Bar : uint32_t {
   B_DKDONE,
   B_DKDVFULL,
   B_DKDVFREE,
+  B_STAGEFREE,
   B_FINAL,
   B_COUNT
 };
@@ -125,7 +126,8 @@ template <typename T, int D>
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_main_kernel(const BwdParams p, const __grid_constant__ CUtensorMap tmQ,
                     const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
-                    const __grid_constant__ CUtensorMap tmDO) {
+                    const __grid_constant__ CUtensorMap tmDO,
+                    const __grid_constant__ CUtensorMap tmDQ) {
   using L = Smem<D>;
   extern __shared__ __align__(1024) unsigned char smem[];
   if (p.input_bad != nullptr && *p.input_bad) return;
@@ -164,6 +166,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(bar(B_DKDONE), 1);
     mbar_init(bar(B_DKDVFULL), 1);
     mbar_init(bar(B_DKDVFREE), 4);
+    mbar_init(bar(B_STAGEFREE), 4);
     mbar_init(bar(B_FINAL), 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     fence_proxy_async_smem();
@@ -184,6 +187,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       prefetch_tmap(&tmK);
       prefetch_tmap(&tmV);
       prefetch_tmap(&tmDO);
+      prefetch_tmap(&tmDQ);
       uint32_t it = 0, uc = 0;  // iterations and units whose loads were issued
       for (int u = blockIdx.x; u < num_units; u += gridDim.x) {
         const Unit un = get_unit(p, u, G);
@@ -394,6 +398,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
         if (!wait_warp(bar(B_FULLDO + s), ph, ctl, 0xA0000023u)) goto done;
         if (!wait_warp(bar(B_DPFULL), it & 1, ctl, 0xA0000024u)) goto done;
+        // the dS^T tile doubles as the dQ staging buffer of the previous iteration
+        if (it > 0 && !wait_warp(bar(B_STAGEFREE), (it - 1) & 1, ctl, 0xA0000026u)) goto done;
         tc_fence_after();
         // dS^T row `jl` = P^T (dP^T - Delta); to TMEM (packed into the upper dP
         // columns) and to the smem dS^T tile.  Chunks go from the last to the first
@@ -479,12 +485,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp >= 8) {
     // ------------------------------------------------------------ dQ drain
-    // Thread = query row (TMEM lane); each warp owns 32 rows of the tile, so the
-    // four warps touch disjoint dQaccum rows and synchronise only through the
-    // semaphore in deterministic mode (4 arrivals per KV tile, no CTA barrier).
+    // Thread = query row (TMEM lane); warp q owns rows [32q, 32q+32) of the tile.
+    // Rows are staged in the dS^T tile (free once the dQ MMA has read it) as
+    // 32x32 fp32 boxes with the 128-byte swizzle, and each box is added to
+    // dQaccum by a TMA reduce (whole 128-byte lines at L2).  Rows past the
+    // sequence end hold exact zeros (their dS is 0) and stay inside the
+    // sequence's padded workspace rows, so they need no mask.  In deterministic
+    // mode a warp waits until key tiles 0..n-1 have completed their adds
+    // (4 arrivals each, one per drain warp) and releases after its own adds
+    // completed.
     const uint32_t quad = warp & 3;
-    const int il = static_cast<int>(quad * 32 + lane);  // query row within the tile
     const uint32_t tl = tmem + ((quad * 32) << 16);
+    const uint32_t stage = sb + L::kDS + quad * 8192;  // 8 KB: two 32x32 fp32 boxes
     uint32_t it = 0;
     for (int u = blockIdx.x; u < num_units; u += gridDim.x) {
       const Unit un = get_unit(p, u, G);
@@ -492,9 +504,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int j = 0; j < un.n_iters; ++j, ++it) {
         int h, m;
         iter_hm(un, j, G, h, m);
-        const bool row_ok = m * BM + il < un.si.sq;
-        const int64_t wrow = static_cast<int64_t>(h) * p.ws_rows + un.si.ws_row0 + m * BM;
-        float* dst = p.dqacc + (wrow + il) * D;
+        const int row0 = static_cast<int>(static_cast<int64_t>(h) * p.ws_rows + un.si.ws_row0 +
+                                          m * BM + quad * 32);
         uint32_t a[D];
         if (!wait_warp(bar(B_DQFULL), it & 1, ctl, 0xA0000031u)) goto done;
         tc_fence_after();
@@ -507,7 +518,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         int* sem = p.sem + static_cast<int64_t>(h) * (p.ws_rows / kTileRows) +
                    un.si.ws_row0 / kTileRows + m;
         if (p.deterministic) {
-          // KV tiles 0..n-1 have each released 4 arrivals for this query tile
           int stop = 0;
           if (lane == 0) {
             const int want = 4 * un.n;
@@ -523,22 +533,49 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
               }
             }
+            fence_proxy_async_global();
           }
           if (__shfl_sync(0xffffffffu, stop, 0)) goto done;
         }
-        if (row_ok) {
 #pragma unroll
-          for (int d = 0; d < D; d += 4)
-            red_add_v4(dst + d, __uint_as_float(a[d]), __uint_as_float(a[d + 1]),
-                       __uint_as_float(a[d + 2]), __uint_as_float(a[d + 3]));
-        }
-        if (p.deterministic) {
-          __threadfence();
+        for (int pass = 0; pass < D / 64; ++pass) {
+          if (pass > 0) {
+            if (lane == 0) bulk_wait_read_all();
+            __syncwarp();
+          }
+#pragma unroll
+          for (int bx = 0; bx < 2; ++bx) {
+            const uint32_t box = L::kDS + quad * 8192 + bx * 4096;
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+              const uint32_t* v = a + pass * 64 + bx * 32 + q * 4;
+              *reinterpret_cast<uint4*>(smem + box + lane * 128 + ((q ^ (lane & 7)) * 16)) =
+                  make_uint4(v[0], v[1], v[2], v[3]);
+            }
+          }
+          fence_proxy_async_smem();
           __syncwarp();
-          if (lane == 0) red_release_add(sem, 1);
+          if (lane == 0) {
+            tma_reduce_add_2d(&tmDQ, stage, pass * 64, row0);
+            tma_reduce_add_2d(&tmDQ, stage + 4096, pass * 64 + 32, row0);
+            bulk_commit();
+          }
         }
+        if (lane == 0) {
+          if (p.deterministic) {
+            bulk_wait_all();
+            fence_proxy_async_global();
+            __threadfence();
+            red_release_add(sem, 1);
+          } else {
+            bulk_wait_read_all();
+          }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(B_STAGEFREE));
       }
     }
+    if (lane == 0) bulk_wait_all();
   }
 
 done:
@@ -558,6 +595,8 @@ cudaError_t launch_t(const BwdParams& p, int dtype, cudaStream_t stream) {
       !encode_tmap_bshd(&tv, p.v, dtype, p.seq.seqlen_k, p.h_k, nb, D, BN) ||
       !encode_tmap_bshd(&tdo, p.dout, dtype, p.seq.seqlen_q, p.h_q, nb, D, BM))
     return cudaErrorInvalidValue;
+  CUtensorMap tdq;
+  if (!encode_tmap_f32_2d(&tdq, p.dqacc, p.ws_rows * p.h_q, D)) return cudaErrorInvalidValue;
   constexpr uint32_t smem = Smem<D>::kTotal;
   static bool attr_done = false;
   if (!attr_done) {
@@ -570,7 +609,7 @@ cudaError_t launch_t(const BwdParams& p, int dtype, cudaStream_t stream) {
   const int units = n_tiles * p.seq.batch * p.h_k;
   if (units <= 0) return cudaSuccess;
   const int grid = units < num_sms() ? units : num_sms();
-  bwd_main_kernel<T, D><<<grid, kThreads, smem, stream>>>(p, tq, tk, tv, tdo);
+  bwd_main_kernel<T, D><<<grid, kThreads, smem, stream>>>(p, tq, tk, tv, tdo, tdq);
   return cudaGetLastError();
 }
 

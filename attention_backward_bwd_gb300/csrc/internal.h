@@ -107,4 +107,8 @@ unsigned int* status_word();
 bool encode_tmap_bshd(CUtensorMap* out, const TensorArg& t, int dtype, int rows, int heads,
                       int batch, int head_dim, int box_rows);
 
+// 2-D TMA map over a row-major fp32 matrix [rows][cols], box {32, 32}, 128-byte
+// swizzle (used to reduce-add dQ tiles into the dQ accumulator).
+bool encode_tmap_f32_2d(CUtensorMap* out, float* base, int64_t rows, int cols);
+
 }  // namespace attn
