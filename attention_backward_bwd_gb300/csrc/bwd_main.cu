@@ -19,16 +19,18 @@
 // ascending KV-tile order behind a per-(head, query tile) semaphore (the
 // dq_semaphore of flash-attention hopper/flash_bwd_launch_template.h).
 //
-// Warp roles (384 threads): warp 0 TMA producer, warp 1 MMA issuer (one
-// thread), warp 2 TMEM allocator, warps 4-7 softmax / dS / dK-dV epilogue
-// (thread = key row = TMEM lane), warps 8-11 dQ drain (thread = query row).
+// Warp roles (512 threads): warp 0 TMA producer, warp 1 MMA issuer (one
+// thread), warp 2 TMEM allocator, warps 4-11 softmax / dS / dK-dV epilogue
+// (two warps per TMEM lane quadrant: thread = key row, warps 4-7 take query
+// columns 0..63 and warps 8-11 columns 64..127), warps 12-15 dQ drain
+// (thread = query row).
 //
 // TMEM columns (512 allocated, 128 lanes):
-//   [  0,128) S^T fp32; its first 64 columns are then reused for packed P^T
-//   [128,256) dP^T fp32; its last 64 columns are then reused for packed dS^T
-//   [ 64,64+D) dQ (the S and dP columns freed once P^T and dS^T are packed),
-//              one N = D MMA: N = 64 MMAs run at 2/3 rate on this part
+//   [  0,128) S^T fp32, then packed P^T in [0,64) and packed dS^T in [64,128)
+//   [128,256) dP^T fp32, then dQ in [128,128+D)
 //   [256,256+D) dK, [384,384+D) dV
+// The tensor pipe runs S, dP, dV, dK, dQ per query tile; the next tile's S waits
+// only for dK (so it overlaps dQ) and its dP for the dQ drain.
 // Every mbarrier wait is bounded (see WaitCtl): on timeout the kernel records
 // the site in the status word and unwinds.
 #include "common.cuh"
@@ -39,12 +41,13 @@ namespace {
 
 constexpr int BM = 128;  // query tile
 constexpr int BN = 128;  // key tile
-constexpr int kThreads = 384;
+constexpr int kThreads = 512;
+constexpr int kSoftmaxWarps = 8;
 constexpr int kStages = 2;
 constexpr uint32_t kChunk = 128 * 128;  // one 64-column (128-byte) slice of a 128-row tile
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t TM_S = 0, TM_P = 0, TM_DP = 128, TM_DS = 192;
-constexpr uint32_t TM_DQ = 64, TM_DK = 256, TM_DV = 384;
+constexpr uint32_t TM_S = 0, TM_P = 0, TM_DS = 64, TM_DP = 128;
+constexpr uint32_t TM_DQ = 128, TM_DK = 256, TM_DV = 384;
 
 enum Bar : uint32_t {
   B_FULLQ = 0,
@@ -56,6 +59,7 @@ enum Bar : uint32_t {
   B_DPFULL,
   B_PREADY,
   B_DSREADY,
+  B_SREAD,
   B_DQFULL,
   B_DQFREE,
   B_DKDONE,
@@ -111,15 +115,19 @@ __device__ __forceinline__ Unit get_unit(const BwdParams& p, int u, int G) {
   return r;
 }
 
-// Iteration j of a unit -> (query head h, query tile m).  Query tiles run from
-// the last to the first, heads of the group innermost: every CTA working on the
-// same (sequence, kv head) then reads the same Q/dO tile at about the same
-// time (the causal start tile only shortens the tail), so those tiles are
-// served from L2 instead of being streamed from HBM once per key tile.
-__device__ __forceinline__ void iter_hm(const Unit& un, int j, int G, int& h, int& m) {
+// Iteration j of a unit -> (query head h, query tile m), heads of the group
+// innermost.  Query tiles run from the last to the first, so every CTA working
+// on the same (sequence, kv head) reads the same Q/dO tile at about the same
+// time (the causal start tile only shortens the tail) and those tiles are
+// served from L2 instead of being streamed from HBM once per key tile.  In
+// deterministic mode they run first to last instead: key tile n then meets
+// query tile m one step after key tile n-1 did, so the ordered dQ adds form a
+// pipeline rather than a chain of waits.
+__device__ __forceinline__ void iter_hm(const Unit& un, int j, int G, bool ascending, int& h,
+                                        int& m) {
   const int jm = j / G;
   h = un.g * G + (j - jm * G);
-  m = un.m_start + un.m_count - 1 - jm;
+  m = ascending ? un.m_start + jm : un.m_start + un.m_count - 1 - jm;
 }
 
 template <typename T, int D>
@@ -146,6 +154,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const bool varlen = p.seq.cu_q != nullptr;
   const int n_tiles = ceil_div(p.max_seqlen_k, BN);
   const int num_units = n_tiles * p.seq.batch * p.h_k;
+  const bool asc = p.deterministic != 0;
   constexpr int kIsBf16 = Pack<T>::kIsBf16;
 
   if (threadIdx.x == 0) {
@@ -153,19 +162,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int s = 0; s < kStages; ++s) {
       mbar_init(bar(B_FULLQ + s), 1);
       mbar_init(bar(B_FULLDO + s), 1);
-      mbar_init(bar(B_EMPTY + s), 1 + 4);  // MMA commit + 4 softmax warps
+      mbar_init(bar(B_EMPTY + s), 1 + kSoftmaxWarps);  // MMA commit + softmax warps
     }
     mbar_init(bar(B_KVFULL), 1);
     mbar_init(bar(B_KVEMPTY), 1);
     mbar_init(bar(B_SFULL), 1);
     mbar_init(bar(B_DPFULL), 1);
-    mbar_init(bar(B_PREADY), 4);
-    mbar_init(bar(B_DSREADY), 4);
+    mbar_init(bar(B_PREADY), kSoftmaxWarps);
+    mbar_init(bar(B_DSREADY), kSoftmaxWarps);
+    mbar_init(bar(B_SREAD), kSoftmaxWarps);
     mbar_init(bar(B_DQFULL), 1);
     mbar_init(bar(B_DQFREE), 4);
     mbar_init(bar(B_DKDONE), 1);
     mbar_init(bar(B_DKDVFULL), 1);
-    mbar_init(bar(B_DKDVFREE), 4);
+    mbar_init(bar(B_DKDVFREE), kSoftmaxWarps);
     mbar_init(bar(B_STAGEFREE), 4);
     mbar_init(bar(B_FINAL), 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -209,7 +219,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t use = it / kStages;
           if (use > 0 && !wait1(bar(B_EMPTY + s), (use - 1) & 1, ctl, 0xA0000002u)) break;
           int h, m;
-          iter_hm(un, j, G, h, m);
+          iter_hm(un, j, G, asc, h, m);
           const int qrow = un.si.q_start + m * BM;
           const int bq = varlen ? 0 : un.b;
           const int64_t ws = static_cast<int64_t>(h) * p.ws_rows + un.si.ws_row0 + m * BM;
@@ -256,8 +266,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t sQ = sb + L::kQ + s * L::kTile;
           const uint32_t sDO = sb + L::kDO + s * L::kTile;
           if (!wait1(bar(B_FULLQ + s), ph, ctl, 0xA0000013u)) goto mma_exit;
-          // S and the dQ columns of the previous iteration must be drained
-          if (it > 0 && !wait1(bar(B_DQFREE), (it - 1) & 1, ctl, 0xA0000014u)) goto mma_exit;
+          // S^T overwrites the packed P^T / dS^T the previous dV / dK read
+          if (it > 0 && !wait1(bar(B_DKDONE), (it - 1) & 1, ctl, 0xA0000014u)) goto mma_exit;
           tc_fence_after();
           // S^T = K Q^T   (M = keys, N = queries, K = head dim; both K-major)
 #pragma unroll
@@ -268,8 +278,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           tc_commit(bar(B_SFULL));
           if (!wait1(bar(B_FULLDO + s), ph, ctl, 0xA0000015u)) goto mma_exit;
-          // dP^T overwrites the packed dS^T the previous dK read
-          if (it > 0 && !wait1(bar(B_DKDONE), (it - 1) & 1, ctl, 0xA0000016u)) goto mma_exit;
+          // dP^T overwrites the previous dQ, which must have been drained
+          if (it > 0 && !wait1(bar(B_DQFREE), (it - 1) & 1, ctl, 0xA0000016u)) goto mma_exit;
           tc_fence_after();
           // dP^T = V dO^T
 #pragma unroll
@@ -291,12 +301,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                    kIdKV, (j > 0 || kk > 0) ? 1u : 0u);
           if (!wait1(bar(B_DSREADY), it & 1, ctl, 0xA0000018u)) goto mma_exit;
           tc_fence_after();
-          // dQ = dS K   (A = dS MN-major from the dS^T tile, B = K MN-major, N = D)
-#pragma unroll
-          for (int kk = 0; kk < BN / 16; ++kk)
-            mma_ss(tmem + TM_DQ, sdesc_sw128(sb + L::kDS + kk * 2048, kChunk, 1024),
-                   sdesc_sw128(sb + L::kK + kk * 2048, kChunk, 1024), kIdDQ, kk > 0);
-          tc_commit(bar(B_DQFULL));
           // dK += dS^T Q   (A = dS^T from TMEM, B = Q MN-major)
 #pragma unroll
           for (int kk = 0; kk < BM / 16; ++kk)
@@ -304,6 +308,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                    kIdKV, (j > 0 || kk > 0) ? 1u : 0u);
           tc_commit(bar(B_DKDONE));
           tc_commit(bar(B_EMPTY + s));
+          // dQ = dS K   (A = dS MN-major from the dS^T tile, B = K MN-major, N = D)
+#pragma unroll
+          for (int kk = 0; kk < BN / 16; ++kk)
+            mma_ss(tmem + TM_DQ, sdesc_sw128(sb + L::kDS + kk * 2048, kChunk, 1024),
+                   sdesc_sw128(sb + L::kK + kk * 2048, kChunk, 1024), kIdDQ, kk > 0);
+          tc_commit(bar(B_DQFULL));
         }
         tc_commit(bar(B_DKDVFULL));
         tc_commit(bar(B_KVEMPTY));
@@ -314,9 +324,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_commit(bar(B_FINAL));
       wait1(bar(B_FINAL), 0, ctl, 0xA000001Fu, false);
     }
-  } else if (warp >= 4 && warp < 8) {
+  } else if (warp >= 4 && warp < 4 + kSoftmaxWarps) {
     // ------------------------------------------------- softmax / dS / epilogue
+    // Thread = key row jl (TMEM lane).  Half `hf` of the softmax warps owns query
+    // columns [64 hf, 64 hf + 64): their S^T and dP^T values, their packed P^T
+    // in TMEM columns [32 hf, +32) and their packed dS^T in [64 + 32 hf, +32).
+    // Half 1's P^T and half 0's dS^T land on S columns of the other half, so
+    // every softmax warp signals SREAD once its S^T values are in registers and
+    // those two writes wait for it.
     const uint32_t quad = warp & 3;
+    const int hf = static_cast<int>(warp - 4) >> 2;
     const int jl = static_cast<int>(quad * 32 + lane);  // key row within the tile
     const uint32_t tl = tmem + ((quad * 32) << 16);    // this warp's TMEM lanes
     const float sl2 = p.scale_log2;
@@ -326,19 +343,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!un.has_keys) continue;
       const int key = un.n * BN + jl;
       const bool key_ok = key < un.si.sk;
-      T* dk_row = static_cast<T*>(const_cast<void*>(p.dk.ptr)) + (varlen ? 0 : un.b * p.dk.sb) +
-                  static_cast<int64_t>(un.si.k_start + key) * p.dk.ss +
-                  static_cast<int64_t>(un.g) * p.dk.sh;
-      T* dv_row = static_cast<T*>(const_cast<void*>(p.dv.ptr)) + (varlen ? 0 : un.b * p.dv.sb) +
-                  static_cast<int64_t>(un.si.k_start + key) * p.dv.ss +
-                  static_cast<int64_t>(un.g) * p.dv.sh;
+      // half 0 writes dK, half 1 writes dV
+      const TensorArg& outp = hf == 0 ? p.dk : p.dv;
+      T* out_row = static_cast<T*>(const_cast<void*>(outp.ptr)) + (varlen ? 0 : un.b * outp.sb) +
+                   static_cast<int64_t>(un.si.k_start + key) * outp.ss +
+                   static_cast<int64_t>(un.g) * outp.sh;
       if (un.n_iters == 0) {  // keys but no queries: dK = dV = 0
         if (key_ok) {
 #pragma unroll
-          for (int c = 0; c < D / 8; ++c) {
-            reinterpret_cast<uint4*>(dk_row)[c] = make_uint4(0, 0, 0, 0);
-            reinterpret_cast<uint4*>(dv_row)[c] = make_uint4(0, 0, 0, 0);
-          }
+          for (int c = 0; c < D / 8; ++c) reinterpret_cast<uint4*>(out_row)[c] = make_uint4(0, 0, 0, 0);
         }
         continue;
       }
@@ -347,49 +360,52 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t s = it % kStages;
         const uint32_t ph = (it / kStages) & 1;
         int h_unused, m;
-        iter_hm(un, j, G, h_unused, m);
+        iter_hm(un, j, G, asc, h_unused, m);
         const int q0 = m * BM;
         const bool need_mask = (q0 + BM > un.si.sq) || (un.n * BN + BN > un.si.sk) ||
                                (p.causal && un.n * BN + BN - 1 > q0 + off);
-        const float* lse2 = reinterpret_cast<const float*>(smem + L::kLSE + s * BM * 4);
-        const float* dlt = reinterpret_cast<const float*>(smem + L::kDelta + s * BM * 4);
+        const float* lse2 = reinterpret_cast<const float*>(smem + L::kLSE + s * BM * 4) + 64 * hf;
+        const float* dlt = reinterpret_cast<const float*>(smem + L::kDelta + s * BM * 4) + 64 * hf;
+        // valid queries of this key row, in this half's column coordinates: lo <= c < hi
+        int lo = 0, hi = key_ok ? min(64, un.si.sq - q0 - 64 * hf) : 0;
+        if (p.causal) lo = max(0, key - off - q0 - 64 * hf);
         if (!wait_warp(bar(B_FULLQ + s), ph, ctl, 0xA0000021u)) goto done;
-        // valid queries of this key row, in tile coordinates: lo <= il < hi
-        int lo = 0, hi = key_ok ? min(BM, un.si.sq - q0) : 0;
-        if (p.causal) lo = max(0, key - off - q0);
         if (!wait_warp(bar(B_SFULL), it & 1, ctl, 0xA0000022u)) goto done;
         tc_fence_after();
-        // P^T row `jl`, 4 chunks of 32 queries.  The TMEM load of chunk c+1 is in
-        // flight while chunk c is computed; packed P overwrites S columns already read.
         {
-          uint32_t sv[2][32];
-          tmem_ld32(tl + TM_S, sv[0]);
+          uint32_t sv[64];
+          tmem_ld32p(tl + TM_S + 64 * hf, sv);
+          tmem_ld32p(tl + TM_S + 64 * hf + 32, sv + 32);
+          tmem_wait_ld();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar(B_SREAD));
+          // P^T = exp2(S^T * scale * log2 e - LSE2[query]), masked
+          uint32_t pk[32];
 #pragma unroll
-          for (int c = 0; c < BM / 32; ++c) {
-            tmem_wait_ld();
-            if (c + 1 < BM / 32) tmem_ld32(tl + TM_S + (c + 1) * 32, sv[(c + 1) & 1]);
-            const float4* l4 = reinterpret_cast<const float4*>(lse2 + c * 32);
-            uint32_t pk[16];
-#pragma unroll
-            for (int e4 = 0; e4 < 8; ++e4) {
-              const float4 l = l4[e4];
-              const uint32_t* v = &sv[c & 1][e4 * 4];
-              float x0 = ex2(fmaf(__uint_as_float(v[0]), sl2, -l.x));
-              float x1 = ex2(fmaf(__uint_as_float(v[1]), sl2, -l.y));
-              float x2 = ex2(fmaf(__uint_as_float(v[2]), sl2, -l.z));
-              float x3 = ex2(fmaf(__uint_as_float(v[3]), sl2, -l.w));
-              if (need_mask) {
-                const int i = c * 32 + e4 * 4;
-                x0 = (i + 0 >= lo && i + 0 < hi) ? x0 : 0.f;
-                x1 = (i + 1 >= lo && i + 1 < hi) ? x1 : 0.f;
-                x2 = (i + 2 >= lo && i + 2 < hi) ? x2 : 0.f;
-                x3 = (i + 3 >= lo && i + 3 < hi) ? x3 : 0.f;
-              }
-              pk[e4 * 2] = Pack<T>::two(x0, x1);
-              pk[e4 * 2 + 1] = Pack<T>::two(x2, x3);
+          for (int e4 = 0; e4 < 16; ++e4) {
+            const float4 l = reinterpret_cast<const float4*>(lse2)[e4];
+            const uint32_t* v = sv + e4 * 4;
+            float x0 = ex2(fmaf(__uint_as_float(v[0]), sl2, -l.x));
+            float x1 = ex2(fmaf(__uint_as_float(v[1]), sl2, -l.y));
+            float x2 = ex2(fmaf(__uint_as_float(v[2]), sl2, -l.z));
+            float x3 = ex2(fmaf(__uint_as_float(v[3]), sl2, -l.w));
+            if (need_mask) {
+              const int c = e4 * 4;
+              x0 = (c + 0 >= lo && c + 0 < hi) ? x0 : 0.f;
+              x1 = (c + 1 >= lo && c + 1 < hi) ? x1 : 0.f;
+              x2 = (c + 2 >= lo && c + 2 < hi) ? x2 : 0.f;
+              x3 = (c + 3 >= lo && c + 3 < hi) ? x3 : 0.f;
             }
-            tmem_st16(tl + TM_P + c * 16, pk);
+            pk[e4 * 2] = Pack<T>::two(x0, x1);
+            pk[e4 * 2 + 1] = Pack<T>::two(x2, x3);
           }
+          if (hf == 1) {
+            if (!wait_warp(bar(B_SREAD), it & 1, ctl, 0xA0000027u)) goto done;
+            tc_fence_after();
+          }
+          tmem_st16(tl + TM_P + 32 * hf, *reinterpret_cast<uint32_t(*)[16]>(pk));
+          tmem_st16(tl + TM_P + 32 * hf + 16, *reinterpret_cast<uint32_t(*)[16]>(pk + 16));
         }
         tmem_wait_st();
         tc_fence_before();
@@ -400,44 +416,37 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!wait_warp(bar(B_DPFULL), it & 1, ctl, 0xA0000024u)) goto done;
         // the dS^T tile doubles as the dQ staging buffer of the previous iteration
         if (it > 0 && !wait_warp(bar(B_STAGEFREE), (it - 1) & 1, ctl, 0xA0000026u)) goto done;
+        if (hf == 0 && !wait_warp(bar(B_SREAD), it & 1, ctl, 0xA0000028u)) goto done;
         tc_fence_after();
-        // dS^T row `jl` = P^T (dP^T - Delta); to TMEM (packed into the upper dP
-        // columns) and to the smem dS^T tile.  Chunks go from the last to the first
-        // so every packed store lands on dP columns already read; the loads of
-        // chunk c-1 overlap the math of chunk c.
         {
-          uint32_t dpv[2][32], pv[2][16];
-          constexpr int kC = BM / 32;
-          tmem_ld32(tl + TM_DP + (kC - 1) * 32, dpv[(kC - 1) & 1]);
-          tmem_ld16(tl + TM_P + (kC - 1) * 16, pv[(kC - 1) & 1]);
+          // dS^T = P^T (dP^T - Delta[query]) for this half's 64 queries, in two
+          // sub-chunks of 32; to TMEM (packed) and to the smem dS^T tile, whose
+          // chunk hf holds queries [64 hf, +64): row jl is 128 bytes and its
+          // 16-byte unit u is stored at u ^ (jl % 8) (128-byte swizzle).
+          uint32_t dpv[64], pv[32];
+          tmem_ld32p(tl + TM_DP + 64 * hf, dpv);
+          tmem_ld32p(tl + TM_DP + 64 * hf + 32, dpv + 32);
+          tmem_ld32p(tl + TM_P + 32 * hf, pv);
+          tmem_wait_ld();
+          const uint32_t row_base = L::kDS + hf * kChunk + jl * 128;
 #pragma unroll
-          for (int cc = 0; cc < kC; ++cc) {
-            const int c = kC - 1 - cc;
-            tmem_wait_ld();
-            if (c > 0) {
-              tmem_ld32(tl + TM_DP + (c - 1) * 32, dpv[(c - 1) & 1]);
-              tmem_ld16(tl + TM_P + (c - 1) * 16, pv[(c - 1) & 1]);
-            }
-            const float4* d4 = reinterpret_cast<const float4*>(dlt + c * 32);
+          for (int sub = 0; sub < 2; ++sub) {
             uint32_t pk[16];
 #pragma unroll
             for (int e4 = 0; e4 < 8; ++e4) {
-              const float4 dl = d4[e4];
-              const float2 p01 = Pack<T>::unpack(pv[c & 1][e4 * 2]);
-              const float2 p23 = Pack<T>::unpack(pv[c & 1][e4 * 2 + 1]);
-              const uint32_t* v = &dpv[c & 1][e4 * 4];
+              const float4 dl = reinterpret_cast<const float4*>(dlt)[sub * 8 + e4];
+              const float2 p01 = Pack<T>::unpack(pv[sub * 16 + e4 * 2]);
+              const float2 p23 = Pack<T>::unpack(pv[sub * 16 + e4 * 2 + 1]);
+              const uint32_t* v = dpv + sub * 32 + e4 * 4;
               pk[e4 * 2] = Pack<T>::two(p01.x * (__uint_as_float(v[0]) - dl.x),
                                         p01.y * (__uint_as_float(v[1]) - dl.y));
               pk[e4 * 2 + 1] = Pack<T>::two(p23.x * (__uint_as_float(v[2]) - dl.z),
                                             p23.y * (__uint_as_float(v[3]) - dl.w));
             }
-            tmem_st16(tl + TM_DS + c * 16, pk);
-            // smem dS^T tile: chunk c/2 holds queries [64*(c/2), +64); row jl is 128
-            // bytes, its 16-byte unit u is stored at u ^ (jl % 8) (128-byte swizzle).
-            const uint32_t row_base = L::kDS + (c >> 1) * kChunk + jl * 128;
+            tmem_st16(tl + TM_DS + 32 * hf + 16 * sub, pk);
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
-              const uint32_t unit = ((c & 1) * 4 + q) ^ (jl & 7);
+              const uint32_t unit = (sub * 4 + q) ^ (jl & 7);
               *reinterpret_cast<uint4*>(smem + row_base + unit * 16) =
                   make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
             }
@@ -452,29 +461,27 @@ __global__ void __launch_bounds__(kThreads, 1)
           mbar_arrive(bar(B_EMPTY + s));
         }
       }
-      // ---- epilogue: dK = scale * acc, dV = acc
+      // ---- epilogue: half 0 writes dK = scale * acc, half 1 writes dV = acc
       if (!wait_warp(bar(B_DKDVFULL), uc & 1, ctl, 0xA0000025u)) goto done;
       tc_fence_after();
+      {
+        const uint32_t src = hf == 0 ? TM_DK : TM_DV;
+        const float mul = hf == 0 ? p.scale : 1.0f;
 #pragma unroll 1
-      for (int c = 0; c < D / 32; ++c) {
-        uint32_t a[32], v[32];
-        tmem_ld32(tl + TM_DK + c * 32, a);
-        tmem_ld32(tl + TM_DV + c * 32, v);
-        tmem_wait_ld();
-        if (key_ok) {
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t a[32];
+          tmem_ld32(tl + src + c * 32, a);
+          tmem_wait_ld();
+          if (key_ok) {
 #pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            uint4 ok, ov;
-            ok.x = Pack<T>::two(__uint_as_float(a[8 * q + 0]) * p.scale, __uint_as_float(a[8 * q + 1]) * p.scale);
-            ok.y = Pack<T>::two(__uint_as_float(a[8 * q + 2]) * p.scale, __uint_as_float(a[8 * q + 3]) * p.scale);
-            ok.z = Pack<T>::two(__uint_as_float(a[8 * q + 4]) * p.scale, __uint_as_float(a[8 * q + 5]) * p.scale);
-            ok.w = Pack<T>::two(__uint_as_float(a[8 * q + 6]) * p.scale, __uint_as_float(a[8 * q + 7]) * p.scale);
-            ov.x = Pack<T>::two(__uint_as_float(v[8 * q + 0]), __uint_as_float(v[8 * q + 1]));
-            ov.y = Pack<T>::two(__uint_as_float(v[8 * q + 2]), __uint_as_float(v[8 * q + 3]));
-            ov.z = Pack<T>::two(__uint_as_float(v[8 * q + 4]), __uint_as_float(v[8 * q + 5]));
-            ov.w = Pack<T>::two(__uint_as_float(v[8 * q + 6]), __uint_as_float(v[8 * q + 7]));
-            reinterpret_cast<uint4*>(dk_row + c * 32)[q] = ok;
-            reinterpret_cast<uint4*>(dv_row + c * 32)[q] = ov;
+            for (int q = 0; q < 4; ++q) {
+              uint4 o;
+              o.x = Pack<T>::two(__uint_as_float(a[8 * q + 0]) * mul, __uint_as_float(a[8 * q + 1]) * mul);
+              o.y = Pack<T>::two(__uint_as_float(a[8 * q + 2]) * mul, __uint_as_float(a[8 * q + 3]) * mul);
+              o.z = Pack<T>::two(__uint_as_float(a[8 * q + 4]) * mul, __uint_as_float(a[8 * q + 5]) * mul);
+              o.w = Pack<T>::two(__uint_as_float(a[8 * q + 6]) * mul, __uint_as_float(a[8 * q + 7]) * mul);
+              reinterpret_cast<uint4*>(out_row + c * 32)[q] = o;
+            }
           }
         }
       }
@@ -483,62 +490,65 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) mbar_arrive(bar(B_DKDVFREE));
       ++uc;
     }
-  } else if (warp >= 8) {
+  } else if (warp >= 4 + kSoftmaxWarps) {
     // ------------------------------------------------------------ dQ drain
     // Thread = query row (TMEM lane); warp q owns rows [32q, 32q+32) of the tile.
-    // Rows are staged in the dS^T tile (free once the dQ MMA has read it) as
-    // 32x32 fp32 boxes with the 128-byte swizzle, and each box is added to
-    // dQaccum by a TMA reduce (whole 128-byte lines at L2).  Rows past the
-    // sequence end hold exact zeros (their dS is 0) and stay inside the
-    // sequence's padded workspace rows, so they need no mask.  In deterministic
-    // mode a warp waits until key tiles 0..n-1 have completed their adds
-    // (4 arrivals each, one per drain warp) and releases after its own adds
-    // completed.
+    // The rows go out in 64-column passes: staged in the dS^T tile (free once
+    // the dQ MMA has read it) as two 32x32 fp32 boxes with the 128-byte
+    // swizzle, each box added to dQaccum by a TMA reduce (whole 128-byte lines
+    // at L2).  Rows past the sequence end hold exact zeros (their dS is 0) and
+    // stay inside the sequence's padded workspace rows, so they need no mask.
+    // In deterministic mode a warp waits until key tiles 0..n-1 have completed
+    // their adds (4 arrivals each, one per drain warp) and releases once its
+    // own adds have completed.
     const uint32_t quad = warp & 3;
     const uint32_t tl = tmem + ((quad * 32) << 16);
     const uint32_t stage = sb + L::kDS + quad * 8192;  // 8 KB: two 32x32 fp32 boxes
+    constexpr int kPasses = D / 64;
     uint32_t it = 0;
     for (int u = blockIdx.x; u < num_units; u += gridDim.x) {
       const Unit un = get_unit(p, u, G);
       if (un.n_iters == 0) continue;
       for (int j = 0; j < un.n_iters; ++j, ++it) {
         int h, m;
-        iter_hm(un, j, G, h, m);
+        iter_hm(un, j, G, asc, h, m);
         const int row0 = static_cast<int>(static_cast<int64_t>(h) * p.ws_rows + un.si.ws_row0 +
                                           m * BM + quad * 32);
-        uint32_t a[D];
+        int* sem = p.sem + static_cast<int64_t>(h) * (p.ws_rows / kTileRows) +
+                   un.si.ws_row0 / kTileRows + m;
         if (!wait_warp(bar(B_DQFULL), it & 1, ctl, 0xA0000031u)) goto done;
         tc_fence_after();
 #pragma unroll
-        for (int c = 0; c < D / 32; ++c) tmem_ld32p(tl + TM_DQ + c * 32, a + c * 32);
-        tmem_wait_ld();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bar(B_DQFREE));
-        int* sem = p.sem + static_cast<int64_t>(h) * (p.ws_rows / kTileRows) +
-                   un.si.ws_row0 / kTileRows + m;
-        if (p.deterministic) {
-          int stop = 0;
-          if (lane == 0) {
-            const int want = 4 * un.n;
-            const uint64_t t0 = globaltimer_ns();
-            for (uint32_t spin = 0;; ++spin) {
-              if (ld_acquire(sem) >= want) break;
-              if ((spin & 15) == 15) {
-                if (*abort_flag) { stop = 1; break; }
-                if (globaltimer_ns() - t0 > p.timeout_ns) {
-                  raise_abort(ctl, 0xA0000033u);
-                  stop = 1;
-                  break;
+        for (int pass = 0; pass < kPasses; ++pass) {
+          uint32_t a[64];
+          tmem_ld32p(tl + TM_DQ + pass * 64, a);
+          tmem_ld32p(tl + TM_DQ + pass * 64 + 32, a + 32);
+          tmem_wait_ld();
+          if (pass == kPasses - 1) {
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(B_DQFREE));
+          }
+          if (pass == 0 && p.deterministic) {
+            int stop = 0;
+            if (lane == 0) {
+              const int want = 4 * un.n;
+              const uint64_t t0 = globaltimer_ns();
+              for (uint32_t spin = 0;; ++spin) {
+                if (ld_acquire(sem) >= want) break;
+                if ((spin & 15) == 15) {
+                  if (*abort_flag) { stop = 1; break; }
+                  if (globaltimer_ns() - t0 > p.timeout_ns) {
+                    raise_abort(ctl, 0xA0000033u);
+                    stop = 1;
+                    break;
+                  }
                 }
               }
+              fence_proxy_async_global();
             }
-            fence_proxy_async_global();
+            if (__shfl_sync(0xffffffffu, stop, 0)) goto done;
           }
-          if (__shfl_sync(0xffffffffu, stop, 0)) goto done;
-        }
-#pragma unroll
-        for (int pass = 0; pass < D / 64; ++pass) {
           if (pass > 0) {
             if (lane == 0) bulk_wait_read_all();
             __syncwarp();
@@ -548,7 +558,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t box = L::kDS + quad * 8192 + bx * 4096;
 #pragma unroll
             for (int q = 0; q < 8; ++q) {
-              const uint32_t* v = a + pass * 64 + bx * 32 + q * 4;
+              const uint32_t* v = a + bx * 32 + q * 4;
               *reinterpret_cast<uint4*>(smem + box + lane * 128 + ((q ^ (lane & 7)) * 16)) =
                   make_uint4(v[0], v[1], v[2], v[3]);
             }
