@@ -52,8 +52,9 @@ constexpr uint32_t TM_DQ = 128, TM_DK = 256, TM_DV = 384;
 enum Bar : uint32_t {
   B_FULLQ = 0,
   B_FULLDO = B_FULLQ + kStages,
-  B_EMPTY = B_FULLDO + kStages,
-  B_KVFULL = B_EMPTY + kStages,
+  B_EMPTY = B_FULLDO + kStages,    // Q stage (+ LSE2) free: after dK and the softmax
+  B_EMPTYDO = B_EMPTY + kStages,   // dO stage (+ Delta) free: after dV and the softmax
+  B_KVFULL = B_EMPTYDO + kStages,
   B_KVEMPTY,
   B_SFULL,
   B_DPFULL,
@@ -163,6 +164,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bar(B_FULLQ + s), 1);
       mbar_init(bar(B_FULLDO + s), 1);
       mbar_init(bar(B_EMPTY + s), 1 + kSoftmaxWarps);  // MMA commit + softmax warps
+      mbar_init(bar(B_EMPTYDO + s), 1 + kSoftmaxWarps);
     }
     mbar_init(bar(B_KVFULL), 1);
     mbar_init(bar(B_KVEMPTY), 1);
@@ -199,6 +201,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       prefetch_tmap(&tmDO);
       prefetch_tmap(&tmDQ);
       uint32_t it = 0, uc = 0;  // iterations and units whose loads were issued
+      bool q_pending_skipped = false;  // last iteration issued dO but not Q
       for (int u = blockIdx.x; u < num_units; u += gridDim.x) {
         const Unit un = get_unit(p, u, G);
         if (un.n_iters == 0) continue;
@@ -217,24 +220,30 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int j = 0; j < un.n_iters; ++j, ++it) {
           const uint32_t s = it % kStages;
           const uint32_t use = it / kStages;
-          if (use > 0 && !wait1(bar(B_EMPTY + s), (use - 1) & 1, ctl, 0xA0000002u)) break;
+          if (use > 0 && !wait1(bar(B_EMPTYDO + s), (use - 1) & 1, ctl, 0xA0000006u)) break;
           int h, m;
           iter_hm(un, j, G, asc, h, m);
           const int qrow = un.si.q_start + m * BM;
           const int bq = varlen ? 0 : un.b;
           const int64_t ws = static_cast<int64_t>(h) * p.ws_rows + un.si.ws_row0 + m * BM;
-          mbar_expect_tx(bar(B_FULLQ + s), L::kTile + BM * 4);
-#pragma unroll
-          for (int c = 0; c < D / 64; ++c)
-            tma_load_4d(sb + L::kQ + s * L::kTile + c * kChunk, &tmQ, bar(B_FULLQ + s), c * 64,
-                        qrow, h, bq);
-          bulk_load(sb + L::kLSE + s * BM * 4, p.lse2 + ws, BM * 4, bar(B_FULLQ + s));
+          // dO is released after dV, earlier than Q (released after dK): load it first
           mbar_expect_tx(bar(B_FULLDO + s), L::kTile + BM * 4);
 #pragma unroll
           for (int c = 0; c < D / 64; ++c)
             tma_load_4d(sb + L::kDO + s * L::kTile + c * kChunk, &tmDO, bar(B_FULLDO + s), c * 64,
                         qrow, h, bq);
           bulk_load(sb + L::kDelta + s * BM * 4, p.delta + ws, BM * 4, bar(B_FULLDO + s));
+          if (use > 0 && !wait1(bar(B_EMPTY + s), (use - 1) & 1, ctl, 0xA0000002u)) {
+            ++it;  // the dO copies of this iteration are in flight
+            q_pending_skipped = true;
+            break;
+          }
+          mbar_expect_tx(bar(B_FULLQ + s), L::kTile + BM * 4);
+#pragma unroll
+          for (int c = 0; c < D / 64; ++c)
+            tma_load_4d(sb + L::kQ + s * L::kTile + c * kChunk, &tmQ, bar(B_FULLQ + s), c * 64,
+                        qrow, h, bq);
+          bulk_load(sb + L::kLSE + s * BM * 4, p.lse2 + ws, BM * 4, bar(B_FULLQ + s));
         }
         if (*abort_flag) break;
       }
@@ -244,7 +253,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (uint32_t s = 0; s < kStages && s < it; ++s) {
         const uint32_t last = (it - 1 - s) / kStages;  // uses of stage (it-1-s) % kStages
         const uint32_t st = (it - 1 - s) % kStages;
-        wait1(bar(B_FULLQ + st), last & 1, ctl, 0xA0000004u, false);
+        if (!(s == 0 && q_pending_skipped))
+          wait1(bar(B_FULLQ + st), last & 1, ctl, 0xA0000004u, false);
         wait1(bar(B_FULLDO + st), last & 1, ctl, 0xA0000005u, false);
       }
     }
@@ -299,6 +309,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int kk = 0; kk < BM / 16; ++kk)
             mma_ts(tmem + TM_DV, tmem + TM_P + kk * 8, sdesc_sw128(sDO + kk * 2048, kChunk, 1024),
                    kIdKV, (j > 0 || kk > 0) ? 1u : 0u);
+          tc_commit(bar(B_EMPTYDO + s));
           if (!wait1(bar(B_DSREADY), it & 1, ctl, 0xA0000018u)) goto mma_exit;
           tc_fence_after();
           // dK += dS^T Q   (A = dS^T from TMEM, B = Q MN-major)
@@ -410,7 +421,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_wait_st();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(bar(B_PREADY));
+        if (lane == 0) {
+          mbar_arrive(bar(B_PREADY));
+          mbar_arrive(bar(B_EMPTY + s));  // LSE2 of this stage is no longer read
+        }
 
         if (!wait_warp(bar(B_FULLDO + s), ph, ctl, 0xA0000023u)) goto done;
         if (!wait_warp(bar(B_DPFULL), it & 1, ctl, 0xA0000024u)) goto done;
@@ -458,7 +472,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
         if (lane == 0) {
           mbar_arrive(bar(B_DSREADY));
-          mbar_arrive(bar(B_EMPTY + s));
+          mbar_arrive(bar(B_EMPTYDO + s));
         }
       }
       // ---- epilogue: half 0 writes dK = scale * acc, half 1 writes dV = acc
