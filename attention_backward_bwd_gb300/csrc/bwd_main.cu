@@ -67,7 +67,9 @@ enum Bar : uint32_t {
   B_DKDVFULL,
   B_DKDVFREE,
   B_STAGEFREE,
-  B_FINAL,
+  B_UNITFULL,                      // 2 slots: next work unit published by the producer
+  B_UNITEMPTY = B_UNITFULL + 2,    // 2 slots: every consumer role has read it
+  B_FINAL = B_UNITEMPTY + 2,
   B_COUNT
 };
 
@@ -82,7 +84,8 @@ struct Smem {
   static constexpr uint32_t kLSE = kDS + 2 * kChunk;
   static constexpr uint32_t kDelta = kLSE + kStages * BM * 4;
   static constexpr uint32_t kBar = kDelta + kStages * BM * 4;
-  static constexpr uint32_t kTmemSlot = kBar + B_COUNT * 8;
+  static constexpr uint32_t kRing = kBar + B_COUNT * 8;  // 2 x int32 unit ring
+  static constexpr uint32_t kTmemSlot = kRing + 8;
   static constexpr uint32_t kAbort = kTmemSlot + 4;
   static constexpr uint32_t kTotal = kAbort + 4;
 };
@@ -179,6 +182,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(bar(B_DKDVFULL), 1);
     mbar_init(bar(B_DKDVFREE), kSoftmaxWarps);
     mbar_init(bar(B_STAGEFREE), 4);
+    for (int k = 0; k < 2; ++k) {
+      mbar_init(bar(B_UNITFULL + k), 1);
+      mbar_init(bar(B_UNITEMPTY + k), 1 + kSoftmaxWarps + 4);  // MMA + softmax + drain warps
+    }
     mbar_init(bar(B_FINAL), 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     fence_proxy_async_smem();
@@ -191,6 +198,21 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + L::kTmemSlot);
+  volatile int* ring = reinterpret_cast<volatile int*>(smem + L::kRing);
+  // Work units come from a persistent scheduler: the first unit of CTA c is c,
+  // later ones are taken by the producer from a global counter in
+  // longest-first order (key tile major) and published through a 2-slot ring
+  // that every role reads.  A published index >= num_units means "done".
+  // Consumer side (single thread when `warp_wide` is false):
+  auto take_unit = [&](uint32_t k, bool warp_wide, int& u) -> bool {
+    const uint32_t slot = k & 1;
+    const bool ok = warp_wide ? wait_warp(bar(B_UNITFULL + slot), (k >> 1) & 1, ctl, 0xA0000041u)
+                              : wait1(bar(B_UNITFULL + slot), (k >> 1) & 1, ctl, 0xA0000042u);
+    if (!ok) return false;
+    u = ring[slot];
+    if (!warp_wide || lane_id() == 0) mbar_arrive(bar(B_UNITEMPTY + slot));
+    return true;
+  };
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
@@ -202,8 +224,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       prefetch_tmap(&tmDQ);
       uint32_t it = 0, uc = 0;  // iterations and units whose loads were issued
       bool q_pending_skipped = false;  // last iteration issued dO but not Q
-      for (int u = blockIdx.x; u < num_units; u += gridDim.x) {
+      int u = blockIdx.x;
+      for (uint32_t k = 0;; ++k) {
+        // publish unit k (slot k & 1 was read by every role for unit k - 2)
+        if (k >= 2 && !wait1(bar(B_UNITEMPTY + (k & 1)), ((k >> 1) - 1) & 1, ctl, 0xA0000043u))
+          break;
+        ring[k & 1] = u;
+        mbar_arrive(bar(B_UNITFULL + (k & 1)));
+        if (u >= num_units) break;
+        // fetch the next unit now; the atomic's latency overlaps this unit's loads
+        const int u_next = static_cast<int>(gridDim.x) + atomicAdd(p.sched, 1);
         const Unit un = get_unit(p, u, G);
+        u = u_next;
         if (un.n_iters == 0) continue;
         if (uc > 0 && !wait1(bar(B_KVEMPTY), (uc - 1) & 1, ctl, 0xA0000001u)) break;
         ++uc;
@@ -265,7 +297,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr uint32_t kIdKV = idesc_f16(kIsBf16, 0, 1, BN, D);
       constexpr uint32_t kIdDQ = idesc_f16(kIsBf16, 1, 1, BM, D);
       uint32_t it = 0, uc = 0;
-      for (int u = blockIdx.x; u < num_units; u += gridDim.x) {
+      for (uint32_t k = 0;; ++k) {
+        int u;
+        if (!take_unit(k, false, u)) goto mma_exit;
+        if (u >= num_units) break;
         const Unit un = get_unit(p, u, G);
         if (un.n_iters == 0) continue;
         if (!wait1(bar(B_KVFULL), uc & 1, ctl, 0xA0000011u)) goto mma_exit;
@@ -349,7 +384,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tl = tmem + ((quad * 32) << 16);    // this warp's TMEM lanes
     const float sl2 = p.scale_log2;
     uint32_t it = 0, uc = 0;
-    for (int u = blockIdx.x; u < num_units; u += gridDim.x) {
+    for (uint32_t k = 0;; ++k) {
+      int u;
+      if (!take_unit(k, true, u)) goto done;
+      if (u >= num_units) break;
       const Unit un = get_unit(p, u, G);
       if (!un.has_keys) continue;
       const int key = un.n * BN + jl;
@@ -520,7 +558,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t stage = sb + L::kDS + quad * 8192;  // 8 KB: two 32x32 fp32 boxes
     constexpr int kPasses = D / 64;
     uint32_t it = 0;
-    for (int u = blockIdx.x; u < num_units; u += gridDim.x) {
+    for (uint32_t k = 0;; ++k) {
+      int u;
+      if (!take_unit(k, true, u)) goto done;
+      if (u >= num_units) break;
       const Unit un = get_unit(p, u, G);
       if (un.n_iters == 0) continue;
       for (int j = 0; j < un.n_iters; ++j, ++it) {

@@ -38,6 +38,7 @@ struct BwdParams {
   float* delta;  // [Hq][ws_rows]
   float* dqacc;  // [Hq][ws_rows][D]
   int* sem;      // [Hq][ws_rows / kTileRows]
+  int* sched;    // work counter of the persistent main kernel (after the semaphores)
   int64_t ws_rows;
   int h_q, h_k, head_dim;
   int causal, deterministic;
@@ -79,7 +80,8 @@ inline WsLayout ws_layout(int batch, int seqlen_q, int h_q, int head_dim, int va
   w.off_delta = align256(w.off_lse2 + per_row * 4);
   w.off_dqacc = align256(w.off_delta + per_row * 4);
   w.off_sem = align256(w.off_dqacc + per_row * static_cast<size_t>(head_dim) * 4);
-  w.total = align256(w.off_sem + static_cast<size_t>(h_q) * (w.rows / kTileRows) * 4);
+  // semaphores, then one int32 work counter for the persistent scheduler
+  w.total = align256(w.off_sem + (static_cast<size_t>(h_q) * (w.rows / kTileRows) + 1) * 4);
   return w;
 }
 

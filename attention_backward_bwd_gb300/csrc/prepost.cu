@@ -113,8 +113,8 @@ __global__ void __launch_bounds__(kThreads) preprocess_kernel(BwdParams p) {
   float4* acc4 = reinterpret_cast<float4*>(p.dqacc);
   for (int64_t e = gtid; e < n4; e += nthreads) acc4[e] = make_float4(0.f, 0.f, 0.f, 0.f);
 
-  // Phase 3: clear the deterministic-mode semaphores.
-  const int64_t ns = p.ws_rows / kTileRows * p.h_q;
+  // Phase 3: clear the deterministic-mode semaphores and the work counter after them.
+  const int64_t ns = p.ws_rows / kTileRows * p.h_q + 1;
   for (int64_t e = gtid; e < ns; e += nthreads) p.sem[e] = 0;
 }
 

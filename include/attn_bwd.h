@@ -99,7 +99,8 @@ size_t attn_bwd_workspace_size(int batch, int seqlen_q, int h_q, int head_dim,
  * attn_bwd_workspace_layout -- where the pieces of the workspace live, for
  * callers that inspect them.  Writes byte offsets of LSE2 (fp32
  * [H_q][rows]), Delta (fp32 [H_q][rows]), dQaccum (fp32 [H_q][rows][D]) and
- * the semaphores (int32 [H_q][rows/128]) into offsets[0..3], and `rows`.
+ * the semaphores (int32 [H_q][rows/128], followed by one int32 work counter of
+ * the main kernel's scheduler) into offsets[0..3], and `rows`.
  * Row of query i of sequence b: padded mode b*round_up(Sq,128) + i; varlen
  * 128*(cu_seqlens_q[b]/128 + b) + i.  Returns ATTN_OK or ATTN_ERR_NULL.
  */
