@@ -433,3 +433,69 @@ const char* attn_last_error(void) { return g_err.c_str(); }
 const char* attn_version(void) { return "attn_gb300 0.1.0 (sm_103a)"; }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// attn_bwd_noalloc: attn_bwd whose workspace is a fixed array in device memory
+// owned by the library, for callers that may not allocate (include/attn_bwd.h
+// says who and why).  The array is a file-scope __device__ variable, so every
+// GPU that loads this library holds kNoAllocScratchBytes of it until the
+// process exits.  In host code the name g_attn_noalloc_scratch is only a
+// host-side handle; the kernels get the device address from
+// cudaGetSymbolAddress, looked up once per device.
+
+static __device__ __align__(256) unsigned char g_attn_noalloc_scratch[32u << 20];
+
+namespace {
+
+constexpr size_t kNoAllocScratchBytes = sizeof(g_attn_noalloc_scratch);
+
+// Device address of g_attn_noalloc_scratch on the current device.  The first
+// call on a device does the lookup (with that device current) and caches it.
+int noalloc_scratch(void** out) {
+  static void* ptrs[kMaxDevices] = {};
+  static std::mutex mu;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (dev < 0 || dev >= kMaxDevices) return fail(ATTN_ERR_CUDA, "device index %d not supported", dev);
+  std::lock_guard<std::mutex> lock(mu);
+  if (ptrs[dev] == nullptr) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_attn_noalloc_scratch);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress of the static scratch array");
+    ptrs[dev] = p;
+  }
+  *out = ptrs[dev];
+  return ATTN_OK;
+}
+
+}  // namespace
+
+extern "C" int attn_bwd_noalloc(const attn_tensor* q, const attn_tensor* k, const attn_tensor* v,
+                                const attn_tensor* o, const float* lse, const attn_tensor* dout,
+                                const attn_tensor* dq, const attn_tensor* dk,
+                                const attn_tensor* dv, int dtype, int batch, int seqlen_q,
+                                int seqlen_k, int h_q, int h_k, int head_dim, float scale,
+                                int causal, const int* cu_seqlens_q, const int* cu_seqlens_k,
+                                int max_seqlen_q, int max_seqlen_k, int deterministic,
+                                attn_stream_t stream) {
+  g_err.clear();
+  int rc = check_common(dtype, batch, seqlen_q, seqlen_k, h_q, h_k, head_dim, scale,
+                        cu_seqlens_q, cu_seqlens_k, max_seqlen_q, max_seqlen_k);
+  if (rc) return rc;
+  const WsLayout w =
+      ws_layout(batch, seqlen_q, h_q, head_dim, cu_seqlens_q != nullptr ? 1 : 0);
+  if (w.total > kNoAllocScratchBytes)
+    return fail(ATTN_ERR_WORKSPACE,
+                "attn_bwd_noalloc: this problem needs %zu bytes of workspace but the library's "
+                "static scratch holds %zu; use attn_bwd with a caller-provided workspace",
+                w.total, kNoAllocScratchBytes);
+  void* scratch = nullptr;
+  if ((rc = noalloc_scratch(&scratch))) return rc;
+  // The preprocess kernel of every call clears the parts of the workspace that
+  // must start at zero (dQ accumulator, semaphores, work counter); the rest is
+  // written before it is read.
+  void* workspace = scratch;
+  const size_t workspace_bytes = kNoAllocScratchBytes;
+  return bwd_entry(kPre | kMain | kPost, ATTN_BWD_ARGS_PASS, stream);
+}

@@ -126,6 +126,36 @@ int attn_bwd(const attn_tensor* q, const attn_tensor* k, const attn_tensor* v,
              size_t workspace_bytes, attn_stream_t stream);
 
 /*
+ * attn_bwd_noalloc -- attn_bwd with no workspace argument, for callers that
+ * must not allocate device memory: code whose device memory all belongs to
+ * another allocator (a framework's memory pool or an arena reserved at
+ * start-up), where a cudaMalloc in the middle of a step would either fail
+ * because the arena already holds the memory or stall the device while the
+ * driver allocates.  The pages describe no counterpart of this call.
+ *
+ * Arguments and results are those of attn_bwd minus workspace and
+ * workspace_bytes; it allocates nothing.  Its workspace is a static array of
+ * 32 MiB in device memory inside the library, which every GPU that loads the
+ * library keeps until the process exits.  A problem whose
+ * attn_bwd_workspace_size(...) exceeds 32 MiB is rejected with
+ * ATTN_ERR_WORKSPACE and a message (use attn_bwd then); 32 MiB covers, for
+ * example, B*H_q*round_up(Sq,128) up to about 1.2e5 query rows at D = 64.
+ * The first call on each device looks up the array's device address
+ * (cudaGetSymbolAddress) with that device current; make that first call
+ * before any stream capture.  Each call clears what must start at zero.
+ * All calls on a device share the one array: calls that overlap on the GPU
+ * (other streams, other host threads) race and corrupt each other's results,
+ * so issue them one after another on one stream.
+ */
+int attn_bwd_noalloc(const attn_tensor* q, const attn_tensor* k, const attn_tensor* v,
+                     const attn_tensor* o, const float* lse, const attn_tensor* dout,
+                     const attn_tensor* dq, const attn_tensor* dk, const attn_tensor* dv,
+                     int dtype, int batch, int seqlen_q, int seqlen_k, int h_q, int h_k,
+                     int head_dim, float scale, int causal, const int* cu_seqlens_q,
+                     const int* cu_seqlens_k, int max_seqlen_q, int max_seqlen_k,
+                     int deterministic, attn_stream_t stream);
+
+/*
  * The three stages of attn_bwd, callable one by one (same arguments, same
  * checks) so that each kernel can be timed on its own.  They must run in this
  * order on one stream with the same workspace.
