@@ -29,8 +29,8 @@
 //   [  0,128) S^T fp32, then packed P^T in [0,64) and packed dS^T in [64,128)
 //   [128,256) dP^T fp32, then dQ in [128,128+D)
 //   [256,256+D) dK, [384,384+D) dV
-// The tensor pipe runs S, dP, dV, dK, dQ per query tile; the next tile's S waits
-// only for dK (so it overlaps dQ) and its dP for the dQ drain.
+// The tensor pipe runs S, dP, dV, dQ, dK per query tile; the next tile's S waits
+// for dK and its dP for the dQ drain (which overlaps dK).
 // Every mbarrier wait is bounded (see WaitCtl): on timeout the kernel records
 // the site in the status word and unwinds.
 #include "common.cuh"
@@ -347,6 +347,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc_commit(bar(B_EMPTYDO + s));
           if (!wait1(bar(B_DSREADY), it & 1, ctl, 0xA0000018u)) goto mma_exit;
           tc_fence_after();
+          // dQ = dS K   (A = dS MN-major from the dS^T tile, B = K MN-major, N = D),
+          // first, so the dQ drain (which frees the dP^T columns for the next
+          // tile) overlaps dK
+#pragma unroll
+          for (int kk = 0; kk < BN / 16; ++kk)
+            mma_ss(tmem + TM_DQ, sdesc_sw128(sb + L::kDS + kk * 2048, kChunk, 1024),
+                   sdesc_sw128(sb + L::kK + kk * 2048, kChunk, 1024), kIdDQ, kk > 0);
+          tc_commit(bar(B_DQFULL));
           // dK += dS^T Q   (A = dS^T from TMEM, B = Q MN-major)
 #pragma unroll
           for (int kk = 0; kk < BM / 16; ++kk)
@@ -354,12 +362,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                    kIdKV, (j > 0 || kk > 0) ? 1u : 0u);
           tc_commit(bar(B_DKDONE));
           tc_commit(bar(B_EMPTY + s));
-          // dQ = dS K   (A = dS MN-major from the dS^T tile, B = K MN-major, N = D)
-#pragma unroll
-          for (int kk = 0; kk < BN / 16; ++kk)
-            mma_ss(tmem + TM_DQ, sdesc_sw128(sb + L::kDS + kk * 2048, kChunk, 1024),
-                   sdesc_sw128(sb + L::kK + kk * 2048, kChunk, 1024), kIdDQ, kk > 0);
-          tc_commit(bar(B_DQFULL));
         }
         tc_commit(bar(B_DKDVFULL));
         tc_commit(bar(B_KVEMPTY));
