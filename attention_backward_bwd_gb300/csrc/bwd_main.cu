@@ -26,7 +26,9 @@
 // (thread = query row).
 //
 // TMEM columns (512 allocated, 128 lanes):
-//   [  0,128) S^T fp32, then packed P^T in [0,64) and packed dS^T in [64,128)
+//   [  0,128) S^T fp32; then each half hf of the queries keeps its packed P^T in
+//             [64 hf, +32) and its packed dS^T in [64 hf + 32, +32), inside the
+//             S^T columns it has already read itself
 //   [128,256) dP^T fp32, then dQ in [128,128+D)
 //   [256,256+D) dK, [384,384+D) dV
 // The tensor pipe runs S, dP, dV, dQ, dK per query tile; the next tile's S waits
@@ -46,27 +48,26 @@ constexpr int kSoftmaxWarps = 8;
 constexpr int kStages = 2;
 constexpr uint32_t kChunk = 128 * 128;  // one 64-column (128-byte) slice of a 128-row tile
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t TM_S = 0, TM_P = 0, TM_DS = 64, TM_DP = 128;
+constexpr uint32_t TM_S = 0, TM_P = 0, TM_DS = 32, TM_DP = 128;  // P^T, dS^T: + 64 per half
 constexpr uint32_t TM_DQ = 128, TM_DK = 256, TM_DV = 384;
 
 enum Bar : uint32_t {
   B_FULLQ = 0,
   B_FULLDO = B_FULLQ + kStages,
   B_EMPTY = B_FULLDO + kStages,    // Q stage (+ LSE2) free: after dK and the softmax
-  B_EMPTYDO = B_EMPTY + kStages,   // dO stage (+ Delta) free: after dV and the softmax
+  B_EMPTYDO = B_EMPTY + kStages,   // dO stage (+ Delta) free: after dV, the softmax and the
+                                   // dQ drain that stages its reduce-adds there
   B_KVFULL = B_EMPTYDO + kStages,
   B_KVEMPTY,
   B_SFULL,
   B_DPFULL,
   B_PREADY,
   B_DSREADY,
-  B_SREAD,
   B_DQFULL,
   B_DQFREE,
   B_DKDONE,
   B_DKDVFULL,
   B_DKDVFREE,
-  B_STAGEFREE,
   B_UNITFULL,                      // 2 slots: next work unit published by the producer
   B_UNITEMPTY = B_UNITFULL + 2,    // 2 slots: every consumer role has read it
   B_FINAL = B_UNITEMPTY + 2,
@@ -167,7 +168,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bar(B_FULLQ + s), 1);
       mbar_init(bar(B_FULLDO + s), 1);
       mbar_init(bar(B_EMPTY + s), 1 + kSoftmaxWarps);  // MMA commit + softmax warps
-      mbar_init(bar(B_EMPTYDO + s), 1 + kSoftmaxWarps);
+      mbar_init(bar(B_EMPTYDO + s), 1 + kSoftmaxWarps + 4);  // + the 4 dQ drain warps
     }
     mbar_init(bar(B_KVFULL), 1);
     mbar_init(bar(B_KVEMPTY), 1);
@@ -175,13 +176,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(bar(B_DPFULL), 1);
     mbar_init(bar(B_PREADY), kSoftmaxWarps);
     mbar_init(bar(B_DSREADY), kSoftmaxWarps);
-    mbar_init(bar(B_SREAD), kSoftmaxWarps);
     mbar_init(bar(B_DQFULL), 1);
     mbar_init(bar(B_DQFREE), 4);
     mbar_init(bar(B_DKDONE), 1);
     mbar_init(bar(B_DKDVFULL), 1);
     mbar_init(bar(B_DKDVFREE), kSoftmaxWarps);
-    mbar_init(bar(B_STAGEFREE), 4);
     for (int k = 0; k < 2; ++k) {
       mbar_init(bar(B_UNITFULL + k), 1);
       mbar_init(bar(B_UNITEMPTY + k), 1 + kSoftmaxWarps + 4);  // MMA + softmax + drain warps
@@ -223,7 +222,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       prefetch_tmap(&tmDO);
       prefetch_tmap(&tmDQ);
       uint32_t it = 0, uc = 0;  // iterations and units whose loads were issued
-      bool q_pending_skipped = false;  // last iteration issued dO but not Q
+      bool do_pending_skipped = false;  // last iteration issued Q but not dO
       int u = blockIdx.x;
       for (uint32_t k = 0;; ++k) {
         // publish unit k (slot k & 1 was read by every role for unit k - 2)
@@ -252,30 +251,31 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int j = 0; j < un.n_iters; ++j, ++it) {
           const uint32_t s = it % kStages;
           const uint32_t use = it / kStages;
-          if (use > 0 && !wait1(bar(B_EMPTYDO + s), (use - 1) & 1, ctl, 0xA0000006u)) break;
           int h, m;
           iter_hm(un, j, G, asc, h, m);
           const int qrow = un.si.q_start + m * BM;
           const int bq = varlen ? 0 : un.b;
           const int64_t ws = static_cast<int64_t>(h) * p.ws_rows + un.si.ws_row0 + m * BM;
-          // dO is released after dV, earlier than Q (released after dK): load it first
-          mbar_expect_tx(bar(B_FULLDO + s), L::kTile + BM * 4);
-#pragma unroll
-          for (int c = 0; c < D / 64; ++c)
-            tma_load_4d(sb + L::kDO + s * L::kTile + c * kChunk, &tmDO, bar(B_FULLDO + s), c * 64,
-                        qrow, h, bq);
-          bulk_load(sb + L::kDelta + s * BM * 4, p.delta + ws, BM * 4, bar(B_FULLDO + s));
-          if (use > 0 && !wait1(bar(B_EMPTY + s), (use - 1) & 1, ctl, 0xA0000002u)) {
-            ++it;  // the dO copies of this iteration are in flight
-            q_pending_skipped = true;
-            break;
-          }
+          // Q (+ LSE2) first: its stage is released after dK, the dO stage only
+          // once the dQ drain of that iteration has read its staged rows
+          if (use > 0 && !wait1(bar(B_EMPTY + s), (use - 1) & 1, ctl, 0xA0000002u)) break;
           mbar_expect_tx(bar(B_FULLQ + s), L::kTile + BM * 4);
 #pragma unroll
           for (int c = 0; c < D / 64; ++c)
             tma_load_4d(sb + L::kQ + s * L::kTile + c * kChunk, &tmQ, bar(B_FULLQ + s), c * 64,
                         qrow, h, bq);
           bulk_load(sb + L::kLSE + s * BM * 4, p.lse2 + ws, BM * 4, bar(B_FULLQ + s));
+          if (use > 0 && !wait1(bar(B_EMPTYDO + s), (use - 1) & 1, ctl, 0xA0000006u)) {
+            ++it;  // the Q copies of this iteration are in flight
+            do_pending_skipped = true;
+            break;
+          }
+          mbar_expect_tx(bar(B_FULLDO + s), L::kTile + BM * 4);
+#pragma unroll
+          for (int c = 0; c < D / 64; ++c)
+            tma_load_4d(sb + L::kDO + s * L::kTile + c * kChunk, &tmDO, bar(B_FULLDO + s), c * 64,
+                        qrow, h, bq);
+          bulk_load(sb + L::kDelta + s * BM * 4, p.delta + ws, BM * 4, bar(B_FULLDO + s));
         }
         if (*abort_flag) break;
       }
@@ -285,9 +285,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (uint32_t s = 0; s < kStages && s < it; ++s) {
         const uint32_t last = (it - 1 - s) / kStages;  // uses of stage (it-1-s) % kStages
         const uint32_t st = (it - 1 - s) % kStages;
-        if (!(s == 0 && q_pending_skipped))
-          wait1(bar(B_FULLQ + st), last & 1, ctl, 0xA0000004u, false);
-        wait1(bar(B_FULLDO + st), last & 1, ctl, 0xA0000005u, false);
+        wait1(bar(B_FULLQ + st), last & 1, ctl, 0xA0000004u, false);
+        if (!(s == 0 && do_pending_skipped))
+          wait1(bar(B_FULLDO + st), last & 1, ctl, 0xA0000005u, false);
       }
     }
   } else if (warp == 1) {
@@ -342,7 +342,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc_fence_after();
 #pragma unroll
           for (int kk = 0; kk < BM / 16; ++kk)
-            mma_ts(tmem + TM_DV, tmem + TM_P + kk * 8, sdesc_sw128(sDO + kk * 2048, kChunk, 1024),
+            mma_ts(tmem + TM_DV, tmem + TM_P + (kk >> 2) * 64 + (kk & 3) * 8,
+                   sdesc_sw128(sDO + kk * 2048, kChunk, 1024),
                    kIdKV, (j > 0 || kk > 0) ? 1u : 0u);
           tc_commit(bar(B_EMPTYDO + s));
           if (!wait1(bar(B_DSREADY), it & 1, ctl, 0xA0000018u)) goto mma_exit;
@@ -358,7 +359,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           // dK += dS^T Q   (A = dS^T from TMEM, B = Q MN-major)
 #pragma unroll
           for (int kk = 0; kk < BM / 16; ++kk)
-            mma_ts(tmem + TM_DK, tmem + TM_DS + kk * 8, sdesc_sw128(sQ + kk * 2048, kChunk, 1024),
+            mma_ts(tmem + TM_DK, tmem + TM_DS + (kk >> 2) * 64 + (kk & 3) * 8,
+                   sdesc_sw128(sQ + kk * 2048, kChunk, 1024),
                    kIdKV, (j > 0 || kk > 0) ? 1u : 0u);
           tc_commit(bar(B_DKDONE));
           tc_commit(bar(B_EMPTY + s));
@@ -375,11 +377,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp >= 4 && warp < 4 + kSoftmaxWarps) {
     // ------------------------------------------------- softmax / dS / epilogue
     // Thread = key row jl (TMEM lane).  Half `hf` of the softmax warps owns query
-    // columns [64 hf, 64 hf + 64): their S^T and dP^T values, their packed P^T
-    // in TMEM columns [32 hf, +32) and their packed dS^T in [64 + 32 hf, +32).
-    // Half 1's P^T and half 0's dS^T land on S columns of the other half, so
-    // every softmax warp signals SREAD once its S^T values are in registers and
-    // those two writes wait for it.
+    // columns [64 hf, 64 hf + 64): their S^T and dP^T values, and keeps their
+    // packed P^T in TMEM columns [64 hf, +32) and their packed dS^T in
+    // [64 hf + 32, +32), both inside the S^T columns the warp itself has read,
+    // so the two halves never wait for each other.
     const uint32_t quad = warp & 3;
     const int hf = static_cast<int>(warp - 4) >> 2;
     const int jl = static_cast<int>(quad * 32 + lane);  // key row within the tile
@@ -428,9 +429,6 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_ld32p(tl + TM_S + 64 * hf, sv);
           tmem_ld32p(tl + TM_S + 64 * hf + 32, sv + 32);
           tmem_wait_ld();
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(bar(B_SREAD));
           // P^T = exp2(S^T * scale * log2 e - LSE2[query]), masked
           uint32_t pk[32];
 #pragma unroll
@@ -451,12 +449,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             pk[e4 * 2] = Pack<T>::two(x0, x1);
             pk[e4 * 2 + 1] = Pack<T>::two(x2, x3);
           }
-          if (hf == 1) {
-            if (!wait_warp(bar(B_SREAD), it & 1, ctl, 0xA0000027u)) goto done;
-            tc_fence_after();
-          }
-          tmem_st16(tl + TM_P + 32 * hf, *reinterpret_cast<uint32_t(*)[16]>(pk));
-          tmem_st16(tl + TM_P + 32 * hf + 16, *reinterpret_cast<uint32_t(*)[16]>(pk + 16));
+          tmem_st16(tl + TM_P + 64 * hf, *reinterpret_cast<uint32_t(*)[16]>(pk));
+          tmem_st16(tl + TM_P + 64 * hf + 16, *reinterpret_cast<uint32_t(*)[16]>(pk + 16));
         }
         tmem_wait_st();
         tc_fence_before();
@@ -468,9 +462,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 
         if (!wait_warp(bar(B_FULLDO + s), ph, ctl, 0xA0000023u)) goto done;
         if (!wait_warp(bar(B_DPFULL), it & 1, ctl, 0xA0000024u)) goto done;
-        // the dS^T tile doubles as the dQ staging buffer of the previous iteration
-        if (it > 0 && !wait_warp(bar(B_STAGEFREE), (it - 1) & 1, ctl, 0xA0000026u)) goto done;
-        if (hf == 0 && !wait_warp(bar(B_SREAD), it & 1, ctl, 0xA0000028u)) goto done;
+        // The dS^T tile was last read by the previous iteration's dQ MMA.  That
+        // MMA completed before this iteration's S^T was issued (S^T waits for
+        // the previous dK, committed after dQ), so SFULL above already covers it.
         tc_fence_after();
         {
           // dS^T = P^T (dP^T - Delta[query]) for this half's 64 queries, in two
@@ -480,7 +474,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           uint32_t dpv[64], pv[32];
           tmem_ld32p(tl + TM_DP + 64 * hf, dpv);
           tmem_ld32p(tl + TM_DP + 64 * hf + 32, dpv + 32);
-          tmem_ld32p(tl + TM_P + 32 * hf, pv);
+          tmem_ld32p(tl + TM_P + 64 * hf, pv);
           tmem_wait_ld();
           const uint32_t row_base = L::kDS + hf * kChunk + jl * 128;
 #pragma unroll
@@ -497,7 +491,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               pk[e4 * 2 + 1] = Pack<T>::two(p23.x * (__uint_as_float(v[2]) - dl.z),
                                             p23.y * (__uint_as_float(v[3]) - dl.w));
             }
-            tmem_st16(tl + TM_DS + 32 * hf + 16 * sub, pk);
+            tmem_st16(tl + TM_DS + 64 * hf + 16 * sub, pk);
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
               const uint32_t unit = (sub * 4 + q) ^ (jl & 7);
@@ -547,18 +541,24 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp >= 4 + kSoftmaxWarps) {
     // ------------------------------------------------------------ dQ drain
     // Thread = query row (TMEM lane); warp q owns rows [32q, 32q+32) of the tile.
-    // The rows go out in 64-column passes: staged in the dS^T tile (free once
-    // the dQ MMA has read it) as two 32x32 fp32 boxes with the 128-byte
-    // swizzle, each box added to dQaccum by a TMA reduce (whole 128-byte lines
-    // at L2).  Rows past the sequence end hold exact zeros (their dS is 0) and
-    // stay inside the sequence's padded workspace rows, so they need no mask.
+    // The rows go out in two passes, staged in the iteration's dO stage (free
+    // once the dV MMA, issued before dQ, has read it) as 32x32 fp32 boxes with
+    // the 128-byte swizzle, each box added to dQaccum by a TMA reduce (whole
+    // 128-byte lines at L2).  The stage goes back to the producer (EMPTYDO)
+    // once the reduces have read it.  Rows past the sequence end hold exact
+    // zeros (their dS is 0) and stay inside the sequence's padded workspace
+    // rows, so they need no mask.
     // In deterministic mode a warp waits until key tiles 0..n-1 have completed
     // their adds (4 arrivals each, one per drain warp) and releases once its
     // own adds have completed.
     const uint32_t quad = warp & 3;
     const uint32_t tl = tmem + ((quad * 32) << 16);
-    const uint32_t stage = sb + L::kDS + quad * 8192;  // 8 KB: two 32x32 fp32 boxes
-    constexpr int kPasses = D / 64;
+    // Per warp and pass: kBoxes boxes of 32 rows x 32 fp32 columns (4 KB each);
+    // the 4 warps' staging fills the dO stage exactly (kTile bytes).
+    constexpr int kBoxes = D / 64;
+    constexpr int kPassCols = 32 * kBoxes;
+    constexpr int kPasses = D / kPassCols;
+    static_assert(4 * kBoxes * 4096 == L::kTile, "dQ staging must fit the dO stage");
     uint32_t it = 0;
     for (uint32_t k = 0;; ++k) {
       int u;
@@ -573,13 +573,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                                           m * BM + quad * 32);
         int* sem = p.sem + static_cast<int64_t>(h) * (p.ws_rows / kTileRows) +
                    un.si.ws_row0 / kTileRows + m;
+        const uint32_t s = it % kStages;
+        const uint32_t stage_off = L::kDO + s * L::kTile + quad * (kBoxes * 4096);
         if (!wait_warp(bar(B_DQFULL), it & 1, ctl, 0xA0000031u)) goto done;
         tc_fence_after();
 #pragma unroll
         for (int pass = 0; pass < kPasses; ++pass) {
-          uint32_t a[64];
-          tmem_ld32p(tl + TM_DQ + pass * 64, a);
-          tmem_ld32p(tl + TM_DQ + pass * 64 + 32, a + 32);
+          uint32_t a[kPassCols];
+#pragma unroll
+          for (int bx = 0; bx < kBoxes; ++bx)
+            tmem_ld32p(tl + TM_DQ + pass * kPassCols + bx * 32, a + bx * 32);
           tmem_wait_ld();
           if (pass == kPasses - 1) {
             tc_fence_before();
@@ -611,8 +614,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             __syncwarp();
           }
 #pragma unroll
-          for (int bx = 0; bx < 2; ++bx) {
-            const uint32_t box = L::kDS + quad * 8192 + bx * 4096;
+          for (int bx = 0; bx < kBoxes; ++bx) {
+            const uint32_t box = stage_off + bx * 4096;
 #pragma unroll
             for (int q = 0; q < 8; ++q) {
               const uint32_t* v = a + bx * 32 + q * 4;
@@ -623,8 +626,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           fence_proxy_async_smem();
           __syncwarp();
           if (lane == 0) {
-            tma_reduce_add_2d(&tmDQ, stage, pass * 64, row0);
-            tma_reduce_add_2d(&tmDQ, stage + 4096, pass * 64 + 32, row0);
+#pragma unroll
+            for (int bx = 0; bx < kBoxes; ++bx)
+              tma_reduce_add_2d(&tmDQ, sb + stage_off + bx * 4096, pass * kPassCols + bx * 32, row0);
             bulk_commit();
           }
         }
@@ -639,7 +643,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
         __syncwarp();
-        if (lane == 0) mbar_arrive(bar(B_STAGEFREE));
+        if (lane == 0) mbar_arrive(bar(B_EMPTYDO + s));
       }
     }
     if (lane == 0) bulk_wait_all();

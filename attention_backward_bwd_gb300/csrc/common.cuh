@@ -85,8 +85,10 @@ static __device__ __noinline__ bool wait1(uint32_t bar, uint32_t parity, const W
 }
 
 // Warp-collective bounded wait: every lane polls, the exit decision is warp
-// uniform (needed before .sync.aligned tcgen05 instructions).
-static __device__ __noinline__ bool wait_warp(uint32_t bar, uint32_t parity, const WaitCtl& c,
+// uniform (needed before .sync.aligned tcgen05 instructions).  Inlined: the
+// warp-wide waits sit on the softmax warps' critical path, where a call costs
+// measurably more than the inlined poll loop.
+static __device__ __forceinline__ bool wait_warp(uint32_t bar, uint32_t parity, const WaitCtl& c,
                                        unsigned int where) {
   uint64_t t0 = 0;
   for (uint32_t it = 0;; ++it) {
