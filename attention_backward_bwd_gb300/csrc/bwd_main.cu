@@ -48,20 +48,24 @@ constexpr int kSoftmaxWarps = 8;
 constexpr int kStages = 2;
 constexpr uint32_t kChunk = 128 * 128;  // one 64-column (128-byte) slice of a 128-row tile
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t TM_S = 0, TM_P = 0, TM_DS = 32, TM_DP = 128;  // P^T, dS^T: + 64 per half
+constexpr uint32_t TM_S = 0, TM_P = 0, TM_DP = 128;  // P^T: + 64 per query half
 constexpr uint32_t TM_DQ = 128, TM_DK = 256, TM_DV = 384;
 
 enum Bar : uint32_t {
   B_FULLQ = 0,
   B_FULLDO = B_FULLQ + kStages,
-  B_EMPTY = B_FULLDO + kStages,    // Q stage (+ LSE2) free: after dK and the softmax
-  B_EMPTYDO = B_EMPTY + kStages,   // dO stage (+ Delta) free: after dV, the softmax and the
-                                   // dQ drain that stages its reduce-adds there
+  B_EMPTY = B_FULLDO + kStages,    // Q stage (+ LSE2) free: dK done (committed after the
+                                   // softmax's DSREADY, so LSE2 has been read too)
+  B_EMPTYDO = B_EMPTY + kStages,   // dO stage (+ Delta) free: dV done and the dQ drain, which
+                                   // stages its reduce-adds there, done with it (the drain
+                                   // starts after dQ, i.e. after the softmax read Delta)
   B_KVFULL = B_EMPTYDO + kStages,
   B_KVEMPTY,
   B_SFULL,
   B_DPFULL,
   B_PREADY,
+  B_PVDONE,                        // dV done: P^T in TMEM no longer read by the tensor pipe
+  B_PREAD,                         // the dS phase has read P^T from TMEM
   B_DSREADY,
   B_DQFULL,
   B_DQFREE,
@@ -167,14 +171,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int s = 0; s < kStages; ++s) {
       mbar_init(bar(B_FULLQ + s), 1);
       mbar_init(bar(B_FULLDO + s), 1);
-      mbar_init(bar(B_EMPTY + s), 1 + kSoftmaxWarps);  // MMA commit + softmax warps
-      mbar_init(bar(B_EMPTYDO + s), 1 + kSoftmaxWarps + 4);  // + the 4 dQ drain warps
+      mbar_init(bar(B_EMPTY + s), 1);       // MMA commit
+      mbar_init(bar(B_EMPTYDO + s), 1 + 4);  // MMA commit + the 4 dQ drain warps
     }
     mbar_init(bar(B_KVFULL), 1);
     mbar_init(bar(B_KVEMPTY), 1);
     mbar_init(bar(B_SFULL), 1);
     mbar_init(bar(B_DPFULL), 1);
     mbar_init(bar(B_PREADY), kSoftmaxWarps);
+    mbar_init(bar(B_PVDONE), 1);
+    mbar_init(bar(B_PREAD), kSoftmaxWarps);
     mbar_init(bar(B_DSREADY), kSoftmaxWarps);
     mbar_init(bar(B_DQFULL), 1);
     mbar_init(bar(B_DQFREE), 4);
@@ -197,6 +203,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + L::kTmemSlot);
+  // Register split (launched with 128 per thread): warpgroup 0 (producer, MMA
+  // issuer, allocator) gives 48 up, the dQ drain warpgroup takes them and holds
+  // a whole dQ row per thread; 80 * 128 + 128 * 256 + 176 * 128 = 512 * 128.
+  static_assert(kThreads == 512 && kSoftmaxWarps == 8, "register split assumes 4 warpgroups");
   volatile int* ring = reinterpret_cast<volatile int*>(smem + L::kRing);
   // Work units come from a persistent scheduler: the first unit of CTA c is c,
   // later ones are taken by the producer from a global counter in
@@ -213,6 +223,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     return true;
   };
 
+  if (warp < 4) {
+    setmaxnreg_dec<80>();
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
@@ -292,10 +304,30 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
+    // Per query tile: dP^T, dV, then the next tile's S^T as soon as dV and the
+    // dS phase have read P^T (so S^T runs while the softmax warps compute dS),
+    // then dQ and dK once dS^T is in shared memory.  The first S^T of a unit
+    // waits for its K/V tiles.
     if (lane == 0) {
       constexpr uint32_t kIdS = idesc_f16(kIsBf16, 0, 0, BN, BM);
       constexpr uint32_t kIdKV = idesc_f16(kIsBf16, 0, 1, BN, D);
       constexpr uint32_t kIdDQ = idesc_f16(kIsBf16, 1, 1, BM, D);
+      // S^T = K Q^T   (M = keys, N = queries, K = head dim; both K-major)
+      auto issue_s = [&](uint32_t sQ) {
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t koff = (kk >> 2) * kChunk + (kk & 3) * 32;
+          mma_ss(tmem + TM_S, sdesc_sw128(sb + L::kK + koff, 16, 1024),
+                 sdesc_sw128(sQ + koff, 16, 1024), kIdS, kk > 0);
+        }
+        tc_commit(bar(B_SFULL));
+      };
+      // S^T of iteration `it` overwrites the packed P^T of iteration it - 1:
+      // dV must have completed and the dS phase must have read it
+      auto wait_p_consumed = [&](uint32_t prev) -> bool {
+        return wait1(bar(B_PVDONE), prev & 1, ctl, 0xA0000014u) &&
+               wait1(bar(B_PREAD), prev & 1, ctl, 0xA0000019u);
+      };
       uint32_t it = 0, uc = 0;
       for (uint32_t k = 0;; ++k) {
         int u;
@@ -304,24 +336,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         const Unit un = get_unit(p, u, G);
         if (un.n_iters == 0) continue;
         if (!wait1(bar(B_KVFULL), uc & 1, ctl, 0xA0000011u)) goto mma_exit;
-        tc_fence_after();
+        {
+          const uint32_t s = it % kStages;
+          if (!wait1(bar(B_FULLQ + s), (it / kStages) & 1, ctl, 0xA0000013u)) goto mma_exit;
+          if (it > 0 && !wait_p_consumed(it - 1)) goto mma_exit;
+          tc_fence_after();
+          issue_s(sb + L::kQ + s * L::kTile);
+        }
         for (int j = 0; j < un.n_iters; ++j, ++it) {
           const uint32_t s = it % kStages;
           const uint32_t ph = (it / kStages) & 1;
           const uint32_t sQ = sb + L::kQ + s * L::kTile;
           const uint32_t sDO = sb + L::kDO + s * L::kTile;
-          if (!wait1(bar(B_FULLQ + s), ph, ctl, 0xA0000013u)) goto mma_exit;
-          // S^T overwrites the packed P^T / dS^T the previous dV / dK read
-          if (it > 0 && !wait1(bar(B_DKDONE), (it - 1) & 1, ctl, 0xA0000014u)) goto mma_exit;
-          tc_fence_after();
-          // S^T = K Q^T   (M = keys, N = queries, K = head dim; both K-major)
-#pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t koff = (kk >> 2) * kChunk + (kk & 3) * 32;
-            mma_ss(tmem + TM_S, sdesc_sw128(sb + L::kK + koff, 16, 1024),
-                   sdesc_sw128(sQ + koff, 16, 1024), kIdS, kk > 0);
-          }
-          tc_commit(bar(B_SFULL));
           if (!wait1(bar(B_FULLDO + s), ph, ctl, 0xA0000015u)) goto mma_exit;
           // dP^T overwrites the previous dQ, which must have been drained
           if (it > 0 && !wait1(bar(B_DQFREE), (it - 1) & 1, ctl, 0xA0000016u)) goto mma_exit;
@@ -345,23 +371,32 @@ __global__ void __launch_bounds__(kThreads, 1)
             mma_ts(tmem + TM_DV, tmem + TM_P + (kk >> 2) * 64 + (kk & 3) * 8,
                    sdesc_sw128(sDO + kk * 2048, kChunk, 1024),
                    kIdKV, (j > 0 || kk > 0) ? 1u : 0u);
+          tc_commit(bar(B_PVDONE));
           tc_commit(bar(B_EMPTYDO + s));
+          // the next tile's S^T, within this unit (same K tile)
+          if (j + 1 < un.n_iters) {
+            const uint32_t s1 = (it + 1) % kStages;
+            if (!wait1(bar(B_FULLQ + s1), ((it + 1) / kStages) & 1, ctl, 0xA000001Au))
+              goto mma_exit;
+            if (!wait_p_consumed(it)) goto mma_exit;
+            tc_fence_after();
+            issue_s(sb + L::kQ + s1 * L::kTile);
+          }
           if (!wait1(bar(B_DSREADY), it & 1, ctl, 0xA0000018u)) goto mma_exit;
           tc_fence_after();
-          // dQ = dS K   (A = dS MN-major from the dS^T tile, B = K MN-major, N = D),
-          // first, so the dQ drain (which frees the dP^T columns for the next
-          // tile) overlaps dK
+          // dQ = dS K   (A = dS MN-major from the dS^T tile, B = K MN-major, N = D)
 #pragma unroll
           for (int kk = 0; kk < BN / 16; ++kk)
             mma_ss(tmem + TM_DQ, sdesc_sw128(sb + L::kDS + kk * 2048, kChunk, 1024),
                    sdesc_sw128(sb + L::kK + kk * 2048, kChunk, 1024), kIdDQ, kk > 0);
           tc_commit(bar(B_DQFULL));
-          // dK += dS^T Q   (A = dS^T from TMEM, B = Q MN-major)
+          // dK += dS^T Q   (A = dS^T K-major from the dS^T tile, B = Q MN-major)
 #pragma unroll
-          for (int kk = 0; kk < BM / 16; ++kk)
-            mma_ts(tmem + TM_DK, tmem + TM_DS + (kk >> 2) * 64 + (kk & 3) * 8,
-                   sdesc_sw128(sQ + kk * 2048, kChunk, 1024),
-                   kIdKV, (j > 0 || kk > 0) ? 1u : 0u);
+          for (int kk = 0; kk < BM / 16; ++kk) {
+            const uint32_t koff = (kk >> 2) * kChunk + (kk & 3) * 32;
+            mma_ss(tmem + TM_DK, sdesc_sw128(sb + L::kDS + koff, 16, 1024),
+                   sdesc_sw128(sQ + kk * 2048, kChunk, 1024), kIdKV, (j > 0 || kk > 0) ? 1u : 0u);
+          }
           tc_commit(bar(B_DKDONE));
           tc_commit(bar(B_EMPTY + s));
         }
@@ -374,7 +409,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_commit(bar(B_FINAL));
       wait1(bar(B_FINAL), 0, ctl, 0xA000001Fu, false);
     }
-  } else if (warp >= 4 && warp < 4 + kSoftmaxWarps) {
+  }
+  } else if (warp < 4 + kSoftmaxWarps) {
     // ------------------------------------------------- softmax / dS / epilogue
     // Thread = key row jl (TMEM lane).  Half `hf` of the softmax warps owns query
     // columns [64 hf, 64 hf + 64): their S^T and dP^T values, and keeps their
@@ -455,27 +491,27 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_wait_st();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) {
-          mbar_arrive(bar(B_PREADY));
-          mbar_arrive(bar(B_EMPTY + s));  // LSE2 of this stage is no longer read
-        }
+        if (lane == 0) mbar_arrive(bar(B_PREADY));
 
         if (!wait_warp(bar(B_FULLDO + s), ph, ctl, 0xA0000023u)) goto done;
         if (!wait_warp(bar(B_DPFULL), it & 1, ctl, 0xA0000024u)) goto done;
-        // The dS^T tile was last read by the previous iteration's dQ MMA.  That
-        // MMA completed before this iteration's S^T was issued (S^T waits for
-        // the previous dK, committed after dQ), so SFULL above already covers it.
         tc_fence_after();
         {
           // dS^T = P^T (dP^T - Delta[query]) for this half's 64 queries, in two
-          // sub-chunks of 32; to TMEM (packed) and to the smem dS^T tile, whose
-          // chunk hf holds queries [64 hf, +64): row jl is 128 bytes and its
-          // 16-byte unit u is stored at u ^ (jl % 8) (128-byte swizzle).
+          // sub-chunks of 32, to the smem dS^T tile, whose chunk hf holds
+          // queries [64 hf, +64): row jl is 128 bytes and its 16-byte unit u is
+          // stored at u ^ (jl % 8) (128-byte swizzle).
           uint32_t dpv[64], pv[32];
           tmem_ld32p(tl + TM_DP + 64 * hf, dpv);
           tmem_ld32p(tl + TM_DP + 64 * hf + 32, dpv + 32);
           tmem_ld32p(tl + TM_P + 64 * hf, pv);
           tmem_wait_ld();
+          // P^T has been read: the next tile's S^T may overwrite it
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar(B_PREAD));
+          // the dS^T tile was last read by the previous tile's dQ and dK MMAs
+          if (it > 0 && !wait_warp(bar(B_DKDONE), (it - 1) & 1, ctl, 0xA0000026u)) goto done;
           const uint32_t row_base = L::kDS + hf * kChunk + jl * 128;
 #pragma unroll
           for (int sub = 0; sub < 2; ++sub) {
@@ -491,7 +527,6 @@ __global__ void __launch_bounds__(kThreads, 1)
               pk[e4 * 2 + 1] = Pack<T>::two(p23.x * (__uint_as_float(v[2]) - dl.z),
                                             p23.y * (__uint_as_float(v[3]) - dl.w));
             }
-            tmem_st16(tl + TM_DS + 64 * hf + 16 * sub, pk);
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
               const uint32_t unit = (sub * 4 + q) ^ (jl & 7);
@@ -500,14 +535,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
         }
-        tmem_wait_st();
         fence_proxy_async_smem();
-        tc_fence_before();
         __syncwarp();
-        if (lane == 0) {
-          mbar_arrive(bar(B_DSREADY));
-          mbar_arrive(bar(B_EMPTYDO + s));
-        }
+        if (lane == 0) mbar_arrive(bar(B_DSREADY));
       }
       // ---- epilogue: half 0 writes dK = scale * acc, half 1 writes dV = acc
       if (!wait_warp(bar(B_DKDVFULL), uc & 1, ctl, 0xA0000025u)) goto done;
@@ -538,7 +568,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) mbar_arrive(bar(B_DKDVFREE));
       ++uc;
     }
-  } else if (warp >= 4 + kSoftmaxWarps) {
+  } else {
+    setmaxnreg_inc<176>();
     // ------------------------------------------------------------ dQ drain
     // Thread = query row (TMEM lane); warp q owns rows [32q, 32q+32) of the tile.
     // The rows go out in two passes, staged in the iteration's dO stage (free
@@ -577,38 +608,36 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t stage_off = L::kDO + s * L::kTile + quad * (kBoxes * 4096);
         if (!wait_warp(bar(B_DQFULL), it & 1, ctl, 0xA0000031u)) goto done;
         tc_fence_after();
+        // the whole row first: the next tile's dP^T reuses these TMEM columns
+        uint32_t a[D];
 #pragma unroll
-        for (int pass = 0; pass < kPasses; ++pass) {
-          uint32_t a[kPassCols];
-#pragma unroll
-          for (int bx = 0; bx < kBoxes; ++bx)
-            tmem_ld32p(tl + TM_DQ + pass * kPassCols + bx * 32, a + bx * 32);
-          tmem_wait_ld();
-          if (pass == kPasses - 1) {
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(bar(B_DQFREE));
-          }
-          if (pass == 0 && p.deterministic) {
-            int stop = 0;
-            if (lane == 0) {
-              const int want = 4 * un.n;
-              const uint64_t t0 = globaltimer_ns();
-              for (uint32_t spin = 0;; ++spin) {
-                if (ld_acquire(sem) >= want) break;
-                if ((spin & 15) == 15) {
-                  if (*abort_flag) { stop = 1; break; }
-                  if (globaltimer_ns() - t0 > p.timeout_ns) {
-                    raise_abort(ctl, 0xA0000033u);
-                    stop = 1;
-                    break;
-                  }
+        for (int c = 0; c < D / 32; ++c) tmem_ld32p(tl + TM_DQ + c * 32, a + c * 32);
+        tmem_wait_ld();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(B_DQFREE));
+        if (p.deterministic) {
+          int stop = 0;
+          if (lane == 0) {
+            const int want = 4 * un.n;
+            const uint64_t t0 = globaltimer_ns();
+            for (uint32_t spin = 0;; ++spin) {
+              if (ld_acquire(sem) >= want) break;
+              if ((spin & 15) == 15) {
+                if (*abort_flag) { stop = 1; break; }
+                if (globaltimer_ns() - t0 > p.timeout_ns) {
+                  raise_abort(ctl, 0xA0000033u);
+                  stop = 1;
+                  break;
                 }
               }
-              fence_proxy_async_global();
             }
-            if (__shfl_sync(0xffffffffu, stop, 0)) goto done;
+            fence_proxy_async_global();
           }
+          if (__shfl_sync(0xffffffffu, stop, 0)) goto done;
+        }
+#pragma unroll
+        for (int pass = 0; pass < kPasses; ++pass) {
           if (pass > 0) {
             if (lane == 0) bulk_wait_read_all();
             __syncwarp();
@@ -618,7 +647,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t box = stage_off + bx * 4096;
 #pragma unroll
             for (int q = 0; q < 8; ++q) {
-              const uint32_t* v = a + bx * 32 + q * 4;
+              const uint32_t* v = a + pass * kPassCols + bx * 32 + q * 4;
               *reinterpret_cast<uint4*>(smem + box + lane * 128 + ((q ^ (lane & 7)) * 16)) =
                   make_uint4(v[0], v[1], v[2], v[3]);
             }

@@ -67,8 +67,9 @@ __device__ __forceinline__ void raise_abort(const WaitCtl& c, unsigned int where
 
 // Single-thread bounded wait.  With honor_abort = false the wait ignores the
 // CTA abort flag (used to drain in-flight copies/MMAs before exit) but still
-// gives up after the timeout.
-static __device__ __noinline__ bool wait1(uint32_t bar, uint32_t parity, const WaitCtl& c,
+// gives up after the timeout.  Inlined: kernels that move registers between
+// warpgroups (setmaxnreg) cannot contain calls.
+static __device__ __forceinline__ bool wait1(uint32_t bar, uint32_t parity, const WaitCtl& c,
                                    unsigned int where, bool honor_abort = true) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
@@ -108,6 +109,18 @@ static __device__ __forceinline__ bool wait_warp(uint32_t bar, uint32_t parity, 
       if (__shfl_sync(0xffffffffu, stop, 0)) return false;
     }
   }
+}
+
+// Warpgroup register reallocation (all 128 threads of the warpgroup execute
+// it).  The per-thread counts of all warpgroups must add up to at most what
+// the block was launched with, or the increase waits forever.
+template <uint32_t N>
+__device__ __forceinline__ void setmaxnreg_dec() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <uint32_t N>
+__device__ __forceinline__ void setmaxnreg_inc() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
 }
 
 // ---------------------------------------------------------------- TMA
