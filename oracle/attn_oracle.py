@@ -35,7 +35,8 @@ Readings where the pages leave a point open:
 
 Every function here is pinned by ``tests/test_oracle_pins.py`` (finite
 differences, algebraic identities, closed forms, an independent fp64 torch
-autograd run and planted-mistake checks).
+autograd run and planted-mistake checks); ``group_backward_rows`` is pinned to
+``mha_backward`` row by row.
 """
 from __future__ import annotations
 
@@ -192,4 +193,53 @@ def mha_backward(q, k, v, do, scale=None, causal=False, cu_seqlens_q=None, cu_se
                     lse[h, qs[0]] = r["LSE"]
                     delta[h, qs[0]] = r["Delta"]
     return {"dQ": dq, "dK": dk, "dV": dv, "O": o, "LSE": lse, "Delta": delta}
+
+
+def group_backward_rows(q, k, v, do, b: int, g: int, q_rows, k_rows, scale=None,
+                        causal=False, block: int = 512):
+    """Exact gradients at selected rows of one (sequence, kv head) group, for
+    problems too large for ``mha_backward`` (padded [B,S,H,D] inputs only).
+
+    Returns (dq_rows [G, len(q_rows), D] for the G query heads of kv head g,
+    dk_rows [len(k_rows), D], dv_rows [len(k_rows), D]), float64.  The same
+    definition as ``head_backward`` (softmax over all allowed keys of a query
+    row, Delta = rowsum(P * dP), dS = P (dP - Delta)), evaluated for query rows
+    ``block`` at a time; the blocks only bound memory, and dK, dV at the chosen
+    key rows accumulate the blocks' sums over query rows in float64.
+    """
+    hq, hk, d = q.shape[2], k.shape[2], q.shape[3]
+    scale = d ** -0.5 if scale is None else scale
+    grp = hq // hk
+    q_rows = [int(i) for i in q_rows]
+    k_rows = np.asarray([int(j) for j in k_rows], dtype=np.int64)
+    kg = _f64(k[b, :, g, :])
+    vg = _f64(v[b, :, g, :])
+    sq, sk = q.shape[1], kg.shape[0]
+    dq = np.zeros((grp, len(q_rows), d))
+    dk = np.zeros((len(k_rows), d))
+    dv = np.zeros((len(k_rows), d))
+    for hh in range(grp):
+        h = g * grp + hh
+        qh = _f64(q[b, :, h, :])
+        doh = _f64(do[b, :, h, :])
+        for i0 in range(0, sq, block):
+            i1 = min(sq, i0 + block)
+            ii = np.arange(i0, i1)[:, None]
+            jj = np.arange(sk)[None, :]
+            allowed = (jj <= ii + (sk - sq)) if causal else np.ones((i1 - i0, sk), dtype=bool)
+            s = np.where(allowed, scale * (qh[i0:i1] @ kg.T), -np.inf)
+            any_key = allowed.any(axis=1)
+            m = np.where(any_key, s.max(axis=1), 0.0)
+            ell = np.where(allowed, np.exp(s - m[:, None]), 0.0).sum(axis=1)
+            lse = np.where(any_key, m + np.log(np.where(any_key, ell, 1.0)), 0.0)
+            p = np.where(allowed, np.exp(s - lse[:, None]), 0.0)
+            dp = doh[i0:i1] @ vg.T
+            delta = (p * dp).sum(axis=1)
+            ds = p * (dp - delta[:, None])
+            for n, i in enumerate(q_rows):
+                if i0 <= i < i1:
+                    dq[hh, n] = scale * (ds[i - i0] @ kg)
+            dk += scale * (ds[:, k_rows].T @ qh[i0:i1])
+            dv += p[:, k_rows].T @ doh[i0:i1]
+    return dq, dk, dv
 

@@ -15,7 +15,8 @@ mistake) and raises ``AssertionError`` when the fact does not hold.  The facts:
 * shift of every key row by one vector leaves dQ, dK, dV unchanged
   (rows of dS sum to zero);  permuting keys permutes dK/dV rows;
 * an independent fp64 torch-autograd run of softmax(Q K^T s) V agrees to 1e-10,
-  and its logsumexp gives LSE.
+  and its logsumexp gives LSE; the same run pins the row-sampled group
+  backward used at full problem sizes.
 """
 from __future__ import annotations
 
@@ -286,7 +287,38 @@ def pin_sympy_exact(o_mod):
             assert _rel(r[key], exact) < 1e-12, f"sympy {key} sq={sq} sk={sk} causal={causal}"
 
 
+def pin_group_rows_autograd(o_mod):
+    """The row-sampled group backward (used at full problem sizes) against an
+    independent fp64 torch-autograd run, with a query-row block smaller than
+    the sequence so the block loop and the causal offsets inside it are used."""
+    rng = np.random.default_rng(77)
+    for (b, hq, hk, sq, sk, d, causal, blk) in ((2, 4, 2, 11, 11, 8, True, 4),
+                                                (1, 3, 1, 9, 13, 8, True, 5),
+                                                (1, 2, 2, 7, 6, 4, False, 3)):
+        q, k, v = (rng.standard_normal((b, sq, hq, d)), rng.standard_normal((b, sk, hk, d)),
+                   rng.standard_normal((b, sk, hk, d)))
+        do = rng.standard_normal((b, sq, hq, d))
+        scale = 0.7 * d ** -0.5
+        grp = hq // hk
+        for bb in range(b):
+            for g in range(hk):
+                q_rows = [0, sq // 2, sq - 1]
+                k_rows = [0, sk // 3, sk - 1]
+                dq, dk, dv = o_mod.group_backward_rows(q, k, v, do, bb, g, q_rows, k_rows,
+                                                       scale, causal, block=blk)
+                dk_ref, dv_ref = np.zeros((sk, d)), np.zeros((sk, d))
+                for hh in range(grp):
+                    h = g * grp + hh
+                    _, _, dq_t, dk_t, dv_t = _torch_head(q[bb, :, h], k[bb, :, g], v[bb, :, g],
+                                                         do[bb, :, h], scale, causal)
+                    assert _rel(dq[hh], dq_t[q_rows]) < 1e-10
+                    dk_ref += dk_t
+                    dv_ref += dv_t
+                assert _rel(dk, dk_ref[k_rows]) < 1e-10
+                assert _rel(dv, dv_ref[k_rows]) < 1e-10
+
+
 ALL_PINS = [pin_sympy_exact, pin_finite_differences, pin_finite_differences_varlen, pin_delta_identity,
             pin_equal_value_rows, pin_causal_row0, pin_causal_bottom_right, pin_zero_query,
             pin_single_key, pin_key_shift_and_permutation, pin_torch_autograd,
-            pin_varlen_matches_padded, pin_empty_cases]
+            pin_varlen_matches_padded, pin_empty_cases, pin_group_rows_autograd]

@@ -175,3 +175,25 @@ def test_full_size_invariants_mha_s1024():
     assert torch.allclose(sdv, sdo, rtol=2e-2, atol=2e-2 * sdo.abs().max().item())
     sdk = dk.double().sum(dim=1).cpu()
     assert sdk.abs().max().item() <= 2e-2 * dk.double().abs().sum(dim=1).max().item()
+
+
+def test_full_size_bench_workload_sampled_rows():
+    """The benchmark's own workload at full size (GQA B=2, Hq=32, Hk=8, S=8192,
+    D=128, bf16, causal) through the same calls bench.py times.  dQ at sampled
+    query rows and dK, dV at sampled key rows of two (sequence, kv head) groups
+    are compared with the fp64 oracle evaluated row by row (tile boundaries,
+    first and last rows, and random rows)."""
+    w = synth.WORKLOADS["gqa_b2_hq32_hk8_s8192_d128_bf16_causal"]
+    x = synth.make_inputs(w)
+    dq, dk, dv = run_gpu(w, x)
+    rng = np.random.default_rng(2024)
+    rows = sorted(set([0, 1, 127, 128, 129, 4095, 4096, 8064, 8190, 8191] +
+                      [int(r) for r in rng.integers(0, w.seqlen_q, 6)]))
+    grp = w.h_q // w.h_k
+    for b, g in ((0, 0), (1, 5)):
+        dq_ref, dk_ref, dv_ref = attn_oracle.group_backward_rows(x.q, x.k, x.v, x.do, b, g, rows,
+                                                                 rows, w.scale, w.causal)
+        got_dq = dq[b, rows, g * grp:(g + 1) * grp].transpose(0, 1)
+        assert_close(f"full-size dQ b={b} g={g}", got_dq, dq_ref)
+        assert_close(f"full-size dK b={b} g={g}", dk[b, rows, g], dk_ref)
+        assert_close(f"full-size dV b={b} g={g}", dv[b, rows, g], dv_ref)
