@@ -373,12 +373,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                    kIdKV, (j > 0 || kk > 0) ? 1u : 0u);
           tc_commit(bar(B_PVDONE));
           tc_commit(bar(B_EMPTYDO + s));
-          // the next tile's S^T, within this unit (same K tile)
+          // the next tile's S^T, within this unit (same K tile); the Q tile usually
+          // lands last, so its wait comes last
           if (j + 1 < un.n_iters) {
             const uint32_t s1 = (it + 1) % kStages;
+            if (!wait_p_consumed(it)) goto mma_exit;
             if (!wait1(bar(B_FULLQ + s1), ((it + 1) / kStages) & 1, ctl, 0xA000001Au))
               goto mma_exit;
-            if (!wait_p_consumed(it)) goto mma_exit;
             tc_fence_after();
             issue_s(sb + L::kQ + s1 * L::kTile);
           }
@@ -494,6 +495,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) mbar_arrive(bar(B_PREADY));
 
         if (!wait_warp(bar(B_FULLDO + s), ph, ctl, 0xA0000023u)) goto done;
+        // the dS^T tile was last read by the previous tile's dQ and dK MMAs (checked
+        // here, while dP^T is usually still running)
+        if (it > 0 && !wait_warp(bar(B_DKDONE), (it - 1) & 1, ctl, 0xA0000026u)) goto done;
         if (!wait_warp(bar(B_DPFULL), it & 1, ctl, 0xA0000024u)) goto done;
         tc_fence_after();
         {
@@ -510,8 +514,6 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(bar(B_PREAD));
-          // the dS^T tile was last read by the previous tile's dQ and dK MMAs
-          if (it > 0 && !wait_warp(bar(B_DKDONE), (it - 1) & 1, ctl, 0xA0000026u)) goto done;
           const uint32_t row_base = L::kDS + hf * kChunk + jl * 128;
 #pragma unroll
           for (int sub = 0; sub < 2; ++sub) {
