@@ -19,20 +19,22 @@
 // ascending KV-tile order behind a per-(head, query tile) semaphore (the
 // dq_semaphore of flash-attention hopper/flash_bwd_launch_template.h).
 //
-// Warp roles (512 threads): warp 0 TMA producer, warp 1 MMA issuer (one
-// thread), warp 2 TMEM allocator, warps 4-11 softmax / dS / dK-dV epilogue
-// (two warps per TMEM lane quadrant: thread = key row, warps 4-7 take query
-// columns 0..63 and warps 8-11 columns 64..127), warps 12-15 dQ drain
-// (thread = query row).
+// Warp roles (768 threads = 6 warpgroups): warp 0 TMA producer, warp 1 MMA
+// issuer (one thread), warp 2 TMEM allocator, warps 4-19 softmax / dS / dK-dV
+// epilogue (four warps per TMEM lane quadrant: thread = key row, warp group g =
+// (warp - 4) / 4 takes query columns [32 g, 32 g + 32)), warps 20-23 dQ drain
+// (thread = query row).  A compile-time switch keeps the 8-softmax-warp form
+// (512 threads, 64 columns per warp).
 //
 // TMEM columns (512 allocated, 128 lanes):
-//   [  0,128) S^T fp32; then each half hf of the queries keeps its packed P^T in
-//             [64 hf, +32) and its packed dS^T in [64 hf + 32, +32), inside the
-//             S^T columns it has already read itself
+//   [  0,128) S^T fp32; each column group keeps its packed P^T in the first half
+//             of the S^T columns it has read itself
 //   [128,256) dP^T fp32, then dQ in [128,128+D)
 //   [256,256+D) dK, [384,384+D) dV
-// The tensor pipe runs S, dP, dV, dQ, dK per query tile; the next tile's S waits
-// for dK and its dP for the dQ drain (which overlaps dK).
+// dS^T goes to a swizzled shared-memory tile read by both the dQ and dK MMAs.
+// The tensor pipe runs dP, dV, then the next tile's S (as soon as dV and the
+// dS phase have read P^T), then dQ and dK; dP of the next tile waits for the dQ
+// drain to have read dQ out of TMEM.
 // Every mbarrier wait is bounded (see WaitCtl): on timeout the kernel records
 // the site in the status word and unwinds.
 #include "common.cuh"
@@ -43,8 +45,14 @@ namespace {
 
 constexpr int BM = 128;  // query tile
 constexpr int BN = 128;  // key tile
-constexpr int kThreads = 512;
-constexpr int kSoftmaxWarps = 8;
+#ifndef ATTN_SOFTMAX_WARPS
+#define ATTN_SOFTMAX_WARPS 16
+#endif
+constexpr int kSoftmaxWarps = ATTN_SOFTMAX_WARPS;  // 8 or 16: 2 or 4 column groups per lane quadrant
+constexpr int kGroups = kSoftmaxWarps / 4;         // query-column groups of the softmax warps
+constexpr int kCols = 128 / kGroups;               // query columns per softmax warp
+constexpr int kThreads = 32 * (4 + kSoftmaxWarps + 4);
+static_assert(kSoftmaxWarps == 8 || kSoftmaxWarps == 16, "softmax warps");
 constexpr int kStages = 2;
 constexpr uint32_t kChunk = 128 * 128;  // one 64-column (128-byte) slice of a 128-row tile
 constexpr uint32_t kTmemCols = 512;
@@ -203,10 +211,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + L::kTmemSlot);
-  // Register split (launched with 128 per thread): warpgroup 0 (producer, MMA
-  // issuer, allocator) gives 48 up, the dQ drain warpgroup takes them and holds
-  // a whole dQ row per thread; 80 * 128 + 128 * 256 + 176 * 128 = 512 * 128.
-  static_assert(kThreads == 512 && kSoftmaxWarps == 8, "register split assumes 4 warpgroups");
+  // Register split.  With 8 softmax warps (512 threads, 128 registers each at
+  // launch) warpgroup 0 (producer, MMA issuer, allocator) gives 48 up and the dQ
+  // drain warpgroup takes them to hold a whole dQ row per thread:
+  // 80 * 128 + 128 * 256 + 176 * 128 = 512 * 128.  With 16 (768 threads, 80 at
+  // launch) the softmax warpgroups give 8 each to the drain:
+  // 80 * 128 + 72 * 512 + 112 * 128 = 768 * 80.
+  constexpr uint32_t kRegWg0 = 80;
+  constexpr uint32_t kRegSoftmax = kSoftmaxWarps == 8 ? 128 : 72;
+  constexpr uint32_t kRegDrain = kSoftmaxWarps == 8 ? 176 : 112;
+  constexpr bool kDrainWholeRow = kSoftmaxWarps == 8;  // else two 64-column passes
   volatile int* ring = reinterpret_cast<volatile int*>(smem + L::kRing);
   // Work units come from a persistent scheduler: the first unit of CTA c is c,
   // later ones are taken by the producer from a global counter in
@@ -222,9 +236,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (!warp_wide || lane_id() == 0) mbar_arrive(bar(B_UNITEMPTY + slot));
     return true;
   };
-
   if (warp < 4) {
-    setmaxnreg_dec<80>();
+    if (kSoftmaxWarps == 8) setmaxnreg_dec<kRegWg0>();
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
@@ -368,7 +381,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc_fence_after();
 #pragma unroll
           for (int kk = 0; kk < BM / 16; ++kk)
-            mma_ts(tmem + TM_DV, tmem + TM_P + (kk >> 2) * 64 + (kk & 3) * 8,
+            mma_ts(tmem + TM_DV, tmem + TM_P + (16 * kk / kCols) * kCols + (16 * kk % kCols) / 2,
                    sdesc_sw128(sDO + kk * 2048, kChunk, 1024),
                    kIdKV, (j > 0 || kk > 0) ? 1u : 0u);
           tc_commit(bar(B_PVDONE));
@@ -412,17 +425,24 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   }
   } else if (warp < 4 + kSoftmaxWarps) {
+    if (kSoftmaxWarps != 8) setmaxnreg_dec<kRegSoftmax>();
     // ------------------------------------------------- softmax / dS / epilogue
-    // Thread = key row jl (TMEM lane).  Half `hf` of the softmax warps owns query
-    // columns [64 hf, 64 hf + 64): their S^T and dP^T values, and keeps their
-    // packed P^T in TMEM columns [64 hf, +32) and their packed dS^T in
-    // [64 hf + 32, +32), both inside the S^T columns the warp itself has read,
-    // so the two halves never wait for each other.
+    // Thread = key row jl (TMEM lane).  Column group `grp` of the softmax warps
+    // owns query columns [c0, c0 + kCols): their S^T and dP^T values, and keeps
+    // their packed P^T in TMEM columns [c0, c0 + kCols / 2), inside the S^T
+    // columns the warp itself has read, so the groups never wait for each other.
     const uint32_t quad = warp & 3;
-    const int hf = static_cast<int>(warp - 4) >> 2;
+    const int grp = static_cast<int>(warp - 4) >> 2;
+    const int c0 = kCols * grp;
     const int jl = static_cast<int>(quad * 32 + lane);  // key row within the tile
     const uint32_t tl = tmem + ((quad * 32) << 16);    // this warp's TMEM lanes
     const float sl2 = p.scale_log2;
+    // epilogue share: the first half of the groups writes dK, the second dV,
+    // each group a contiguous block of eCols head-dim columns
+    constexpr int kEGroups = kGroups / 2;
+    constexpr int eCols = D / kEGroups;
+    const bool writes_dk = grp < kEGroups;
+    const int e0 = (grp % kEGroups) * eCols;
     uint32_t it = 0, uc = 0;
     for (uint32_t k = 0;; ++k) {
       int u;
@@ -432,15 +452,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!un.has_keys) continue;
       const int key = un.n * BN + jl;
       const bool key_ok = key < un.si.sk;
-      // half 0 writes dK, half 1 writes dV
-      const TensorArg& outp = hf == 0 ? p.dk : p.dv;
+      const TensorArg& outp = writes_dk ? p.dk : p.dv;
       T* out_row = static_cast<T*>(const_cast<void*>(outp.ptr)) + (varlen ? 0 : un.b * outp.sb) +
                    static_cast<int64_t>(un.si.k_start + key) * outp.ss +
-                   static_cast<int64_t>(un.g) * outp.sh;
+                   static_cast<int64_t>(un.g) * outp.sh + e0;
       if (un.n_iters == 0) {  // keys but no queries: dK = dV = 0
         if (key_ok) {
 #pragma unroll
-          for (int c = 0; c < D / 8; ++c) reinterpret_cast<uint4*>(out_row)[c] = make_uint4(0, 0, 0, 0);
+          for (int c = 0; c < eCols / 8; ++c) reinterpret_cast<uint4*>(out_row)[c] = make_uint4(0, 0, 0, 0);
         }
         continue;
       }
@@ -453,23 +472,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int q0 = m * BM;
         const bool need_mask = (q0 + BM > un.si.sq) || (un.n * BN + BN > un.si.sk) ||
                                (p.causal && un.n * BN + BN - 1 > q0 + off);
-        const float* lse2 = reinterpret_cast<const float*>(smem + L::kLSE + s * BM * 4) + 64 * hf;
-        const float* dlt = reinterpret_cast<const float*>(smem + L::kDelta + s * BM * 4) + 64 * hf;
-        // valid queries of this key row, in this half's column coordinates: lo <= c < hi
-        int lo = 0, hi = key_ok ? min(64, un.si.sq - q0 - 64 * hf) : 0;
-        if (p.causal) lo = max(0, key - off - q0 - 64 * hf);
+        const float* lse2 = reinterpret_cast<const float*>(smem + L::kLSE + s * BM * 4) + c0;
+        const float* dlt = reinterpret_cast<const float*>(smem + L::kDelta + s * BM * 4) + c0;
+        // valid queries of this key row, in this group's column coordinates: lo <= c < hi
+        int lo = 0, hi = key_ok ? min(kCols, un.si.sq - q0 - c0) : 0;
+        if (p.causal) lo = max(0, key - off - q0 - c0);
         if (!wait_warp(bar(B_FULLQ + s), ph, ctl, 0xA0000021u)) goto done;
         if (!wait_warp(bar(B_SFULL), it & 1, ctl, 0xA0000022u)) goto done;
         tc_fence_after();
         {
-          uint32_t sv[64];
-          tmem_ld32p(tl + TM_S + 64 * hf, sv);
-          tmem_ld32p(tl + TM_S + 64 * hf + 32, sv + 32);
+          uint32_t sv[kCols];
+#pragma unroll
+          for (int c = 0; c < kCols / 32; ++c) tmem_ld32p(tl + TM_S + c0 + 32 * c, sv + 32 * c);
           tmem_wait_ld();
           // P^T = exp2(S^T * scale * log2 e - LSE2[query]), masked
-          uint32_t pk[32];
+          uint32_t pk[kCols / 2];
 #pragma unroll
-          for (int e4 = 0; e4 < 16; ++e4) {
+          for (int e4 = 0; e4 < kCols / 4; ++e4) {
             const float4 l = reinterpret_cast<const float4*>(lse2)[e4];
             const uint32_t* v = sv + e4 * 4;
             float x0 = ex2(fmaf(__uint_as_float(v[0]), sl2, -l.x));
@@ -486,8 +505,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             pk[e4 * 2] = Pack<T>::two(x0, x1);
             pk[e4 * 2 + 1] = Pack<T>::two(x2, x3);
           }
-          tmem_st16(tl + TM_P + 64 * hf, *reinterpret_cast<uint32_t(*)[16]>(pk));
-          tmem_st16(tl + TM_P + 64 * hf + 16, *reinterpret_cast<uint32_t(*)[16]>(pk + 16));
+#pragma unroll
+          for (int c = 0; c < kCols / 32; ++c)
+            tmem_st16(tl + TM_P + c0 + 16 * c, *reinterpret_cast<uint32_t(*)[16]>(pk + 16 * c));
         }
         tmem_wait_st();
         tc_fence_before();
@@ -501,22 +521,27 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!wait_warp(bar(B_DPFULL), it & 1, ctl, 0xA0000024u)) goto done;
         tc_fence_after();
         {
-          // dS^T = P^T (dP^T - Delta[query]) for this half's 64 queries, in two
-          // sub-chunks of 32, to the smem dS^T tile, whose chunk hf holds
-          // queries [64 hf, +64): row jl is 128 bytes and its 16-byte unit u is
-          // stored at u ^ (jl % 8) (128-byte swizzle).
-          uint32_t dpv[64], pv[32];
-          tmem_ld32p(tl + TM_DP + 64 * hf, dpv);
-          tmem_ld32p(tl + TM_DP + 64 * hf + 32, dpv + 32);
-          tmem_ld32p(tl + TM_P + 64 * hf, pv);
+          // dS^T = P^T (dP^T - Delta[query]) for this group's queries, in
+          // sub-chunks of 32, to the smem dS^T tile, whose chunk c holds queries
+          // [64 c, +64): row jl is 128 bytes and its 16-byte unit u is stored
+          // at u ^ (jl % 8) (128-byte swizzle).
+          uint32_t dpv[kCols], pv[kCols / 2];
+#pragma unroll
+          for (int c = 0; c < kCols / 32; ++c) tmem_ld32p(tl + TM_DP + c0 + 32 * c, dpv + 32 * c);
+          if (kCols == 64) {
+            tmem_ld32p(tl + TM_P + c0, pv);
+          } else {
+            tmem_ld16(tl + TM_P + c0, *reinterpret_cast<uint32_t(*)[16]>(pv));
+          }
           tmem_wait_ld();
           // P^T has been read: the next tile's S^T may overwrite it
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(bar(B_PREAD));
-          const uint32_t row_base = L::kDS + hf * kChunk + jl * 128;
 #pragma unroll
-          for (int sub = 0; sub < 2; ++sub) {
+          for (int sub = 0; sub < kCols / 32; ++sub) {
+            const int qc = c0 + 32 * sub;  // first query column of this sub-chunk
+            const uint32_t row_base = L::kDS + (qc / 64) * kChunk + jl * 128;
             uint32_t pk[16];
 #pragma unroll
             for (int e4 = 0; e4 < 8; ++e4) {
@@ -531,7 +556,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
-              const uint32_t unit = (sub * 4 + q) ^ (jl & 7);
+              const uint32_t unit = (((qc % 64) / 8) + q) ^ (jl & 7);
               *reinterpret_cast<uint4*>(smem + row_base + unit * 16) =
                   make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
             }
@@ -541,14 +566,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
         if (lane == 0) mbar_arrive(bar(B_DSREADY));
       }
-      // ---- epilogue: half 0 writes dK = scale * acc, half 1 writes dV = acc
+      // ---- epilogue: this group's columns of dK = scale * acc or dV = acc
       if (!wait_warp(bar(B_DKDVFULL), uc & 1, ctl, 0xA0000025u)) goto done;
       tc_fence_after();
       {
-        const uint32_t src = hf == 0 ? TM_DK : TM_DV;
-        const float mul = hf == 0 ? p.scale : 1.0f;
+        const uint32_t src = (writes_dk ? TM_DK : TM_DV) + e0;
+        const float mul = writes_dk ? p.scale : 1.0f;
 #pragma unroll 1
-        for (int c = 0; c < D / 32; ++c) {
+        for (int c = 0; c < eCols / 32; ++c) {
           uint32_t a[32];
           tmem_ld32(tl + src + c * 32, a);
           tmem_wait_ld();
@@ -571,7 +596,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       ++uc;
     }
   } else {
-    setmaxnreg_inc<176>();
+    setmaxnreg_inc<kRegDrain>();
     // ------------------------------------------------------------ dQ drain
     // Thread = query row (TMEM lane); warp q owns rows [32q, 32q+32) of the tile.
     // The rows go out in two passes, staged in the iteration's dO stage (free
@@ -610,14 +635,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t stage_off = L::kDO + s * L::kTile + quad * (kBoxes * 4096);
         if (!wait_warp(bar(B_DQFULL), it & 1, ctl, 0xA0000031u)) goto done;
         tc_fence_after();
-        // the whole row first: the next tile's dP^T reuses these TMEM columns
-        uint32_t a[D];
+        // With registers for it, the whole row first (the next tile's dP^T reuses
+        // these TMEM columns); otherwise one pass at a time.
+        constexpr int kHeld = kDrainWholeRow ? D : kPassCols;
+        uint32_t a[kHeld];
 #pragma unroll
-        for (int c = 0; c < D / 32; ++c) tmem_ld32p(tl + TM_DQ + c * 32, a + c * 32);
+        for (int c = 0; c < kHeld / 32; ++c) tmem_ld32p(tl + TM_DQ + c * 32, a + c * 32);
         tmem_wait_ld();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bar(B_DQFREE));
+        if (kDrainWholeRow) {
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar(B_DQFREE));
+        }
         if (p.deterministic) {
           int stop = 0;
           if (lane == 0) {
@@ -640,6 +669,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
 #pragma unroll
         for (int pass = 0; pass < kPasses; ++pass) {
+          if (!kDrainWholeRow && pass > 0) {
+#pragma unroll
+            for (int c = 0; c < kPassCols / 32; ++c)
+              tmem_ld32p(tl + TM_DQ + pass * kPassCols + c * 32, a + c * 32);
+            tmem_wait_ld();
+            if (pass == kPasses - 1) {
+              tc_fence_before();
+              __syncwarp();
+              if (lane == 0) mbar_arrive(bar(B_DQFREE));
+            }
+          }
           if (pass > 0) {
             if (lane == 0) bulk_wait_read_all();
             __syncwarp();
@@ -649,7 +689,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t box = stage_off + bx * 4096;
 #pragma unroll
             for (int q = 0; q < 8; ++q) {
-              const uint32_t* v = a + pass * kPassCols + bx * 32 + q * 4;
+              const uint32_t* v = a + (kDrainWholeRow ? pass * kPassCols : 0) + bx * 32 + q * 4;
               *reinterpret_cast<uint4*>(smem + box + lane * 128 + ((q ^ (lane & 7)) * 16)) =
                   make_uint4(v[0], v[1], v[2], v[3]);
             }
