@@ -215,11 +215,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   // launch) warpgroup 0 (producer, MMA issuer, allocator) gives 48 up and the dQ
   // drain warpgroup takes them to hold a whole dQ row per thread:
   // 80 * 128 + 128 * 256 + 176 * 128 = 512 * 128.  With 16 (768 threads, 80 at
-  // launch) the softmax warpgroups give 8 each to the drain:
-  // 80 * 128 + 72 * 512 + 112 * 128 = 768 * 80.
-  constexpr uint32_t kRegWg0 = 80;
-  constexpr uint32_t kRegSoftmax = kSoftmaxWarps == 8 ? 128 : 72;
-  constexpr uint32_t kRegDrain = kSoftmaxWarps == 8 ? 176 : 112;
+  // launch) warpgroup 0 gives 16 to the drain: 64 * 128 + 80 * 512 + 96 * 128 =
+  // 768 * 80 (measured best of the splits that fit).
+  constexpr uint32_t kRegWg0 = kSoftmaxWarps == 8 ? 80 : 64;
+  constexpr uint32_t kRegDrain = kSoftmaxWarps == 8 ? 176 : 96;
   constexpr bool kDrainWholeRow = kSoftmaxWarps == 8;  // else two 64-column passes
   volatile int* ring = reinterpret_cast<volatile int*>(smem + L::kRing);
   // Work units come from a persistent scheduler: the first unit of CTA c is c,
@@ -237,7 +236,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     return true;
   };
   if (warp < 4) {
-    if (kSoftmaxWarps == 8) setmaxnreg_dec<kRegWg0>();
+    setmaxnreg_dec<kRegWg0>();
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
@@ -425,7 +424,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   }
   } else if (warp < 4 + kSoftmaxWarps) {
-    if (kSoftmaxWarps != 8) setmaxnreg_dec<kRegSoftmax>();
     // ------------------------------------------------- softmax / dS / epilogue
     // Thread = key row jl (TMEM lane).  Column group `grp` of the softmax warps
     // owns query columns [c0, c0 + kCols): their S^T and dP^T values, and keeps
