@@ -147,15 +147,24 @@ def dist_setup(n_gpus: int):
 def barrier(dist):
     if dist is not None:
         dist.barrier()
-    torch.cuda.synchronize()
+    if torch.cuda.is_available():
+        torch.cuda.synchronize()
 
 
 def max_over_ranks(x: float, dist) -> float:
+    """The slowest rank's time: the replicas' job ends when the last one does."""
     if dist is None:
         return x
-    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def replica_value(flops_per_rank: float, ms_max: float, world: int) -> float:
+    """Whole-job TFLOP/s of `world` independent replicas: every rank does the
+    same work, the job takes as long as the slowest rank."""
+    return world * flops_per_rank / (ms_max * 1e-3) / 1e12
 
 
 def run_ours(args):
@@ -254,7 +263,7 @@ def run_ours(args):
     esz = 2
     pre_bytes = rows_heads * (2 * w.head_dim * esz + 4 + 8 + 4 * w.head_dim)
     post_bytes = rows_heads * (4 * w.head_dim + esz * w.head_dim)
-    value = world * flops / (ms_max * 1e-3) / 1e12
+    value = replica_value(flops, ms_max, world)
     cfg = {"workload": w.name, "batch": w.batch if not w.varlen else len(x.lengths),
            "h_q": w.h_q, "h_k": w.h_k, "seqlen": w.seqlen_q if not w.varlen else "varlen",
            "head_dim": w.head_dim, "causal": w.causal, "deterministic": det,
