@@ -197,3 +197,54 @@ def test_full_size_bench_workload_sampled_rows():
         assert_close(f"full-size dQ b={b} g={g}", got_dq, dq_ref)
         assert_close(f"full-size dK b={b} g={g}", dk[b, rows, g], dk_ref)
         assert_close(f"full-size dV b={b} g={g}", dv[b, rows, g], dv_ref)
+
+
+def _sampled_rows(n, rng, extra=6):
+    base = [0, 1, 127, 128, 129, n // 2, n - 2, n - 1]
+    return sorted(set(r for r in base + [int(v) for v in rng.integers(0, n, extra)] if 0 <= r < n))
+
+
+@pytest.mark.parametrize("name", ["mha_b2_h16_s4096_d128_bf16", "mha_b2_h16_s4096_d128_bf16_causal",
+                                  "gqa_b2_hq32_hk8_s8192_d128_bf16_causal_det"])
+def test_full_size_configs_sampled_rows(name):
+    """The other padded benchmark configs at full size, through the calls bench.py
+    times, on sampled rows of one (sequence, kv head) group against the row-wise
+    fp64 oracle; the deterministic config is also checked bit for bit against a
+    second run."""
+    w = synth.WORKLOADS[name]
+    x = synth.make_inputs(w)
+    dq, dk, dv = run_gpu(w, x)
+    rng = np.random.default_rng(7)
+    rows = _sampled_rows(w.seqlen_q, rng)
+    grp = w.h_q // w.h_k
+    b, g = w.batch - 1, w.h_k - 1
+    dq_ref, dk_ref, dv_ref = attn_oracle.group_backward_rows(x.q, x.k, x.v, x.do, b, g, rows, rows,
+                                                             w.scale, w.causal)
+    assert_close(f"{name} dQ", dq[b, rows, g * grp:(g + 1) * grp].transpose(0, 1), dq_ref)
+    assert_close(f"{name} dK", dk[b, rows, g], dk_ref)
+    assert_close(f"{name} dV", dv[b, rows, g], dv_ref)
+    if w.deterministic:
+        dq2, dk2, dv2 = run_gpu(w, x)
+        assert torch.equal(dq, dq2) and torch.equal(dk, dk2) and torch.equal(dv, dv2)
+
+
+def test_full_size_varlen_sampled_rows():
+    """The varlen config at full size (16 packed sequences, lengths drawn from
+    [128, 8192]); the shortest and the longest sequence are checked on sampled
+    rows of one head each against the row-wise fp64 oracle on that sequence."""
+    w = synth.WORKLOADS["varlen16_h16_d128_bf16_causal"]
+    x = synth.make_inputs(w)
+    dq, dk, dv = run_gpu(w, x)
+    cu = [int(c) for c in x.cu_seqlens_q]
+    lens = x.lengths
+    rng = np.random.default_rng(11)
+    for bsel, h in ((int(np.argmin(lens)), 3), (int(np.argmax(lens)), 12)):
+        lo, hi = cu[bsel], cu[bsel + 1]
+        rows = _sampled_rows(hi - lo, rng)
+        seq = [t[lo:hi].unsqueeze(0) for t in (x.q, x.k, x.v, x.do)]
+        dq_ref, dk_ref, dv_ref = attn_oracle.group_backward_rows(*seq, 0, h, rows, rows, w.scale,
+                                                                 w.causal)
+        idx = [lo + r for r in rows]
+        assert_close(f"varlen seq {bsel} dQ", dq[idx, h].unsqueeze(0), dq_ref)
+        assert_close(f"varlen seq {bsel} dK", dk[idx, h], dk_ref)
+        assert_close(f"varlen seq {bsel} dV", dv[idx, h], dv_ref)
