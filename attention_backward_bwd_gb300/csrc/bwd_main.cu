@@ -9,15 +9,15 @@
 //   P^T  = exp2(S^T * scale * log2 e - LSE2[query]), masked  (bf16/fp16, TMEM)
 //   dP^T = V_n dO_m^T                       (TMEM, fp32)
 //   dV  += P^T dO_m                         (TMEM accumulator, A operand from TMEM)
-//   dS^T = P^T * (dP^T - Delta[query])      (TMEM and smem, bf16/fp16)
-//   dK  += dS^T Q_m                         (TMEM accumulator, A operand from TMEM)
+//   dS^T = P^T * (dP^T - Delta[query])      (smem, bf16/fp16)
+//   dK  += dS^T Q_m                         (TMEM accumulator, A operand from smem)
 //   dQ_m = dS K_n -> reduced into the fp32 dQaccum in global memory
 // dK (times scale) and dV are written once per unit; dK/dV of a GQA group are
 // summed in TMEM over the group's query heads (the group sum of
 // flash-attention csrc/flash_attn_ck/mha_bwd.cpp, done without extra memory).
-// dQaccum is reduced with fp32 vector atomics, or, in deterministic mode, in
-// ascending KV-tile order behind a per-(head, query tile) semaphore (the
-// dq_semaphore of flash-attention hopper/flash_bwd_launch_template.h).
+// dQaccum is reduced with TMA tensor reduce-adds (fp32), or, in deterministic
+// mode, in ascending KV-tile order behind a per-(head, query tile) semaphore
+// (the dq_semaphore of flash-attention hopper/flash_bwd_launch_template.h).
 //
 // Warp roles (768 threads = 6 warpgroups): warp 0 TMA producer, warp 1 MMA
 // issuer (one thread), warp 2 TMEM allocator, warps 4-19 softmax / dS / dK-dV
