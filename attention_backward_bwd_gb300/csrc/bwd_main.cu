@@ -53,6 +53,17 @@ constexpr int kGroups = kSoftmaxWarps / 4;         // query-column groups of the
 constexpr int kCols = 128 / kGroups;               // query columns per softmax warp
 constexpr int kThreads = 32 * (4 + kSoftmaxWarps + 4);
 static_assert(kSoftmaxWarps == 8 || kSoftmaxWarps == 16, "softmax warps");
+// Per-thread registers of the warpgroups after the split done at kernel entry:
+// warpgroup 0 (producer, MMA issuer, allocator), the softmax warpgroups (which
+// keep their launch count) and the dQ drain warpgroup.  An increase that the
+// launch allocation cannot cover would wait forever, so the host checks the
+// kernel's launch register count against kRegLaunch before every launch.
+constexpr uint32_t kRegLaunch = kSoftmaxWarps == 8 ? 128 : 80;
+constexpr uint32_t kRegWg0 = kSoftmaxWarps == 8 ? 80 : 64;
+constexpr uint32_t kRegDrain = kSoftmaxWarps == 8 ? 176 : 96;
+static_assert(kRegWg0 * 128 + kRegLaunch * 32 * kSoftmaxWarps + kRegDrain * 128 ==
+                  kRegLaunch * kThreads,
+              "register split must use exactly the launch allocation");
 constexpr int kStages = 2;
 constexpr uint32_t kChunk = 128 * 128;  // one 64-column (128-byte) slice of a 128-row tile
 constexpr uint32_t kTmemCols = 512;
@@ -217,8 +228,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   // 80 * 128 + 128 * 256 + 176 * 128 = 512 * 128.  With 16 (768 threads, 80 at
   // launch) warpgroup 0 gives 16 to the drain: 64 * 128 + 80 * 512 + 96 * 128 =
   // 768 * 80 (measured best of the splits that fit).
-  constexpr uint32_t kRegWg0 = kSoftmaxWarps == 8 ? 80 : 64;
-  constexpr uint32_t kRegDrain = kSoftmaxWarps == 8 ? 176 : 96;
   constexpr bool kDrainWholeRow = kSoftmaxWarps == 8;  // else two 64-column passes
   volatile int* ring = reinterpret_cast<volatile int*>(smem + L::kRing);
   // Work units come from a persistent scheduler: the first unit of CTA c is c,
@@ -743,6 +752,12 @@ cudaError_t launch_t(const BwdParams& p, int dtype, cudaStream_t stream) {
     cudaError_t e = cudaFuncSetAttribute(bwd_main_kernel<T, D>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
+    // The warpgroup register split assumes exactly kRegLaunch registers per
+    // thread at launch; anything else could leave a register increase waiting.
+    cudaFuncAttributes fa;
+    e = cudaFuncGetAttributes(&fa, bwd_main_kernel<T, D>);
+    if (e != cudaSuccess) return e;
+    if (fa.numRegs != static_cast<int>(kRegLaunch)) return cudaErrorInvalidConfiguration;
     attr_done = true;
   }
   const int n_tiles = ceil_div(p.max_seqlen_k, BN);
