@@ -68,6 +68,10 @@ EDGE = [
     (1, 2, 2, 100, 300, 64, "fp16", True),    # causal, bottom-right alignment
     (1, 2, 2, 300, 100, 128, "bf16", True),   # causal Sq > Sk: leading rows see no key
     (1, 8, 2, 384, 384, 128, "bf16", True),   # GQA 4:1, several tiles
+    (1, 8, 1, 520, 520, 128, "bf16", True),   # GQA 8:1, ragged last tile
+    (2, 4, 2, 257, 700, 64, "bf16", True),    # causal Sq < Sk, D=64 GQA, ragged both sides
+    (1, 4, 4, 640, 333, 128, "fp16", True),   # causal Sq > Sk over several query tiles
+    (1, 2, 2, 1000, 1000, 128, "fp16", False),  # fp16, 8 tiles, ragged
 ]
 
 
@@ -78,7 +82,7 @@ def test_edge_shapes(case):
     check(w, synth.make_inputs(w))
 
 
-@pytest.mark.parametrize("case", EDGE[3:7], ids=str)
+@pytest.mark.parametrize("case", EDGE[3:7] + EDGE[-4:-1], ids=str)
 def test_edge_shapes_deterministic(case):
     b, hq, hk, sq, sk, d, dtype, causal = case
     w = synth.small("edge_det", b, hq, hk, sq, sk, d, dtype, causal, 60 + sq, deterministic=True)
