@@ -57,7 +57,7 @@ __device__ __forceinline__ bool ws_row_to_seq(const SeqParams& s, int64_t row, i
 }
 
 template <typename T, int D>
-__global__ void __launch_bounds__(kThreads) preprocess_kernel(BwdParams p) {
+__global__ void __launch_bounds__(kThreads, 8) preprocess_kernel(BwdParams p) {
   if (p.input_bad != nullptr && *p.input_bad) return;
   constexpr int kGroup = D / 8;  // threads per head row, 16 B each
   const int64_t n_groups = p.ws_rows * p.h_q;
@@ -65,7 +65,8 @@ __global__ void __launch_bounds__(kThreads) preprocess_kernel(BwdParams p) {
   const int64_t nthreads = static_cast<int64_t>(gridDim.x) * kThreads;
   const int c = threadIdx.x % kGroup;
 
-  // Phase 1: Delta and LSE2 for every workspace row (0 for padding rows).
+  // Phase 1: Delta and LSE2 for every workspace row (0 for padding rows), and the
+  // row's fp32 dQ accumulator cleared (those stores and the O/dO loads are in flight together).
   // Iterate per warp so every lane reaches the shuffles below.
   constexpr int kGroupsPerWarp = 32 / kGroup;
   const int64_t warp_g = gtid / 32;
@@ -78,6 +79,12 @@ __global__ void __launch_bounds__(kThreads) preprocess_kernel(BwdParams p) {
     int b = 0, i = 0;
     SeqInfo si;
     const bool valid = in_range && ws_row_to_seq(p.seq, row, b, i, si);
+    if (in_range) {
+      float4* z = reinterpret_cast<float4*>(
+          p.dqacc + (static_cast<int64_t>(h) * p.ws_rows + row) * D + c * 8);
+      z[0] = make_float4(0.f, 0.f, 0.f, 0.f);
+      z[1] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
     float acc = 0.f;
     if (valid) {
       const uint4 ov = *reinterpret_cast<const uint4*>(row_ptr<T>(p.o, p.seq.cu_q != nullptr, si, b, i, h) + c * 8);
@@ -108,12 +115,7 @@ __global__ void __launch_bounds__(kThreads) preprocess_kernel(BwdParams p) {
     }
   }
 
-  // Phase 2: clear the fp32 dQ accumulator.
-  const int64_t n4 = p.ws_rows * p.h_q * p.head_dim / 4;
-  float4* acc4 = reinterpret_cast<float4*>(p.dqacc);
-  for (int64_t e = gtid; e < n4; e += nthreads) acc4[e] = make_float4(0.f, 0.f, 0.f, 0.f);
-
-  // Phase 3: clear the deterministic-mode semaphores and the work counter after them.
+  // Phase 2: clear the deterministic-mode semaphores and the work counter after them.
   const int64_t ns = p.ws_rows / kTileRows * p.h_q + 1;
   for (int64_t e = gtid; e < ns; e += nthreads) p.sem[e] = 0;
 }
@@ -198,9 +200,16 @@ __global__ void validate_cu_kernel(const int* cu_q, const int* cu_k, int batch, 
   }
 }
 
-inline int grid_for(int64_t work_threads) {
+// Grid-stride launches: one full wave (as many blocks as fit on every SM at once), so
+// no block starts late and runs in a half-empty second wave.
+template <typename K>
+inline int grid_for(int64_t work_threads, K kernel) {
+  int per_sm = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, kThreads, 0) != cudaSuccess ||
+      per_sm < 1)
+    per_sm = 1;
   const int64_t want = (work_threads + kThreads - 1) / kThreads;
-  const int64_t cap = static_cast<int64_t>(num_sms()) * 8;
+  const int64_t cap = static_cast<int64_t>(num_sms()) * per_sm;
   return static_cast<int>(want < 1 ? 1 : (want > cap ? cap : want));
 }
 
@@ -209,9 +218,10 @@ inline int grid_for(int64_t work_threads) {
 template <typename T>
 static cudaError_t launch_pre_t(const BwdParams& p, cudaStream_t stream) {
   const int64_t work = p.ws_rows * p.h_q * (p.head_dim / 8);
-  const int grid = grid_for(work);
-  if (p.head_dim == 64) preprocess_kernel<T, 64><<<grid, kThreads, 0, stream>>>(p);
-  else preprocess_kernel<T, 128><<<grid, kThreads, 0, stream>>>(p);
+  if (p.head_dim == 64)
+    preprocess_kernel<T, 64><<<grid_for(work, preprocess_kernel<T, 64>), kThreads, 0, stream>>>(p);
+  else
+    preprocess_kernel<T, 128><<<grid_for(work, preprocess_kernel<T, 128>), kThreads, 0, stream>>>(p);
   return cudaGetLastError();
 }
 
@@ -226,9 +236,10 @@ static cudaError_t launch_post_t(const BwdParams& p, cudaStream_t stream) {
                              : static_cast<int64_t>(p.seq.seqlen_q);
   const int64_t work = tokens * p.h_q * (p.head_dim / 8);
   if (work == 0) return cudaSuccess;
-  const int grid = grid_for(work);
-  if (p.head_dim == 64) postprocess_kernel<T, 64><<<grid, kThreads, 0, stream>>>(p);
-  else postprocess_kernel<T, 128><<<grid, kThreads, 0, stream>>>(p);
+  if (p.head_dim == 64)
+    postprocess_kernel<T, 64><<<grid_for(work, postprocess_kernel<T, 64>), kThreads, 0, stream>>>(p);
+  else
+    postprocess_kernel<T, 128><<<grid_for(work, postprocess_kernel<T, 128>), kThreads, 0, stream>>>(p);
   return cudaGetLastError();
 }
 
@@ -242,11 +253,12 @@ static cudaError_t launch_zero_t(const TensorArg& t, int nseq, int rows_per_seq,
   const int64_t rows = (cu == nullptr) ? static_cast<int64_t>(nseq) * rows_per_seq : total_rows;
   const int64_t work = rows * heads * (head_dim / 8);
   if (work == 0) return cudaSuccess;
-  const int grid = grid_for(work);
   if (head_dim == 64)
-    zero_rows_kernel<T, 64><<<grid, kThreads, 0, stream>>>(t, nseq, rows_per_seq, cu, total_rows, heads);
+    zero_rows_kernel<T, 64><<<grid_for(work, zero_rows_kernel<T, 64>), kThreads, 0, stream>>>(
+        t, nseq, rows_per_seq, cu, total_rows, heads);
   else
-    zero_rows_kernel<T, 128><<<grid, kThreads, 0, stream>>>(t, nseq, rows_per_seq, cu, total_rows, heads);
+    zero_rows_kernel<T, 128><<<grid_for(work, zero_rows_kernel<T, 128>), kThreads, 0, stream>>>(
+        t, nseq, rows_per_seq, cu, total_rows, heads);
   return cudaGetLastError();
 }
 
