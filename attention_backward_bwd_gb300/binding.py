@@ -45,7 +45,8 @@ _lib = None
 _lock = threading.Lock()
 
 EXPORTS = ("attn_fwd", "attn_bwd", "attn_bwd_preprocess", "attn_bwd_main", "attn_bwd_postprocess",
-           "attn_bwd_workspace_size", "attn_bwd_workspace_layout", "attn_check_device_status",
+           "attn_bwd_workspace_size", "attn_bwd_workspace_layout", "attn_bwd_noalloc",
+           "attn_bwd_host", "attn_bwd_host_buffer_size", "attn_check_device_status",
            "attn_set_wait_timeout_ns", "attn_last_error", "attn_version", "attn_diag_mma",
            "attn_diag_wait_timeout", "attn_diag_exp2")
 
@@ -68,6 +69,11 @@ def lib() -> ctypes.CDLL:
             f = getattr(L, name)
             f.argtypes = _BWD_ARGS
             f.restype = _I
+        L.attn_bwd_host.argtypes = [_T, _T, _T, _T, _P, _T, _T, _T, _T, _I, _I, _I, _I, _I, _I,
+                                    _I, ctypes.c_float, _I, _I, _I, _P, ctypes.c_size_t, _P]
+        L.attn_bwd_host.restype = _I
+        L.attn_bwd_host_buffer_size.argtypes = [_I, _I, _I, _I, _I, _I, _I]
+        L.attn_bwd_host_buffer_size.restype = ctypes.c_size_t
         L.attn_bwd_workspace_size.argtypes = [_I, _I, _I, _I, _I, _I]
         L.attn_bwd_workspace_size.restype = ctypes.c_size_t
         L.attn_bwd_workspace_layout.argtypes = [_I, _I, _I, _I, _I,
@@ -217,6 +223,46 @@ def attn_bwd(q, k, v, o, lse, do, causal: bool = False, scale: Optional[float] =
             ctypes.byref(d_dk), ctypes.byref(d_dv), _dtype_code(q), b, sq, sk, hq, hk, d, scale,
             int(bool(causal)), _ptr(cu_seqlens_q), _ptr(cu_seqlens_k), mq, mk,
             int(bool(deterministic)), workspace.data_ptr(), workspace.numel(), _stream(stream))
+    _check(rc)
+    return dq, dk, dv
+
+
+def host_buffer_size(batch: int, seqlen_q: int, seqlen_k: int, h_q: int, h_k: int,
+                     head_dim: int, chunks: int = 0) -> int:
+    """Device bytes that attn_bwd_host needs for this problem and chunk count."""
+    return int(lib().attn_bwd_host_buffer_size(batch, seqlen_q, seqlen_k, h_q, h_k, head_dim,
+                                               chunks))
+
+
+def attn_bwd_host(q, k, v, o, lse, do, dq=None, dk=None, dv=None, causal: bool = False,
+                  scale: Optional[float] = None, deterministic: bool = False, chunks: int = 0,
+                  device_buffer: Optional[torch.Tensor] = None, device=None, stream=None):
+    """Backward on HOST tensors ([B, S, H, D], heads adjacent; lse [B, H_q, Sq]).
+
+    Inputs are copied to the device, the backward runs, and dQ, dK, dV are
+    copied back into host tensors (pinned, allocated here if not given), all on
+    ``stream``; synchronise the stream before reading them.  ``device_buffer``
+    (uint8 on the device, at least ``host_buffer_size(...)`` bytes) is
+    allocated on ``device`` if not given.  Returns (dq, dk, dv).
+    """
+    L = lib()
+    b, sq, sk, hq, hk, d = q.shape[0], q.shape[1], k.shape[1], q.shape[2], k.shape[2], q.shape[3]
+    scale = d ** -0.5 if scale is None else float(scale)
+    pin = torch.cuda.is_available()
+    dq = torch.empty(q.shape, dtype=q.dtype, pin_memory=pin) if dq is None else dq
+    dk = torch.empty(k.shape, dtype=k.dtype, pin_memory=pin) if dk is None else dk
+    dv = torch.empty(v.shape, dtype=v.dtype, pin_memory=pin) if dv is None else dv
+    need = host_buffer_size(b, sq, sk, hq, hk, d, chunks)
+    if device_buffer is None:
+        device_buffer = torch.empty(max(need, 256), dtype=torch.uint8,
+                                    device=device if device is not None else "cuda")
+    descs = [_desc(t) for t in (q, k, v, o)]
+    d_do, d_dq, d_dk, d_dv = _desc(do), _desc(dq), _desc(dk), _desc(dv)
+    rc = L.attn_bwd_host(*(ctypes.byref(x) for x in descs), _ptr(lse), ctypes.byref(d_do),
+                         ctypes.byref(d_dq), ctypes.byref(d_dk), ctypes.byref(d_dv),
+                         _dtype_code(q), b, sq, sk, hq, hk, d, scale, int(bool(causal)),
+                         int(bool(deterministic)), int(chunks), device_buffer.data_ptr(),
+                         device_buffer.numel(), _stream(stream))
     _check(rc)
     return dq, dk, dv
 

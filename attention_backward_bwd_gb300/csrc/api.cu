@@ -27,7 +27,10 @@ namespace {
 thread_local std::string g_err;
 std::atomic<long long> g_timeout_ns{4000000000LL};
 
-int fail(int code, const char* fmt, ...) __attribute__((format(printf, 2, 3)));
+}  // namespace
+
+void clear_error() { g_err.clear(); }
+
 int fail(int code, const char* fmt, ...) {
   char buf[512];
   va_list ap;
@@ -41,8 +44,6 @@ int fail(int code, const char* fmt, ...) {
 int cuda_fail(cudaError_t e, const char* what) {
   return fail(ATTN_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
 }
-
-}  // namespace
 
 // Device status words: [0] = 0 or the site of a bounded wait that gave up;
 // [1] = 0 or the code of a failed cu_seqlens validation.
@@ -160,11 +161,7 @@ TensorArg targ(const attn_tensor* t) {
   return TensorArg{t->ptr, t->stride_b, t->stride_s, t->stride_h};
 }
 
-struct Prepared {
-  BwdParams p;
-  int dtype;
-  bool empty_q, empty_k;
-};
+}  // namespace
 
 int check_common(int dtype, int batch, int seqlen_q, int seqlen_k, int h_q, int h_k,
                  int head_dim, float scale, const int* cu_q, const int* cu_k,
@@ -261,8 +258,6 @@ int prepare_bwd(const attn_tensor* q, const attn_tensor* k, const attn_tensor* v
   return ATTN_OK;
 }
 
-enum Stage { kPre = 1, kMain = 2, kPost = 4 };
-
 int run_stages(int stages, const Prepared& pr, cudaStream_t stream) {
   const BwdParams& p = pr.p;
   cudaError_t e;
@@ -309,7 +304,6 @@ int run_stages(int stages, const Prepared& pr, cudaStream_t stream) {
   return ATTN_OK;
 }
 
-}  // namespace
 }  // namespace attn
 
 using namespace attn;

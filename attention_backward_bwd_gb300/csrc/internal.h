@@ -7,6 +7,8 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include "../../include/attn_bwd.h"
+
 namespace attn {
 
 // Query/key tile height of the backward kernels; workspace rows are padded to it.
@@ -112,5 +114,36 @@ bool encode_tmap_bshd(CUtensorMap* out, const TensorArg& t, int dtype, int rows,
 // 2-D TMA map over a row-major fp32 matrix [rows][cols], box {32, 32}, 128-byte
 // swizzle (used to reduce-add dQ tiles into the dQ accumulator).
 bool encode_tmap_f32_2d(CUtensorMap* out, float* base, int64_t rows, int cols);
+
+// ---- host side of one backward call (api.cu) ----
+
+// Error message of the calling thread, read back by attn_last_error().
+void clear_error();
+int fail(int code, const char* fmt, ...) __attribute__((format(printf, 2, 3)));
+int cuda_fail(cudaError_t e, const char* what);
+
+// Arguments checked and bound to kernel parameters; nothing launched yet.
+struct Prepared {
+  BwdParams p;
+  int dtype;
+  bool empty_q, empty_k;
+};
+
+int check_common(int dtype, int batch, int seqlen_q, int seqlen_k, int h_q, int h_k,
+                 int head_dim, float scale, const int* cu_q, const int* cu_k, int max_seqlen_q,
+                 int max_seqlen_k);
+
+int prepare_bwd(const attn_tensor* q, const attn_tensor* k, const attn_tensor* v,
+                const attn_tensor* o, const float* lse, const attn_tensor* dout,
+                const attn_tensor* dq, const attn_tensor* dk, const attn_tensor* dv, int dtype,
+                int batch, int seqlen_q, int seqlen_k, int h_q, int h_k, int head_dim,
+                float scale, int causal, const int* cu_q, const int* cu_k, int max_seqlen_q,
+                int max_seqlen_k, int deterministic, void* workspace, size_t workspace_bytes,
+                Prepared* out);
+
+enum Stage { kPre = 1, kMain = 2, kPost = 4 };
+
+// Launches the selected stages (preprocess, main, postprocess) on `stream`.
+int run_stages(int stages, const Prepared& pr, cudaStream_t stream);
 
 }  // namespace attn

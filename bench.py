@@ -224,20 +224,34 @@ def run_ours(args):
     t_main = statistics.mean(e[1].elapsed_time(e[2]) for e in evs)
     t_post = statistics.mean(e[2].elapsed_time(e[3]) for e in evs)
 
-    # --- end to end: pinned host inputs -> device -> attn_bwd -> host results
+    # --- end to end: pinned host inputs -> device -> backward -> pinned host results.
+    # Padded workloads go through attn_bwd_host (chunks whose copies overlap the
+    # kernels of other chunks); varlen ones copy in, call attn_bwd, copy out.
     hq_ = [t.cpu().pin_memory() for t in (q, k, v, o, do, lse)]
-    dev_in = [torch.empty_like(t) for t in (q, k, v, o, do, lse)]
     host_out = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in (dq, dk, dv)]
     h2d = sum(t.numel() * t.element_size() for t in hq_)
     d2h = sum(t.numel() * t.element_size() for t in host_out)
+    if not w.varlen:
+        b_, sq_, hq_n, d_ = q.shape
+        hbuf = torch.empty(ab.host_buffer_size(b_, sq_, k.shape[1], hq_n, k.shape[2], d_,
+                                               args.chunks), dtype=torch.uint8, device=dev)
+        e2e_path = f"attn_bwd_host, chunks={args.chunks or 'auto'}"
 
-    def e2e_step():
-        for dst, src in zip(dev_in, hq_):
-            dst.copy_(src, non_blocking=True)
-        ab.attn_bwd(dev_in[0], dev_in[1], dev_in[2], dev_in[3], dev_in[5], dev_in[4],
-                    stream=stream, **kw)
-        for dst, src in zip(host_out, (dq, dk, dv)):
-            dst.copy_(src, non_blocking=True)
+        def e2e_step():
+            ab.attn_bwd_host(hq_[0], hq_[1], hq_[2], hq_[3], hq_[5], hq_[4], *host_out,
+                             causal=w.causal, deterministic=det, chunks=args.chunks,
+                             device_buffer=hbuf, stream=stream)
+    else:
+        dev_in = [torch.empty_like(t) for t in (q, k, v, o, do, lse)]
+        e2e_path = "copies + attn_bwd"
+
+        def e2e_step():
+            for dst, src in zip(dev_in, hq_):
+                dst.copy_(src, non_blocking=True)
+            ab.attn_bwd(dev_in[0], dev_in[1], dev_in[2], dev_in[3], dev_in[5], dev_in[4],
+                        stream=stream, **kw)
+            for dst, src in zip(host_out, (dq, dk, dv)):
+                dst.copy_(src, non_blocking=True)
 
     for _ in range(2):
         e2e_step()
@@ -288,7 +302,7 @@ def run_ours(args):
                 "peak_gbs": peaks["hbm_gbs"]},
         "e2e": {"value": round(world * flops / (e2e_ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
                 "ms_per_step": round(e2e_ms, 3), "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h},
+                "d2h_bytes_per_step": d2h, "path": e2e_path},
         "gpu_launches": 3 * args.steps,
         "clocks": clk.summary(),
     }
@@ -384,6 +398,8 @@ def main():
     ap.add_argument("--deterministic", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=20.0)
+    ap.add_argument("--chunks", type=int, default=0,
+                    help="attn_bwd_host chunk count for the end-to-end number (0: library default)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     if args.impl == "reference":

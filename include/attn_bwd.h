@@ -29,7 +29,8 @@
  *
  * Ownership.  The caller owns every buffer, including the workspace; the
  * library allocates nothing per call and keeps no state across calls except
- * one-time kernel attributes and a device status word.  All compute calls
+ * one-time kernel attributes, a device status word and, once attn_bwd_host
+ * has been called on a device, that call's internal streams and events.  All compute calls
  * are asynchronous on `stream` (a cudaStream_t; NULL = legacy default stream).
  *
  * Errors.  Every call returns ATTN_OK (0) or a negative code and then
@@ -154,6 +155,47 @@ int attn_bwd_noalloc(const attn_tensor* q, const attn_tensor* k, const attn_tens
                      int head_dim, float scale, int causal, const int* cu_seqlens_q,
                      const int* cu_seqlens_k, int max_seqlen_q, int max_seqlen_k,
                      int deterministic, attn_stream_t stream);
+
+/*
+ * attn_bwd_host -- attn_bwd on tensors in HOST memory: copies q, k, v, o,
+ * dout and lse to the device, runs the backward, and copies dq, dk, dv back,
+ * all enqueued on `stream` (the call returns before the work is done; the
+ * results are in host memory once `stream` has passed this call, e.g. after
+ * cudaStreamSynchronize).  The pages describe no counterpart of this call:
+ * it serves callers whose activations live in host memory (offloaded
+ * activations), where the copies would otherwise cost more than the kernels.
+ *
+ * The problem is cut into `chunks` independent pieces (0 = the library
+ * chooses, currently 8; at most 64): runs of whole sequences when batch >=
+ * chunks, else one sequence and a range of key/value heads with their query
+ * heads.  Each piece's copies in, kernels and copies out run on internal
+ * streams, so the copies of one piece overlap the kernels of the others.
+ * Results equal attn_bwd's on the same data (bit for bit in deterministic
+ * mode and for dK, dV; dQ's fp32 adds may be ordered differently otherwise).
+ *
+ * Host tensors: padded [B, S, H, D] (no varlen), the heads of a position
+ * adjacent (stride_h == D), D contiguous, and positions and sequences not
+ * overlapping; lse is [B, H_q, Sq] contiguous.  Page-locked memory
+ * (cudaHostAlloc / cudaHostRegister) is needed for the copies to overlap;
+ * pageable memory works but serialises them.
+ * device_buffer: device memory of at least
+ * attn_bwd_host_buffer_size(batch, seqlen_q, seqlen_k, h_q, h_k, head_dim,
+ * chunks) bytes, 256-byte aligned, owned by the caller, not used by any other
+ * call while this one runs.  It holds device copies of all eight tensors and
+ * of lse plus three chunk-sized workspaces (one per internal compute stream).
+ * Errors as attn_bwd (argument errors before anything is enqueued; a
+ * stride_h other than D is ATTN_ERR_STRIDE).  The first call on a device
+ * creates the library's internal streams and events for that device; make
+ * it before any stream capture.
+ */
+size_t attn_bwd_host_buffer_size(int batch, int seqlen_q, int seqlen_k, int h_q, int h_k,
+                                 int head_dim, int chunks);
+int attn_bwd_host(const attn_tensor* q, const attn_tensor* k, const attn_tensor* v,
+                  const attn_tensor* o, const float* lse, const attn_tensor* dout,
+                  const attn_tensor* dq, const attn_tensor* dk, const attn_tensor* dv, int dtype,
+                  int batch, int seqlen_q, int seqlen_k, int h_q, int h_k, int head_dim,
+                  float scale, int causal, int deterministic, int chunks, void* device_buffer,
+                  size_t device_buffer_bytes, attn_stream_t stream);
 
 /*
  * The three stages of attn_bwd, callable one by one (same arguments, same
