@@ -37,6 +37,8 @@
 // drain to have read dQ out of TMEM.
 // Every mbarrier wait is bounded (see WaitCtl): on timeout the kernel records
 // the site in the status word and unwinds.
+#include <atomic>
+
 #include "common.cuh"
 
 namespace attn {
@@ -747,8 +749,13 @@ cudaError_t launch_t(const BwdParams& p, int dtype, cudaStream_t stream) {
   CUtensorMap tdq;
   if (!encode_tmap_f32_2d(&tdq, p.dqacc, p.ws_rows * p.h_q, D)) return cudaErrorInvalidValue;
   constexpr uint32_t smem = Smem<D>::kTotal;
-  static bool attr_done = false;
-  if (!attr_done) {
+  // Kernel attributes are per device: set (and check) them once on each.
+  constexpr int kMaxDevices = 64;
+  static std::atomic<bool> attr_done[kMaxDevices];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
+    return cudaErrorInvalidDevice;
+  if (!attr_done[dev].load(std::memory_order_acquire)) {
     cudaError_t e = cudaFuncSetAttribute(bwd_main_kernel<T, D>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
@@ -758,7 +765,7 @@ cudaError_t launch_t(const BwdParams& p, int dtype, cudaStream_t stream) {
     e = cudaFuncGetAttributes(&fa, bwd_main_kernel<T, D>);
     if (e != cudaSuccess) return e;
     if (fa.numRegs != static_cast<int>(kRegLaunch)) return cudaErrorInvalidConfiguration;
-    attr_done = true;
+    attr_done[dev].store(true, std::memory_order_release);
   }
   const int n_tiles = ceil_div(p.max_seqlen_k, BN);
   const int units = n_tiles * p.seq.batch * p.h_k;

@@ -12,6 +12,8 @@
 //
 // Both walk rows in [token][head] order so that each group of D/8 threads
 // reads or writes one contiguous 16-byte-per-thread head row.
+#include <atomic>
+
 #include "common.cuh"
 
 namespace attn {
@@ -200,14 +202,30 @@ __global__ void validate_cu_kernel(const int* cu_q, const int* cu_k, int batch, 
   }
 }
 
+// Blocks per SM of one kernel, looked up once per device (the first launch on a
+// device must not happen inside a stream capture).
+struct Occupancy {
+  static constexpr int kMaxDevices = 64;
+  std::atomic<int> per_sm[kMaxDevices];
+};
+
 // Grid-stride launches: one full wave (as many blocks as fit on every SM at once), so
 // no block starts late and runs in a half-empty second wave.
 template <typename K>
-inline int grid_for(int64_t work_threads, K kernel) {
+inline int grid_for(int64_t work_threads, K kernel, Occupancy& occ) {
+  int dev = 0;
   int per_sm = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, kThreads, 0) != cudaSuccess ||
-      per_sm < 1)
-    per_sm = 1;
+  const bool dev_ok =
+      cudaGetDevice(&dev) == cudaSuccess && dev >= 0 && dev < Occupancy::kMaxDevices;
+  if (dev_ok) per_sm = occ.per_sm[dev].load(std::memory_order_relaxed);
+  if (per_sm < 1) {
+    const cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel,
+                                                                        kThreads, 0);
+    if (e != cudaSuccess || per_sm < 1)
+      per_sm = 1;
+    else if (dev_ok)
+      occ.per_sm[dev].store(per_sm, std::memory_order_relaxed);
+  }
   const int64_t want = (work_threads + kThreads - 1) / kThreads;
   const int64_t cap = static_cast<int64_t>(num_sms()) * per_sm;
   return static_cast<int>(want < 1 ? 1 : (want > cap ? cap : want));
@@ -218,10 +236,13 @@ inline int grid_for(int64_t work_threads, K kernel) {
 template <typename T>
 static cudaError_t launch_pre_t(const BwdParams& p, cudaStream_t stream) {
   const int64_t work = p.ws_rows * p.h_q * (p.head_dim / 8);
+  static Occupancy occ64, occ128;
   if (p.head_dim == 64)
-    preprocess_kernel<T, 64><<<grid_for(work, preprocess_kernel<T, 64>), kThreads, 0, stream>>>(p);
+    preprocess_kernel<T, 64>
+        <<<grid_for(work, preprocess_kernel<T, 64>, occ64), kThreads, 0, stream>>>(p);
   else
-    preprocess_kernel<T, 128><<<grid_for(work, preprocess_kernel<T, 128>), kThreads, 0, stream>>>(p);
+    preprocess_kernel<T, 128>
+        <<<grid_for(work, preprocess_kernel<T, 128>, occ128), kThreads, 0, stream>>>(p);
   return cudaGetLastError();
 }
 
@@ -236,10 +257,13 @@ static cudaError_t launch_post_t(const BwdParams& p, cudaStream_t stream) {
                              : static_cast<int64_t>(p.seq.seqlen_q);
   const int64_t work = tokens * p.h_q * (p.head_dim / 8);
   if (work == 0) return cudaSuccess;
+  static Occupancy occ64, occ128;
   if (p.head_dim == 64)
-    postprocess_kernel<T, 64><<<grid_for(work, postprocess_kernel<T, 64>), kThreads, 0, stream>>>(p);
+    postprocess_kernel<T, 64>
+        <<<grid_for(work, postprocess_kernel<T, 64>, occ64), kThreads, 0, stream>>>(p);
   else
-    postprocess_kernel<T, 128><<<grid_for(work, postprocess_kernel<T, 128>), kThreads, 0, stream>>>(p);
+    postprocess_kernel<T, 128>
+        <<<grid_for(work, postprocess_kernel<T, 128>, occ128), kThreads, 0, stream>>>(p);
   return cudaGetLastError();
 }
 
@@ -253,12 +277,13 @@ static cudaError_t launch_zero_t(const TensorArg& t, int nseq, int rows_per_seq,
   const int64_t rows = (cu == nullptr) ? static_cast<int64_t>(nseq) * rows_per_seq : total_rows;
   const int64_t work = rows * heads * (head_dim / 8);
   if (work == 0) return cudaSuccess;
+  static Occupancy occ64, occ128;
   if (head_dim == 64)
-    zero_rows_kernel<T, 64><<<grid_for(work, zero_rows_kernel<T, 64>), kThreads, 0, stream>>>(
-        t, nseq, rows_per_seq, cu, total_rows, heads);
+    zero_rows_kernel<T, 64><<<grid_for(work, zero_rows_kernel<T, 64>, occ64), kThreads, 0,
+                              stream>>>(t, nseq, rows_per_seq, cu, total_rows, heads);
   else
-    zero_rows_kernel<T, 128><<<grid_for(work, zero_rows_kernel<T, 128>), kThreads, 0, stream>>>(
-        t, nseq, rows_per_seq, cu, total_rows, heads);
+    zero_rows_kernel<T, 128><<<grid_for(work, zero_rows_kernel<T, 128>, occ128), kThreads, 0,
+                               stream>>>(t, nseq, rows_per_seq, cu, total_rows, heads);
   return cudaGetLastError();
 }
 
