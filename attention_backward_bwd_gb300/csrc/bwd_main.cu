@@ -96,7 +96,8 @@ enum Bar : uint32_t {
   B_UNITFULL,                      // 2 slots: next work unit published by the producer
   B_UNITEMPTY = B_UNITFULL + 2,    // 2 slots: every consumer role has read it
   B_FINAL = B_UNITEMPTY + 2,
-  B_COUNT
+  B_FULLQ2,                        // 2 slots: second head-dim chunk of the Q tile (D = 128)
+  B_COUNT = B_FULLQ2 + kStages
 };
 
 template <int D>
@@ -186,11 +187,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int n_tiles = ceil_div(p.max_seqlen_k, BN);
   const int num_units = n_tiles * p.seq.batch * p.h_k;
   constexpr int kIsBf16 = Pack<T>::kIsBf16;
+  constexpr bool kSplitQ = D == 128;
 
   if (threadIdx.x == 0) {
     *abort_flag = 0;
     for (int s = 0; s < kStages; ++s) {
       mbar_init(bar(B_FULLQ + s), 1);
+      mbar_init(bar(B_FULLQ2 + s), 1);
       mbar_init(bar(B_FULLDO + s), 1);
       mbar_init(bar(B_EMPTY + s), 1);       // MMA commit
       mbar_init(bar(B_EMPTYDO + s), 1 + 4);  // MMA commit + the 4 dQ drain warps
@@ -294,12 +297,23 @@ __global__ void __launch_bounds__(kThreads, 1)
           // Q (+ LSE2) first: its stage is released after dK, the dO stage only
           // once the dQ drain of that iteration has read its staged rows
           if (use > 0 && !wait1(bar(B_EMPTY + s), (use - 1) & 1, ctl, 0xA0000002u)) break;
-          mbar_expect_tx(bar(B_FULLQ + s), L::kTile + BM * 4);
+          // With D = 128 the two 64-column chunks of Q complete separate barriers:
+          // the first half of S^T needs only the first (and the softmax only LSE2).
+          if (kSplitQ) {
+            mbar_expect_tx(bar(B_FULLQ + s), kChunk + BM * 4);
+            tma_load_4d(sb + L::kQ + s * L::kTile, &tmQ, bar(B_FULLQ + s), 0, qrow, h, bq);
+            bulk_load(sb + L::kLSE + s * BM * 4, p.lse2 + ws, BM * 4, bar(B_FULLQ + s));
+            mbar_expect_tx(bar(B_FULLQ2 + s), kChunk);
+            tma_load_4d(sb + L::kQ + s * L::kTile + kChunk, &tmQ, bar(B_FULLQ2 + s), 64, qrow, h,
+                        bq);
+          } else {
+            mbar_expect_tx(bar(B_FULLQ + s), L::kTile + BM * 4);
 #pragma unroll
-          for (int c = 0; c < D / 64; ++c)
-            tma_load_4d(sb + L::kQ + s * L::kTile + c * kChunk, &tmQ, bar(B_FULLQ + s), c * 64,
-                        qrow, h, bq);
-          bulk_load(sb + L::kLSE + s * BM * 4, p.lse2 + ws, BM * 4, bar(B_FULLQ + s));
+            for (int c = 0; c < D / 64; ++c)
+              tma_load_4d(sb + L::kQ + s * L::kTile + c * kChunk, &tmQ, bar(B_FULLQ + s), c * 64,
+                          qrow, h, bq);
+            bulk_load(sb + L::kLSE + s * BM * 4, p.lse2 + ws, BM * 4, bar(B_FULLQ + s));
+          }
           if (use > 0 && !wait1(bar(B_EMPTYDO + s), (use - 1) & 1, ctl, 0xA0000006u)) {
             ++it;  // the Q copies of this iteration are in flight
             do_pending_skipped = true;
@@ -321,6 +335,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t last = (it - 1 - s) / kStages;  // uses of stage (it-1-s) % kStages
         const uint32_t st = (it - 1 - s) % kStages;
         wait1(bar(B_FULLQ + st), last & 1, ctl, 0xA0000004u, false);
+        if (kSplitQ) wait1(bar(B_FULLQ2 + st), last & 1, ctl, 0xA0000007u, false);
         if (!(s == 0 && do_pending_skipped))
           wait1(bar(B_FULLDO + st), last & 1, ctl, 0xA0000005u, false);
       }
@@ -336,14 +351,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr uint32_t kIdKV = idesc_f16(kIsBf16, 0, 1, BN, D);
       constexpr uint32_t kIdDQ = idesc_f16(kIsBf16, 1, 1, BM, D);
       // S^T = K Q^T   (M = keys, N = queries, K = head dim; both K-major)
-      auto issue_s = [&](uint32_t sQ) {
+      auto issue_s = [&](uint32_t sQ, uint32_t st, uint32_t ph) -> bool {
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
+          if (kSplitQ && kk == 4) {  // the second head-dim chunk of Q lands separately
+            if (!wait1(bar(B_FULLQ2 + st), ph, ctl, 0xA000001Bu)) return false;
+            tc_fence_after();
+          }
           const uint32_t koff = (kk >> 2) * kChunk + (kk & 3) * 32;
           mma_ss(tmem + TM_S, sdesc_sw128(sb + L::kK + koff, 16, 1024),
                  sdesc_sw128(sQ + koff, 16, 1024), kIdS, kk > 0);
         }
         tc_commit(bar(B_SFULL));
+        return true;
       };
       // S^T of iteration `it` overwrites the packed P^T of iteration it - 1:
       // dV must have completed and the dS phase must have read it
@@ -364,7 +384,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!wait1(bar(B_FULLQ + s), (it / kStages) & 1, ctl, 0xA0000013u)) goto mma_exit;
           if (it > 0 && !wait_p_consumed(it - 1)) goto mma_exit;
           tc_fence_after();
-          issue_s(sb + L::kQ + s * L::kTile);
+          if (!issue_s(sb + L::kQ + s * L::kTile, s, (it / kStages) & 1)) goto mma_exit;
         }
         for (int j = 0; j < un.n_iters; ++j, ++it) {
           const uint32_t s = it % kStages;
@@ -404,7 +424,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!wait1(bar(B_FULLQ + s1), ((it + 1) / kStages) & 1, ctl, 0xA000001Au))
               goto mma_exit;
             tc_fence_after();
-            issue_s(sb + L::kQ + s1 * L::kTile);
+            if (!issue_s(sb + L::kQ + s1 * L::kTile, s1, ((it + 1) / kStages) & 1)) goto mma_exit;
           }
           if (!wait1(bar(B_DSREADY), it & 1, ctl, 0xA0000018u)) goto mma_exit;
           tc_fence_after();
