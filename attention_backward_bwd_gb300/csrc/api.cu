@@ -296,6 +296,8 @@ int run_stages(int stages, const Prepared& pr, cudaStream_t stream) {
     if (e == cudaErrorInvalidValue)
       return fail(ATTN_ERR_CUDA, "main kernel: TMA descriptor encoding or launch failed");
     if (e != cudaSuccess) return cuda_fail(e, "main kernel launch");
+    e = launch_zero_kv_of_empty_q(p, pr.dtype, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "dK/dV clear of query-less sequences");
   }
   if (stages & kPost) {
     e = launch_postprocess(p, pr.dtype, stream);

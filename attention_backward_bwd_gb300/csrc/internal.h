@@ -92,6 +92,8 @@ cudaError_t launch_preprocess(const BwdParams& p, int dtype, cudaStream_t stream
 cudaError_t launch_postprocess(const BwdParams& p, int dtype, cudaStream_t stream);
 cudaError_t launch_bwd_main(const BwdParams& p, int dtype, cudaStream_t stream);
 cudaError_t launch_fwd(const FwdParams& p, int dtype, cudaStream_t stream);
+// Varlen: dK = dV = 0 on the key rows of sequences that have no query rows.
+cudaError_t launch_zero_kv_of_empty_q(const BwdParams& p, int dtype, cudaStream_t stream);
 cudaError_t launch_zero_rows(const TensorArg& t, int dtype, int nseq, int rows_per_seq,
                              const int* cu, int total_rows, int heads, int head_dim,
                              cudaStream_t stream);

@@ -84,7 +84,8 @@ class Inputs:
     do: torch.Tensor
     cu_seqlens_q: Optional[torch.Tensor] = None  # int32 [n_seqs + 1]
     cu_seqlens_k: Optional[torch.Tensor] = None
-    lengths: Optional[list] = None
+    lengths: Optional[list] = None      # query lengths (varlen)
+    lengths_k: Optional[list] = None    # key lengths (varlen)
 
 
 def draw_lengths(g: torch.Generator, n: int, lo: int, hi: int) -> list:
@@ -99,28 +100,35 @@ def cu_from_lengths(lengths) -> torch.Tensor:
     return torch.tensor(cu, dtype=torch.int32)
 
 
-def make_inputs(w: Workload, lengths: Optional[list] = None) -> Inputs:
-    """Draw the inputs of workload ``w`` from its seed (N(0,1) entries)."""
+def make_inputs(w: Workload, lengths: Optional[list] = None,
+                lengths_k: Optional[list] = None) -> Inputs:
+    """Draw the inputs of workload ``w`` from its seed (N(0,1) entries).
+
+    Varlen: ``lengths`` are the query lengths (drawn if not given) and
+    ``lengths_k`` the key lengths (default: the same, self-attention)."""
     g = torch.Generator("cpu").manual_seed(w.seed)
     dt = DTYPES[w.dtype]
     if w.varlen:
         if lengths is None:
             lengths = draw_lengths(g, w.n_seqs, w.len_lo, w.len_hi)
-        total = int(sum(lengths))
-        qs, ks = (total, w.h_q, w.head_dim), (total, w.h_k, w.head_dim)
+        if lengths_k is None:
+            lengths_k = lengths
+        assert len(lengths_k) == len(lengths)
+        qs = (int(sum(lengths)), w.h_q, w.head_dim)
+        ks = (int(sum(lengths_k)), w.h_k, w.head_dim)
         cu = cu_from_lengths(lengths)
+        cu_k = cu_from_lengths(lengths_k)
     else:
         qs = (w.batch, w.seqlen_q, w.h_q, w.head_dim)
         ks = (w.batch, w.seqlen_k, w.h_k, w.head_dim)
-        cu = None
+        cu = cu_k = None
     q = torch.randn(qs, generator=g)
     k = torch.randn(ks, generator=g)
     v = torch.randn(ks, generator=g)
     do = torch.randn(qs, generator=g)
     if w.do_scale != 1.0:
         do = do * w.do_scale
-    return Inputs(q.to(dt), k.to(dt), v.to(dt), do.to(dt), cu, cu if cu is None else cu.clone(),
-                  lengths)
+    return Inputs(q.to(dt), k.to(dt), v.to(dt), do.to(dt), cu, cu_k, lengths, lengths_k)
 
 
 def small(name: str, batch: int, h_q: int, h_k: int, sq: int, sk: int, d: int, dtype: str,

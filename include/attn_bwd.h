@@ -19,7 +19,11 @@
  * and head dimensions; the head dimension is contiguous (stride 1).  In varlen
  * mode (cu_seqlens given) tensors are packed [total, H, D], stride_b is
  * ignored, and seqlen_q / seqlen_k are the TOTAL packed row counts while
- * max_seqlen_q / max_seqlen_k bound the per-sequence lengths.
+ * max_seqlen_q / max_seqlen_k bound the per-sequence lengths.  cu_seqlens_q
+ * and cu_seqlens_k may differ (cross attention: sequence b has
+ * cu_q[b+1]-cu_q[b] queries and cu_k[b+1]-cu_k[b] keys, causal masks aligned
+ * bottom-right per sequence); a sequence with keys but no queries gets
+ * dK = dV = 0, one with queries but no keys dQ = 0.
  * LSE is fp32, natural log: [B, H_q, Sq] contiguous, or [H_q, total_q] in
  * varlen mode (flash-attention's softmax_lse).
  *

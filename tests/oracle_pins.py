@@ -240,6 +240,34 @@ def pin_varlen_matches_padded(o_mod):
         assert _rel(r["LSE"][:, sl], rb["LSE"][0]) < 1e-13
 
 
+def pin_cross_varlen_matches_padded(o_mod):
+    """Packed sequences whose query and key lengths differ (cross attention,
+    including a sequence with keys but no queries and one with queries but no
+    keys): each sequence's gradients equal those of the same sequence alone,
+    and the query-less sequence has dK = dV = 0."""
+    rng = np.random.default_rng(6)
+    lq, lk = [3, 0, 5, 2], [6, 4, 2, 0]
+    cq, ck = np.cumsum([0] + lq), np.cumsum([0] + lk)
+    q, do = rng.standard_normal((cq[-1], 4, 8)), rng.standard_normal((cq[-1], 4, 8))
+    k, v = rng.standard_normal((ck[-1], 2, 8)), rng.standard_normal((ck[-1], 2, 8))
+    for causal in (False, True):
+        r = o_mod.mha_backward(q, k, v, do, 0.3, causal, cq, ck)
+        for b in range(len(lq)):
+            qs, ks = slice(cq[b], cq[b + 1]), slice(ck[b], ck[b + 1])
+            if lq[b] == 0:
+                assert np.abs(r["dK"][ks]).max(initial=0.0) == 0
+                assert np.abs(r["dV"][ks]).max(initial=0.0) == 0
+                continue
+            rb = o_mod.mha_backward(q[None, qs], k[None, ks], v[None, ks], do[None, qs], 0.3,
+                                    causal)
+            assert _rel(r["dQ"][qs], rb["dQ"][0]) < 1e-13
+            if lk[b] > 0:
+                assert _rel(r["dK"][ks], rb["dK"][0]) < 1e-13
+                assert _rel(r["dV"][ks], rb["dV"][0]) < 1e-13
+            else:
+                assert np.abs(r["dQ"][qs]).max() == 0  # no keys: dQ = 0
+
+
 def pin_empty_cases(o_mod):
     # seqlen_q == 0: dK = dV = 0
     q, do = np.zeros((1, 0, 2, 4)), np.zeros((1, 0, 2, 4))
@@ -321,4 +349,5 @@ def pin_group_rows_autograd(o_mod):
 ALL_PINS = [pin_sympy_exact, pin_finite_differences, pin_finite_differences_varlen, pin_delta_identity,
             pin_equal_value_rows, pin_causal_row0, pin_causal_bottom_right, pin_zero_query,
             pin_single_key, pin_key_shift_and_permutation, pin_torch_autograd,
-            pin_varlen_matches_padded, pin_empty_cases, pin_group_rows_autograd]
+            pin_varlen_matches_padded, pin_cross_varlen_matches_padded, pin_empty_cases,
+            pin_group_rows_autograd]

@@ -23,7 +23,8 @@ def run_gpu(w, x, deterministic=False, o=None, lse=None):
     (q, k, v, do), cu_q, cu_k = to_dev(x)
     mq = mk = None
     if cu_q is not None:
-        mq = mk = max(x.lengths) if x.lengths else 0
+        mq = max(x.lengths) if x.lengths else 0
+        mk = max(x.lengths_k) if x.lengths_k else 0
     if o is None:
         o, lse = ab.attn_fwd(q, k, v, causal=w.causal, cu_seqlens_q=cu_q, cu_seqlens_k=cu_k,
                              max_seqlen_q=mq, max_seqlen_k=mk)
@@ -113,6 +114,55 @@ def test_varlen_deterministic_d64():
     w = synth.Workload("vl64", 0, 2, 2, 0, 0, 64, "fp16", False, 82, n_seqs=3, len_lo=1,
                        len_hi=300, deterministic=True)
     check(w, synth.make_inputs(w, lengths=lens), deterministic=True)
+
+
+CROSS = [
+    # query lengths, key lengths, Hq, Hk, D, dtype, causal, deterministic
+    ([300, 0, 17, 129, 5, 640], [200, 150, 0, 513, 5, 64], 4, 2, 128, "bf16", True, False),
+    ([300, 0, 17, 129, 5, 640], [200, 150, 0, 513, 5, 64], 4, 2, 128, "bf16", False, False),
+    ([1000, 64, 0, 257], [257, 700, 333, 0], 2, 2, 64, "fp16", True, False),
+    ([300, 0, 17, 129, 5, 640], [200, 150, 0, 513, 5, 64], 8, 2, 128, "bf16", True, True),
+]
+
+
+@pytest.mark.parametrize("case", CROSS, ids=[f"cross{i}" for i in range(len(CROSS))])
+def test_cross_attention_varlen(case):
+    """Packed sequences whose query and key lengths differ (cu_seqlens_q !=
+    cu_seqlens_k): causal masks align bottom-right per sequence, a sequence
+    with keys but no queries gets dK = dV = 0 exactly, one with queries but no
+    keys gets dQ = 0.  Outputs start as NaN so an unwritten row shows."""
+    lq, lk, hq, hk, d, dt, causal, det = case
+    w = synth.Workload("cross", 0, hq, hk, 0, 0, d, dt, causal, 83 + len(lq), n_seqs=len(lq),
+                       len_lo=0, len_hi=1000, deterministic=det)
+    x = synth.make_inputs(w, lengths=lq, lengths_k=lk)
+    (q, k, v, do), cu_q, cu_k = to_dev(x)
+    mq, mk = max(lq), max(lk)
+    o, lse = ab.attn_fwd(q, k, v, causal=causal, cu_seqlens_q=cu_q, cu_seqlens_k=cu_k,
+                         max_seqlen_q=mq, max_seqlen_k=mk)
+    runs = []
+    for _ in range(2 if det else 1):
+        outs = [torch.full_like(t, float("nan")) for t in (q, k, v)]
+        ab.attn_bwd(q, k, v, o, lse, do, causal=causal, cu_seqlens_q=cu_q, cu_seqlens_k=cu_k,
+                    max_seqlen_q=mq, max_seqlen_k=mk, deterministic=det, dq=outs[0],
+                    dk=outs[1], dv=outs[2])
+        ab.check_device_status()
+        runs.append(outs)
+    if det:
+        for a, b in zip(*runs):
+            assert torch.equal(a, b)
+    dq, dk, dv = runs[0]
+    for t in (dq, dk, dv):
+        assert not t.isnan().any()
+    cq, ck = np.cumsum([0] + lq), np.cumsum([0] + lk)
+    for b in range(len(lq)):
+        if lq[b] == 0:
+            assert (dk[ck[b]:ck[b + 1]] == 0).all() and (dv[ck[b]:ck[b + 1]] == 0).all()
+        if lk[b] == 0:
+            assert (dq[cq[b]:cq[b + 1]] == 0).all()
+    ref = oracle_grads(w, x)
+    floor = float(np.abs(ref["dV"]).max())
+    for name, got in (("dQ", dq), ("dK", dk), ("dV", dv)):
+        assert_close(f"cross {name}", got, ref[name], floor=floor)
 
 
 def test_deterministic_is_bitwise_repeatable():

@@ -31,6 +31,8 @@ MUTANTS = {
     "gqa_no_group_sum": ("_put(dk, ks, hkv, r[\"dK\"], add=True)", "_put(dk, ks, hkv, r[\"dK\"])"),
     "delta_from_output_axis": ("np.asarray(do, dtype=np.float64)).sum(axis=-1)", "np.asarray(do, dtype=np.float64)).sum(axis=0)"),
     "softmax_no_max_shift_sign": ("np.exp(s - m[:, None])", "np.exp(s + m[:, None])"),
+    "varlen_keys_by_query_offsets": ("yield b, (slice(cq[b], cq[b + 1]),), (slice(ck[b], ck[b + 1]),)",
+                                     "yield b, (slice(cq[b], cq[b + 1]),), (slice(cq[b], cq[b + 1]),)"),
     # the row-sampled group backward
     "rows_drop_delta": ("            ds = p * (dp - delta[:, None])", "            ds = p * dp"),
     "rows_dv_from_ds": ("dv += p[:, k_rows].T @ doh[i0:i1]", "dv += ds[:, k_rows].T @ doh[i0:i1]"),
