@@ -27,8 +27,17 @@ Sources (page title, section):
     varlen tensors are packed [total, H, D] with per-sequence offsets from
     cu_seqlens; LSE is natural-log (the preprocess makes the log2 copy).
 
+  * same CK page, the mask set-up of ``mha_bwd``: a local (sliding-window)
+    mask is a window (left, right) around each query's aligned key, -1 meaning
+    unbounded on that side, in the same bottom-right alignment; causal is the
+    window (-1, 0).
+
 Readings where the pages leave a point open:
   * causal with Sq != Sk: key j is allowed for query i iff j <= i + (Sk - Sq).
+  * window (left, right): with off = Sk - Sq, key j is allowed for query i iff
+    j >= i + off - left (when left >= 0) and j <= i + off + right (when
+    right >= 0); causal together with a window keeps the window's left side
+    and bounds the right side at 0.
   * a query row with no allowed key: O = 0, LSE = +inf, dQ = 0, and it adds
     nothing to dK or dV.
   * scale defaults to 1/sqrt(D).
@@ -43,23 +52,39 @@ from __future__ import annotations
 import numpy as np
 
 
-def allowed_mask(sq: int, sk: int, causal: bool) -> np.ndarray:
+def _window_sides(causal: bool, window) -> tuple:
+    """(left, right) of the mask, -1 = unbounded; causal bounds the right at 0."""
+    left, right = (-1, -1) if window is None else (int(window[0]), int(window[1]))
+    if causal:
+        right = 0
+    return left, right
+
+
+def allowed_pairs(i, j, sq: int, sk: int, causal: bool, window=None) -> np.ndarray:
+    """True where query i may attend key j (i, j broadcastable index arrays)."""
+    left, right = _window_sides(causal, window)
+    ok = np.ones(np.broadcast_shapes(np.shape(i), np.shape(j)), dtype=bool)
+    if right >= 0:
+        ok &= j <= i + (sk - sq) + right
+    if left >= 0:
+        ok &= j >= i + (sk - sq) - left
+    return ok
+
+
+def allowed_mask(sq: int, sk: int, causal: bool, window=None) -> np.ndarray:
     """Boolean [sq, sk]: True where query i may attend key j."""
-    if not causal:
-        return np.ones((sq, sk), dtype=bool)
-    i = np.arange(sq)[:, None]
-    j = np.arange(sk)[None, :]
-    return j <= i + (sk - sq)
+    return allowed_pairs(np.arange(sq)[:, None], np.arange(sk)[None, :], sq, sk, causal, window)
 
 
-def head_forward(q: np.ndarray, k: np.ndarray, v: np.ndarray, scale: float, causal: bool):
+def head_forward(q: np.ndarray, k: np.ndarray, v: np.ndarray, scale: float, causal: bool,
+                 window=None):
     """Forward of one head.  q [Sq, D], k and v [Sk, D], float64.
 
     Returns (O [Sq, D], LSE [Sq] natural log, P [Sq, Sk]).
     """
     sq, sk = q.shape[0], k.shape[0]
     s = scale * (q @ k.T)
-    allowed = allowed_mask(sq, sk, causal)
+    allowed = allowed_mask(sq, sk, causal, window)
     s = np.where(allowed, s, -np.inf)
     any_key = allowed.any(axis=1) if sk > 0 else np.zeros(sq, dtype=bool)
     m = np.where(any_key, s.max(axis=1, initial=-np.inf), 0.0)
@@ -71,12 +96,12 @@ def head_forward(q: np.ndarray, k: np.ndarray, v: np.ndarray, scale: float, caus
     return o, lse, p
 
 
-def head_backward(q, k, v, do, scale: float, causal: bool):
+def head_backward(q, k, v, do, scale: float, causal: bool, window=None):
     """Gradient of one head, by the definition.  All arrays float64.
 
     Returns a dict with O, LSE, P, dP, Delta (= rowsum(P * dP)), dS, dQ, dK, dV.
     """
-    o, lse, p = head_forward(q, k, v, scale, causal)
+    o, lse, p = head_forward(q, k, v, scale, causal, window)
     dv = p.T @ do
     dp = do @ v.T
     delta = (p * dp).sum(axis=1)
@@ -130,7 +155,7 @@ def _put(x, sel, h, val, add=False):
 
 
 def mha_forward(q, k, v, scale=None, causal=False, cu_seqlens_q=None, cu_seqlens_k=None,
-                heads=None):
+                heads=None, window=None):
     """Multi-head forward.  q [B,Sq,H,D] (or packed [total,H,D]), k/v with H_k heads.
 
     Returns (O like q, LSE [B,H,Sq] or [H,total_q]).  ``heads`` restricts the
@@ -149,7 +174,7 @@ def mha_forward(q, k, v, scale=None, causal=False, cu_seqlens_q=None, cu_seqlens
     for b, qs, ks in _sequences(q, k, cu_seqlens_q, cu_seqlens_k):
         for h in hs:
             oh, lh, _ = head_forward(_take(q, qs, h), _take(k, ks, h // g), _take(v, ks, h // g),
-                                     scale, causal)
+                                     scale, causal, window)
             _put(o, qs, h, oh)
             if cu_seqlens_q is None:
                 lse[b, h, :] = lh
@@ -159,7 +184,7 @@ def mha_forward(q, k, v, scale=None, causal=False, cu_seqlens_q=None, cu_seqlens
 
 
 def mha_backward(q, k, v, do, scale=None, causal=False, cu_seqlens_q=None, cu_seqlens_k=None,
-                 kv_heads=None):
+                 kv_heads=None, window=None):
     """Multi-head backward by the definition, with GQA group sums.
 
     Returns dict(dQ, dK, dV, O, LSE, Delta) in the input layouts (LSE/Delta as
@@ -181,7 +206,7 @@ def mha_backward(q, k, v, do, scale=None, causal=False, cu_seqlens_q=None, cu_se
         for hkv in kvs:
             for h in range(hkv * g, hkv * g + g):
                 r = head_backward(_take(q, qs, h), _take(k, ks, hkv), _take(v, ks, hkv),
-                                  _take(do, qs, h), scale, causal)
+                                  _take(do, qs, h), scale, causal, window)
                 _put(dq, qs, h, r["dQ"])
                 _put(o, qs, h, r["O"])
                 _put(dk, ks, hkv, r["dK"], add=True)
@@ -196,7 +221,7 @@ def mha_backward(q, k, v, do, scale=None, causal=False, cu_seqlens_q=None, cu_se
 
 
 def group_backward_rows(q, k, v, do, b: int, g: int, q_rows, k_rows, scale=None,
-                        causal=False, block: int = 512):
+                        causal=False, block: int = 512, window=None):
     """Exact gradients at selected rows of one (sequence, kv head) group, for
     problems too large for ``mha_backward`` (padded [B,S,H,D] inputs only).
 
@@ -226,7 +251,7 @@ def group_backward_rows(q, k, v, do, b: int, g: int, q_rows, k_rows, scale=None,
             i1 = min(sq, i0 + block)
             ii = np.arange(i0, i1)[:, None]
             jj = np.arange(sk)[None, :]
-            allowed = (jj <= ii + (sk - sq)) if causal else np.ones((i1 - i0, sk), dtype=bool)
+            allowed = allowed_pairs(ii, jj, sq, sk, causal, window)
             s = np.where(allowed, scale * (qh[i0:i1] @ kg.T), -np.inf)
             any_key = allowed.any(axis=1)
             m = np.where(any_key, s.max(axis=1), 0.0)

@@ -14,6 +14,11 @@ mistake) and raises ``AssertionError`` when the fact does not hold.  The facts:
 * Sk = 1  =>  P = 1, dQ = dK = 0, dV = sum_i dO_i;
 * shift of every key row by one vector leaves dQ, dK, dV unchanged
   (rows of dS sum to zero);  permuting keys permutes dK/dV rows;
+* local windows: (-1, -1) is no mask, (-1, 0) is causal, a window wider than
+  both lengths is no mask; (0, 0) with Sq != Sk makes query i see only key
+  i + Sk - Sq (O_i = V_{i+Sk-Sq}, dQ = dK = 0, dV = dO moved to those rows);
+  a brute-force forward that writes the window as a distance band agrees;
+  finite differences hold under a window;
 * an independent fp64 torch-autograd run of softmax(Q K^T s) V agrees to 1e-10,
   and its logsumexp gives LSE; the same run pins the row-sampled group
   backward used at full problem sizes.
@@ -93,6 +98,82 @@ def pin_finite_differences_varlen(o_mod):
             g = _fd_grad(o_mod, name, q, k, v, do, 0.6, causal, cu)
             err = _rel(r[key], g)
             assert err < 1e-6, f"varlen finite differences {key} causal={causal}: {err}"
+
+
+def _brute_forward(q, k, v, scale, off, left, right):
+    """Softmax attention of one head with plain loops; key j is inside the band
+    of query i when its distance d = j - i - off lies in [-left, right] (a side
+    given as -1 is open)."""
+    sq, sk, d = q.shape[0], k.shape[0], v.shape[1]
+    o = np.zeros((sq, d))
+    for i in range(sq):
+        keys = [j for j in range(sk)
+                if (left < 0 or j - i - off >= -left) and (right < 0 or j - i - off <= right)]
+        if not keys:
+            continue
+        w = [np.exp(scale * float(np.dot(q[i], k[j]))) for j in keys]
+        tot = sum(w)
+        for wj, j in zip(w, keys):
+            o[i] += (wj / tot) * v[j]
+    return o
+
+
+def pin_window(o_mod):
+    rng = np.random.default_rng(31)
+    # special cases of the window
+    for sq, sk in ((4, 4), (3, 6), (6, 3)):
+        q, k, v, do = _rand(sq, 5, rng=rng), _rand(sk, 5, rng=rng), _rand(sk, 5, rng=rng), \
+            _rand(sq, 5, rng=rng)
+        plain = o_mod.head_backward(q, k, v, do, 0.4, False)
+        causal = o_mod.head_backward(q, k, v, do, 0.4, True)
+        for win, ref in (((-1, -1), plain), ((sq + sk, sq + sk), plain), ((-1, 0), causal)):
+            r = o_mod.head_backward(q, k, v, do, 0.4, False, win)
+            for key in ("dQ", "dK", "dV", "O"):
+                assert _rel(r[key], ref[key]) < 1e-14, (sq, sk, win, key)
+    # window (0, 0): one key per query, at distance Sk - Sq
+    sq, sk = 4, 7
+    q, k, v, do = _rand(sq, 3, rng=rng), _rand(sk, 3, rng=rng), _rand(sk, 3, rng=rng), \
+        _rand(sq, 3, rng=rng)
+    r = o_mod.head_backward(q, k, v, do, 0.9, False, (0, 0))
+    assert _rel(r["O"], v[sk - sq:]) < 1e-14
+    assert np.abs(r["dQ"]).max() < 1e-13 and np.abs(r["dK"]).max() < 1e-13
+    dv = np.zeros_like(v)
+    dv[sk - sq:] = do
+    assert _rel(r["dV"], dv) < 1e-14
+    # brute force, bands of several shapes, Sq = Sk, Sq < Sk and Sq > Sk
+    for sq, sk, left, right in ((6, 6, 2, 1), (4, 9, 3, 0), (9, 4, 1, -1), (5, 8, -1, 2)):
+        q, k, v = _rand(sq, 4, rng=rng), _rand(sk, 4, rng=rng), _rand(sk, 4, rng=rng)
+        o, _, _ = o_mod.head_forward(q, k, v, 0.5, False, (left, right))
+        assert _rel(o, _brute_forward(q, k, v, 0.5, sk - sq, left, right)) < 1e-12, \
+            (sq, sk, left, right)
+    # causal together with a left window is the band [-left, 0]
+    q, k, v = _rand(7, 4, rng=rng), _rand(9, 4, rng=rng), _rand(9, 4, rng=rng)
+    o, _, _ = o_mod.head_forward(q, k, v, 0.5, True, (2, -1))
+    assert _rel(o, _brute_forward(q, k, v, 0.5, 2, 2, 0)) < 1e-12
+
+
+def pin_finite_differences_window(o_mod):
+    rng = np.random.default_rng(55)
+    for sq, sk, win, causal in ((5, 5, (1, 1), False), (3, 6, (2, 0), False), (6, 4, (1, -1), True)):
+        q, k, v = _rand(1, sq, 2, 4, rng=rng), _rand(1, sk, 1, 4, rng=rng), \
+            _rand(1, sk, 1, 4, rng=rng)
+        do = _rand(1, sq, 2, 4, rng=rng)
+        r = o_mod.mha_backward(q, k, v, do, 0.6, causal, window=win)
+        arrs = {"q": q, "k": k, "v": v}
+        for name, key in (("q", "dQ"), ("k", "dK"), ("v", "dV")):
+            x = arrs[name]
+            g = np.zeros_like(x)
+            it = np.nditer(x, flags=["multi_index"])
+            for _ in it:
+                idx = it.multi_index
+                old = x[idx]
+                x[idx] = old + 1e-6
+                lp = float((o_mod.mha_forward(q, k, v, 0.6, causal, window=win)[0] * do).sum())
+                x[idx] = old - 1e-6
+                lm = float((o_mod.mha_forward(q, k, v, 0.6, causal, window=win)[0] * do).sum())
+                x[idx] = old
+                g[idx] = (lp - lm) / 2e-6
+            assert _rel(r[key], g) < 1e-6, (sq, sk, win, causal, key)
 
 
 def pin_delta_identity(o_mod):
@@ -344,10 +425,25 @@ def pin_group_rows_autograd(o_mod):
                     dv_ref += dv_t
                 assert _rel(dk, dk_ref[k_rows]) < 1e-10
                 assert _rel(dv, dv_ref[k_rows]) < 1e-10
+    # under a window, against the full backward (pinned under windows by pin_window)
+    b, hq, hk, sq, sk, d = 1, 4, 2, 13, 10, 8
+    q, k, v = (rng.standard_normal((b, sq, hq, d)), rng.standard_normal((b, sk, hk, d)),
+               rng.standard_normal((b, sk, hk, d)))
+    do = rng.standard_normal((b, sq, hq, d))
+    for win, causal in (((3, 1), False), ((2, -1), True)):
+        full = o_mod.mha_backward(q, k, v, do, 0.3, causal, window=win)
+        q_rows, k_rows = [0, 5, sq - 1], [0, 4, sk - 1]
+        for g in range(hk):
+            dq, dk, dv = o_mod.group_backward_rows(q, k, v, do, 0, g, q_rows, k_rows, 0.3, causal,
+                                                   block=4, window=win)
+            for hh in range(hq // hk):
+                assert _rel(dq[hh], full["dQ"][0, q_rows, g * (hq // hk) + hh]) < 1e-12
+            assert _rel(dk, full["dK"][0, k_rows, g]) < 1e-12
+            assert _rel(dv, full["dV"][0, k_rows, g]) < 1e-12
 
 
 ALL_PINS = [pin_sympy_exact, pin_finite_differences, pin_finite_differences_varlen, pin_delta_identity,
             pin_equal_value_rows, pin_causal_row0, pin_causal_bottom_right, pin_zero_query,
             pin_single_key, pin_key_shift_and_permutation, pin_torch_autograd,
             pin_varlen_matches_padded, pin_cross_varlen_matches_padded, pin_empty_cases,
-            pin_group_rows_autograd]
+            pin_group_rows_autograd, pin_window, pin_finite_differences_window]

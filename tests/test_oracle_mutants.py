@@ -24,8 +24,11 @@ MUTANTS = {
     "dv_untransposed": ("dv = p.T @ do", "dv = p @ do"),
     "dp_wrong_operand": ("dp = do @ v.T", "dp = do @ k.T"),
     "delta_axis": ("delta = (p * dp).sum(axis=1)", "delta = (p * dp).mean(axis=1)"),
-    "causal_direction": ("return j <= i + (sk - sq)", "return j >= i"),
-    "causal_top_left": ("return j <= i + (sk - sq)", "return j <= i"),
+    "causal_direction": ("ok &= j <= i + (sk - sq) + right", "ok &= j >= i + (sk - sq) + right"),
+    "causal_top_left": ("ok &= j <= i + (sk - sq) + right", "ok &= j <= i + right"),
+    "window_left_sign": ("ok &= j >= i + (sk - sq) - left", "ok &= j >= i + (sk - sq) + left"),
+    "window_left_top_left": ("ok &= j >= i + (sk - sq) - left", "ok &= j >= i - left"),
+    "window_left_strict": ("ok &= j >= i + (sk - sq) - left", "ok &= j > i + (sk - sq) - left"),
     "lse_log2": ("m + np.log(np.where(any_key, ell, 1.0))", "m + np.log2(np.where(any_key, ell, 1.0))"),
     "gqa_head_map_fwd": ("_take(k, ks, h // g), _take(v, ks, h // g)", "_take(k, ks, h % hk), _take(v, ks, h % hk)"),
     "gqa_no_group_sum": ("_put(dk, ks, hkv, r[\"dK\"], add=True)", "_put(dk, ks, hkv, r[\"dK\"])"),
@@ -36,7 +39,8 @@ MUTANTS = {
     # the row-sampled group backward
     "rows_drop_delta": ("            ds = p * (dp - delta[:, None])", "            ds = p * dp"),
     "rows_dv_from_ds": ("dv += p[:, k_rows].T @ doh[i0:i1]", "dv += ds[:, k_rows].T @ doh[i0:i1]"),
-    "rows_causal_offset": ("allowed = (jj <= ii + (sk - sq))", "allowed = (jj <= ii)"),
+    "rows_window_dropped": ("allowed = allowed_pairs(ii, jj, sq, sk, causal, window)",
+                            "allowed = allowed_pairs(ii, jj, sq, sk, causal)"),
     "rows_unnormalised": ("p = np.where(allowed, np.exp(s - lse[:, None]), 0.0)",
                           "p = np.where(allowed, np.exp(s - m[:, None]), 0.0)"),
 }
