@@ -46,7 +46,8 @@ _lock = threading.Lock()
 
 EXPORTS = ("attn_fwd", "attn_bwd", "attn_bwd_preprocess", "attn_bwd_main", "attn_bwd_postprocess",
            "attn_bwd_workspace_size", "attn_bwd_workspace_layout", "attn_bwd_noalloc",
-           "attn_bwd_host", "attn_bwd_host_buffer_size", "attn_check_device_status",
+           "attn_bwd_host", "attn_bwd_host_buffer_size", "attn_bwd_local", "attn_fwd_local",
+           "attn_check_device_status",
            "attn_set_wait_timeout_ns", "attn_last_error", "attn_version", "attn_diag_mma",
            "attn_diag_wait_timeout", "attn_diag_exp2")
 
@@ -65,6 +66,11 @@ def lib() -> ctypes.CDLL:
         L.attn_fwd.argtypes = [_T, _T, _T, _T, _P, _I, _I, _I, _I, _I, _I, _I, ctypes.c_float, _I,
                                _P, _P, _I, _I, _P]
         L.attn_fwd.restype = _I
+        L.attn_fwd_local.argtypes = [_T, _T, _T, _T, _P, _I, _I, _I, _I, _I, _I, _I,
+                                     ctypes.c_float, _I, _P, _P, _I, _I, _I, _I, _P]
+        L.attn_fwd_local.restype = _I
+        L.attn_bwd_local.argtypes = _BWD_ARGS[:23] + [_I, _I, _I] + _BWD_ARGS[23:]
+        L.attn_bwd_local.restype = _I
         for name in ("attn_bwd", "attn_bwd_preprocess", "attn_bwd_main", "attn_bwd_postprocess"):
             f = getattr(L, name)
             f.argtypes = _BWD_ARGS
@@ -152,8 +158,10 @@ def version() -> str:
 
 def attn_fwd(q, k, v, causal: bool = False, scale: Optional[float] = None, cu_seqlens_q=None,
              cu_seqlens_k=None, max_seqlen_q=None, max_seqlen_k=None, out=None, lse=None,
-             stream=None) -> Tuple[torch.Tensor, torch.Tensor]:
-    """Forward pass: returns (O like q, LSE fp32 [B,H,Sq] or [H,total_q], natural log)."""
+             stream=None, window=None) -> Tuple[torch.Tensor, torch.Tensor]:
+    """Forward pass: returns (O like q, LSE fp32 [B,H,Sq] or [H,total_q], natural log).
+
+    ``window=(left, right)`` selects a local mask (-1 = unbounded side)."""
     L = lib()
     b, sq, sk, hq, hk, d, mq, mk = _dims(q, k, cu_seqlens_q, cu_seqlens_k, max_seqlen_q,
                                          max_seqlen_k)
@@ -163,9 +171,13 @@ def attn_fwd(q, k, v, causal: bool = False, scale: Optional[float] = None, cu_se
         shape = (hq, sq) if cu_seqlens_q is not None else (b, hq, sq)
         lse = torch.empty(shape, dtype=torch.float32, device=q.device)
     dq_, dk_, dv_, do_ = _desc(q), _desc(k), _desc(v), _desc(o)
-    rc = L.attn_fwd(ctypes.byref(dq_), ctypes.byref(dk_), ctypes.byref(dv_), ctypes.byref(do_),
-                    _ptr(lse), _dtype_code(q), b, sq, sk, hq, hk, d, scale, int(bool(causal)),
-                    _ptr(cu_seqlens_q), _ptr(cu_seqlens_k), mq, mk, _stream(stream))
+    args = [ctypes.byref(dq_), ctypes.byref(dk_), ctypes.byref(dv_), ctypes.byref(do_), _ptr(lse),
+            _dtype_code(q), b, sq, sk, hq, hk, d, scale, int(bool(causal)), _ptr(cu_seqlens_q),
+            _ptr(cu_seqlens_k), mq, mk]
+    if window is None:
+        rc = L.attn_fwd(*args, _stream(stream))
+    else:
+        rc = L.attn_fwd_local(*args, int(window[0]), int(window[1]), _stream(stream))
     _check(rc)
     return o, lse
 
@@ -196,16 +208,19 @@ def alloc_workspace(q, cu_seqlens_q=None, deterministic=False) -> torch.Tensor:
 
 _STAGE_FN = {"all": "attn_bwd", "pre": "attn_bwd_preprocess", "main": "attn_bwd_main",
              "post": "attn_bwd_postprocess"}
+_STAGE_MASK = {"all": 7, "pre": 1, "main": 2, "post": 4}
 
 
 def attn_bwd(q, k, v, o, lse, do, causal: bool = False, scale: Optional[float] = None,
              cu_seqlens_q=None, cu_seqlens_k=None, max_seqlen_q=None, max_seqlen_k=None,
              deterministic: bool = False, workspace: Optional[torch.Tensor] = None, dq=None,
-             dk=None, dv=None, stream=None, stage: str = "all"):
+             dk=None, dv=None, stream=None, stage: str = "all", window=None):
     """Backward pass: returns (dQ, dK, dV), each like its input.
 
     ``stage`` selects one of the three kernels ("pre", "main", "post") or all
     of them in order ("all"); the stages must share the workspace.
+    ``window=(left, right)`` selects a local mask (-1 = unbounded side; causal
+    bounds the right side at 0).
     """
     L = lib()
     b, sq, sk, hq, hk, d, mq, mk = _dims(q, k, cu_seqlens_q, cu_seqlens_k, max_seqlen_q,
@@ -218,11 +233,15 @@ def attn_bwd(q, k, v, o, lse, do, causal: bool = False, scale: Optional[float] =
         workspace = alloc_workspace(q, cu_seqlens_q, deterministic)
     descs = [_desc(t) for t in (q, k, v, o)]
     d_do, d_dq, d_dk, d_dv = _desc(do), _desc(dq), _desc(dk), _desc(dv)
-    fn = getattr(L, _STAGE_FN[stage])
-    rc = fn(*(ctypes.byref(x) for x in descs), _ptr(lse), ctypes.byref(d_do), ctypes.byref(d_dq),
+    args = [*(ctypes.byref(x) for x in descs), _ptr(lse), ctypes.byref(d_do), ctypes.byref(d_dq),
             ctypes.byref(d_dk), ctypes.byref(d_dv), _dtype_code(q), b, sq, sk, hq, hk, d, scale,
             int(bool(causal)), _ptr(cu_seqlens_q), _ptr(cu_seqlens_k), mq, mk,
-            int(bool(deterministic)), workspace.data_ptr(), workspace.numel(), _stream(stream))
+            int(bool(deterministic))]
+    tail = [workspace.data_ptr(), workspace.numel(), _stream(stream)]
+    if window is None:
+        rc = getattr(L, _STAGE_FN[stage])(*args, *tail)
+    else:
+        rc = L.attn_bwd_local(*args, int(window[0]), int(window[1]), _STAGE_MASK[stage], *tail)
     _check(rc)
     return dq, dk, dv
 

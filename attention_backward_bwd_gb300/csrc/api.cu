@@ -193,11 +193,14 @@ int prepare_bwd(const attn_tensor* q, const attn_tensor* k, const attn_tensor* v
                 const attn_tensor* dq, const attn_tensor* dk, const attn_tensor* dv, int dtype,
                 int batch, int seqlen_q, int seqlen_k, int h_q, int h_k, int head_dim,
                 float scale, int causal, const int* cu_q, const int* cu_k, int max_seqlen_q,
-                int max_seqlen_k, int deterministic, void* workspace, size_t workspace_bytes,
-                Prepared* out) {
+                int max_seqlen_k, int deterministic, int window_left, int window_right,
+                void* workspace, size_t workspace_bytes, Prepared* out) {
   int rc = check_common(dtype, batch, seqlen_q, seqlen_k, h_q, h_k, head_dim, scale, cu_q, cu_k,
                         max_seqlen_q, max_seqlen_k);
   if (rc) return rc;
+  if (window_left < -1 || window_right < -1)
+    return fail(ATTN_ERR_ARG, "window sides must be >= -1 (-1 = unbounded), got (%d, %d)",
+                window_left, window_right);
   const bool varlen = cu_q != nullptr;
   const bool hq = seqlen_q > 0, hk = seqlen_k > 0;
   if ((rc = check_tensor(q, "q", varlen, hq && hk))) return rc;
@@ -242,7 +245,8 @@ int prepare_bwd(const attn_tensor* q, const attn_tensor* k, const attn_tensor* v
   p.h_q = h_q;
   p.h_k = h_k;
   p.head_dim = head_dim;
-  p.causal = causal ? 1 : 0;
+  p.win_left = window_left;
+  p.win_right = causal ? 0 : window_right;  // causal bounds the right side at 0
   p.deterministic = deterministic ? 1 : 0;
   p.scale = scale;
   p.scale_log2 = scale * 1.4426950408889634f;
@@ -296,8 +300,6 @@ int run_stages(int stages, const Prepared& pr, cudaStream_t stream) {
     if (e == cudaErrorInvalidValue)
       return fail(ATTN_ERR_CUDA, "main kernel: TMA descriptor encoding or launch failed");
     if (e != cudaSuccess) return cuda_fail(e, "main kernel launch");
-    e = launch_zero_kv_of_empty_q(p, pr.dtype, stream);
-    if (e != cudaSuccess) return cuda_fail(e, "dK/dV clear of query-less sequences");
   }
   if (stages & kPost) {
     e = launch_postprocess(p, pr.dtype, stream);
@@ -322,12 +324,19 @@ using namespace attn;
       scale, causal, cu_seqlens_q, cu_seqlens_k, max_seqlen_q, max_seqlen_k, deterministic, \
       workspace, workspace_bytes
 
-static int bwd_entry(int stages, ATTN_BWD_ARGS_DECL) {
+static int bwd_entry_window(int stages, int window_left, int window_right, ATTN_BWD_ARGS_DECL) {
   g_err.clear();
   Prepared pr;
-  const int rc = prepare_bwd(ATTN_BWD_ARGS_PASS, &pr);
+  const int rc = prepare_bwd(q, k, v, o, lse, dout, dq, dk, dv, dtype, batch, seqlen_q, seqlen_k,
+                             h_q, h_k, head_dim, scale, causal, cu_seqlens_q, cu_seqlens_k,
+                             max_seqlen_q, max_seqlen_k, deterministic, window_left, window_right,
+                             workspace, workspace_bytes, &pr);
   if (rc) return rc;
   return run_stages(stages, pr, reinterpret_cast<cudaStream_t>(stream));
+}
+
+static int bwd_entry(int stages, ATTN_BWD_ARGS_DECL) {
+  return bwd_entry_window(stages, -1, -1, ATTN_BWD_ARGS_PASS, stream);
 }
 
 extern "C" {
@@ -337,6 +346,21 @@ int attn_bwd_preprocess(ATTN_BWD_ARGS_DECL) { return bwd_entry(kPre, ATTN_BWD_AR
 int attn_bwd_main(ATTN_BWD_ARGS_DECL) { return bwd_entry(kMain, ATTN_BWD_ARGS_PASS, stream); }
 int attn_bwd_postprocess(ATTN_BWD_ARGS_DECL) {
   return bwd_entry(kPost, ATTN_BWD_ARGS_PASS, stream);
+}
+
+int attn_bwd_local(const attn_tensor* q, const attn_tensor* k, const attn_tensor* v,
+                   const attn_tensor* o, const float* lse, const attn_tensor* dout,
+                   const attn_tensor* dq, const attn_tensor* dk, const attn_tensor* dv, int dtype,
+                   int batch, int seqlen_q, int seqlen_k, int h_q, int h_k, int head_dim,
+                   float scale, int causal, const int* cu_seqlens_q, const int* cu_seqlens_k,
+                   int max_seqlen_q, int max_seqlen_k, int deterministic, int window_left,
+                   int window_right, int stages, void* workspace, size_t workspace_bytes,
+                   attn_stream_t stream) {
+  if (stages <= 0 || stages > (kPre | kMain | kPost)) {
+    g_err.clear();
+    return fail(ATTN_ERR_ARG, "stages must be a nonzero mask of 1, 2 and 4, got %d", stages);
+  }
+  return bwd_entry_window(stages, window_left, window_right, ATTN_BWD_ARGS_PASS, stream);
 }
 
 size_t attn_bwd_workspace_size(int batch, int seqlen_q, int h_q, int head_dim, int deterministic,
@@ -358,14 +382,18 @@ int attn_bwd_workspace_layout(int batch, int seqlen_q, int h_q, int head_dim, in
   return ATTN_OK;
 }
 
-int attn_fwd(const attn_tensor* q, const attn_tensor* k, const attn_tensor* v,
-             const attn_tensor* o, float* lse, int dtype, int batch, int seqlen_q, int seqlen_k,
-             int h_q, int h_k, int head_dim, float scale, int causal, const int* cu_seqlens_q,
-             const int* cu_seqlens_k, int max_seqlen_q, int max_seqlen_k, attn_stream_t stream) {
+int attn_fwd_local(const attn_tensor* q, const attn_tensor* k, const attn_tensor* v,
+                   const attn_tensor* o, float* lse, int dtype, int batch, int seqlen_q,
+                   int seqlen_k, int h_q, int h_k, int head_dim, float scale, int causal,
+                   const int* cu_seqlens_q, const int* cu_seqlens_k, int max_seqlen_q,
+                   int max_seqlen_k, int window_left, int window_right, attn_stream_t stream) {
   g_err.clear();
   int rc = check_common(dtype, batch, seqlen_q, seqlen_k, h_q, h_k, head_dim, scale,
                         cu_seqlens_q, cu_seqlens_k, max_seqlen_q, max_seqlen_k);
   if (rc) return rc;
+  if (window_left < -1 || window_right < -1)
+    return fail(ATTN_ERR_ARG, "window sides must be >= -1 (-1 = unbounded), got (%d, %d)",
+                window_left, window_right);
   const bool varlen = cu_seqlens_q != nullptr;
   if (seqlen_q == 0) return ATTN_OK;
   if ((rc = check_tensor(q, "q", varlen, true))) return rc;
@@ -384,7 +412,8 @@ int attn_fwd(const attn_tensor* q, const attn_tensor* k, const attn_tensor* v,
   p.h_q = h_q;
   p.h_k = h_k;
   p.head_dim = head_dim;
-  p.causal = causal ? 1 : 0;
+  p.win_left = window_left;
+  p.win_right = causal ? 0 : window_right;  // causal bounds the right side at 0
   p.scale_log2 = scale * 1.4426950408889634f;
   p.max_seqlen_q = varlen ? max_seqlen_q : seqlen_q;
   if (p.max_seqlen_q == 0) return ATTN_OK;
@@ -400,6 +429,15 @@ int attn_fwd(const attn_tensor* q, const attn_tensor* k, const attn_tensor* v,
   e = launch_fwd(p, dtype, reinterpret_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "forward launch");
   return ATTN_OK;
+}
+
+int attn_fwd(const attn_tensor* q, const attn_tensor* k, const attn_tensor* v,
+             const attn_tensor* o, float* lse, int dtype, int batch, int seqlen_q, int seqlen_k,
+             int h_q, int h_k, int head_dim, float scale, int causal, const int* cu_seqlens_q,
+             const int* cu_seqlens_k, int max_seqlen_q, int max_seqlen_k, attn_stream_t stream) {
+  return attn_fwd_local(q, k, v, o, lse, dtype, batch, seqlen_q, seqlen_k, h_q, h_k, head_dim,
+                        scale, causal, cu_seqlens_q, cu_seqlens_k, max_seqlen_q, max_seqlen_k, -1,
+                        -1, stream);
 }
 
 int attn_check_device_status(attn_stream_t stream) {

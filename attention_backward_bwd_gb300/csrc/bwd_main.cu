@@ -134,14 +134,13 @@ __device__ __forceinline__ Unit get_unit(const BwdParams& p, int u, int G) {
   r.g = rem - r.b * p.h_k;
   r.si = seq_info(p.seq, r.b);
   r.has_keys = r.n * BN < r.si.sk;
-  const int m_end = ceil_div(r.si.sq, BM);
-  int m_start = 0;
-  if (p.causal) {
-    const int lo = r.n * BN - (r.si.sk - r.si.sq);  // first query that sees key n*BN
-    m_start = lo > 0 ? lo / BM : 0;
-  }
-  r.m_start = m_start;
-  r.m_count = m_end > m_start ? m_end - m_start : 0;
+  // query tiles holding a query that sees a key of this tile (all of them
+  // without a mask; causal or a window narrows the range)
+  const int k1 = min(r.n * BN + BN, r.si.sk);
+  int lo, hi;
+  window_queries(r.n * BN, k1, r.si.sq, r.si.sk, p.win_left, p.win_right, lo, hi);
+  r.m_start = lo / BM;
+  r.m_count = lo < hi ? ceil_div(hi, BM) - r.m_start : 0;
   r.n_iters = r.has_keys ? G * r.m_count : 0;
   return r;
 }
@@ -499,13 +498,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         int h_unused, m;
         iter_hm(un, j, G, h_unused, m);
         const int q0 = m * BM;
-        const bool need_mask = (q0 + BM > un.si.sq) || (un.n * BN + BN > un.si.sk) ||
-                               (p.causal && un.n * BN + BN - 1 > q0 + off);
+        const bool need_mask =
+            (q0 + BM > un.si.sq) || (un.n * BN + BN > un.si.sk) ||
+            (p.win_right >= 0 && un.n * BN + BN - 1 > q0 + off + p.win_right) ||
+            (p.win_left >= 0 && un.n * BN < q0 + BM - 1 + off - p.win_left);
         const float* lse2 = reinterpret_cast<const float*>(smem + L::kLSE + s * BM * 4) + c0;
         const float* dlt = reinterpret_cast<const float*>(smem + L::kDelta + s * BM * 4) + c0;
         // valid queries of this key row, in this group's column coordinates: lo <= c < hi
         int lo = 0, hi = key_ok ? min(kCols, un.si.sq - q0 - c0) : 0;
-        if (p.causal) lo = max(0, key - off - q0 - c0);
+        if (p.win_right >= 0) lo = max(0, key - off - p.win_right - q0 - c0);
+        if (p.win_left >= 0) hi = min(hi, key - off + p.win_left - q0 - c0 + 1);
         if (!wait_warp(bar(B_FULLQ + s), ph, ctl, 0xA0000021u)) goto done;
         if (!wait_warp(bar(B_SFULL), it & 1, ctl, 0xA0000022u)) goto done;
         tc_fence_after();
@@ -635,9 +637,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     // once the reduces have read it.  Rows past the sequence end hold exact
     // zeros (their dS is 0) and stay inside the sequence's padded workspace
     // rows, so they need no mask.
-    // In deterministic mode a warp waits until key tiles 0..n-1 have completed
-    // their adds (4 arrivals each, one per drain warp) and releases once its
-    // own adds have completed.
+    // In deterministic mode a warp waits until the key tiles before n that see
+    // this query tile (0..n-1, or from the first one inside a left window) have
+    // completed their adds (4 arrivals each, one per drain warp) and releases
+    // once its own adds have completed.
     const uint32_t quad = warp & 3;
     const uint32_t tl = tmem + ((quad * 32) << 16);
     // Per warp and pass: kBoxes boxes of 32 rows x 32 fp32 columns (4 KB each);
@@ -679,7 +682,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (p.deterministic) {
           int stop = 0;
           if (lane == 0) {
-            const int want = 4 * un.n;
+            // key tiles before this one that see query tile m (all of them
+            // unless a left window starts the range later)
+            const int want =
+                4 * (un.n - window_first_key(m * BM, un.si.sq, un.si.sk, p.win_left) / BN);
             const uint64_t t0 = globaltimer_ns();
             for (uint32_t spin = 0;; ++spin) {
               if (ld_acquire(sem) >= want) break;

@@ -388,6 +388,27 @@ __device__ __forceinline__ SeqInfo seq_info(const SeqParams& s, int b) {
   return r;
 }
 
+// Local (sliding-window) mask in bottom-right alignment (the CK wrapper's
+// window (left, right); causal is (-1, 0)): with off = sk - sq, query i sees
+// key j iff (left < 0 || j >= i + off - left) && (right < 0 || j <= i + off + right).
+// Queries [lo, hi) (clipped to [0, sq)) see some key of [k0, k1); empty when
+// lo >= hi.  The set is an interval because each query's keys are one.
+__host__ __device__ __forceinline__ void window_queries(int k0, int k1, int sq, int sk, int left,
+                                                        int right, int& lo, int& hi) {
+  const int off = sk - sq;
+  lo = right >= 0 ? k0 - off - right : 0;
+  hi = left >= 0 ? k1 - 1 - off + left + 1 : sq;
+  lo = lo > 0 ? lo : 0;
+  hi = hi < sq ? hi : sq;
+}
+
+// First key that some query of [q0, q1) sees (the keys such a tile sees are an
+// interval starting there, when it is not empty).
+__host__ __device__ __forceinline__ int window_first_key(int q0, int sq, int sk, int left) {
+  const int first = left >= 0 ? q0 + (sk - sq) - left : 0;
+  return first > 0 ? first : 0;
+}
+
 // Which sequence a packed query row belongs to (binary search on cu_seqlens).
 __device__ __forceinline__ int seq_of_row(const int* cu, int nseq, int row) {
   int lo = 0, hi = nseq - 1;

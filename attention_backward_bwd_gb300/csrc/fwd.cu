@@ -108,18 +108,20 @@ __global__ void __launch_bounds__(kFwdThreads) fwd_kernel(FwdParams p) {
   T* og = const_cast<T*>(static_cast<const T*>(p.o.ptr)) + (varlen ? 0 : b * p.o.sb) +
           static_cast<int64_t>(si.q_start) * p.o.ss + static_cast<int64_t>(h) * p.o.sh;
 
-  const int off = si.sk - si.sq;  // bottom-right causal alignment
+  const int off = si.sk - si.sq;  // bottom-right alignment of causal / window masks
+  // key tiles holding a key that some query of this tile sees
+  const int n_start = window_first_key(m0, si.sq, si.sk, p.win_left) / kBN;
   int n_end = ceil_div(si.sk, kBN);
-  if (p.causal) {
-    const int last_key = m0 + kBM - 1 + off;
+  if (p.win_right >= 0) {
+    const int last_key = m0 + kBM - 1 + off + p.win_right;
     n_end = min(n_end, last_key < 0 ? 0 : last_key / kBN + 1);
   }
 
   load_tile<T, D, LD>(sQ, qg, p.q.ss, m0, si.sq);
   cp_async_commit();
-  if (n_end > 0) {
-    load_tile<T, D, LD>(sK, kg, p.k.ss, 0, si.sk);
-    load_tile<T, D, LD>(sV, vg, p.v.ss, 0, si.sk);
+  if (n_end > n_start) {
+    load_tile<T, D, LD>(sK, kg, p.k.ss, n_start * kBN, si.sk);
+    load_tile<T, D, LD>(sV, vg, p.v.ss, n_start * kBN, si.sk);
   }
   cp_async_commit();
   cp_async_wait_all();
@@ -141,8 +143,8 @@ __global__ void __launch_bounds__(kFwdThreads) fwd_kernel(FwdParams p) {
   float lpart[2] = {0.f, 0.f};
   const int row_lo = m0 + warp * 16 + g;
 
-  for (int n = 0; n < n_end; ++n) {
-    const int buf = n & 1;
+  for (int n = n_start; n < n_end; ++n) {
+    const int buf = (n - n_start) & 1;
     if (n + 1 < n_end) {
       load_tile<T, D, LD>(sK + (buf ^ 1) * kBN * LD, kg, p.k.ss, (n + 1) * kBN, si.sk);
       load_tile<T, D, LD>(sV + (buf ^ 1) * kBN * LD, vg, p.v.ss, (n + 1) * kBN, si.sk);
@@ -167,7 +169,9 @@ __global__ void __launch_bounds__(kFwdThreads) fwd_kernel(FwdParams p) {
       }
     }
 
-    const bool need_mask = (n * kBN + kBN > si.sk) || (p.causal && n * kBN + kBN - 1 > m0 + off);
+    const bool need_mask = (n * kBN + kBN > si.sk) ||
+                           (p.win_right >= 0 && n * kBN + kBN - 1 > m0 + off + p.win_right) ||
+                           (p.win_left >= 0 && n * kBN < m0 + kBM - 1 + off - p.win_left);
     float tmax[2] = {-INFINITY, -INFINITY};
 #pragma unroll
     for (int nt = 0; nt < 8; ++nt) {
@@ -177,7 +181,8 @@ __global__ void __launch_bounds__(kFwdThreads) fwd_kernel(FwdParams p) {
         if (need_mask) {
           const int key = n * kBN + nt * 8 + 2 * t + (e & 1);
           const int row = row_lo + (e >> 1) * 8;
-          const bool ok = key < si.sk && (!p.causal || key <= row + off);
+          const bool ok = key < si.sk && (p.win_right < 0 || key <= row + off + p.win_right) &&
+                          (p.win_left < 0 || key >= row + off - p.win_left);
           x = ok ? x : -INFINITY;
         }
         s[nt][e] = x;

@@ -43,7 +43,8 @@ struct BwdParams {
   int* sched;    // work counter of the persistent main kernel (after the semaphores)
   int64_t ws_rows;
   int h_q, h_k, head_dim;
-  int causal, deterministic;
+  int win_left, win_right;  // local mask sides, -1 = unbounded; causal is (-1, 0)
+  int deterministic;
   float scale, scale_log2;
   int max_seqlen_q, max_seqlen_k;
   unsigned int* status;
@@ -56,7 +57,7 @@ struct FwdParams {
   TensorArg q, k, v, o;
   float* lse;
   int h_q, h_k, head_dim;
-  int causal;
+  int win_left, win_right;  // local mask sides, -1 = unbounded; causal is (-1, 0)
   float scale_log2;
   int max_seqlen_q;
   const unsigned int* input_bad;
@@ -92,8 +93,6 @@ cudaError_t launch_preprocess(const BwdParams& p, int dtype, cudaStream_t stream
 cudaError_t launch_postprocess(const BwdParams& p, int dtype, cudaStream_t stream);
 cudaError_t launch_bwd_main(const BwdParams& p, int dtype, cudaStream_t stream);
 cudaError_t launch_fwd(const FwdParams& p, int dtype, cudaStream_t stream);
-// Varlen: dK = dV = 0 on the key rows of sequences that have no query rows.
-cudaError_t launch_zero_kv_of_empty_q(const BwdParams& p, int dtype, cudaStream_t stream);
 cudaError_t launch_zero_rows(const TensorArg& t, int dtype, int nseq, int rows_per_seq,
                              const int* cu, int total_rows, int heads, int head_dim,
                              cudaStream_t stream);
@@ -140,8 +139,8 @@ int prepare_bwd(const attn_tensor* q, const attn_tensor* k, const attn_tensor* v
                 const attn_tensor* dq, const attn_tensor* dk, const attn_tensor* dv, int dtype,
                 int batch, int seqlen_q, int seqlen_k, int h_q, int h_k, int head_dim,
                 float scale, int causal, const int* cu_q, const int* cu_k, int max_seqlen_q,
-                int max_seqlen_k, int deterministic, void* workspace, size_t workspace_bytes,
-                Prepared* out);
+                int max_seqlen_k, int deterministic, int window_left, int window_right,
+                void* workspace, size_t workspace_bytes, Prepared* out);
 
 enum Stage { kPre = 1, kMain = 2, kPost = 4 };
 

@@ -183,33 +183,6 @@ __global__ void __launch_bounds__(kThreads)
   }
 }
 
-// Varlen sequences with keys but no queries get no work unit in the main kernel
-// (every key tile has an empty query range), yet their dK and dV are defined:
-// zero, as for a whole problem with Sq = 0.  Block b clears the key rows of
-// sequence b in dK and dV when cu_q gives it no query rows.
-template <typename T, int D>
-__global__ void __launch_bounds__(kThreads)
-    zero_kv_of_empty_q_kernel(TensorArg dk, TensorArg dv, const int* cu_q, const int* cu_k,
-                              int heads, const unsigned int* input_bad) {
-  if (input_bad != nullptr && *input_bad) return;
-  const int b = blockIdx.x;
-  if (cu_q[b + 1] != cu_q[b]) return;
-  const int k0 = cu_k[b], k1 = cu_k[b + 1];
-  constexpr int kGroup = D / 8;  // threads per head row, 16 B each
-  const int c = threadIdx.x % kGroup;
-  const int64_t n_groups = static_cast<int64_t>(k1 - k0) * heads;
-  for (int64_t g = threadIdx.x / kGroup; g < n_groups; g += kThreads / kGroup) {
-    const int64_t r = k0 + g / heads;
-    const int h = static_cast<int>(g % heads);
-    const int64_t off = r * dk.ss + static_cast<int64_t>(h) * dk.sh + c * 8;
-    const int64_t offv = r * dv.ss + static_cast<int64_t>(h) * dv.sh + c * 8;
-    *reinterpret_cast<uint4*>(const_cast<T*>(static_cast<const T*>(dk.ptr)) + off) =
-        make_uint4(0u, 0u, 0u, 0u);
-    *reinterpret_cast<uint4*>(const_cast<T*>(static_cast<const T*>(dv.ptr)) + offv) =
-        make_uint4(0u, 0u, 0u, 0u);
-  }
-}
-
 // Checks that cu_seqlens describe a valid packing: start at 0, nondecreasing,
 // end at the total row count, no sequence longer than max_seqlen.  Any
 // violation sets *bad, and every later kernel of the call returns at once.
@@ -319,23 +292,6 @@ cudaError_t launch_validate_cu(const int* cu_q, const int* cu_k, int batch, int 
                                cudaStream_t stream) {
   validate_cu_kernel<<<1, 256, 0, stream>>>(cu_q, cu_k, batch, total_q, total_k, max_q, max_k, bad);
   return cudaGetLastError();
-}
-
-template <typename T>
-static cudaError_t launch_zero_kv_t(const BwdParams& p, cudaStream_t stream) {
-  if (p.head_dim == 64)
-    zero_kv_of_empty_q_kernel<T, 64><<<p.seq.batch, kThreads, 0, stream>>>(
-        p.dk, p.dv, p.seq.cu_q, p.seq.cu_k, p.h_k, p.input_bad);
-  else
-    zero_kv_of_empty_q_kernel<T, 128><<<p.seq.batch, kThreads, 0, stream>>>(
-        p.dk, p.dv, p.seq.cu_q, p.seq.cu_k, p.h_k, p.input_bad);
-  return cudaGetLastError();
-}
-
-cudaError_t launch_zero_kv_of_empty_q(const BwdParams& p, int dtype, cudaStream_t stream) {
-  if (p.seq.cu_q == nullptr || p.seq.batch <= 0) return cudaSuccess;
-  return dtype == 1 ? launch_zero_kv_t<__nv_bfloat16>(p, stream)
-                    : launch_zero_kv_t<__half>(p, stream);
 }
 
 cudaError_t launch_zero_rows(const TensorArg& t, int dtype, int nseq, int rows_per_seq,

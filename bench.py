@@ -303,9 +303,8 @@ def run_ours(args):
         "e2e": {"value": round(world * flops / (e2e_ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
                 "ms_per_step": round(e2e_ms, 3), "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "path": e2e_path},
-        # preprocess, main, postprocess; varlen adds the cu_seqlens check and the
-        # dK/dV clear of query-less sequences
-        "gpu_launches": (5 if w.varlen else 3) * args.steps,
+        # preprocess, main, postprocess; varlen adds the cu_seqlens check
+        "gpu_launches": (4 if w.varlen else 3) * args.steps,
         "clocks": clk.summary(),
     }
     if not args.no_cpu_baseline:

@@ -131,6 +131,37 @@ int attn_bwd(const attn_tensor* q, const attn_tensor* k, const attn_tensor* v,
              size_t workspace_bytes, attn_stream_t stream);
 
 /*
+ * attn_bwd_local / attn_fwd_local -- the same calls with a local
+ * (sliding-window) mask, the window (window_left, window_right) of
+ * flash-attention csrc/flash_attn_ck/mha_bwd.cpp (mha_bwd's mask set-up),
+ * -1 meaning unbounded on that side.  Bottom-right aligned like causal: with
+ * off = Sk - Sq (per sequence in varlen mode), query i attends key j iff
+ * j >= i + off - window_left (when window_left >= 0) and
+ * j <= i + off + window_right (when window_right >= 0).  causal != 0 sets
+ * window_right to 0, so (window_left = W, causal = 1) is sliding-window causal
+ * attention and (-1, -1, causal = 0) is attn_bwd / attn_fwd.  Rows that see no
+ * key get O = 0, LSE = +inf, dQ = 0; keys that no query sees get dK = dV = 0.
+ * attn_bwd_local runs the stages selected by the bit mask `stages` (1 =
+ * preprocess, 2 = main, 4 = postprocess; 7 = all, in that order); the stages
+ * of one backward must share the workspace and the window.  Window sides
+ * below -1, or a stage mask outside 1..7, give ATTN_ERR_ARG.  Deterministic
+ * mode orders the dQ adds of each query tile over the key tiles that see it.
+ */
+int attn_bwd_local(const attn_tensor* q, const attn_tensor* k, const attn_tensor* v,
+                   const attn_tensor* o, const float* lse, const attn_tensor* dout,
+                   const attn_tensor* dq, const attn_tensor* dk, const attn_tensor* dv, int dtype,
+                   int batch, int seqlen_q, int seqlen_k, int h_q, int h_k, int head_dim,
+                   float scale, int causal, const int* cu_seqlens_q, const int* cu_seqlens_k,
+                   int max_seqlen_q, int max_seqlen_k, int deterministic, int window_left,
+                   int window_right, int stages, void* workspace, size_t workspace_bytes,
+                   attn_stream_t stream);
+int attn_fwd_local(const attn_tensor* q, const attn_tensor* k, const attn_tensor* v,
+                   const attn_tensor* o, float* lse, int dtype, int batch, int seqlen_q,
+                   int seqlen_k, int h_q, int h_k, int head_dim, float scale, int causal,
+                   const int* cu_seqlens_q, const int* cu_seqlens_k, int max_seqlen_q,
+                   int max_seqlen_k, int window_left, int window_right, attn_stream_t stream);
+
+/*
  * attn_bwd_noalloc -- attn_bwd with no workspace argument, for callers that
  * must not allocate device memory: code whose device memory all belongs to
  * another allocator (a framework's memory pool or an arena reserved at
