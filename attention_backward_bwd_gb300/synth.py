@@ -42,6 +42,11 @@ class Workload:
     n_seqs: int = 0
     len_lo: int = 0
     len_hi: int = 0
+    window: tuple = (-1, -1)  # local mask (left, right), -1 = unbounded side
+
+    @property
+    def windowed(self) -> bool:
+        return tuple(self.window) != (-1, -1)
 
     @property
     def varlen(self) -> bool:
@@ -68,6 +73,9 @@ WORKLOADS = {
     "gqa_b2_hq32_hk8_s8192_d128_bf16_causal_det": Workload(
         "gqa_b2_hq32_hk8_s8192_d128_bf16_causal_det", 2, 32, 8, 8192, 8192, 128, "bf16", True,
         3, deterministic=True),
+    "gqa_b2_hq32_hk8_s8192_d128_bf16_causal_win1024": Workload(
+        "gqa_b2_hq32_hk8_s8192_d128_bf16_causal_win1024", 2, 32, 8, 8192, 8192, 128, "bf16", True,
+        3, window=(1024, -1)),
     "varlen16_h16_d128_bf16_causal": Workload(
         "varlen16_h16_d128_bf16_causal", 0, 16, 16, 0, 0, 128, "bf16", True, 4,
         n_seqs=16, len_lo=128, len_hi=8192),

@@ -28,6 +28,7 @@ import time
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
+import numpy as np  # noqa: E402
 import torch  # noqa: E402
 
 from attention_backward_bwd_gb300 import synth  # noqa: E402
@@ -37,8 +38,26 @@ METRIC = "attention-backward TFLOPS (bf16, 1xGB300) and % of dense tensor-core p
 L2_BYTES = 129 * 2 ** 20
 
 
+def window_pairs(sq: int, sk: int, causal: bool, window) -> int:
+    """Number of (query, key) pairs a local mask allows (bottom-right aligned)."""
+    left, right = window
+    if causal:
+        right = 0
+    i = np.arange(sq, dtype=np.int64)
+    lo = np.maximum(0, i + (sk - sq) - left) if left >= 0 else np.zeros_like(i)
+    hi = np.minimum(sk - 1, i + (sk - sq) + right) if right >= 0 else np.full_like(i, sk - 1)
+    return int(np.maximum(0, hi - lo + 1).sum())
+
+
 def bwd_flops(w: synth.Workload, lengths=None) -> float:
-    """2.5 x forward FLOPs (4 B H Sq Sk D), halved when causal; varlen sums sequences."""
+    """2.5 x forward FLOPs (4 B H Sq Sk D), halved when causal; varlen sums sequences.
+    With a local window: 10 D FLOPs per allowed (query, key) pair, counted exactly."""
+    if w.windowed:
+        if w.varlen:
+            pairs = sum(window_pairs(n, n, w.causal, w.window) for n in lengths)
+        else:
+            pairs = w.batch * window_pairs(w.seqlen_q, w.seqlen_k, w.causal, w.window)
+        return 10.0 * w.head_dim * w.h_q * pairs
     if w.varlen:
         f = sum(2.5 * 4.0 * w.h_q * n * n * w.head_dim for n in lengths)
     else:
@@ -179,12 +198,14 @@ def run_ours(args):
     cu_q = x.cu_seqlens_q.to(dev) if w.varlen else None
     cu_k = x.cu_seqlens_k.to(dev) if w.varlen else None
     q, k, v, do = (t.to(dev) for t in (x.q, x.k, x.v, x.do))
+    window = tuple(w.window) if w.windowed else None
     o, lse = ab.attn_fwd(q, k, v, causal=w.causal, cu_seqlens_q=cu_q, cu_seqlens_k=cu_k,
-                         max_seqlen_q=mq, max_seqlen_k=mk)
+                         max_seqlen_q=mq, max_seqlen_k=mk, window=window)
     ws = ab.alloc_workspace(q, cu_q, det)
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
     kw = dict(causal=w.causal, cu_seqlens_q=cu_q, cu_seqlens_k=cu_k, max_seqlen_q=mq,
-              max_seqlen_k=mk, deterministic=det, workspace=ws, dq=dq, dk=dk, dv=dv)
+              max_seqlen_k=mk, deterministic=det, workspace=ws, dq=dq, dk=dk, dv=dv,
+              window=window)
     stream = torch.cuda.current_stream()
     flops = bwd_flops(w, x.lengths)
     in_bytes = sum(t.numel() * t.element_size() for t in (q, k, v, o, do, lse))
@@ -225,13 +246,14 @@ def run_ours(args):
     t_post = statistics.mean(e[2].elapsed_time(e[3]) for e in evs)
 
     # --- end to end: pinned host inputs -> device -> backward -> pinned host results.
-    # Padded workloads go through attn_bwd_host (chunks whose copies overlap the
-    # kernels of other chunks); varlen ones copy in, call attn_bwd, copy out.
+    # Padded unmasked or causal workloads go through attn_bwd_host (chunks whose
+    # copies overlap the kernels of other chunks); varlen and windowed ones copy
+    # in, call attn_bwd, copy out.
     hq_ = [t.cpu().pin_memory() for t in (q, k, v, o, do, lse)]
     host_out = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in (dq, dk, dv)]
     h2d = sum(t.numel() * t.element_size() for t in hq_)
     d2h = sum(t.numel() * t.element_size() for t in host_out)
-    if not w.varlen:
+    if not w.varlen and not w.windowed:
         b_, sq_, hq_n, d_ = q.shape
         hbuf = torch.empty(ab.host_buffer_size(b_, sq_, k.shape[1], hq_n, k.shape[2], d_,
                                                args.chunks), dtype=torch.uint8, device=dev)
@@ -285,6 +307,9 @@ def run_ours(args):
            "parallelism": f"replicas x{world}" if world > 1 else "single GPU"}
     if w.varlen:
         cfg["lengths"] = x.lengths
+    if w.windowed:
+        cfg["window"] = list(w.window)
+        cfg["flops"] = "10 D per allowed (query, key) pair, counted exactly"
     out = {
         "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_max, 4),
@@ -336,11 +361,16 @@ def oracle_sample(w, x, n_heads=1):
         L = w.seqlen_q
     g = w.h_q // w.h_k
 
+    window = tuple(w.window) if w.windowed else None
+
     def run(h):
         return attn_oracle.head_backward(sl(q, h).double().numpy(), sl(k, h // g).double().numpy(),
                                          sl(v, h // g).double().numpy(),
-                                         sl(do, h).double().numpy(), w.scale, w.causal)
-    f_one = 2.5 * 4.0 * L * L * w.head_dim / (2 if w.causal else 1)
+                                         sl(do, h).double().numpy(), w.scale, w.causal, window)
+    if w.windowed:
+        f_one = 10.0 * w.head_dim * window_pairs(L, L, w.causal, w.window)
+    else:
+        f_one = 2.5 * 4.0 * L * L * w.head_dim / (2 if w.causal else 1)
     return run, f_one, L
 
 
