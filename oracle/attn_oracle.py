@@ -32,12 +32,18 @@ Sources (page title, section):
     unbounded on that side, in the same bottom-right alignment; causal is the
     window (-1, 0).
 
+  * flash-attention hopper/flash_bwd_launch_template.h: ``Has_softcap`` /
+    ``params.softcap`` select a logit cap (no formula is given there).
+
 Readings where the pages leave a point open:
   * causal with Sq != Sk: key j is allowed for query i iff j <= i + (Sk - Sq).
   * window (left, right): with off = Sk - Sq, key j is allowed for query i iff
     j >= i + off - left (when left >= 0) and j <= i + off + right (when
     right >= 0); causal together with a window keeps the window's left side
     and bounds the right side at 0.
+  * softcap c > 0: the logits s = scale * q.k are capped as c * tanh(s / c)
+    before the softmax (the usual logit cap); the backward multiplies dS by
+    the cap's derivative 1 - tanh(s / c)^2.  c = 0 means no cap.
   * a query row with no allowed key: O = 0, LSE = +inf, dQ = 0, and it adds
     nothing to dK or dV.
   * scale defaults to 1/sqrt(D).
@@ -77,13 +83,15 @@ def allowed_mask(sq: int, sk: int, causal: bool, window=None) -> np.ndarray:
 
 
 def head_forward(q: np.ndarray, k: np.ndarray, v: np.ndarray, scale: float, causal: bool,
-                 window=None):
+                 window=None, softcap: float = 0.0):
     """Forward of one head.  q [Sq, D], k and v [Sk, D], float64.
 
     Returns (O [Sq, D], LSE [Sq] natural log, P [Sq, Sk]).
     """
     sq, sk = q.shape[0], k.shape[0]
     s = scale * (q @ k.T)
+    if softcap > 0:
+        s = softcap * np.tanh(s / softcap)
     allowed = allowed_mask(sq, sk, causal, window)
     s = np.where(allowed, s, -np.inf)
     any_key = allowed.any(axis=1) if sk > 0 else np.zeros(sq, dtype=bool)
@@ -96,16 +104,19 @@ def head_forward(q: np.ndarray, k: np.ndarray, v: np.ndarray, scale: float, caus
     return o, lse, p
 
 
-def head_backward(q, k, v, do, scale: float, causal: bool, window=None):
+def head_backward(q, k, v, do, scale: float, causal: bool, window=None, softcap: float = 0.0):
     """Gradient of one head, by the definition.  All arrays float64.
 
-    Returns a dict with O, LSE, P, dP, Delta (= rowsum(P * dP)), dS, dQ, dK, dV.
+    Returns a dict with O, LSE, P, dP, Delta (= rowsum(P * dP)), dS, dQ, dK, dV;
+    dS is the gradient with respect to the (uncapped) logits scale * q.k.
     """
-    o, lse, p = head_forward(q, k, v, scale, causal, window)
+    o, lse, p = head_forward(q, k, v, scale, causal, window, softcap)
     dv = p.T @ do
     dp = do @ v.T
     delta = (p * dp).sum(axis=1)
     ds = p * (dp - delta[:, None])
+    if softcap > 0:
+        ds = ds * (1.0 - np.tanh(scale * (q @ k.T) / softcap) ** 2)
     dq = scale * (ds @ k)
     dk = scale * (ds.T @ q)
     return {"O": o, "LSE": lse, "P": p, "dP": dp, "Delta": delta, "dS": ds,
@@ -155,7 +166,7 @@ def _put(x, sel, h, val, add=False):
 
 
 def mha_forward(q, k, v, scale=None, causal=False, cu_seqlens_q=None, cu_seqlens_k=None,
-                heads=None, window=None):
+                heads=None, window=None, softcap=0.0):
     """Multi-head forward.  q [B,Sq,H,D] (or packed [total,H,D]), k/v with H_k heads.
 
     Returns (O like q, LSE [B,H,Sq] or [H,total_q]).  ``heads`` restricts the
@@ -174,7 +185,7 @@ def mha_forward(q, k, v, scale=None, causal=False, cu_seqlens_q=None, cu_seqlens
     for b, qs, ks in _sequences(q, k, cu_seqlens_q, cu_seqlens_k):
         for h in hs:
             oh, lh, _ = head_forward(_take(q, qs, h), _take(k, ks, h // g), _take(v, ks, h // g),
-                                     scale, causal, window)
+                                     scale, causal, window, softcap)
             _put(o, qs, h, oh)
             if cu_seqlens_q is None:
                 lse[b, h, :] = lh
@@ -184,7 +195,7 @@ def mha_forward(q, k, v, scale=None, causal=False, cu_seqlens_q=None, cu_seqlens
 
 
 def mha_backward(q, k, v, do, scale=None, causal=False, cu_seqlens_q=None, cu_seqlens_k=None,
-                 kv_heads=None, window=None):
+                 kv_heads=None, window=None, softcap=0.0):
     """Multi-head backward by the definition, with GQA group sums.
 
     Returns dict(dQ, dK, dV, O, LSE, Delta) in the input layouts (LSE/Delta as
@@ -206,7 +217,7 @@ def mha_backward(q, k, v, do, scale=None, causal=False, cu_seqlens_q=None, cu_se
         for hkv in kvs:
             for h in range(hkv * g, hkv * g + g):
                 r = head_backward(_take(q, qs, h), _take(k, ks, hkv), _take(v, ks, hkv),
-                                  _take(do, qs, h), scale, causal, window)
+                                  _take(do, qs, h), scale, causal, window, softcap)
                 _put(dq, qs, h, r["dQ"])
                 _put(o, qs, h, r["O"])
                 _put(dk, ks, hkv, r["dK"], add=True)

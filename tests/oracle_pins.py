@@ -19,6 +19,9 @@ mistake) and raises ``AssertionError`` when the fact does not hold.  The facts:
   i + Sk - Sq (O_i = V_{i+Sk-Sq}, dQ = dK = 0, dV = dO moved to those rows);
   a brute-force forward that writes the window as a distance band agrees;
   finite differences hold under a window;
+* softcap: finite differences hold with the cap, an independent torch-autograd
+  run through c * tanh(s / c) agrees, and a cap far above every logit changes
+  nothing measurable;
 * an independent fp64 torch-autograd run of softmax(Q K^T s) V agrees to 1e-10,
   and its logsumexp gives LSE; the same run pins the row-sampled group
   backward used at full problem sizes.
@@ -174,6 +177,58 @@ def pin_finite_differences_window(o_mod):
                 x[idx] = old
                 g[idx] = (lp - lm) / 2e-6
             assert _rel(r[key], g) < 1e-6, (sq, sk, win, causal, key)
+
+
+def pin_softcap(o_mod):
+    rng = np.random.default_rng(91)
+    # torch autograd through the capped logits (shares nothing with the oracle)
+    for sq, sk, causal, win, cap in ((5, 5, True, None, 1.5), (4, 7, False, (2, 1), 0.8)):
+        q, k, v, do = _rand(sq, 6, rng=rng) * 2, _rand(sk, 6, rng=rng) * 2, \
+            _rand(sk, 6, rng=rng), _rand(sq, 6, rng=rng)
+        r = o_mod.head_backward(q, k, v, do, 0.7, causal, win, cap)
+        tq, tk, tv = (torch.tensor(x, dtype=torch.float64, requires_grad=True) for x in (q, k, v))
+        s = cap * torch.tanh(0.7 * (tq @ tk.T) / cap)
+        i = torch.arange(sq)[:, None]
+        j = torch.arange(sk)[None, :]
+        band = torch.ones(sq, sk, dtype=torch.bool)
+        left, right = (-1, -1) if win is None else win
+        if causal:
+            right = 0
+        if right >= 0:
+            band &= j - i - (sk - sq) <= right
+        if left >= 0:
+            band &= j - i - (sk - sq) >= -left
+        o = torch.softmax(s.masked_fill(~band, float("-inf")), dim=1) @ tv
+        (o * torch.tensor(do)).sum().backward()
+        assert _rel(r["O"], o.detach().numpy()) < 1e-12
+        for key, t in (("dQ", tq), ("dK", tk), ("dV", tv)):
+            assert _rel(r[key], t.grad.numpy()) < 1e-10, (key, sq, sk)
+    # finite differences, multi-head with GQA
+    q, k, v = _rand(1, 4, 2, 4, rng=rng), _rand(1, 5, 1, 4, rng=rng), _rand(1, 5, 1, 4, rng=rng)
+    do = _rand(1, 4, 2, 4, rng=rng)
+    r = o_mod.mha_backward(q, k, v, do, 0.9, True, softcap=0.6)
+    arrs = {"q": q, "k": k, "v": v}
+    for name, key in (("q", "dQ"), ("k", "dK"), ("v", "dV")):
+        x = arrs[name]
+        g = np.zeros_like(x)
+        it = np.nditer(x, flags=["multi_index"])
+        for _ in it:
+            idx = it.multi_index
+            old = x[idx]
+            x[idx] = old + 1e-6
+            lp = float((o_mod.mha_forward(q, k, v, 0.9, True, softcap=0.6)[0] * do).sum())
+            x[idx] = old - 1e-6
+            lm = float((o_mod.mha_forward(q, k, v, 0.9, True, softcap=0.6)[0] * do).sum())
+            x[idx] = old
+            g[idx] = (lp - lm) / 2e-6
+        assert _rel(r[key], g) < 1e-6, key
+    # a cap far above every logit: tanh is linear there
+    q, k, v, do = _rand(6, 4, rng=rng), _rand(6, 4, rng=rng), _rand(6, 4, rng=rng), \
+        _rand(6, 4, rng=rng)
+    a = o_mod.head_backward(q, k, v, do, 0.5, True)
+    b = o_mod.head_backward(q, k, v, do, 0.5, True, None, 1e5)
+    for key in ("dQ", "dK", "dV", "O"):
+        assert _rel(b[key], a[key]) < 1e-8, key
 
 
 def pin_delta_identity(o_mod):
@@ -446,4 +501,4 @@ ALL_PINS = [pin_sympy_exact, pin_finite_differences, pin_finite_differences_varl
             pin_equal_value_rows, pin_causal_row0, pin_causal_bottom_right, pin_zero_query,
             pin_single_key, pin_key_shift_and_permutation, pin_torch_autograd,
             pin_varlen_matches_padded, pin_cross_varlen_matches_padded, pin_empty_cases,
-            pin_group_rows_autograd, pin_window, pin_finite_differences_window]
+            pin_group_rows_autograd, pin_window, pin_finite_differences_window, pin_softcap]
