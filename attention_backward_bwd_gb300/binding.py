@@ -35,6 +35,19 @@ class AttnTensor(ctypes.Structure):
                 ("stride_s", ctypes.c_int64), ("stride_h", ctypes.c_int64)]
 
 
+class AttnOpts(ctypes.Structure):
+    _fields_ = [("window_left", ctypes.c_int), ("window_right", ctypes.c_int),
+                ("softcap", ctypes.c_float)]
+
+
+def _opts(window, softcap):
+    """None when neither a window nor a cap is asked for (plain entry points)."""
+    if window is None and not softcap:
+        return None
+    left, right = (-1, -1) if window is None else (int(window[0]), int(window[1]))
+    return AttnOpts(left, right, float(softcap or 0.0))
+
+
 _T = ctypes.POINTER(AttnTensor)
 _P = ctypes.c_void_p
 _I = ctypes.c_int
@@ -46,7 +59,7 @@ _lock = threading.Lock()
 
 EXPORTS = ("attn_fwd", "attn_bwd", "attn_bwd_preprocess", "attn_bwd_main", "attn_bwd_postprocess",
            "attn_bwd_workspace_size", "attn_bwd_workspace_layout", "attn_bwd_noalloc",
-           "attn_bwd_host", "attn_bwd_host_buffer_size", "attn_bwd_local", "attn_fwd_local",
+           "attn_bwd_host", "attn_bwd_host_buffer_size", "attn_bwd_ex", "attn_fwd_ex",
            "attn_check_device_status",
            "attn_set_wait_timeout_ns", "attn_last_error", "attn_version", "attn_diag_mma",
            "attn_diag_wait_timeout", "attn_diag_exp2")
@@ -66,11 +79,12 @@ def lib() -> ctypes.CDLL:
         L.attn_fwd.argtypes = [_T, _T, _T, _T, _P, _I, _I, _I, _I, _I, _I, _I, ctypes.c_float, _I,
                                _P, _P, _I, _I, _P]
         L.attn_fwd.restype = _I
-        L.attn_fwd_local.argtypes = [_T, _T, _T, _T, _P, _I, _I, _I, _I, _I, _I, _I,
-                                     ctypes.c_float, _I, _P, _P, _I, _I, _I, _I, _P]
-        L.attn_fwd_local.restype = _I
-        L.attn_bwd_local.argtypes = _BWD_ARGS[:23] + [_I, _I, _I] + _BWD_ARGS[23:]
-        L.attn_bwd_local.restype = _I
+        L.attn_fwd_ex.argtypes = [_T, _T, _T, _T, _P, _I, _I, _I, _I, _I, _I, _I, ctypes.c_float,
+                                  _I, _P, _P, _I, _I, ctypes.POINTER(AttnOpts), _P]
+        L.attn_fwd_ex.restype = _I
+        L.attn_bwd_ex.argtypes = (_BWD_ARGS[:23] + [ctypes.POINTER(AttnOpts), _I] +
+                                  _BWD_ARGS[23:])
+        L.attn_bwd_ex.restype = _I
         for name in ("attn_bwd", "attn_bwd_preprocess", "attn_bwd_main", "attn_bwd_postprocess"):
             f = getattr(L, name)
             f.argtypes = _BWD_ARGS
@@ -158,10 +172,11 @@ def version() -> str:
 
 def attn_fwd(q, k, v, causal: bool = False, scale: Optional[float] = None, cu_seqlens_q=None,
              cu_seqlens_k=None, max_seqlen_q=None, max_seqlen_k=None, out=None, lse=None,
-             stream=None, window=None) -> Tuple[torch.Tensor, torch.Tensor]:
+             stream=None, window=None, softcap: float = 0.0) -> Tuple[torch.Tensor, torch.Tensor]:
     """Forward pass: returns (O like q, LSE fp32 [B,H,Sq] or [H,total_q], natural log).
 
-    ``window=(left, right)`` selects a local mask (-1 = unbounded side)."""
+    ``window=(left, right)`` selects a local mask (-1 = unbounded side);
+    ``softcap > 0`` caps the logits as softcap * tanh(logit / softcap)."""
     L = lib()
     b, sq, sk, hq, hk, d, mq, mk = _dims(q, k, cu_seqlens_q, cu_seqlens_k, max_seqlen_q,
                                          max_seqlen_k)
@@ -174,10 +189,11 @@ def attn_fwd(q, k, v, causal: bool = False, scale: Optional[float] = None, cu_se
     args = [ctypes.byref(dq_), ctypes.byref(dk_), ctypes.byref(dv_), ctypes.byref(do_), _ptr(lse),
             _dtype_code(q), b, sq, sk, hq, hk, d, scale, int(bool(causal)), _ptr(cu_seqlens_q),
             _ptr(cu_seqlens_k), mq, mk]
-    if window is None:
+    opts = _opts(window, softcap)
+    if opts is None:
         rc = L.attn_fwd(*args, _stream(stream))
     else:
-        rc = L.attn_fwd_local(*args, int(window[0]), int(window[1]), _stream(stream))
+        rc = L.attn_fwd_ex(*args, ctypes.byref(opts), _stream(stream))
     _check(rc)
     return o, lse
 
@@ -214,13 +230,15 @@ _STAGE_MASK = {"all": 7, "pre": 1, "main": 2, "post": 4}
 def attn_bwd(q, k, v, o, lse, do, causal: bool = False, scale: Optional[float] = None,
              cu_seqlens_q=None, cu_seqlens_k=None, max_seqlen_q=None, max_seqlen_k=None,
              deterministic: bool = False, workspace: Optional[torch.Tensor] = None, dq=None,
-             dk=None, dv=None, stream=None, stage: str = "all", window=None):
+             dk=None, dv=None, stream=None, stage: str = "all", window=None,
+             softcap: float = 0.0):
     """Backward pass: returns (dQ, dK, dV), each like its input.
 
     ``stage`` selects one of the three kernels ("pre", "main", "post") or all
     of them in order ("all"); the stages must share the workspace.
     ``window=(left, right)`` selects a local mask (-1 = unbounded side; causal
-    bounds the right side at 0).
+    bounds the right side at 0); ``softcap > 0`` caps the logits as
+    softcap * tanh(logit / softcap) (use the forward's settings).
     """
     L = lib()
     b, sq, sk, hq, hk, d, mq, mk = _dims(q, k, cu_seqlens_q, cu_seqlens_k, max_seqlen_q,
@@ -238,10 +256,11 @@ def attn_bwd(q, k, v, o, lse, do, causal: bool = False, scale: Optional[float] =
             int(bool(causal)), _ptr(cu_seqlens_q), _ptr(cu_seqlens_k), mq, mk,
             int(bool(deterministic))]
     tail = [workspace.data_ptr(), workspace.numel(), _stream(stream)]
-    if window is None:
+    opts = _opts(window, softcap)
+    if opts is None:
         rc = getattr(L, _STAGE_FN[stage])(*args, *tail)
     else:
-        rc = L.attn_bwd_local(*args, int(window[0]), int(window[1]), _STAGE_MASK[stage], *tail)
+        rc = L.attn_bwd_ex(*args, ctypes.byref(opts), _STAGE_MASK[stage], *tail)
     _check(rc)
     return dq, dk, dv
 

@@ -188,19 +188,31 @@ int check_common(int dtype, int batch, int seqlen_q, int seqlen_k, int h_q, int 
   return ATTN_OK;
 }
 
+int resolve_opts(const attn_opts* in, attn_opts* out) {
+  *out = attn_opts{-1, -1, 0.f};
+  if (in == nullptr) return ATTN_OK;
+  if (in->window_left < -1 || in->window_right < -1)
+    return fail(ATTN_ERR_ARG, "window sides must be >= -1 (-1 = unbounded), got (%d, %d)",
+                in->window_left, in->window_right);
+  if (!std::isfinite(in->softcap) || in->softcap < 0.f)
+    return fail(ATTN_ERR_ARG, "softcap must be finite and >= 0 (0 = off), got %g",
+                static_cast<double>(in->softcap));
+  *out = *in;
+  return ATTN_OK;
+}
+
 int prepare_bwd(const attn_tensor* q, const attn_tensor* k, const attn_tensor* v,
                 const attn_tensor* o, const float* lse, const attn_tensor* dout,
                 const attn_tensor* dq, const attn_tensor* dk, const attn_tensor* dv, int dtype,
                 int batch, int seqlen_q, int seqlen_k, int h_q, int h_k, int head_dim,
                 float scale, int causal, const int* cu_q, const int* cu_k, int max_seqlen_q,
-                int max_seqlen_k, int deterministic, int window_left, int window_right,
-                void* workspace, size_t workspace_bytes, Prepared* out) {
+                int max_seqlen_k, int deterministic, const attn_opts* opts_in, void* workspace,
+                size_t workspace_bytes, Prepared* out) {
   int rc = check_common(dtype, batch, seqlen_q, seqlen_k, h_q, h_k, head_dim, scale, cu_q, cu_k,
                         max_seqlen_q, max_seqlen_k);
   if (rc) return rc;
-  if (window_left < -1 || window_right < -1)
-    return fail(ATTN_ERR_ARG, "window sides must be >= -1 (-1 = unbounded), got (%d, %d)",
-                window_left, window_right);
+  attn_opts opts;
+  if ((rc = resolve_opts(opts_in, &opts))) return rc;
   const bool varlen = cu_q != nullptr;
   const bool hq = seqlen_q > 0, hk = seqlen_k > 0;
   if ((rc = check_tensor(q, "q", varlen, hq && hk))) return rc;
@@ -245,8 +257,11 @@ int prepare_bwd(const attn_tensor* q, const attn_tensor* k, const attn_tensor* v
   p.h_q = h_q;
   p.h_k = h_k;
   p.head_dim = head_dim;
-  p.win_left = window_left;
-  p.win_right = causal ? 0 : window_right;  // causal bounds the right side at 0
+  p.win_left = opts.window_left;
+  p.win_right = causal ? 0 : opts.window_right;  // causal bounds the right side at 0
+  p.softcap = opts.softcap;
+  p.cap_in = opts.softcap > 0.f ? scale / opts.softcap : 0.f;
+  p.cap_out = opts.softcap * 1.4426950408889634f;
   p.deterministic = deterministic ? 1 : 0;
   p.scale = scale;
   p.scale_log2 = scale * 1.4426950408889634f;
@@ -324,19 +339,19 @@ using namespace attn;
       scale, causal, cu_seqlens_q, cu_seqlens_k, max_seqlen_q, max_seqlen_k, deterministic, \
       workspace, workspace_bytes
 
-static int bwd_entry_window(int stages, int window_left, int window_right, ATTN_BWD_ARGS_DECL) {
+static int bwd_entry_opts(int stages, const attn_opts* opts, ATTN_BWD_ARGS_DECL) {
   g_err.clear();
   Prepared pr;
   const int rc = prepare_bwd(q, k, v, o, lse, dout, dq, dk, dv, dtype, batch, seqlen_q, seqlen_k,
                              h_q, h_k, head_dim, scale, causal, cu_seqlens_q, cu_seqlens_k,
-                             max_seqlen_q, max_seqlen_k, deterministic, window_left, window_right,
-                             workspace, workspace_bytes, &pr);
+                             max_seqlen_q, max_seqlen_k, deterministic, opts, workspace,
+                             workspace_bytes, &pr);
   if (rc) return rc;
   return run_stages(stages, pr, reinterpret_cast<cudaStream_t>(stream));
 }
 
 static int bwd_entry(int stages, ATTN_BWD_ARGS_DECL) {
-  return bwd_entry_window(stages, -1, -1, ATTN_BWD_ARGS_PASS, stream);
+  return bwd_entry_opts(stages, nullptr, ATTN_BWD_ARGS_PASS, stream);
 }
 
 extern "C" {
@@ -348,19 +363,18 @@ int attn_bwd_postprocess(ATTN_BWD_ARGS_DECL) {
   return bwd_entry(kPost, ATTN_BWD_ARGS_PASS, stream);
 }
 
-int attn_bwd_local(const attn_tensor* q, const attn_tensor* k, const attn_tensor* v,
-                   const attn_tensor* o, const float* lse, const attn_tensor* dout,
-                   const attn_tensor* dq, const attn_tensor* dk, const attn_tensor* dv, int dtype,
-                   int batch, int seqlen_q, int seqlen_k, int h_q, int h_k, int head_dim,
-                   float scale, int causal, const int* cu_seqlens_q, const int* cu_seqlens_k,
-                   int max_seqlen_q, int max_seqlen_k, int deterministic, int window_left,
-                   int window_right, int stages, void* workspace, size_t workspace_bytes,
-                   attn_stream_t stream) {
+int attn_bwd_ex(const attn_tensor* q, const attn_tensor* k, const attn_tensor* v,
+                const attn_tensor* o, const float* lse, const attn_tensor* dout,
+                const attn_tensor* dq, const attn_tensor* dk, const attn_tensor* dv, int dtype,
+                int batch, int seqlen_q, int seqlen_k, int h_q, int h_k, int head_dim, float scale,
+                int causal, const int* cu_seqlens_q, const int* cu_seqlens_k, int max_seqlen_q,
+                int max_seqlen_k, int deterministic, const attn_opts* opts, int stages,
+                void* workspace, size_t workspace_bytes, attn_stream_t stream) {
   if (stages <= 0 || stages > (kPre | kMain | kPost)) {
     g_err.clear();
     return fail(ATTN_ERR_ARG, "stages must be a nonzero mask of 1, 2 and 4, got %d", stages);
   }
-  return bwd_entry_window(stages, window_left, window_right, ATTN_BWD_ARGS_PASS, stream);
+  return bwd_entry_opts(stages, opts, ATTN_BWD_ARGS_PASS, stream);
 }
 
 size_t attn_bwd_workspace_size(int batch, int seqlen_q, int h_q, int head_dim, int deterministic,
@@ -382,18 +396,17 @@ int attn_bwd_workspace_layout(int batch, int seqlen_q, int h_q, int head_dim, in
   return ATTN_OK;
 }
 
-int attn_fwd_local(const attn_tensor* q, const attn_tensor* k, const attn_tensor* v,
-                   const attn_tensor* o, float* lse, int dtype, int batch, int seqlen_q,
-                   int seqlen_k, int h_q, int h_k, int head_dim, float scale, int causal,
-                   const int* cu_seqlens_q, const int* cu_seqlens_k, int max_seqlen_q,
-                   int max_seqlen_k, int window_left, int window_right, attn_stream_t stream) {
+int attn_fwd_ex(const attn_tensor* q, const attn_tensor* k, const attn_tensor* v,
+                const attn_tensor* o, float* lse, int dtype, int batch, int seqlen_q, int seqlen_k,
+                int h_q, int h_k, int head_dim, float scale, int causal, const int* cu_seqlens_q,
+                const int* cu_seqlens_k, int max_seqlen_q, int max_seqlen_k,
+                const attn_opts* opts_in, attn_stream_t stream) {
   g_err.clear();
   int rc = check_common(dtype, batch, seqlen_q, seqlen_k, h_q, h_k, head_dim, scale,
                         cu_seqlens_q, cu_seqlens_k, max_seqlen_q, max_seqlen_k);
   if (rc) return rc;
-  if (window_left < -1 || window_right < -1)
-    return fail(ATTN_ERR_ARG, "window sides must be >= -1 (-1 = unbounded), got (%d, %d)",
-                window_left, window_right);
+  attn_opts opts;
+  if ((rc = resolve_opts(opts_in, &opts))) return rc;
   const bool varlen = cu_seqlens_q != nullptr;
   if (seqlen_q == 0) return ATTN_OK;
   if ((rc = check_tensor(q, "q", varlen, true))) return rc;
@@ -412,8 +425,11 @@ int attn_fwd_local(const attn_tensor* q, const attn_tensor* k, const attn_tensor
   p.h_q = h_q;
   p.h_k = h_k;
   p.head_dim = head_dim;
-  p.win_left = window_left;
-  p.win_right = causal ? 0 : window_right;  // causal bounds the right side at 0
+  p.win_left = opts.window_left;
+  p.win_right = causal ? 0 : opts.window_right;  // causal bounds the right side at 0
+  p.softcap = opts.softcap;
+  p.cap_in = opts.softcap > 0.f ? scale / opts.softcap : 0.f;
+  p.cap_out = opts.softcap * 1.4426950408889634f;
   p.scale_log2 = scale * 1.4426950408889634f;
   p.max_seqlen_q = varlen ? max_seqlen_q : seqlen_q;
   if (p.max_seqlen_q == 0) return ATTN_OK;
@@ -435,9 +451,9 @@ int attn_fwd(const attn_tensor* q, const attn_tensor* k, const attn_tensor* v,
              const attn_tensor* o, float* lse, int dtype, int batch, int seqlen_q, int seqlen_k,
              int h_q, int h_k, int head_dim, float scale, int causal, const int* cu_seqlens_q,
              const int* cu_seqlens_k, int max_seqlen_q, int max_seqlen_k, attn_stream_t stream) {
-  return attn_fwd_local(q, k, v, o, lse, dtype, batch, seqlen_q, seqlen_k, h_q, h_k, head_dim,
-                        scale, causal, cu_seqlens_q, cu_seqlens_k, max_seqlen_q, max_seqlen_k, -1,
-                        -1, stream);
+  return attn_fwd_ex(q, k, v, o, lse, dtype, batch, seqlen_q, seqlen_k, h_q, h_k, head_dim,
+                     scale, causal, cu_seqlens_q, cu_seqlens_k, max_seqlen_q, max_seqlen_k,
+                     nullptr, stream);
 }
 
 int attn_check_device_status(attn_stream_t stream) {

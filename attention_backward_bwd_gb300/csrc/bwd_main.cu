@@ -161,7 +161,7 @@ __device__ __forceinline__ void iter_hm(const Unit& un, int j, int G, int& h, in
   m = un.m_start + un.m_count - 1 - jm;
 }
 
-template <typename T, int D>
+template <typename T, int D, bool kCap>
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_main_kernel(const BwdParams p, const __grid_constant__ CUtensorMap tmQ,
                     const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
@@ -516,16 +516,34 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int c = 0; c < kCols / 32; ++c) tmem_ld32p(tl + TM_S + c0 + 32 * c, sv + 32 * c);
           tmem_wait_ld();
-          // P^T = exp2(S^T * scale * log2 e - LSE2[query]), masked
+          // P^T = exp2(S^T * scale * log2 e - LSE2[query]), masked.  With a logit
+          // cap the logit is c tanh(S^T scale / c), and the cap's derivative
+          // 1 - tanh^2 goes (packed) into the half of this group's S^T columns
+          // that P^T does not use, for the dS phase.
           uint32_t pk[kCols / 2];
 #pragma unroll
           for (int e4 = 0; e4 < kCols / 4; ++e4) {
             const float4 l = reinterpret_cast<const float4*>(lse2)[e4];
             const uint32_t* v = sv + e4 * 4;
-            float x0 = ex2(fmaf(__uint_as_float(v[0]), sl2, -l.x));
-            float x1 = ex2(fmaf(__uint_as_float(v[1]), sl2, -l.y));
-            float x2 = ex2(fmaf(__uint_as_float(v[2]), sl2, -l.z));
-            float x3 = ex2(fmaf(__uint_as_float(v[3]), sl2, -l.w));
+            float x0, x1, x2, x3;
+            if constexpr (kCap) {
+              const float t0 = tanhf(__uint_as_float(v[0]) * p.cap_in);
+              const float t1 = tanhf(__uint_as_float(v[1]) * p.cap_in);
+              const float t2 = tanhf(__uint_as_float(v[2]) * p.cap_in);
+              const float t3 = tanhf(__uint_as_float(v[3]) * p.cap_in);
+              x0 = ex2(fmaf(t0, p.cap_out, -l.x));
+              x1 = ex2(fmaf(t1, p.cap_out, -l.y));
+              x2 = ex2(fmaf(t2, p.cap_out, -l.z));
+              x3 = ex2(fmaf(t3, p.cap_out, -l.w));
+              // sv is no longer needed: its first half holds the packed derivative
+              sv[e4 * 2] = Pack<T>::two(fmaf(-t0, t0, 1.f), fmaf(-t1, t1, 1.f));
+              sv[e4 * 2 + 1] = Pack<T>::two(fmaf(-t2, t2, 1.f), fmaf(-t3, t3, 1.f));
+            } else {
+              x0 = ex2(fmaf(__uint_as_float(v[0]), sl2, -l.x));
+              x1 = ex2(fmaf(__uint_as_float(v[1]), sl2, -l.y));
+              x2 = ex2(fmaf(__uint_as_float(v[2]), sl2, -l.z));
+              x3 = ex2(fmaf(__uint_as_float(v[3]), sl2, -l.w));
+            }
             if (need_mask) {
               const int c = e4 * 4;
               x0 = (c + 0 >= lo && c + 0 < hi) ? x0 : 0.f;
@@ -539,6 +557,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int c = 0; c < kCols / 32; ++c)
             tmem_st16(tl + TM_P + c0 + 16 * c, *reinterpret_cast<uint32_t(*)[16]>(pk + 16 * c));
+          if constexpr (kCap) {
+#pragma unroll
+            for (int c = 0; c < kCols / 32; ++c)
+              tmem_st16(tl + TM_S + c0 + kCols / 2 + 16 * c,
+                        *reinterpret_cast<uint32_t(*)[16]>(sv + 16 * c));
+          }
         }
         tmem_wait_st();
         tc_fence_before();
@@ -557,12 +581,19 @@ __global__ void __launch_bounds__(kThreads, 1)
           // [64 c, +64): row jl is 128 bytes and its 16-byte unit u is stored
           // at u ^ (jl % 8) (128-byte swizzle).
           uint32_t dpv[kCols], pv[kCols / 2];
+          uint32_t cv[kCap ? kCols / 2 : 1];  // packed cap derivative (logit cap only)
 #pragma unroll
           for (int c = 0; c < kCols / 32; ++c) tmem_ld32p(tl + TM_DP + c0 + 32 * c, dpv + 32 * c);
           if (kCols == 64) {
             tmem_ld32p(tl + TM_P + c0, pv);
           } else {
             tmem_ld16(tl + TM_P + c0, *reinterpret_cast<uint32_t(*)[16]>(pv));
+          }
+          if constexpr (kCap) {
+#pragma unroll
+            for (int c = 0; c < kCols / 32; ++c)
+              tmem_ld16(tl + TM_S + c0 + kCols / 2 + 16 * c,
+                        *reinterpret_cast<uint32_t(*)[16]>(cv + 16 * c));
           }
           tmem_wait_ld();
           // P^T has been read: the next tile's S^T may overwrite it
@@ -577,8 +608,16 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int e4 = 0; e4 < 8; ++e4) {
               const float4 dl = reinterpret_cast<const float4*>(dlt)[sub * 8 + e4];
-              const float2 p01 = Pack<T>::unpack(pv[sub * 16 + e4 * 2]);
-              const float2 p23 = Pack<T>::unpack(pv[sub * 16 + e4 * 2 + 1]);
+              float2 p01 = Pack<T>::unpack(pv[sub * 16 + e4 * 2]);
+              float2 p23 = Pack<T>::unpack(pv[sub * 16 + e4 * 2 + 1]);
+              if constexpr (kCap) {  // dS of the uncapped logit: times 1 - tanh^2
+                const float2 c01 = Pack<T>::unpack(cv[sub * 16 + e4 * 2]);
+                const float2 c23 = Pack<T>::unpack(cv[sub * 16 + e4 * 2 + 1]);
+                p01.x *= c01.x;
+                p01.y *= c01.y;
+                p23.x *= c23.x;
+                p23.y *= c23.y;
+              }
               const uint32_t* v = dpv + sub * 32 + e4 * 4;
               pk[e4 * 2] = Pack<T>::two(p01.x * (__uint_as_float(v[0]) - dl.x),
                                         p01.y * (__uint_as_float(v[1]) - dl.y));
@@ -762,7 +801,7 @@ done:
   if (warp == 2) tmem_dealloc(tmem, kTmemCols);
 }
 
-template <typename T, int D>
+template <typename T, int D, bool kCap>
 cudaError_t launch_t(const BwdParams& p, int dtype, cudaStream_t stream) {
   const bool varlen = p.seq.cu_q != nullptr;
   const int nb = varlen ? 1 : p.seq.batch;
@@ -782,13 +821,13 @@ cudaError_t launch_t(const BwdParams& p, int dtype, cudaStream_t stream) {
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
     return cudaErrorInvalidDevice;
   if (!attr_done[dev].load(std::memory_order_acquire)) {
-    cudaError_t e = cudaFuncSetAttribute(bwd_main_kernel<T, D>,
+    cudaError_t e = cudaFuncSetAttribute(bwd_main_kernel<T, D, kCap>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     // The warpgroup register split assumes exactly kRegLaunch registers per
     // thread at launch; anything else could leave a register increase waiting.
     cudaFuncAttributes fa;
-    e = cudaFuncGetAttributes(&fa, bwd_main_kernel<T, D>);
+    e = cudaFuncGetAttributes(&fa, bwd_main_kernel<T, D, kCap>);
     if (e != cudaSuccess) return e;
     if (fa.numRegs != static_cast<int>(kRegLaunch)) return cudaErrorInvalidConfiguration;
     attr_done[dev].store(true, std::memory_order_release);
@@ -797,19 +836,26 @@ cudaError_t launch_t(const BwdParams& p, int dtype, cudaStream_t stream) {
   const int units = n_tiles * p.seq.batch * p.h_k;
   if (units <= 0) return cudaSuccess;
   const int grid = units < num_sms() ? units : num_sms();
-  bwd_main_kernel<T, D><<<grid, kThreads, smem, stream>>>(p, tq, tk, tv, tdo, tdq);
+  bwd_main_kernel<T, D, kCap><<<grid, kThreads, smem, stream>>>(p, tq, tk, tv, tdo, tdq);
   return cudaGetLastError();
+}
+
+template <bool kCap>
+cudaError_t launch_cap(const BwdParams& p, int dtype, cudaStream_t stream) {
+  if (dtype == 1) {
+    return p.head_dim == 64 ? launch_t<__nv_bfloat16, 64, kCap>(p, dtype, stream)
+                            : launch_t<__nv_bfloat16, 128, kCap>(p, dtype, stream);
+  }
+  return p.head_dim == 64 ? launch_t<__half, 64, kCap>(p, dtype, stream)
+                          : launch_t<__half, 128, kCap>(p, dtype, stream);
 }
 
 }  // namespace
 
 cudaError_t launch_bwd_main(const BwdParams& p, int dtype, cudaStream_t stream) {
-  if (dtype == 1) {
-    return p.head_dim == 64 ? launch_t<__nv_bfloat16, 64>(p, dtype, stream)
-                            : launch_t<__nv_bfloat16, 128>(p, dtype, stream);
-  }
-  return p.head_dim == 64 ? launch_t<__half, 64>(p, dtype, stream)
-                          : launch_t<__half, 128>(p, dtype, stream);
+  // the logit cap is a separate instantiation: the default kernel keeps its code
+  return p.softcap > 0.f ? launch_cap<true>(p, dtype, stream)
+                         : launch_cap<false>(p, dtype, stream);
 }
 
 }  // namespace attn

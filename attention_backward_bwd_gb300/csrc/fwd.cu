@@ -177,7 +177,9 @@ __global__ void __launch_bounds__(kFwdThreads) fwd_kernel(FwdParams p) {
     for (int nt = 0; nt < 8; ++nt) {
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
-        float x = s[nt][e] * p.scale_log2;
+        // logit in log2 units; with a cap c: c tanh(S scale / c) log2 e
+        float x = p.softcap > 0.f ? tanhf(s[nt][e] * p.cap_in) * p.cap_out
+                                  : s[nt][e] * p.scale_log2;
         if (need_mask) {
           const int key = n * kBN + nt * 8 + 2 * t + (e & 1);
           const int row = row_lo + (e >> 1) * 8;

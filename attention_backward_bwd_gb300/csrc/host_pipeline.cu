@@ -292,7 +292,8 @@ extern "C" int attn_bwd_host(const attn_tensor* q, const attn_tensor* k, const a
     Prepared pr;
     rc = prepare_bwd(&tq, &tk, &tv, &to, tlse, &tdo, &tdq, &tdk, &tdv, dtype, nb, seqlen_q,
                      seqlen_k, ni, nj, head_dim, scale, causal, nullptr, nullptr, seqlen_q,
-                     seqlen_k, deterministic, -1, -1, buf + L.ws[c % kSlots], L.ws_bytes, &pr);
+                     seqlen_k, deterministic, nullptr, buf + L.ws[c % kSlots], L.ws_bytes,
+                     &pr);
     if (rc) return rc;
     if ((rc = run_stages(kPre | kMain | kPost, pr, cs))) return rc;
     if ((e = cudaEventRecord(P->comp_done[c], cs)) != cudaSuccess) return cuda_fail(e, "record");

@@ -46,6 +46,9 @@ struct BwdParams {
   int win_left, win_right;  // local mask sides, -1 = unbounded; causal is (-1, 0)
   int deterministic;
   float scale, scale_log2;
+  // logit cap c (0 = off): P = exp2(cap_out * tanh(S * cap_in) - LSE2) with
+  // cap_in = scale / c and cap_out = c * log2(e); dS gains the factor 1 - tanh^2
+  float softcap, cap_in, cap_out;
   int max_seqlen_q, max_seqlen_k;
   unsigned int* status;
   const unsigned int* input_bad;  // nonzero after cu_seqlens failed validation (varlen)
@@ -59,6 +62,7 @@ struct FwdParams {
   int h_q, h_k, head_dim;
   int win_left, win_right;  // local mask sides, -1 = unbounded; causal is (-1, 0)
   float scale_log2;
+  float softcap, cap_in, cap_out;  // logit cap as in BwdParams (0 = off)
   int max_seqlen_q;
   const unsigned int* input_bad;
 };
@@ -139,8 +143,11 @@ int prepare_bwd(const attn_tensor* q, const attn_tensor* k, const attn_tensor* v
                 const attn_tensor* dq, const attn_tensor* dk, const attn_tensor* dv, int dtype,
                 int batch, int seqlen_q, int seqlen_k, int h_q, int h_k, int head_dim,
                 float scale, int causal, const int* cu_q, const int* cu_k, int max_seqlen_q,
-                int max_seqlen_k, int deterministic, int window_left, int window_right,
-                void* workspace, size_t workspace_bytes, Prepared* out);
+                int max_seqlen_k, int deterministic, const attn_opts* opts, void* workspace,
+                size_t workspace_bytes, Prepared* out);
+
+// NULL -> no window, no cap; checks the values (ATTN_ERR_ARG).
+int resolve_opts(const attn_opts* in, attn_opts* out);
 
 enum Stage { kPre = 1, kMain = 2, kPost = 4 };
 

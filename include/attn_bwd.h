@@ -131,35 +131,52 @@ int attn_bwd(const attn_tensor* q, const attn_tensor* k, const attn_tensor* v,
              size_t workspace_bytes, attn_stream_t stream);
 
 /*
- * attn_bwd_local / attn_fwd_local -- the same calls with a local
- * (sliding-window) mask, the window (window_left, window_right) of
- * flash-attention csrc/flash_attn_ck/mha_bwd.cpp (mha_bwd's mask set-up),
- * -1 meaning unbounded on that side.  Bottom-right aligned like causal: with
- * off = Sk - Sq (per sequence in varlen mode), query i attends key j iff
- * j >= i + off - window_left (when window_left >= 0) and
- * j <= i + off + window_right (when window_right >= 0).  causal != 0 sets
- * window_right to 0, so (window_left = W, causal = 1) is sliding-window causal
- * attention and (-1, -1, causal = 0) is attn_bwd / attn_fwd.  Rows that see no
- * key get O = 0, LSE = +inf, dQ = 0; keys that no query sees get dK = dV = 0.
- * attn_bwd_local runs the stages selected by the bit mask `stages` (1 =
- * preprocess, 2 = main, 4 = postprocess; 7 = all, in that order); the stages
- * of one backward must share the workspace and the window.  Window sides
- * below -1, or a stage mask outside 1..7, give ATTN_ERR_ARG.  Deterministic
- * mode orders the dQ adds of each query tile over the key tiles that see it.
+ * attn_opts -- optional mask and logit settings of attn_fwd_ex / attn_bwd_ex
+ * (NULL = no window, no cap: the behaviour of attn_fwd / attn_bwd).  Note
+ * that a zeroed struct is NOT that default: window (0, 0) lets each query see
+ * one key.
+ *   window_left, window_right: a local (sliding-window) mask, the window of
+ *     flash-attention csrc/flash_attn_ck/mha_bwd.cpp (mha_bwd's mask set-up),
+ *     -1 meaning unbounded on that side.  Bottom-right aligned like causal:
+ *     with off = Sk - Sq (per sequence in varlen mode), query i attends key j
+ *     iff j >= i + off - window_left (when window_left >= 0) and
+ *     j <= i + off + window_right (when window_right >= 0).  causal != 0 sets
+ *     window_right to 0, so (window_left = W, causal = 1) is sliding-window
+ *     causal attention.  Rows that see no key get O = 0, LSE = +inf, dQ = 0;
+ *     keys that no query sees get dK = dV = 0.
+ *   softcap: > 0 caps the logits s = scale * q.k as softcap * tanh(s / softcap)
+ *     before the softmax (the Has_softcap path of flash-attention
+ *     hopper/flash_bwd_launch_template.h; the formula is the usual logit cap);
+ *     the backward applies the cap's derivative.  0 = no cap.
+ * Window sides below -1, a negative or non-finite softcap give ATTN_ERR_ARG.
  */
-int attn_bwd_local(const attn_tensor* q, const attn_tensor* k, const attn_tensor* v,
-                   const attn_tensor* o, const float* lse, const attn_tensor* dout,
-                   const attn_tensor* dq, const attn_tensor* dk, const attn_tensor* dv, int dtype,
-                   int batch, int seqlen_q, int seqlen_k, int h_q, int h_k, int head_dim,
-                   float scale, int causal, const int* cu_seqlens_q, const int* cu_seqlens_k,
-                   int max_seqlen_q, int max_seqlen_k, int deterministic, int window_left,
-                   int window_right, int stages, void* workspace, size_t workspace_bytes,
-                   attn_stream_t stream);
-int attn_fwd_local(const attn_tensor* q, const attn_tensor* k, const attn_tensor* v,
-                   const attn_tensor* o, float* lse, int dtype, int batch, int seqlen_q,
-                   int seqlen_k, int h_q, int h_k, int head_dim, float scale, int causal,
-                   const int* cu_seqlens_q, const int* cu_seqlens_k, int max_seqlen_q,
-                   int max_seqlen_k, int window_left, int window_right, attn_stream_t stream);
+typedef struct {
+  int window_left;
+  int window_right;
+  float softcap;
+} attn_opts;
+
+/*
+ * attn_bwd_ex -- attn_bwd with attn_opts, running the stages selected by the
+ * bit mask `stages` (1 = preprocess, 2 = main, 4 = postprocess; 7 = all, in
+ * that order; outside 1..7: ATTN_ERR_ARG).  The stages of one backward must
+ * share the workspace and the options.  Deterministic mode orders the dQ adds
+ * of each query tile over the key tiles that see it.
+ * attn_fwd_ex -- attn_fwd with attn_opts (produces the O and LSE that
+ * attn_bwd_ex with the same options consumes).
+ */
+int attn_bwd_ex(const attn_tensor* q, const attn_tensor* k, const attn_tensor* v,
+                const attn_tensor* o, const float* lse, const attn_tensor* dout,
+                const attn_tensor* dq, const attn_tensor* dk, const attn_tensor* dv, int dtype,
+                int batch, int seqlen_q, int seqlen_k, int h_q, int h_k, int head_dim, float scale,
+                int causal, const int* cu_seqlens_q, const int* cu_seqlens_k, int max_seqlen_q,
+                int max_seqlen_k, int deterministic, const attn_opts* opts, int stages,
+                void* workspace, size_t workspace_bytes, attn_stream_t stream);
+int attn_fwd_ex(const attn_tensor* q, const attn_tensor* k, const attn_tensor* v,
+                const attn_tensor* o, float* lse, int dtype, int batch, int seqlen_q, int seqlen_k,
+                int h_q, int h_k, int head_dim, float scale, int causal, const int* cu_seqlens_q,
+                const int* cu_seqlens_k, int max_seqlen_q, int max_seqlen_k,
+                const attn_opts* opts, attn_stream_t stream);
 
 /*
  * attn_bwd_noalloc -- attn_bwd with no workspace argument, for callers that

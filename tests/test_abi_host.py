@@ -155,24 +155,28 @@ def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
         binding.lib()
 
 
-def test_local_window_argument_errors(lib):
-    """attn_bwd_local / attn_fwd_local reject window sides below -1 and stage
-    masks outside 1..7 before launching anything."""
+def test_extended_options_argument_errors(lib):
+    """attn_bwd_ex / attn_fwd_ex reject window sides below -1, a negative or
+    non-finite softcap and stage masks outside 1..7 before launching anything."""
     from attention_backward_bwd_gb300 import binding as bd
     q, k, v, o, do = shapes()
     ds = [bd._desc(t) for t in (q, k, v, o)]
     d_do, d_dq, d_dk, d_dv = bd._desc(do), bd._desc(q), bd._desc(k), bd._desc(v)
 
-    def bwd(left, right, stages):
-        return lib.attn_bwd_local(*(ctypes.byref(x) for x in ds), 1 << 21, ctypes.byref(d_do),
-                                  ctypes.byref(d_dq), ctypes.byref(d_dk), ctypes.byref(d_dv), 1,
-                                  1, 64, 64, 2, 2, 64, 0.125, 0, None, None, 64, 64, 0, left,
-                                  right, stages, 1 << 24, 1 << 30, None)
+    def bwd(left, right, cap, stages):
+        opts = bd.AttnOpts(left, right, cap)
+        return lib.attn_bwd_ex(*(ctypes.byref(x) for x in ds), 1 << 21, ctypes.byref(d_do),
+                               ctypes.byref(d_dq), ctypes.byref(d_dk), ctypes.byref(d_dv), 1, 1,
+                               64, 64, 2, 2, 64, 0.125, 0, None, None, 64, 64, 0,
+                               ctypes.byref(opts), stages, 1 << 24, 1 << 30, None)
 
-    assert bwd(-2, 0, 7) == -9 and b"window" in lib.attn_last_error()
-    assert bwd(3, -5, 7) == -9
-    assert bwd(3, 0, 0) == -9 and b"stages" in lib.attn_last_error()
-    assert bwd(3, 0, 8) == -9
-    rc = lib.attn_fwd_local(*(ctypes.byref(x) for x in ds), 1 << 21, 1, 1, 64, 64, 2, 2, 64,
-                            0.125, 0, None, None, 64, 64, -3, 0, None)
+    assert bwd(-2, 0, 0.0, 7) == -9 and b"window" in lib.attn_last_error()
+    assert bwd(3, -5, 0.0, 7) == -9
+    assert bwd(3, 0, -1.0, 7) == -9 and b"softcap" in lib.attn_last_error()
+    assert bwd(3, 0, float("inf"), 7) == -9
+    assert bwd(3, 0, 0.0, 0) == -9 and b"stages" in lib.attn_last_error()
+    assert bwd(3, 0, 0.0, 8) == -9
+    bad = bd.AttnOpts(-3, 0, 0.0)
+    rc = lib.attn_fwd_ex(*(ctypes.byref(x) for x in ds), 1 << 21, 1, 1, 64, 64, 2, 2, 64, 0.125,
+                         0, None, None, 64, 64, ctypes.byref(bad), None)
     assert rc == -9 and b"window" in lib.attn_last_error()

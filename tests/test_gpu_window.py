@@ -1,6 +1,6 @@
 """Local (sliding-window) masks on the GPU against the fp64 oracle.
 
-attn_fwd_local + attn_bwd_local (through the binding's ``window=``) on shapes
+attn_fwd_ex + attn_bwd_ex (through the binding's ``window=``) on shapes
 that put the window's edges inside tiles, leave whole key tiles unseen
 (dK = dV = 0 there) or whole query rows without keys (dQ = 0, O = 0), and in
 deterministic mode, where the dQ adds of a query tile are ordered over the key
