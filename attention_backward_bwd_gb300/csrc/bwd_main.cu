@@ -527,10 +527,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t* v = sv + e4 * 4;
             float x0, x1, x2, x3;
             if constexpr (kCap) {
-              const float t0 = tanhf(__uint_as_float(v[0]) * p.cap_in);
-              const float t1 = tanhf(__uint_as_float(v[1]) * p.cap_in);
-              const float t2 = tanhf(__uint_as_float(v[2]) * p.cap_in);
-              const float t3 = tanhf(__uint_as_float(v[3]) * p.cap_in);
+              const float t0 = tanh_exp(__uint_as_float(v[0]) * p.cap_in);
+              const float t1 = tanh_exp(__uint_as_float(v[1]) * p.cap_in);
+              const float t2 = tanh_exp(__uint_as_float(v[2]) * p.cap_in);
+              const float t3 = tanh_exp(__uint_as_float(v[3]) * p.cap_in);
               x0 = ex2(fmaf(t0, p.cap_out, -l.x));
               x1 = ex2(fmaf(t1, p.cap_out, -l.y));
               x2 = ex2(fmaf(t2, p.cap_out, -l.z));

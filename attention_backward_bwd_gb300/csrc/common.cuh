@@ -297,6 +297,21 @@ __device__ __forceinline__ float ex2(float x) {
   return y;
 }
 
+__device__ __forceinline__ float rcp_approx(float x) {
+  float y;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// tanh(x) from the identity tanh(x) = 1 - 2 / (e^{2x} + 1), with e^{2x} =
+// 2^{2x log2 e} from the hardware exponential and a hardware reciprocal: two
+// special-function operations.  The absolute error stays near 1e-7 (the
+// exponential's and the reciprocal's rounding), and the limits come out
+// exactly: e^{2x} = inf gives 1, e^{2x} = 0 gives -1.
+__device__ __forceinline__ float tanh_exp(float x) {
+  return 1.f - 2.f * rcp_approx(ex2(x * 2.8853900817779268f) + 1.f);
+}
+
 // 2^x on the FMA/ALU pipes (no MUFU), for x in [-125, 1].  Range reduction
 // x = j + f with j = round(x) (the 1.5 * 2^23 rounding trick) and f in
 // [-0.5, 0.5]; 2^f by a degree-3 polynomial whose coefficients were fitted for

@@ -151,6 +151,11 @@ __global__ void diag_exp2_kernel(const float* x, float* y, int n) {
     y[i] = ex2_poly(x[i]);
 }
 
+__global__ void diag_tanh_kernel(const float* x, float* y, int n) {
+  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x)
+    y[i] = tanh_exp(x[i]);
+}
+
 template <typename T, int D>
 int diag_mma_t(int mode, const void* a, const void* b, float* c, cudaStream_t stream,
                unsigned int* status, unsigned long long timeout_ns) {
@@ -197,6 +202,13 @@ int attn_diag_exp2(const float* x, float* y, int n, attn_stream_t stream) {
   if (x == nullptr || y == nullptr) return ATTN_ERR_NULL;
   if (n <= 0) return ATTN_ERR_ARG;
   diag_exp2_kernel<<<64, 256, 0, reinterpret_cast<cudaStream_t>(stream)>>>(x, y, n);
+  return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+int attn_diag_tanh(const float* x, float* y, int n, attn_stream_t stream) {
+  if (x == nullptr || y == nullptr) return ATTN_ERR_NULL;
+  if (n <= 0) return ATTN_ERR_ARG;
+  diag_tanh_kernel<<<64, 256, 0, reinterpret_cast<cudaStream_t>(stream)>>>(x, y, n);
   return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 

@@ -178,7 +178,7 @@ __global__ void __launch_bounds__(kFwdThreads) fwd_kernel(FwdParams p) {
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
         // logit in log2 units; with a cap c: c tanh(S scale / c) log2 e
-        float x = p.softcap > 0.f ? tanhf(s[nt][e] * p.cap_in) * p.cap_out
+        float x = p.softcap > 0.f ? tanh_exp(s[nt][e] * p.cap_in) * p.cap_out
                                   : s[nt][e] * p.scale_log2;
         if (need_mask) {
           const int key = n * kBN + nt * 8 + 2 * t + (e & 1);

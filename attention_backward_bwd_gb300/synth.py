@@ -43,6 +43,7 @@ class Workload:
     len_lo: int = 0
     len_hi: int = 0
     window: tuple = (-1, -1)  # local mask (left, right), -1 = unbounded side
+    softcap: float = 0.0      # logit cap c (0 = none)
 
     @property
     def windowed(self) -> bool:
@@ -76,6 +77,9 @@ WORKLOADS = {
     "gqa_b2_hq32_hk8_s8192_d128_bf16_causal_win1024": Workload(
         "gqa_b2_hq32_hk8_s8192_d128_bf16_causal_win1024", 2, 32, 8, 8192, 8192, 128, "bf16", True,
         3, window=(1024, -1)),
+    "gqa_b2_hq32_hk8_s8192_d128_bf16_causal_cap30": Workload(
+        "gqa_b2_hq32_hk8_s8192_d128_bf16_causal_cap30", 2, 32, 8, 8192, 8192, 128, "bf16", True,
+        3, softcap=30.0),
     "varlen16_h16_d128_bf16_causal": Workload(
         "varlen16_h16_d128_bf16_causal", 0, 16, 16, 0, 0, 128, "bf16", True, 4,
         n_seqs=16, len_lo=128, len_hi=8192),

@@ -200,12 +200,12 @@ def run_ours(args):
     q, k, v, do = (t.to(dev) for t in (x.q, x.k, x.v, x.do))
     window = tuple(w.window) if w.windowed else None
     o, lse = ab.attn_fwd(q, k, v, causal=w.causal, cu_seqlens_q=cu_q, cu_seqlens_k=cu_k,
-                         max_seqlen_q=mq, max_seqlen_k=mk, window=window)
+                         max_seqlen_q=mq, max_seqlen_k=mk, window=window, softcap=w.softcap)
     ws = ab.alloc_workspace(q, cu_q, det)
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
     kw = dict(causal=w.causal, cu_seqlens_q=cu_q, cu_seqlens_k=cu_k, max_seqlen_q=mq,
               max_seqlen_k=mk, deterministic=det, workspace=ws, dq=dq, dk=dk, dv=dv,
-              window=window)
+              window=window, softcap=w.softcap)
     stream = torch.cuda.current_stream()
     flops = bwd_flops(w, x.lengths)
     in_bytes = sum(t.numel() * t.element_size() for t in (q, k, v, o, do, lse))
@@ -247,13 +247,13 @@ def run_ours(args):
 
     # --- end to end: pinned host inputs -> device -> backward -> pinned host results.
     # Padded unmasked or causal workloads go through attn_bwd_host (chunks whose
-    # copies overlap the kernels of other chunks); varlen and windowed ones copy
-    # in, call attn_bwd, copy out.
+    # copies overlap the kernels of other chunks); varlen, windowed and capped
+    # ones copy in, call attn_bwd, copy out.
     hq_ = [t.cpu().pin_memory() for t in (q, k, v, o, do, lse)]
     host_out = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in (dq, dk, dv)]
     h2d = sum(t.numel() * t.element_size() for t in hq_)
     d2h = sum(t.numel() * t.element_size() for t in host_out)
-    if not w.varlen and not w.windowed:
+    if not w.varlen and not w.windowed and not w.softcap:
         b_, sq_, hq_n, d_ = q.shape
         hbuf = torch.empty(ab.host_buffer_size(b_, sq_, k.shape[1], hq_n, k.shape[2], d_,
                                                args.chunks), dtype=torch.uint8, device=dev)
@@ -307,6 +307,8 @@ def run_ours(args):
            "parallelism": f"replicas x{world}" if world > 1 else "single GPU"}
     if w.varlen:
         cfg["lengths"] = x.lengths
+    if w.softcap:
+        cfg["softcap"] = w.softcap
     if w.windowed:
         cfg["window"] = list(w.window)
         cfg["flops"] = "10 D per allowed (query, key) pair, counted exactly"
@@ -366,7 +368,8 @@ def oracle_sample(w, x, n_heads=1):
     def run(h):
         return attn_oracle.head_backward(sl(q, h).double().numpy(), sl(k, h // g).double().numpy(),
                                          sl(v, h // g).double().numpy(),
-                                         sl(do, h).double().numpy(), w.scale, w.causal, window)
+                                         sl(do, h).double().numpy(), w.scale, w.causal, window,
+                                         w.softcap)
     if w.windowed:
         f_one = 10.0 * w.head_dim * window_pairs(L, L, w.causal, w.window)
     else:

@@ -42,6 +42,14 @@ int attn_diag_mma(int mode, int dtype, int head_dim, const void* a, const void* 
 int attn_diag_exp2(const float* x, float* y, int n, attn_stream_t stream);
 
 /*
+ * attn_diag_tanh -- y[i] = tanh(x[i]) computed as the logit cap of the
+ * kernels does (1 - 2 / (e^{2x} + 1) from the hardware exponential and
+ * reciprocal), so its error can be checked against a reference.
+ * x, y: device fp32 arrays of n elements.
+ */
+int attn_diag_tanh(const float* x, float* y, int n, attn_stream_t stream);
+
+/*
  * attn_diag_wait_timeout -- launches a kernel whose only work is a bounded wait
  * on a barrier that nothing completes.  After timeout_ns (1 .. 2e9) the wait
  * gives up, so attn_check_device_status(stream) must then return

@@ -46,6 +46,19 @@ def test_diag_exp2_polynomial_accuracy():
     assert rel <= 1e-4, rel
 
 
+def test_diag_tanh_accuracy():
+    """The logit cap's tanh (1 - 2 / (e^{2x} + 1) from the hardware exponential
+    and reciprocal): absolute error <= 2e-6 against float64 over the range the
+    cap feeds it, exact limits at +-inf-like inputs, odd to within the bound."""
+    x = torch.cat([torch.linspace(-40.0, 40.0, 1 << 20),
+                   torch.tensor([0.0, 1e-6, -1e-6, 1e4, -1e4, 89.0, -89.0])])
+    y = ab.diag_tanh(x.cuda()).cpu().double()
+    ref = torch.tanh(x.double())
+    assert (y - ref).abs().max().item() <= 2e-6
+    assert y[-4].item() == 1.0 and y[-3].item() == -1.0
+    assert (y + ab.diag_tanh(-x.cuda()).cpu().double()).abs().max().item() <= 4e-6
+
+
 def test_device_wait_timeout_is_reported():
     ab.diag_wait_timeout(50_000_000)  # 50 ms on a barrier nothing completes
     with pytest.raises(ab.AttnError) as e:
