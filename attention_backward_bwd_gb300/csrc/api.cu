@@ -168,8 +168,8 @@ int check_common(int dtype, int batch, int seqlen_q, int seqlen_k, int h_q, int 
                  int max_seqlen_q, int max_seqlen_k) {
   if (dtype != ATTN_FP16 && dtype != ATTN_BF16)
     return fail(ATTN_ERR_DTYPE, "dtype must be ATTN_FP16 (0) or ATTN_BF16 (1), got %d", dtype);
-  if (head_dim != 64 && head_dim != 128)
-    return fail(ATTN_ERR_SHAPE, "head_dim must be 64 or 128, got %d", head_dim);
+  if (head_dim < 8 || head_dim > 128 || head_dim % 8 != 0)
+    return fail(ATTN_ERR_SHAPE, "head_dim must be a multiple of 8 in [8, 128], got %d", head_dim);
   if (batch <= 0) return fail(ATTN_ERR_SHAPE, "batch must be positive, got %d", batch);
   if (h_q <= 0 || h_k <= 0 || h_q % h_k != 0)
     return fail(ATTN_ERR_SHAPE, "h_q (%d) must be a positive multiple of h_k (%d)", h_q, h_k);

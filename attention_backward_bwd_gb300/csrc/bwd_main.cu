@@ -487,7 +487,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (un.n_iters == 0) {  // keys but no queries: dK = dV = 0
         if (key_ok) {
 #pragma unroll
-          for (int c = 0; c < eCols / 8; ++c) reinterpret_cast<uint4*>(out_row)[c] = make_uint4(0, 0, 0, 0);
+          for (int c = 0; c < eCols / 8; ++c)
+            if (e0 + 8 * c < p.head_dim)  // a padded head dimension stops early
+              reinterpret_cast<uint4*>(out_row)[c] = make_uint4(0, 0, 0, 0);
         }
         continue;
       }
@@ -655,7 +657,8 @@ __global__ void __launch_bounds__(kThreads, 1)
               o.y = Pack<T>::two(__uint_as_float(a[8 * q + 2]) * mul, __uint_as_float(a[8 * q + 3]) * mul);
               o.z = Pack<T>::two(__uint_as_float(a[8 * q + 4]) * mul, __uint_as_float(a[8 * q + 5]) * mul);
               o.w = Pack<T>::two(__uint_as_float(a[8 * q + 6]) * mul, __uint_as_float(a[8 * q + 7]) * mul);
-              reinterpret_cast<uint4*>(out_row + c * 32)[q] = o;
+              if (e0 + c * 32 + 8 * q < p.head_dim)  // a padded head dimension stops early
+                reinterpret_cast<uint4*>(out_row + c * 32)[q] = o;
             }
           }
         }
@@ -806,10 +809,12 @@ cudaError_t launch_t(const BwdParams& p, int dtype, cudaStream_t stream) {
   const bool varlen = p.seq.cu_q != nullptr;
   const int nb = varlen ? 1 : p.seq.batch;
   CUtensorMap tq, tk, tv, tdo;
-  if (!encode_tmap_bshd(&tq, p.q, dtype, p.seq.seqlen_q, p.h_q, nb, D, BM) ||
-      !encode_tmap_bshd(&tk, p.k, dtype, p.seq.seqlen_k, p.h_k, nb, D, BN) ||
-      !encode_tmap_bshd(&tv, p.v, dtype, p.seq.seqlen_k, p.h_k, nb, D, BN) ||
-      !encode_tmap_bshd(&tdo, p.dout, dtype, p.seq.seqlen_q, p.h_q, nb, D, BM))
+  // the maps span the logical head dimension: columns up to D read as zero
+  const int d = p.head_dim;
+  if (!encode_tmap_bshd(&tq, p.q, dtype, p.seq.seqlen_q, p.h_q, nb, d, BM) ||
+      !encode_tmap_bshd(&tk, p.k, dtype, p.seq.seqlen_k, p.h_k, nb, d, BN) ||
+      !encode_tmap_bshd(&tv, p.v, dtype, p.seq.seqlen_k, p.h_k, nb, d, BN) ||
+      !encode_tmap_bshd(&tdo, p.dout, dtype, p.seq.seqlen_q, p.h_q, nb, d, BM))
     return cudaErrorInvalidValue;
   CUtensorMap tdq;
   if (!encode_tmap_f32_2d(&tdq, p.dqacc, p.ws_rows * p.h_q, D)) return cudaErrorInvalidValue;
@@ -842,12 +847,13 @@ cudaError_t launch_t(const BwdParams& p, int dtype, cudaStream_t stream) {
 
 template <bool kCap>
 cudaError_t launch_cap(const BwdParams& p, int dtype, cudaStream_t stream) {
+  const bool d64 = pad_head_dim(p.head_dim) == 64;
   if (dtype == 1) {
-    return p.head_dim == 64 ? launch_t<__nv_bfloat16, 64, kCap>(p, dtype, stream)
-                            : launch_t<__nv_bfloat16, 128, kCap>(p, dtype, stream);
+    return d64 ? launch_t<__nv_bfloat16, 64, kCap>(p, dtype, stream)
+               : launch_t<__nv_bfloat16, 128, kCap>(p, dtype, stream);
   }
-  return p.head_dim == 64 ? launch_t<__half, 64, kCap>(p, dtype, stream)
-                          : launch_t<__half, 128, kCap>(p, dtype, stream);
+  return d64 ? launch_t<__half, 64, kCap>(p, dtype, stream)
+             : launch_t<__half, 128, kCap>(p, dtype, stream);
 }
 
 }  // namespace

@@ -72,14 +72,15 @@ __device__ __forceinline__ void cp_async_wait_all() {
 // zero-filling rows at or beyond `valid_rows`.
 template <typename T, int D, int LD>
 __device__ __forceinline__ void load_tile(T* dst, const T* src, int64_t row_stride, int row0,
-                                          int valid_rows) {
+                                          int valid_rows, int valid_cols) {
   constexpr int kChunks = kBN * D / 8;
   for (int c = threadIdx.x; c < kChunks; c += kFwdThreads) {
     const int r = c / (D / 8);
     const int col = (c % (D / 8)) * 8;
     const int gr = row0 + r;
-    const bool ok = gr < valid_rows;
-    const T* g = src + static_cast<int64_t>(ok ? gr : 0) * row_stride + col;
+    // rows past the sequence and columns past a padded head dimension read as 0
+    const bool ok = gr < valid_rows && col < valid_cols;
+    const T* g = ok ? src + static_cast<int64_t>(gr) * row_stride + col : src;  // no read if !ok
     cp_async16(smem_u32(dst + r * LD + col), g, ok);
   }
 }
@@ -117,11 +118,11 @@ __global__ void __launch_bounds__(kFwdThreads) fwd_kernel(FwdParams p) {
     n_end = min(n_end, last_key < 0 ? 0 : last_key / kBN + 1);
   }
 
-  load_tile<T, D, LD>(sQ, qg, p.q.ss, m0, si.sq);
+  load_tile<T, D, LD>(sQ, qg, p.q.ss, m0, si.sq, p.head_dim);
   cp_async_commit();
   if (n_end > n_start) {
-    load_tile<T, D, LD>(sK, kg, p.k.ss, n_start * kBN, si.sk);
-    load_tile<T, D, LD>(sV, vg, p.v.ss, n_start * kBN, si.sk);
+    load_tile<T, D, LD>(sK, kg, p.k.ss, n_start * kBN, si.sk, p.head_dim);
+    load_tile<T, D, LD>(sV, vg, p.v.ss, n_start * kBN, si.sk, p.head_dim);
   }
   cp_async_commit();
   cp_async_wait_all();
@@ -146,8 +147,10 @@ __global__ void __launch_bounds__(kFwdThreads) fwd_kernel(FwdParams p) {
   for (int n = n_start; n < n_end; ++n) {
     const int buf = (n - n_start) & 1;
     if (n + 1 < n_end) {
-      load_tile<T, D, LD>(sK + (buf ^ 1) * kBN * LD, kg, p.k.ss, (n + 1) * kBN, si.sk);
-      load_tile<T, D, LD>(sV + (buf ^ 1) * kBN * LD, vg, p.v.ss, (n + 1) * kBN, si.sk);
+      load_tile<T, D, LD>(sK + (buf ^ 1) * kBN * LD, kg, p.k.ss, (n + 1) * kBN, si.sk,
+                          p.head_dim);
+      load_tile<T, D, LD>(sV + (buf ^ 1) * kBN * LD, vg, p.v.ss, (n + 1) * kBN, si.sk,
+                          p.head_dim);
     }
     cp_async_commit();
     const T* cK = sK + buf * kBN * LD;
@@ -257,7 +260,8 @@ __global__ void __launch_bounds__(kFwdThreads) fwd_kernel(FwdParams p) {
 #pragma unroll
       for (int dn = 0; dn < D / 8; ++dn) {
         const uint32_t v = Pack<T>::two(o[dn][2 * r] * inv[r], o[dn][2 * r + 1] * inv[r]);
-        *reinterpret_cast<uint32_t*>(orow + dn * 8 + 2 * t) = v;
+        if (dn * 8 < p.head_dim)  // a padded head dimension stops early
+          *reinterpret_cast<uint32_t*>(orow + dn * 8 + 2 * t) = v;
       }
       if (t == 0) {
         const int64_t li = varlen ? static_cast<int64_t>(h) * p.seq.seqlen_q + si.q_start + row
@@ -289,11 +293,11 @@ cudaError_t launch_fwd_t(const FwdParams& p, cudaStream_t stream) {
 
 cudaError_t launch_fwd(const FwdParams& p, int dtype, cudaStream_t stream) {
   if (dtype == 1) {
-    return p.head_dim == 64 ? launch_fwd_t<__nv_bfloat16, 64>(p, stream)
-                            : launch_fwd_t<__nv_bfloat16, 128>(p, stream);
+    return pad_head_dim(p.head_dim) == 64 ? launch_fwd_t<__nv_bfloat16, 64>(p, stream)
+                                          : launch_fwd_t<__nv_bfloat16, 128>(p, stream);
   }
-  return p.head_dim == 64 ? launch_fwd_t<__half, 64>(p, stream)
-                          : launch_fwd_t<__half, 128>(p, stream);
+  return pad_head_dim(p.head_dim) == 64 ? launch_fwd_t<__half, 64>(p, stream)
+                                        : launch_fwd_t<__half, 128>(p, stream);
 }
 
 }  // namespace attn

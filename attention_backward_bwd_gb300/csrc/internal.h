@@ -75,6 +75,12 @@ struct WsLayout {
 
 inline size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
+// The kernels run D = 64 or 128; a head dimension that is a multiple of 8 below
+// either runs on the next one with the extra columns zero (TMA's out-of-bounds
+// fill on loads, masked stores), and the fp32 dQ accumulator is laid out at
+// the padded width.
+__host__ __device__ inline int pad_head_dim(int d) { return d <= 64 ? 64 : 128; }
+
 inline WsLayout ws_layout(int batch, int seqlen_q, int h_q, int head_dim, int varlen) {
   WsLayout w;
   if (varlen) {
@@ -86,7 +92,7 @@ inline WsLayout ws_layout(int batch, int seqlen_q, int h_q, int head_dim, int va
   w.off_lse2 = 0;
   w.off_delta = align256(w.off_lse2 + per_row * 4);
   w.off_dqacc = align256(w.off_delta + per_row * 4);
-  w.off_sem = align256(w.off_dqacc + per_row * static_cast<size_t>(head_dim) * 4);
+  w.off_sem = align256(w.off_dqacc + per_row * static_cast<size_t>(pad_head_dim(head_dim)) * 4);
   // semaphores, then one int32 work counter for the persistent scheduler
   w.total = align256(w.off_sem + (static_cast<size_t>(h_q) * (w.rows / kTileRows) + 1) * 4);
   return w;

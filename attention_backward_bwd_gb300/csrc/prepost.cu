@@ -88,7 +88,7 @@ __global__ void __launch_bounds__(kThreads, 8) preprocess_kernel(BwdParams p) {
       z[1] = make_float4(0.f, 0.f, 0.f, 0.f);
     }
     float acc = 0.f;
-    if (valid) {
+    if (valid && c * 8 < p.head_dim) {  // a padded head dimension has fewer columns
       const uint4 ov = *reinterpret_cast<const uint4*>(row_ptr<T>(p.o, p.seq.cu_q != nullptr, si, b, i, h) + c * 8);
       const uint4 dv = *reinterpret_cast<const uint4*>(row_ptr<T>(p.dout, p.seq.cu_q != nullptr, si, b, i, h) + c * 8);
       const uint32_t* o32 = reinterpret_cast<const uint32_t*>(&ov);
@@ -154,14 +154,14 @@ __global__ void __launch_bounds__(kThreads) postprocess_kernel(BwdParams p) {
     out.z = Pack<T>::two(d.x * p.scale, d.y * p.scale);
     out.w = Pack<T>::two(d.z * p.scale, d.w * p.scale);
     T* dst = const_cast<T*>(row_ptr<T>(p.dq, p.seq.cu_q != nullptr, si, b, i, h)) + c * 8;
-    *reinterpret_cast<uint4*>(dst) = out;
+    if (c * 8 < p.head_dim) *reinterpret_cast<uint4*>(dst) = out;
   }
 }
 
 template <typename T, int D>
 __global__ void __launch_bounds__(kThreads)
     zero_rows_kernel(TensorArg t, int nseq, int rows_per_seq, const int* cu, int total_rows,
-                     int heads) {
+                     int heads, int head_dim) {
   constexpr int kGroup = D / 8;
   const int64_t rows = (cu == nullptr) ? static_cast<int64_t>(nseq) * rows_per_seq : total_rows;
   const int64_t n_groups = rows * heads;
@@ -179,7 +179,7 @@ __global__ void __launch_bounds__(kThreads)
       off = r * t.ss + static_cast<int64_t>(h) * t.sh;
     }
     T* dst = const_cast<T*>(static_cast<const T*>(t.ptr)) + off + c * 8;
-    *reinterpret_cast<uint4*>(dst) = make_uint4(0u, 0u, 0u, 0u);
+    if (c * 8 < head_dim) *reinterpret_cast<uint4*>(dst) = make_uint4(0u, 0u, 0u, 0u);
   }
 }
 
@@ -235,9 +235,9 @@ inline int grid_for(int64_t work_threads, K kernel, Occupancy& occ) {
 
 template <typename T>
 static cudaError_t launch_pre_t(const BwdParams& p, cudaStream_t stream) {
-  const int64_t work = p.ws_rows * p.h_q * (p.head_dim / 8);
+  const int64_t work = p.ws_rows * p.h_q * (pad_head_dim(p.head_dim) / 8);
   static Occupancy occ64, occ128;
-  if (p.head_dim == 64)
+  if (pad_head_dim(p.head_dim) == 64)
     preprocess_kernel<T, 64>
         <<<grid_for(work, preprocess_kernel<T, 64>, occ64), kThreads, 0, stream>>>(p);
   else
@@ -255,10 +255,10 @@ static cudaError_t launch_post_t(const BwdParams& p, cudaStream_t stream) {
   const int64_t tokens = (p.seq.cu_q == nullptr)
                              ? static_cast<int64_t>(p.seq.batch) * p.seq.seqlen_q
                              : static_cast<int64_t>(p.seq.seqlen_q);
-  const int64_t work = tokens * p.h_q * (p.head_dim / 8);
+  const int64_t work = tokens * p.h_q * (pad_head_dim(p.head_dim) / 8);
   if (work == 0) return cudaSuccess;
   static Occupancy occ64, occ128;
-  if (p.head_dim == 64)
+  if (pad_head_dim(p.head_dim) == 64)
     postprocess_kernel<T, 64>
         <<<grid_for(work, postprocess_kernel<T, 64>, occ64), kThreads, 0, stream>>>(p);
   else
@@ -275,15 +275,15 @@ template <typename T>
 static cudaError_t launch_zero_t(const TensorArg& t, int nseq, int rows_per_seq, const int* cu,
                                  int total_rows, int heads, int head_dim, cudaStream_t stream) {
   const int64_t rows = (cu == nullptr) ? static_cast<int64_t>(nseq) * rows_per_seq : total_rows;
-  const int64_t work = rows * heads * (head_dim / 8);
+  const int64_t work = rows * heads * (pad_head_dim(head_dim) / 8);
   if (work == 0) return cudaSuccess;
   static Occupancy occ64, occ128;
-  if (head_dim == 64)
+  if (pad_head_dim(head_dim) == 64)
     zero_rows_kernel<T, 64><<<grid_for(work, zero_rows_kernel<T, 64>, occ64), kThreads, 0,
-                              stream>>>(t, nseq, rows_per_seq, cu, total_rows, heads);
+                              stream>>>(t, nseq, rows_per_seq, cu, total_rows, heads, head_dim);
   else
     zero_rows_kernel<T, 128><<<grid_for(work, zero_rows_kernel<T, 128>, occ128), kThreads, 0,
-                               stream>>>(t, nseq, rows_per_seq, cu, total_rows, heads);
+                               stream>>>(t, nseq, rows_per_seq, cu, total_rows, heads, head_dim);
   return cudaGetLastError();
 }
 

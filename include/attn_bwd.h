@@ -27,9 +27,10 @@
  * LSE is fp32, natural log: [B, H_q, Sq] contiguous, or [H_q, total_q] in
  * varlen mode (flash-attention's softmax_lse).
  *
- * Supported: dtype fp16 or bf16 (all of Q,K,V,O,dO,dQ,dK,dV share it), D in
- * {64, 128}, H_q % H_k == 0, base pointers and strides 16-byte aligned
- * (strides multiples of 8 elements).
+ * Supported: dtype fp16 or bf16 (all of Q,K,V,O,dO,dQ,dK,dV share it), D a
+ * multiple of 8 in [8, 128] (64 and 128 run natively; any other D runs on the
+ * next of those with the extra head-dimension columns zero), H_q % H_k == 0,
+ * base pointers and strides 16-byte aligned (strides multiples of 8 elements).
  *
  * Ownership.  The caller owns every buffer, including the workspace; the
  * library allocates nothing per call and keeps no state across calls except

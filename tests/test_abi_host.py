@@ -106,7 +106,7 @@ def shapes(b=1, sq=64, sk=64, hq=2, hk=2, d=64, dtype="bf16", ptr=1 << 20):
 
 
 @pytest.mark.parametrize("case,code", [
-    ("dtype", -1), ("head_dim", -2), ("gqa_ratio", -2), ("align", -4), ("stride", -3),
+    ("dtype", -1), ("head_dim", -2), ("head_dim_large", -2), ("gqa_ratio", -2), ("align", -4), ("stride", -3),
     ("null", -5), ("workspace_small", -6), ("workspace_align", -6), ("varlen_half", -9),
 ])
 def test_argument_errors(lib, case, code):
@@ -115,7 +115,9 @@ def test_argument_errors(lib, case, code):
     if case == "dtype":
         q, k, v, o, do = shapes(dtype="f32")
     elif case == "head_dim":
-        q, k, v, o, do = shapes(d=96)
+        q, k, v, o, do = shapes(d=100)  # not a multiple of 8
+    elif case == "head_dim_large":
+        q, k, v, o, do = shapes(d=136)  # above 128
     elif case == "gqa_ratio":
         q, k, v, o, do = shapes(hq=3, hk=2)
     elif case == "align":

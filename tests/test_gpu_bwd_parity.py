@@ -165,6 +165,38 @@ def test_cross_attention_varlen(case):
         assert_close(f"cross {name}", got, ref[name], floor=floor)
 
 
+HEAD_DIMS = [
+    # B, Hq, Hk, Sq, Sk, D, dtype, causal: D below 64 or between 64 and 128 runs on the
+    # D = 64 / 128 kernels with the extra head-dimension columns zero
+    (1, 4, 2, 300, 300, 32, "bf16", True),
+    (2, 2, 2, 257, 257, 48, "fp16", False),
+    (1, 4, 4, 513, 513, 80, "bf16", True),
+    (1, 8, 2, 700, 700, 96, "bf16", True),
+    (1, 2, 1, 200, 333, 112, "bf16", False),
+    (1, 2, 2, 129, 129, 8, "bf16", True),
+]
+
+
+@pytest.mark.parametrize("case", HEAD_DIMS, ids=[f"d{c[5]}" for c in HEAD_DIMS])
+def test_padded_head_dims(case):
+    b, hq, hk, sq, sk, d, dt, causal = case
+    w = synth.small(f"d{d}", b, hq, hk, sq, sk, d, dt, causal, 500 + d)
+    check(w, synth.make_inputs(w))
+
+
+def test_padded_head_dim_deterministic_varlen():
+    lens = [300, 0, 129, 640]
+    w = synth.Workload("d96vl", 0, 8, 2, 0, 0, 96, "bf16", True, 597, n_seqs=len(lens),
+                       len_lo=0, len_hi=700, deterministic=True)
+    x = synth.make_inputs(w, lengths=lens)
+    runs = [run_gpu(w, x, deterministic=True) for _ in range(2)]
+    for a, r in zip(*runs):
+        assert torch.equal(a, r)
+    ref = oracle_grads(w, x)
+    for name, got in zip(("dQ", "dK", "dV"), runs[0]):
+        assert_close(f"d96 varlen {name}", got, ref[name])
+
+
 def test_deterministic_is_bitwise_repeatable():
     w = synth.small("det", 1, 8, 2, 1000, 1000, 128, "bf16", True, 91, deterministic=True)
     x = synth.make_inputs(w)

@@ -57,7 +57,7 @@ def test_argument_errors(lib, case, code):
     if case == "dtype":
         kw["dtype"] = 7
     elif case == "head_dim":
-        kw["d"] = 96
+        kw["d"] = 100  # not a multiple of 8
     elif case == "gqa_ratio":
         kw.update(hq=6, hk=4)
     elif case == "heads_not_adjacent":
