@@ -125,7 +125,9 @@ struct Unit {
   bool has_keys;
 };
 
-__device__ __forceinline__ Unit get_unit(const BwdParams& p, int u, int G) {
+// win_left: the left window side (-1 = none; a compile-time -1 in the
+// instantiation without a left window), win_right: p.win_right.
+__device__ __forceinline__ Unit get_unit(const BwdParams& p, int u, int G, int win_left) {
   Unit r;
   const int per_n = p.seq.batch * p.h_k;
   r.n = u / per_n;
@@ -138,7 +140,7 @@ __device__ __forceinline__ Unit get_unit(const BwdParams& p, int u, int G) {
   // without a mask; causal or a window narrows the range)
   const int k1 = min(r.n * BN + BN, r.si.sk);
   int lo, hi;
-  window_queries(r.n * BN, k1, r.si.sq, r.si.sk, p.win_left, p.win_right, lo, hi);
+  window_queries(r.n * BN, k1, r.si.sq, r.si.sk, win_left, p.win_right, lo, hi);
   r.m_start = lo / BM;
   r.m_count = lo < hi ? ceil_div(hi, BM) - r.m_start : 0;
   r.n_iters = r.has_keys ? G * r.m_count : 0;
@@ -161,7 +163,7 @@ __device__ __forceinline__ void iter_hm(const Unit& un, int j, int G, int& h, in
   m = un.m_start + un.m_count - 1 - jm;
 }
 
-template <typename T, int D, bool kCap>
+template <typename T, int D, bool kCap, bool kLeft>
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_main_kernel(const BwdParams p, const __grid_constant__ CUtensorMap tmQ,
                     const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
@@ -187,6 +189,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int num_units = n_tiles * p.seq.batch * p.h_k;
   constexpr int kIsBf16 = Pack<T>::kIsBf16;
   constexpr bool kSplitQ = D == 128;
+  // the left side of a local window; without one (the usual case) a constant,
+  // so the unmasked and causal schedules carry none of its arithmetic
+  const int wleft = kLeft ? p.win_left : -1;
 
   if (threadIdx.x == 0) {
     *abort_flag = 0;
@@ -270,7 +275,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (u >= num_units) break;
         // fetch the next unit now; the atomic's latency overlaps this unit's loads
         const int u_next = static_cast<int>(gridDim.x) + atomicAdd(p.sched, 1);
-        const Unit un = get_unit(p, u, G);
+        const Unit un = get_unit(p, u, G, wleft);
         u = u_next;
         if (un.n_iters == 0) continue;
         if (uc > 0 && !wait1(bar(B_KVEMPTY), (uc - 1) & 1, ctl, 0xA0000001u)) break;
@@ -375,7 +380,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         int u;
         if (!take_unit(k, false, u)) goto mma_exit;
         if (u >= num_units) break;
-        const Unit un = get_unit(p, u, G);
+        const Unit un = get_unit(p, u, G, wleft);
         if (un.n_iters == 0) continue;
         if (!wait1(bar(B_KVFULL), uc & 1, ctl, 0xA0000011u)) goto mma_exit;
         {
@@ -476,7 +481,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       int u;
       if (!take_unit(k, true, u)) goto done;
       if (u >= num_units) break;
-      const Unit un = get_unit(p, u, G);
+      const Unit un = get_unit(p, u, G, wleft);
       if (!un.has_keys) continue;
       const int key = un.n * BN + jl;
       const bool key_ok = key < un.si.sk;
@@ -503,13 +508,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         const bool need_mask =
             (q0 + BM > un.si.sq) || (un.n * BN + BN > un.si.sk) ||
             (p.win_right >= 0 && un.n * BN + BN - 1 > q0 + off + p.win_right) ||
-            (p.win_left >= 0 && un.n * BN < q0 + BM - 1 + off - p.win_left);
+            (wleft >= 0 && un.n * BN < q0 + BM - 1 + off - wleft);
         const float* lse2 = reinterpret_cast<const float*>(smem + L::kLSE + s * BM * 4) + c0;
         const float* dlt = reinterpret_cast<const float*>(smem + L::kDelta + s * BM * 4) + c0;
         // valid queries of this key row, in this group's column coordinates: lo <= c < hi
         int lo = 0, hi = key_ok ? min(kCols, un.si.sq - q0 - c0) : 0;
         if (p.win_right >= 0) lo = max(0, key - off - p.win_right - q0 - c0);
-        if (p.win_left >= 0) hi = min(hi, key - off + p.win_left - q0 - c0 + 1);
+        if (wleft >= 0) hi = min(hi, key - off + wleft - q0 - c0 + 1);
         if (!wait_warp(bar(B_FULLQ + s), ph, ctl, 0xA0000021u)) goto done;
         if (!wait_warp(bar(B_SFULL), it & 1, ctl, 0xA0000022u)) goto done;
         tc_fence_after();
@@ -696,7 +701,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       int u;
       if (!take_unit(k, true, u)) goto done;
       if (u >= num_units) break;
-      const Unit un = get_unit(p, u, G);
+      const Unit un = get_unit(p, u, G, wleft);
       if (un.n_iters == 0) continue;
       for (int j = 0; j < un.n_iters; ++j, ++it) {
         int h, m;
@@ -727,7 +732,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             // key tiles before this one that see query tile m (all of them
             // unless a left window starts the range later)
             const int want =
-                4 * (un.n - window_first_key(m * BM, un.si.sq, un.si.sk, p.win_left) / BN);
+                4 * (un.n - window_first_key(m * BM, un.si.sq, un.si.sk, wleft) / BN);
             const uint64_t t0 = globaltimer_ns();
             for (uint32_t spin = 0;; ++spin) {
               if (ld_acquire(sem) >= want) break;
@@ -804,7 +809,7 @@ done:
   if (warp == 2) tmem_dealloc(tmem, kTmemCols);
 }
 
-template <typename T, int D, bool kCap>
+template <typename T, int D, bool kCap, bool kLeft>
 cudaError_t launch_t(const BwdParams& p, int dtype, cudaStream_t stream) {
   const bool varlen = p.seq.cu_q != nullptr;
   const int nb = varlen ? 1 : p.seq.batch;
@@ -826,13 +831,13 @@ cudaError_t launch_t(const BwdParams& p, int dtype, cudaStream_t stream) {
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
     return cudaErrorInvalidDevice;
   if (!attr_done[dev].load(std::memory_order_acquire)) {
-    cudaError_t e = cudaFuncSetAttribute(bwd_main_kernel<T, D, kCap>,
+    cudaError_t e = cudaFuncSetAttribute(bwd_main_kernel<T, D, kCap, kLeft>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     // The warpgroup register split assumes exactly kRegLaunch registers per
     // thread at launch; anything else could leave a register increase waiting.
     cudaFuncAttributes fa;
-    e = cudaFuncGetAttributes(&fa, bwd_main_kernel<T, D, kCap>);
+    e = cudaFuncGetAttributes(&fa, bwd_main_kernel<T, D, kCap, kLeft>);
     if (e != cudaSuccess) return e;
     if (fa.numRegs != static_cast<int>(kRegLaunch)) return cudaErrorInvalidConfiguration;
     attr_done[dev].store(true, std::memory_order_release);
@@ -841,27 +846,31 @@ cudaError_t launch_t(const BwdParams& p, int dtype, cudaStream_t stream) {
   const int units = n_tiles * p.seq.batch * p.h_k;
   if (units <= 0) return cudaSuccess;
   const int grid = units < num_sms() ? units : num_sms();
-  bwd_main_kernel<T, D, kCap><<<grid, kThreads, smem, stream>>>(p, tq, tk, tv, tdo, tdq);
+  bwd_main_kernel<T, D, kCap, kLeft><<<grid, kThreads, smem, stream>>>(p, tq, tk, tv, tdo, tdq);
   return cudaGetLastError();
 }
 
-template <bool kCap>
+template <bool kCap, bool kLeft>
 cudaError_t launch_cap(const BwdParams& p, int dtype, cudaStream_t stream) {
   const bool d64 = pad_head_dim(p.head_dim) == 64;
   if (dtype == 1) {
-    return d64 ? launch_t<__nv_bfloat16, 64, kCap>(p, dtype, stream)
-               : launch_t<__nv_bfloat16, 128, kCap>(p, dtype, stream);
+    return d64 ? launch_t<__nv_bfloat16, 64, kCap, kLeft>(p, dtype, stream)
+               : launch_t<__nv_bfloat16, 128, kCap, kLeft>(p, dtype, stream);
   }
-  return d64 ? launch_t<__half, 64, kCap>(p, dtype, stream)
-             : launch_t<__half, 128, kCap>(p, dtype, stream);
+  return d64 ? launch_t<__half, 64, kCap, kLeft>(p, dtype, stream)
+             : launch_t<__half, 128, kCap, kLeft>(p, dtype, stream);
 }
 
 }  // namespace
 
 cudaError_t launch_bwd_main(const BwdParams& p, int dtype, cudaStream_t stream) {
-  // the logit cap is a separate instantiation: the default kernel keeps its code
-  return p.softcap > 0.f ? launch_cap<true>(p, dtype, stream)
-                         : launch_cap<false>(p, dtype, stream);
+  // the logit cap and a left window side are separate instantiations: the
+  // default kernel keeps the code of the unmasked / causal schedule
+  const bool cap = p.softcap > 0.f, left = p.win_left >= 0;
+  if (cap) return left ? launch_cap<true, true>(p, dtype, stream)
+                       : launch_cap<true, false>(p, dtype, stream);
+  return left ? launch_cap<false, true>(p, dtype, stream)
+              : launch_cap<false, false>(p, dtype, stream);
 }
 
 }  // namespace attn
