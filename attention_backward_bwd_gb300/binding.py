@@ -90,7 +90,8 @@ def lib() -> ctypes.CDLL:
             f.argtypes = _BWD_ARGS
             f.restype = _I
         L.attn_bwd_host.argtypes = [_T, _T, _T, _T, _P, _T, _T, _T, _T, _I, _I, _I, _I, _I, _I,
-                                    _I, ctypes.c_float, _I, _I, _I, _P, ctypes.c_size_t, _P]
+                                    _I, ctypes.c_float, _I, _I, ctypes.POINTER(AttnOpts), _I, _P,
+                                    ctypes.c_size_t, _P]
         L.attn_bwd_host.restype = _I
         L.attn_bwd_host_buffer_size.argtypes = [_I, _I, _I, _I, _I, _I, _I]
         L.attn_bwd_host_buffer_size.restype = ctypes.c_size_t
@@ -276,7 +277,8 @@ def host_buffer_size(batch: int, seqlen_q: int, seqlen_k: int, h_q: int, h_k: in
 
 def attn_bwd_host(q, k, v, o, lse, do, dq=None, dk=None, dv=None, causal: bool = False,
                   scale: Optional[float] = None, deterministic: bool = False, chunks: int = 0,
-                  device_buffer: Optional[torch.Tensor] = None, device=None, stream=None):
+                  device_buffer: Optional[torch.Tensor] = None, device=None, stream=None,
+                  window=None, softcap: float = 0.0):
     """Backward on HOST tensors ([B, S, H, D], heads adjacent; lse [B, H_q, Sq]).
 
     Inputs are copied to the device, the backward runs, and dQ, dK, dV are
@@ -298,10 +300,12 @@ def attn_bwd_host(q, k, v, o, lse, do, dq=None, dk=None, dv=None, causal: bool =
                                     device=device if device is not None else "cuda")
     descs = [_desc(t) for t in (q, k, v, o)]
     d_do, d_dq, d_dk, d_dv = _desc(do), _desc(dq), _desc(dk), _desc(dv)
+    opts = _opts(window, softcap)
+    opts_ref = None if opts is None else ctypes.byref(opts)
     rc = L.attn_bwd_host(*(ctypes.byref(x) for x in descs), _ptr(lse), ctypes.byref(d_do),
                          ctypes.byref(d_dq), ctypes.byref(d_dk), ctypes.byref(d_dv),
                          _dtype_code(q), b, sq, sk, hq, hk, d, scale, int(bool(causal)),
-                         int(bool(deterministic)), int(chunks), device_buffer.data_ptr(),
+                         int(bool(deterministic)), opts_ref, int(chunks), device_buffer.data_ptr(),
                          device_buffer.numel(), _stream(stream))
     _check(rc)
     return dq, dk, dv

@@ -209,9 +209,9 @@ extern "C" int attn_bwd_host(const attn_tensor* q, const attn_tensor* k, const a
                              const attn_tensor* o, const float* lse, const attn_tensor* dout,
                              const attn_tensor* dq, const attn_tensor* dk, const attn_tensor* dv,
                              int dtype, int batch, int seqlen_q, int seqlen_k, int h_q, int h_k,
-                             int head_dim, float scale, int causal, int deterministic, int chunks,
-                             void* device_buffer, size_t device_buffer_bytes,
-                             attn_stream_t stream) {
+                             int head_dim, float scale, int causal, int deterministic,
+                             const attn_opts* opts, int chunks, void* device_buffer,
+                             size_t device_buffer_bytes, attn_stream_t stream) {
   clear_error();
   int rc = check_common(dtype, batch, seqlen_q, seqlen_k, h_q, h_k, head_dim, scale, nullptr,
                         nullptr, 0, 0);
@@ -226,6 +226,8 @@ extern "C" int attn_bwd_host(const attn_tensor* q, const attn_tensor* k, const a
   if ((rc = check_host_tensor(dk, "dk", h_k, head_dim, seqlen_k, hk))) return rc;
   if ((rc = check_host_tensor(dv, "dv", h_k, head_dim, seqlen_k, hk))) return rc;
   if (hq && hk && lse == nullptr) return fail(ATTN_ERR_NULL, "lse is NULL");
+  attn_opts checked;
+  if ((rc = resolve_opts(opts, &checked))) return rc;
   const Chunking ch = chunking(batch, h_k, chunks);
   const BufLayout L = buf_layout(batch, seqlen_q, seqlen_k, h_q, h_k, head_dim, ch);
   if (device_buffer == nullptr) return fail(ATTN_ERR_WORKSPACE, "device_buffer is NULL");
@@ -292,7 +294,7 @@ extern "C" int attn_bwd_host(const attn_tensor* q, const attn_tensor* k, const a
     Prepared pr;
     rc = prepare_bwd(&tq, &tk, &tv, &to, tlse, &tdo, &tdq, &tdk, &tdv, dtype, nb, seqlen_q,
                      seqlen_k, ni, nj, head_dim, scale, causal, nullptr, nullptr, seqlen_q,
-                     seqlen_k, deterministic, nullptr, buf + L.ws[c % kSlots], L.ws_bytes,
+                     seqlen_k, deterministic, &checked, buf + L.ws[c % kSlots], L.ws_bytes,
                      &pr);
     if (rc) return rc;
     if ((rc = run_stages(kPre | kMain | kPost, pr, cs))) return rc;

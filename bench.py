@@ -246,14 +246,13 @@ def run_ours(args):
     t_post = statistics.mean(e[2].elapsed_time(e[3]) for e in evs)
 
     # --- end to end: pinned host inputs -> device -> backward -> pinned host results.
-    # Padded unmasked or causal workloads go through attn_bwd_host (chunks whose
-    # copies overlap the kernels of other chunks); varlen, windowed and capped
-    # ones copy in, call attn_bwd, copy out.
+    # Padded workloads go through attn_bwd_host (chunks whose copies overlap the
+    # kernels of other chunks); varlen ones copy in, call attn_bwd, copy out.
     hq_ = [t.cpu().pin_memory() for t in (q, k, v, o, do, lse)]
     host_out = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in (dq, dk, dv)]
     h2d = sum(t.numel() * t.element_size() for t in hq_)
     d2h = sum(t.numel() * t.element_size() for t in host_out)
-    if not w.varlen and not w.windowed and not w.softcap:
+    if not w.varlen:
         b_, sq_, hq_n, d_ = q.shape
         hbuf = torch.empty(ab.host_buffer_size(b_, sq_, k.shape[1], hq_n, k.shape[2], d_,
                                                args.chunks), dtype=torch.uint8, device=dev)
@@ -262,7 +261,8 @@ def run_ours(args):
         def e2e_step():
             ab.attn_bwd_host(hq_[0], hq_[1], hq_[2], hq_[3], hq_[5], hq_[4], *host_out,
                              causal=w.causal, deterministic=det, chunks=args.chunks,
-                             device_buffer=hbuf, stream=stream)
+                             device_buffer=hbuf, stream=stream, window=window,
+                             softcap=w.softcap)
     else:
         dev_in = [torch.empty_like(t) for t in (q, k, v, o, do, lse)]
         e2e_path = "copies + attn_bwd"

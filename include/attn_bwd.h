@@ -236,6 +236,7 @@ int attn_bwd_noalloc(const attn_tensor* q, const attn_tensor* k, const attn_tens
  * chunks) bytes, 256-byte aligned, owned by the caller, not used by any other
  * call while this one runs.  It holds device copies of all eight tensors and
  * of lse plus three chunk-sized workspaces (one per internal compute stream).
+ * opts: a local window and a logit cap as for attn_bwd_ex (NULL: none).
  * Errors as attn_bwd (argument errors before anything is enqueued; a
  * stride_h other than D is ATTN_ERR_STRIDE).  The first call on a device
  * creates the library's internal streams and events for that device; make
@@ -247,8 +248,8 @@ int attn_bwd_host(const attn_tensor* q, const attn_tensor* k, const attn_tensor*
                   const attn_tensor* o, const float* lse, const attn_tensor* dout,
                   const attn_tensor* dq, const attn_tensor* dk, const attn_tensor* dv, int dtype,
                   int batch, int seqlen_q, int seqlen_k, int h_q, int h_k, int head_dim,
-                  float scale, int causal, int deterministic, int chunks, void* device_buffer,
-                  size_t device_buffer_bytes, attn_stream_t stream);
+                  float scale, int causal, int deterministic, const attn_opts* opts, int chunks,
+                  void* device_buffer, size_t device_buffer_bytes, attn_stream_t stream);
 
 /*
  * The three stages of attn_bwd, callable one by one (same arguments, same

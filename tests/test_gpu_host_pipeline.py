@@ -137,3 +137,18 @@ def test_host_two_calls_reuse_buffer_and_stream_order():
     ab.check_device_status()
     for out in outs:
         _compare(dev, out, True, "two calls")
+
+
+def test_host_with_window_and_softcap():
+    """attn_opts pass through the host pipeline: a sliding window and a logit cap
+    give attn_bwd's results (deterministic mode: bit for bit)."""
+    w, x, (q, k, v, o, lse, do) = _problem(2, 8, 2, 700, 700, 128, "bf16", True, 13)
+    o, lse = ab.attn_fwd(q, k, v, causal=True, window=(200, -1), softcap=3.0)
+    dev = ab.attn_bwd(q, k, v, o, lse, do, causal=True, deterministic=True, window=(200, -1),
+                      softcap=3.0)
+    host_in = [_pinned(t.cpu()) for t in (q, k, v, o, lse, do)]
+    got = ab.attn_bwd_host(*host_in, causal=True, deterministic=True, window=(200, -1),
+                           softcap=3.0)
+    torch.cuda.synchronize()
+    ab.check_device_status()
+    _compare(dev, got, True, "host window softcap")

@@ -29,8 +29,8 @@ def _call(lib, b=2, sq=256, sk=256, hq=8, hk=2, d=128, dtype=1, chunks=0, buf=1 
         buf_bytes = lib.attn_bwd_host_buffer_size(b, sq, sk, hq, hk, d, chunks)
     return lib.attn_bwd_host(ctypes.byref(q), ctypes.byref(k), ctypes.byref(k), ctypes.byref(qo),
                              lse, ctypes.byref(qo), ctypes.byref(qo), ctypes.byref(k),
-                             ctypes.byref(k), dtype, b, sq, sk, hq, hk, d, 0.1, 1, 0, chunks, buf,
-                             buf_bytes, None)
+                             ctypes.byref(k), dtype, b, sq, sk, hq, hk, d, 0.1, 1, 0, None, chunks,
+                             buf, buf_bytes, None)
 
 
 def test_buffer_size_covers_tensors_and_follows_chunks(lib):
@@ -75,3 +75,16 @@ def test_argument_errors(lib, case, code):
     rc = _call(lib, **kw)
     assert rc == code, (rc, lib.attn_last_error())
     assert lib.attn_last_error()
+
+
+def test_bad_options_rejected(lib):
+    from attention_backward_bwd_gb300.binding import AttnOpts
+    q = _t(1 << 20, 2, 256, 8, 128)
+    k = _t(1 << 20, 2, 256, 2, 128)
+    opts = AttnOpts(-2, 0, 0.0)
+    size = lib.attn_bwd_host_buffer_size(2, 256, 256, 8, 2, 128, 0)
+    rc = lib.attn_bwd_host(ctypes.byref(q), ctypes.byref(k), ctypes.byref(k), ctypes.byref(q),
+                           1 << 21, ctypes.byref(q), ctypes.byref(q), ctypes.byref(k),
+                           ctypes.byref(k), 1, 2, 256, 256, 8, 2, 128, 0.1, 1, 0,
+                           ctypes.byref(opts), 0, 1 << 24, size, None)
+    assert rc == -9 and b"window" in lib.attn_last_error()
