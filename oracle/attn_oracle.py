@@ -33,7 +33,9 @@ Sources (page title, section):
     window (-1, 0).
 
   * flash-attention hopper/flash_bwd_launch_template.h: ``Has_softcap`` /
-    ``params.softcap`` select a logit cap (no formula is given there).
+    ``params.softcap`` select a logit cap (no formula is given there);
+    ``seqused_q`` / ``seqused_k`` give each sequence a used length inside its
+    padded or packed rows.
 
 Readings where the pages leave a point open:
   * causal with Sq != Sk: key j is allowed for query i iff j <= i + (Sk - Sq).
@@ -41,6 +43,9 @@ Readings where the pages leave a point open:
     j >= i + off - left (when left >= 0) and j <= i + off + right (when
     right >= 0); causal together with a window keeps the window's left side
     and bounds the right side at 0.
+  * seqused: sequence b is the first seqused[b] rows of its rows (padded slab or
+    packed range); the rest of its rows take no part, and their gradients are
+    left as they were (zero here).
   * softcap c > 0: the logits s = scale * q.k are capped as c * tanh(s / c)
     before the softmax (the usual logit cap); the backward multiplies dS by
     the cap's derivative 1 - tanh(s / c)^2.  c = 0 means no cap.
@@ -134,16 +139,23 @@ def _f64(x):
     return np.asarray(x, dtype=np.float64)
 
 
-def _sequences(q, k, cu_q, cu_k):
-    """Yield (b, q_rows, k_rows) slices for padded [B,S,H,D] or packed [total,H,D]."""
+def _sequences(q, k, cu_q, cu_k, used_q=None, used_k=None):
+    """Yield (b, q_rows, k_rows) slices for padded [B,S,H,D] or packed [total,H,D];
+    ``used_q`` / ``used_k`` (per sequence) keep only each sequence's first rows."""
+    uq = None if used_q is None else [int(x) for x in _f64(used_q)]
+    uk = None if used_k is None else [int(x) for x in _f64(used_k)]
     if cu_q is None:
         for b in range(q.shape[0]):
-            yield b, (b, slice(None)), (b, slice(None))
+            qs = slice(None) if uq is None else slice(0, uq[b])
+            ks = slice(None) if uk is None else slice(0, uk[b])
+            yield b, (b, qs), (b, ks)
     else:
         cq = [int(x) for x in _f64(cu_q)]
         ck = [int(x) for x in _f64(cu_k)]
         for b in range(len(cq) - 1):
-            yield b, (slice(cq[b], cq[b + 1]),), (slice(ck[b], ck[b + 1]),)
+            nq = cq[b + 1] - cq[b] if uq is None else uq[b]
+            nk = ck[b + 1] - ck[b] if uk is None else uk[b]
+            yield b, (slice(cq[b], cq[b] + nq),), (slice(ck[b], ck[b] + nk),)
 
 
 def _take(x, sel, h):
@@ -166,7 +178,7 @@ def _put(x, sel, h, val, add=False):
 
 
 def mha_forward(q, k, v, scale=None, causal=False, cu_seqlens_q=None, cu_seqlens_k=None,
-                heads=None, window=None, softcap=0.0):
+                heads=None, window=None, softcap=0.0, seqused_q=None, seqused_k=None):
     """Multi-head forward.  q [B,Sq,H,D] (or packed [total,H,D]), k/v with H_k heads.
 
     Returns (O like q, LSE [B,H,Sq] or [H,total_q]).  ``heads`` restricts the
@@ -182,20 +194,20 @@ def mha_forward(q, k, v, scale=None, causal=False, cu_seqlens_q=None, cu_seqlens
     else:
         lse = np.zeros((hq, q.shape[0]))
     hs = range(hq) if heads is None else heads
-    for b, qs, ks in _sequences(q, k, cu_seqlens_q, cu_seqlens_k):
+    for b, qs, ks in _sequences(q, k, cu_seqlens_q, cu_seqlens_k, seqused_q, seqused_k):
         for h in hs:
             oh, lh, _ = head_forward(_take(q, qs, h), _take(k, ks, h // g), _take(v, ks, h // g),
                                      scale, causal, window, softcap)
             _put(o, qs, h, oh)
             if cu_seqlens_q is None:
-                lse[b, h, :] = lh
+                lse[b, h, qs[1]] = lh
             else:
                 lse[h, qs[0]] = lh
     return o, lse
 
 
 def mha_backward(q, k, v, do, scale=None, causal=False, cu_seqlens_q=None, cu_seqlens_k=None,
-                 kv_heads=None, window=None, softcap=0.0):
+                 kv_heads=None, window=None, softcap=0.0, seqused_q=None, seqused_k=None):
     """Multi-head backward by the definition, with GQA group sums.
 
     Returns dict(dQ, dK, dV, O, LSE, Delta) in the input layouts (LSE/Delta as
@@ -213,7 +225,7 @@ def mha_backward(q, k, v, do, scale=None, causal=False, cu_seqlens_q=None, cu_se
         lse = np.zeros((hq, q.shape[0]))
     delta = np.zeros_like(lse)
     kvs = range(hk) if kv_heads is None else kv_heads
-    for b, qs, ks in _sequences(q, k, cu_seqlens_q, cu_seqlens_k):
+    for b, qs, ks in _sequences(q, k, cu_seqlens_q, cu_seqlens_k, seqused_q, seqused_k):
         for hkv in kvs:
             for h in range(hkv * g, hkv * g + g):
                 r = head_backward(_take(q, qs, h), _take(k, ks, hkv), _take(v, ks, hkv),
@@ -223,8 +235,8 @@ def mha_backward(q, k, v, do, scale=None, causal=False, cu_seqlens_q=None, cu_se
                 _put(dk, ks, hkv, r["dK"], add=True)
                 _put(dv, ks, hkv, r["dV"], add=True)
                 if cu_seqlens_q is None:
-                    lse[b, h, :] = r["LSE"]
-                    delta[b, h, :] = r["Delta"]
+                    lse[b, h, qs[1]] = r["LSE"]
+                    delta[b, h, qs[1]] = r["Delta"]
                 else:
                     lse[h, qs[0]] = r["LSE"]
                     delta[h, qs[0]] = r["Delta"]

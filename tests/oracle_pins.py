@@ -404,6 +404,47 @@ def pin_cross_varlen_matches_padded(o_mod):
                 assert np.abs(r["dQ"][qs]).max() == 0  # no keys: dQ = 0
 
 
+def pin_seqused(o_mod):
+    """Used lengths inside padded and packed buffers: each sequence's gradients
+    equal those of its used rows alone, the unused rows change nothing (filled
+    with other values, the results stay) and get zero gradients."""
+    rng = np.random.default_rng(12)
+    # padded: B = 3 slabs of 7 query / 9 key rows, used (5, 0, 7) / (9, 4, 2)
+    uq, uk = [5, 0, 7], [9, 4, 2]
+    q, do = rng.standard_normal((3, 7, 4, 8)), rng.standard_normal((3, 7, 4, 8))
+    k, v = rng.standard_normal((3, 9, 2, 8)), rng.standard_normal((3, 9, 2, 8))
+    for causal in (False, True):
+        r = o_mod.mha_backward(q, k, v, do, 0.4, causal, seqused_q=uq, seqused_k=uk)
+        q2, k2, v2, do2 = q.copy(), k.copy(), v.copy(), do.copy()
+        for b in range(3):
+            q2[b, uq[b]:] = 5.0
+            do2[b, uq[b]:] = -3.0
+            k2[b, uk[b]:] = 7.0
+            v2[b, uk[b]:] = 2.0
+        r2 = o_mod.mha_backward(q2, k2, v2, do2, 0.4, causal, seqused_q=uq, seqused_k=uk)
+        for key in ("dQ", "dK", "dV"):
+            assert _rel(r2[key], r[key]) < 1e-14, key
+        for b in range(3):
+            if uq[b] == 0 or uk[b] == 0:
+                continue
+            rb = o_mod.mha_backward(q[b:b + 1, :uq[b]], k[b:b + 1, :uk[b]], v[b:b + 1, :uk[b]],
+                                    do[b:b + 1, :uq[b]], 0.4, causal)
+            assert _rel(r["dQ"][b, :uq[b]], rb["dQ"][0]) < 1e-13
+            assert _rel(r["dK"][b, :uk[b]], rb["dK"][0]) < 1e-13
+            assert _rel(r["dV"][b, :uk[b]], rb["dV"][0]) < 1e-13
+            assert np.abs(r["dQ"][b, uq[b]:]).max(initial=0.0) == 0
+            assert np.abs(r["dK"][b, uk[b]:]).max(initial=0.0) == 0
+    # packed: the used rows start at each sequence's offset
+    cq, ck = np.array([0, 4, 10]), np.array([0, 6, 9])
+    q, do = rng.standard_normal((10, 2, 4)), rng.standard_normal((10, 2, 4))
+    k, v = rng.standard_normal((9, 1, 4)), rng.standard_normal((9, 1, 4))
+    r = o_mod.mha_backward(q, k, v, do, 0.5, True, cq, ck, seqused_q=[3, 6], seqused_k=[6, 2])
+    rb = o_mod.mha_backward(q[None, 4:10], k[None, 6:8], v[None, 6:8], do[None, 4:10], 0.5, True)
+    assert _rel(r["dQ"][4:10], rb["dQ"][0]) < 1e-13 and _rel(r["dK"][6:8], rb["dK"][0]) < 1e-13
+    rb = o_mod.mha_backward(q[None, 0:3], k[None, 0:6], v[None, 0:6], do[None, 0:3], 0.5, True)
+    assert _rel(r["dV"][0:6], rb["dV"][0]) < 1e-13 and np.abs(r["dQ"][3]).max() == 0
+
+
 def pin_empty_cases(o_mod):
     # seqlen_q == 0: dK = dV = 0
     q, do = np.zeros((1, 0, 2, 4)), np.zeros((1, 0, 2, 4))
@@ -501,4 +542,5 @@ ALL_PINS = [pin_sympy_exact, pin_finite_differences, pin_finite_differences_varl
             pin_equal_value_rows, pin_causal_row0, pin_causal_bottom_right, pin_zero_query,
             pin_single_key, pin_key_shift_and_permutation, pin_torch_autograd,
             pin_varlen_matches_padded, pin_cross_varlen_matches_padded, pin_empty_cases,
-            pin_group_rows_autograd, pin_window, pin_finite_differences_window, pin_softcap]
+            pin_group_rows_autograd, pin_window, pin_finite_differences_window, pin_softcap,
+            pin_seqused]

@@ -34,13 +34,17 @@ MUTANTS = {
     "gqa_no_group_sum": ("_put(dk, ks, hkv, r[\"dK\"], add=True)", "_put(dk, ks, hkv, r[\"dK\"])"),
     "delta_from_output_axis": ("np.asarray(do, dtype=np.float64)).sum(axis=-1)", "np.asarray(do, dtype=np.float64)).sum(axis=0)"),
     "softmax_no_max_shift_sign": ("np.exp(s - m[:, None])", "np.exp(s + m[:, None])"),
-    "varlen_keys_by_query_offsets": ("yield b, (slice(cq[b], cq[b + 1]),), (slice(ck[b], ck[b + 1]),)",
-                                     "yield b, (slice(cq[b], cq[b + 1]),), (slice(cq[b], cq[b + 1]),)"),
+    "varlen_keys_by_query_offsets": ("yield b, (slice(cq[b], cq[b] + nq),), (slice(ck[b], ck[b] + nk),)",
+                                     "yield b, (slice(cq[b], cq[b] + nq),), (slice(cq[b], cq[b] + nk),)"),
     "softcap_no_derivative": ("ds = ds * (1.0 - np.tanh(scale * (q @ k.T) / softcap) ** 2)",
                               "ds = ds * 1.0"),
     "softcap_derivative_unscaled": ("ds = ds * (1.0 - np.tanh(scale * (q @ k.T) / softcap) ** 2)",
                                     "ds = ds * (1.0 - np.tanh((q @ k.T) / softcap) ** 2)"),
     "softcap_inside_scale": ("s = softcap * np.tanh(s / softcap)", "s = np.tanh(s / softcap)"),
+    "seqused_ignored_padded": ("qs = slice(None) if uq is None else slice(0, uq[b])",
+                               "qs = slice(None)"),
+    "seqused_packed_from_zero": ("yield b, (slice(cq[b], cq[b] + nq),), (slice(ck[b], ck[b] + nk),)",
+                                 "yield b, (slice(cq[b], cq[b] + nq),), (slice(0, nk),)"),
     # the row-sampled group backward
     "rows_drop_delta": ("            ds = p * (dp - delta[:, None])", "            ds = p * dp"),
     "rows_dv_from_ds": ("dv += p[:, k_rows].T @ doh[i0:i1]", "dv += ds[:, k_rows].T @ doh[i0:i1]"),
