@@ -37,15 +37,17 @@ class AttnTensor(ctypes.Structure):
 
 class AttnOpts(ctypes.Structure):
     _fields_ = [("window_left", ctypes.c_int), ("window_right", ctypes.c_int),
-                ("softcap", ctypes.c_float)]
+                ("softcap", ctypes.c_float), ("seqused_q", ctypes.c_void_p),
+                ("seqused_k", ctypes.c_void_p)]
 
 
-def _opts(window, softcap):
-    """None when neither a window nor a cap is asked for (plain entry points)."""
-    if window is None and not softcap:
+def _opts(window, softcap, seqused_q=None, seqused_k=None):
+    """None when no option is asked for (plain entry points).  seqused_q/k:
+    device int32 tensors [batch] of used lengths, or None."""
+    if window is None and not softcap and seqused_q is None and seqused_k is None:
         return None
     left, right = (-1, -1) if window is None else (int(window[0]), int(window[1]))
-    return AttnOpts(left, right, float(softcap or 0.0))
+    return AttnOpts(left, right, float(softcap or 0.0), _ptr(seqused_q), _ptr(seqused_k))
 
 
 _T = ctypes.POINTER(AttnTensor)
@@ -175,11 +177,13 @@ def version() -> str:
 
 def attn_fwd(q, k, v, causal: bool = False, scale: Optional[float] = None, cu_seqlens_q=None,
              cu_seqlens_k=None, max_seqlen_q=None, max_seqlen_k=None, out=None, lse=None,
-             stream=None, window=None, softcap: float = 0.0) -> Tuple[torch.Tensor, torch.Tensor]:
+             stream=None, window=None, softcap: float = 0.0, seqused_q=None,
+             seqused_k=None) -> Tuple[torch.Tensor, torch.Tensor]:
     """Forward pass: returns (O like q, LSE fp32 [B,H,Sq] or [H,total_q], natural log).
 
     ``window=(left, right)`` selects a local mask (-1 = unbounded side);
-    ``softcap > 0`` caps the logits as softcap * tanh(logit / softcap)."""
+    ``softcap > 0`` caps the logits as softcap * tanh(logit / softcap);
+    ``seqused_q/k`` (device int32 [batch]) are per-sequence used lengths."""
     L = lib()
     b, sq, sk, hq, hk, d, mq, mk = _dims(q, k, cu_seqlens_q, cu_seqlens_k, max_seqlen_q,
                                          max_seqlen_k)
@@ -192,7 +196,7 @@ def attn_fwd(q, k, v, causal: bool = False, scale: Optional[float] = None, cu_se
     args = [ctypes.byref(dq_), ctypes.byref(dk_), ctypes.byref(dv_), ctypes.byref(do_), _ptr(lse),
             _dtype_code(q), b, sq, sk, hq, hk, d, scale, int(bool(causal)), _ptr(cu_seqlens_q),
             _ptr(cu_seqlens_k), mq, mk]
-    opts = _opts(window, softcap)
+    opts = _opts(window, softcap, seqused_q, seqused_k)
     if opts is None:
         rc = L.attn_fwd(*args, _stream(stream))
     else:
@@ -234,14 +238,16 @@ def attn_bwd(q, k, v, o, lse, do, causal: bool = False, scale: Optional[float] =
              cu_seqlens_q=None, cu_seqlens_k=None, max_seqlen_q=None, max_seqlen_k=None,
              deterministic: bool = False, workspace: Optional[torch.Tensor] = None, dq=None,
              dk=None, dv=None, stream=None, stage: str = "all", window=None,
-             softcap: float = 0.0):
+             softcap: float = 0.0, seqused_q=None, seqused_k=None):
     """Backward pass: returns (dQ, dK, dV), each like its input.
 
     ``stage`` selects one of the three kernels ("pre", "main", "post") or all
     of them in order ("all"); the stages must share the workspace.
     ``window=(left, right)`` selects a local mask (-1 = unbounded side; causal
     bounds the right side at 0); ``softcap > 0`` caps the logits as
-    softcap * tanh(logit / softcap) (use the forward's settings).
+    softcap * tanh(logit / softcap) (use the forward's settings); ``seqused_q/k``
+    (device int32 [batch]) are per-sequence used lengths (rows past them are
+    left as they were).
     """
     L = lib()
     b, sq, sk, hq, hk, d, mq, mk = _dims(q, k, cu_seqlens_q, cu_seqlens_k, max_seqlen_q,
@@ -259,7 +265,7 @@ def attn_bwd(q, k, v, o, lse, do, causal: bool = False, scale: Optional[float] =
             int(bool(causal)), _ptr(cu_seqlens_q), _ptr(cu_seqlens_k), mq, mk,
             int(bool(deterministic))]
     tail = [workspace.data_ptr(), workspace.numel(), _stream(stream)]
-    opts = _opts(window, softcap)
+    opts = _opts(window, softcap, seqused_q, seqused_k)
     if opts is None:
         rc = getattr(L, _STAGE_FN[stage])(*args, *tail)
     else:

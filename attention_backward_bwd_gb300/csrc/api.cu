@@ -189,7 +189,7 @@ int check_common(int dtype, int batch, int seqlen_q, int seqlen_k, int h_q, int 
 }
 
 int resolve_opts(const attn_opts* in, attn_opts* out) {
-  *out = attn_opts{-1, -1, 0.f};
+  *out = attn_opts{-1, -1, 0.f, nullptr, nullptr};
   if (in == nullptr) return ATTN_OK;
   if (in->window_left < -1 || in->window_right < -1)
     return fail(ATTN_ERR_ARG, "window sides must be >= -1 (-1 = unbounded), got (%d, %d)",
@@ -269,7 +269,10 @@ int prepare_bwd(const attn_tensor* q, const attn_tensor* k, const attn_tensor* v
   p.max_seqlen_k = varlen ? max_seqlen_k : seqlen_k;
   p.status = status_word();
   if (p.status == nullptr) return fail(ATTN_ERR_CUDA, "cannot resolve the device status word");
-  p.input_bad = varlen ? p.status + 1 : nullptr;
+  p.seq.used_q = opts.seqused_q;
+  p.seq.used_k = opts.seqused_k;
+  const bool used = opts.seqused_q != nullptr || opts.seqused_k != nullptr;
+  p.input_bad = (varlen || used) ? p.status + 1 : nullptr;
   p.timeout_ns = static_cast<unsigned long long>(g_timeout_ns.load());
   out->dtype = dtype;
   out->empty_q = !hq;
@@ -284,6 +287,10 @@ int run_stages(int stages, const Prepared& pr, cudaStream_t stream) {
     e = launch_validate_cu(p.seq.cu_q, p.seq.cu_k, p.seq.batch, p.seq.seqlen_q, p.seq.seqlen_k,
                            p.max_seqlen_q, p.max_seqlen_k, p.status + 1, stream);
     if (e != cudaSuccess) return cuda_fail(e, "cu_seqlens validation launch");
+  }
+  if ((p.seq.used_q != nullptr || p.seq.used_k != nullptr) && !(pr.empty_q || pr.empty_k)) {
+    e = launch_validate_used(p.seq, p.status + 1, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "seqused validation launch");
   }
   if (pr.empty_q || pr.empty_k) {
     // Nothing to reduce.  Empty query side: dK = dV = 0.  Empty key side: dQ = 0.
@@ -417,6 +424,8 @@ int attn_fwd_ex(const attn_tensor* q, const attn_tensor* k, const attn_tensor* v
   FwdParams p;
   std::memset(&p, 0, sizeof(p));
   p.seq = SeqParams{cu_seqlens_q, cu_seqlens_k, seqlen_q, seqlen_k, batch};
+  p.seq.used_q = opts.seqused_q;
+  p.seq.used_k = opts.seqused_k;
   p.q = targ(q);
   p.k = targ(k);
   p.v = targ(v);
@@ -441,6 +450,11 @@ int attn_fwd_ex(const attn_tensor* q, const attn_tensor* k, const attn_tensor* v
     e = launch_validate_cu(cu_seqlens_q, cu_seqlens_k, batch, seqlen_q, seqlen_k, max_seqlen_q,
                            max_seqlen_k, st + 1, reinterpret_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "cu_seqlens validation launch");
+  }
+  if (p.seq.used_q != nullptr || p.seq.used_k != nullptr) {
+    p.input_bad = st + 1;
+    e = launch_validate_used(p.seq, st + 1, reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "seqused validation launch");
   }
   e = launch_fwd(p, dtype, reinterpret_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "forward launch");

@@ -400,6 +400,9 @@ __device__ __forceinline__ SeqInfo seq_info(const SeqParams& s, int b) {
     r.sk = s.seqlen_k;
     r.ws_row0 = static_cast<int64_t>(b) * round_up(s.seqlen_q, kTileRows);
   }
+  // used lengths (clamped to the sequence's rows): the rest of its rows take no part
+  if (s.used_q != nullptr) r.sq = max(0, min(r.sq, s.used_q[b]));
+  if (s.used_k != nullptr) r.sk = max(0, min(r.sk, s.used_k[b]));
   return r;
 }
 

@@ -292,10 +292,12 @@ extern "C" int attn_bwd_host(const attn_tensor* q, const attn_tensor* k, const a
     const float* tlse = reinterpret_cast<const float*>(buf + L.lse) +
                         (static_cast<size_t>(b0) * h_q + i0) * seqlen_q;
     Prepared pr;
+    attn_opts co = checked;  // used lengths of this chunk's sequences
+    if (co.seqused_q != nullptr) co.seqused_q += b0;
+    if (co.seqused_k != nullptr) co.seqused_k += b0;
     rc = prepare_bwd(&tq, &tk, &tv, &to, tlse, &tdo, &tdq, &tdk, &tdv, dtype, nb, seqlen_q,
                      seqlen_k, ni, nj, head_dim, scale, causal, nullptr, nullptr, seqlen_q,
-                     seqlen_k, deterministic, &checked, buf + L.ws[c % kSlots], L.ws_bytes,
-                     &pr);
+                     seqlen_k, deterministic, &co, buf + L.ws[c % kSlots], L.ws_bytes, &pr);
     if (rc) return rc;
     if ((rc = run_stages(kPre | kMain | kPost, pr, cs))) return rc;
     if ((e = cudaEventRecord(P->comp_done[c], cs)) != cudaSuccess) return cuda_fail(e, "record");

@@ -23,6 +23,8 @@ struct SeqParams {
   int seqlen_q;     // padded: per-sequence length; varlen: total packed rows
   int seqlen_k;
   int batch;        // number of sequences
+  const int* used_q = nullptr;  // optional used length of each sequence (<= its rows)
+  const int* used_k = nullptr;
 };
 
 // A [B, S, H, D] (or packed [total, H, D]) tensor: element strides, last dim contiguous.
@@ -110,6 +112,8 @@ cudaError_t launch_zero_rows(const TensorArg& t, int dtype, int nseq, int rows_p
 cudaError_t launch_validate_cu(const int* cu_q, const int* cu_k, int batch, int total_q,
                                int total_k, int max_q, int max_k, unsigned int* bad,
                                cudaStream_t stream);
+// Checks 0 <= used[b] <= rows of sequence b for the used-length arrays given.
+cudaError_t launch_validate_used(const SeqParams& s, unsigned int* bad, cudaStream_t stream);
 
 int num_sms();
 

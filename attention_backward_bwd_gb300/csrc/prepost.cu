@@ -145,6 +145,7 @@ __global__ void __launch_bounds__(kThreads) postprocess_kernel(BwdParams p) {
       i = static_cast<int>(tok) - p.seq.cu_q[b];
     }
     const SeqInfo si = seq_info(p.seq, b);
+    if (i >= si.sq) continue;  // past a used length: left as it was
     const float* src = p.dqacc + ((static_cast<int64_t>(h) * p.ws_rows + si.ws_row0 + i) * D + c * 8);
     const float4 a = reinterpret_cast<const float4*>(src)[0];
     const float4 d = reinterpret_cast<const float4*>(src)[1];
@@ -180,6 +181,18 @@ __global__ void __launch_bounds__(kThreads)
     }
     T* dst = const_cast<T*>(static_cast<const T*>(t.ptr)) + off + c * 8;
     if (c * 8 < head_dim) *reinterpret_cast<uint4*>(dst) = make_uint4(0u, 0u, 0u, 0u);
+  }
+}
+
+// Checks the used-length arrays: 0 <= used[b] <= the rows of sequence b.
+__global__ void validate_used_kernel(SeqParams s, unsigned int* bad) {
+  for (int b = threadIdx.x; b < s.batch; b += blockDim.x) {
+    unsigned int code = 0;
+    const int cap_q = s.cu_q != nullptr ? s.cu_q[b + 1] - s.cu_q[b] : s.seqlen_q;
+    const int cap_k = s.cu_k != nullptr ? s.cu_k[b + 1] - s.cu_k[b] : s.seqlen_k;
+    if (s.used_q != nullptr && (s.used_q[b] < 0 || s.used_q[b] > cap_q)) code = 0xB0000005u;
+    if (s.used_k != nullptr && (s.used_k[b] < 0 || s.used_k[b] > cap_k)) code = 0xB0000006u;
+    if (code) atomicCAS(bad, 0u, code);
   }
 }
 
@@ -291,6 +304,11 @@ cudaError_t launch_validate_cu(const int* cu_q, const int* cu_k, int batch, int 
                                int total_k, int max_q, int max_k, unsigned int* bad,
                                cudaStream_t stream) {
   validate_cu_kernel<<<1, 256, 0, stream>>>(cu_q, cu_k, batch, total_q, total_k, max_q, max_k, bad);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_validate_used(const SeqParams& s, unsigned int* bad, cudaStream_t stream) {
+  validate_used_kernel<<<1, 256, 0, stream>>>(s, bad);
   return cudaGetLastError();
 }
 

@@ -149,12 +149,24 @@ int attn_bwd(const attn_tensor* q, const attn_tensor* k, const attn_tensor* v,
  *     before the softmax (the Has_softcap path of flash-attention
  *     hopper/flash_bwd_launch_template.h; the formula is the usual logit cap);
  *     the backward applies the cap's derivative.  0 = no cap.
+ *   seqused_q, seqused_k: NULL, or device int32 arrays [batch]: sequence b
+ *     is the first seqused[b] of its rows (its padded slab, or its packed
+ *     range from cu_seqlens), the seqused_q / seqused_k of the FA3 launcher
+ *     (flash-attention hopper/flash_bwd_launch_template.h).  The other rows of
+ *     the sequence take no part in the result and their dq / dk / dv rows (O
+ *     and LSE rows in the forward) are left as they were.  Like the packed
+ *     rows of a neighbouring sequence, they may be read inside a tile and
+ *     masked out, so they must hold finite values (0 x NaN is NaN in a tensor
+ *     core sum).  Values outside [0, rows of the sequence] are reported by
+ *     attn_check_device_status as ATTN_ERR_ARG and make the kernels return.
  * Window sides below -1, a negative or non-finite softcap give ATTN_ERR_ARG.
  */
 typedef struct {
   int window_left;
   int window_right;
   float softcap;
+  const int* seqused_q;
+  const int* seqused_k;
 } attn_opts;
 
 /*
