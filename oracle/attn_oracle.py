@@ -244,7 +244,7 @@ def mha_backward(q, k, v, do, scale=None, causal=False, cu_seqlens_q=None, cu_se
 
 
 def group_backward_rows(q, k, v, do, b: int, g: int, q_rows, k_rows, scale=None,
-                        causal=False, block: int = 512, window=None):
+                        causal=False, block: int = 512, window=None, softcap: float = 0.0):
     """Exact gradients at selected rows of one (sequence, kv head) group, for
     problems too large for ``mha_backward`` (padded [B,S,H,D] inputs only).
 
@@ -275,7 +275,9 @@ def group_backward_rows(q, k, v, do, b: int, g: int, q_rows, k_rows, scale=None,
             ii = np.arange(i0, i1)[:, None]
             jj = np.arange(sk)[None, :]
             allowed = allowed_pairs(ii, jj, sq, sk, causal, window)
-            s = np.where(allowed, scale * (qh[i0:i1] @ kg.T), -np.inf)
+            s_raw = scale * (qh[i0:i1] @ kg.T)
+            s = softcap * np.tanh(s_raw / softcap) if softcap > 0 else s_raw
+            s = np.where(allowed, s, -np.inf)
             any_key = allowed.any(axis=1)
             m = np.where(any_key, s.max(axis=1), 0.0)
             ell = np.where(allowed, np.exp(s - m[:, None]), 0.0).sum(axis=1)
@@ -284,6 +286,8 @@ def group_backward_rows(q, k, v, do, b: int, g: int, q_rows, k_rows, scale=None,
             dp = doh[i0:i1] @ vg.T
             delta = (p * dp).sum(axis=1)
             ds = p * (dp - delta[:, None])
+            if softcap > 0:
+                ds = ds * (1.0 - np.tanh(s_raw / softcap) ** 2)
             for n, i in enumerate(q_rows):
                 if i0 <= i < i1:
                     dq[hh, n] = scale * (ds[i - i0] @ kg)

@@ -526,12 +526,12 @@ def pin_group_rows_autograd(o_mod):
     q, k, v = (rng.standard_normal((b, sq, hq, d)), rng.standard_normal((b, sk, hk, d)),
                rng.standard_normal((b, sk, hk, d)))
     do = rng.standard_normal((b, sq, hq, d))
-    for win, causal in (((3, 1), False), ((2, -1), True)):
-        full = o_mod.mha_backward(q, k, v, do, 0.3, causal, window=win)
+    for win, causal, cap in (((3, 1), False, 0.0), ((2, -1), True, 0.0), (None, True, 0.4)):
+        full = o_mod.mha_backward(q, k, v, do, 0.3, causal, window=win, softcap=cap)
         q_rows, k_rows = [0, 5, sq - 1], [0, 4, sk - 1]
         for g in range(hk):
             dq, dk, dv = o_mod.group_backward_rows(q, k, v, do, 0, g, q_rows, k_rows, 0.3, causal,
-                                                   block=4, window=win)
+                                                   block=4, window=win, softcap=cap)
             for hh in range(hq // hk):
                 assert _rel(dq[hh], full["dQ"][0, q_rows, g * (hq // hk) + hh]) < 1e-12
             assert _rel(dk, full["dK"][0, k_rows, g]) < 1e-12

@@ -285,6 +285,32 @@ def test_full_size_bench_workload_sampled_rows():
         assert_close(f"full-size dV b={b} g={g}", dv[b, rows, g], dv_ref)
 
 
+@pytest.mark.parametrize("name", ["gqa_b2_hq32_hk8_s8192_d128_bf16_causal_win1024",
+                                  "gqa_b2_hq32_hk8_s8192_d128_bf16_causal_cap30"])
+def test_full_size_window_and_softcap_sampled_rows(name):
+    """The sliding-window and logit-cap bench workloads at full size, through
+    the options bench.py passes, on sampled rows (including rows around the
+    window's edge) of one group against the row-wise fp64 oracle."""
+    w = synth.WORKLOADS[name]
+    x = synth.make_inputs(w)
+    q, k, v, do = (t.cuda() for t in (x.q, x.k, x.v, x.do))
+    window = tuple(w.window) if w.windowed else None
+    o, lse = ab.attn_fwd(q, k, v, causal=w.causal, window=window, softcap=w.softcap)
+    dq, dk, dv = ab.attn_bwd(q, k, v, o, lse, do, causal=w.causal, window=window,
+                             softcap=w.softcap)
+    ab.check_device_status()
+    rng = np.random.default_rng(11)
+    rows = sorted(set(_sampled_rows(w.seqlen_q, rng) + [1023, 1024, 1025, 1151, 1152, 5000]))
+    grp = w.h_q // w.h_k
+    b, g = 1, 3
+    dq_ref, dk_ref, dv_ref = attn_oracle.group_backward_rows(
+        x.q, x.k, x.v, x.do, b, g, rows, rows, w.scale, w.causal, window=window,
+        softcap=w.softcap)
+    assert_close(f"{name} dQ", dq[b, rows, g * grp:(g + 1) * grp].transpose(0, 1), dq_ref)
+    assert_close(f"{name} dK", dk[b, rows, g], dk_ref)
+    assert_close(f"{name} dV", dv[b, rows, g], dv_ref)
+
+
 def _sampled_rows(n, rng, extra=6):
     base = [0, 1, 127, 128, 129, n // 2, n - 2, n - 1]
     return sorted(set(r for r in base + [int(v) for v in rng.integers(0, n, extra)] if 0 <= r < n))

@@ -45,6 +45,8 @@ MUTANTS = {
                                "qs = slice(None)"),
     "seqused_packed_from_zero": ("yield b, (slice(cq[b], cq[b] + nq),), (slice(ck[b], ck[b] + nk),)",
                                  "yield b, (slice(cq[b], cq[b] + nq),), (slice(0, nk),)"),
+    "rows_softcap_no_derivative": ("                ds = ds * (1.0 - np.tanh(s_raw / softcap) ** 2)",
+                                   "                ds = ds * 1.0"),
     # the row-sampled group backward
     "rows_drop_delta": ("            ds = p * (dp - delta[:, None])", "            ds = p * dp"),
     "rows_dv_from_ds": ("dv += p[:, k_rows].T @ doh[i0:i1]", "dv += ds[:, k_rows].T @ doh[i0:i1]"),
