@@ -4,12 +4,14 @@
 // Algorithm (TileLang test_tilelang_kernel_mha_bwd.py, flashattn_bwd): KV
 // stationary.  One work unit = (KV tile n of BN=128 keys, kv head g, sequence
 // b).  K_n and V_n are loaded once; for each of the G query heads of the
-// group and each query tile m of BM=128 rows in the causal range:
+// group and each query tile m of BM=128 rows that sees key tile n (all of them,
+// or the causal / local-window range, bottom-right aligned):
 //   S^T  = K_n Q_m^T                        (TMEM, fp32)
 //   P^T  = exp2(S^T * scale * log2 e - LSE2[query]), masked  (bf16/fp16, TMEM)
+//          (with a logit cap c: exp2(c tanh(S^T scale / c) log2 e - LSE2))
 //   dP^T = V_n dO_m^T                       (TMEM, fp32)
 //   dV  += P^T dO_m                         (TMEM accumulator, A operand from TMEM)
-//   dS^T = P^T * (dP^T - Delta[query])      (smem, bf16/fp16)
+//   dS^T = P^T * (dP^T - Delta[query])      (smem, bf16/fp16; times 1 - tanh^2 with a cap)
 //   dK  += dS^T Q_m                         (TMEM accumulator, A operand from smem)
 //   dQ_m = dS K_n -> reduced into the fp32 dQaccum in global memory
 // dK (times scale) and dV are written once per unit; dK/dV of a GQA group are
@@ -18,6 +20,9 @@
 // dQaccum is reduced with TMA tensor reduce-adds (fp32), or, in deterministic
 // mode, in ascending KV-tile order behind a per-(head, query tile) semaphore
 // (the dq_semaphore of flash-attention hopper/flash_bwd_launch_template.h).
+// D is 64 or 128 here; smaller head dims (multiples of 8) run zero-padded to
+// the next of those.  Template switches: kCap (logit cap), kLeft (a left
+// window side); the default instantiation has neither.
 //
 // Warp roles (768 threads = 6 warpgroups): warp 0 TMA producer, warp 1 MMA
 // issuer (one thread), warp 2 TMEM allocator, warps 4-19 softmax / dS / dK-dV
