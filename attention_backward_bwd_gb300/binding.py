@@ -61,7 +61,8 @@ _lock = threading.Lock()
 
 EXPORTS = ("attn_fwd", "attn_bwd", "attn_bwd_preprocess", "attn_bwd_main", "attn_bwd_postprocess",
            "attn_bwd_workspace_size", "attn_bwd_workspace_layout", "attn_bwd_noalloc",
-           "attn_bwd_host", "attn_bwd_host_buffer_size", "attn_bwd_ex", "attn_fwd_ex",
+           "attn_bwd_host", "attn_bwd_host_buffer_size", "attn_bwd_host_varlen",
+           "attn_bwd_host_varlen_buffer_size", "attn_bwd_ex", "attn_fwd_ex",
            "attn_check_device_status",
            "attn_set_wait_timeout_ns", "attn_last_error", "attn_version", "attn_diag_mma",
            "attn_diag_wait_timeout", "attn_diag_exp2", "attn_diag_tanh")
@@ -97,6 +98,12 @@ def lib() -> ctypes.CDLL:
         L.attn_bwd_host.restype = _I
         L.attn_bwd_host_buffer_size.argtypes = [_I, _I, _I, _I, _I, _I, _I]
         L.attn_bwd_host_buffer_size.restype = ctypes.c_size_t
+        L.attn_bwd_host_varlen.argtypes = [_T, _T, _T, _T, _P, _T, _T, _T, _T, _I, _I, _I, _I,
+                                           _I, _I, _I, ctypes.c_float, _I, _P, _P, _I,
+                                           ctypes.POINTER(AttnOpts), _I, _P, ctypes.c_size_t, _P]
+        L.attn_bwd_host_varlen.restype = _I
+        L.attn_bwd_host_varlen_buffer_size.argtypes = [_P, _P, _I, _I, _I, _I, _I, _I, _I]
+        L.attn_bwd_host_varlen_buffer_size.restype = ctypes.c_size_t
         L.attn_bwd_workspace_size.argtypes = [_I, _I, _I, _I, _I, _I]
         L.attn_bwd_workspace_size.restype = ctypes.c_size_t
         L.attn_bwd_workspace_layout.argtypes = [_I, _I, _I, _I, _I,
@@ -313,6 +320,44 @@ def attn_bwd_host(q, k, v, o, lse, do, dq=None, dk=None, dv=None, causal: bool =
                          _dtype_code(q), b, sq, sk, hq, hk, d, scale, int(bool(causal)),
                          int(bool(deterministic)), opts_ref, int(chunks), device_buffer.data_ptr(),
                          device_buffer.numel(), _stream(stream))
+    _check(rc)
+    return dq, dk, dv
+
+
+def attn_bwd_host_varlen(q, k, v, o, lse, do, cu_seqlens_q, cu_seqlens_k, dq=None, dk=None,
+                         dv=None, causal: bool = False, scale: Optional[float] = None,
+                         deterministic: bool = False, chunks: int = 0,
+                         device_buffer: Optional[torch.Tensor] = None, device=None, stream=None,
+                         window=None, softcap: float = 0.0):
+    """Backward on packed HOST tensors ([total, H, D], heads adjacent; lse
+    [H_q, total_q]) with host int32 cu_seqlens; results in host tensors (pinned,
+    allocated here if not given), valid once ``stream`` has passed the call."""
+    L = lib()
+    b = int(cu_seqlens_q.numel()) - 1
+    tq, tk, hq, hk, d = q.shape[0], k.shape[0], q.shape[1], k.shape[1], q.shape[2]
+    scale = d ** -0.5 if scale is None else float(scale)
+    cu_q = cu_seqlens_q.to(torch.int32).contiguous().cpu()
+    cu_k = cu_seqlens_k.to(torch.int32).contiguous().cpu()
+    pin = torch.cuda.is_available()
+    dq = torch.empty(q.shape, dtype=q.dtype, pin_memory=pin) if dq is None else dq
+    dk = torch.empty(k.shape, dtype=k.dtype, pin_memory=pin) if dk is None else dk
+    dv = torch.empty(v.shape, dtype=v.dtype, pin_memory=pin) if dv is None else dv
+    need = int(L.attn_bwd_host_varlen_buffer_size(cu_q.data_ptr(), cu_k.data_ptr(), b, tq, tk, hq,
+                                                  hk, d, chunks))
+    if need == 0:
+        raise AttnError(-9, L.attn_last_error().decode() or "invalid varlen arguments")
+    if device_buffer is None:
+        device_buffer = torch.empty(need, dtype=torch.uint8,
+                                    device=device if device is not None else "cuda")
+    descs = [_desc(t) for t in (q, k, v, o)]
+    d_do, d_dq, d_dk, d_dv = _desc(do), _desc(dq), _desc(dk), _desc(dv)
+    opts = _opts(window, softcap)
+    rc = L.attn_bwd_host_varlen(*(ctypes.byref(x) for x in descs), _ptr(lse), ctypes.byref(d_do),
+                                ctypes.byref(d_dq), ctypes.byref(d_dk), ctypes.byref(d_dv),
+                                _dtype_code(q), b, tq, tk, hq, hk, d, scale, int(bool(causal)),
+                                cu_q.data_ptr(), cu_k.data_ptr(), int(bool(deterministic)),
+                                None if opts is None else ctypes.byref(opts), int(chunks),
+                                device_buffer.data_ptr(), device_buffer.numel(), _stream(stream))
     _check(rc)
     return dq, dk, dv
 

@@ -26,6 +26,7 @@
 #include <cuda_runtime.h>
 
 #include <mutex>
+#include <vector>
 
 #include "../../include/attn_bwd.h"
 #include "internal.h"
@@ -310,6 +311,265 @@ extern "C" int attn_bwd_host(const attn_tensor* q, const attn_tensor* k, const a
         (e = copy_heads(*dk, buf + L.dk, b0, nb, j0, nj, seqlen_k, h_k, head_dim, false,
                         P->out)) ||
         (e = copy_heads(*dv, buf + L.dv, b0, nb, j0, nj, seqlen_k, h_k, head_dim, false, P->out)))
+      return cuda_fail(e, "copy results to the host");
+  }
+  if ((e = cudaEventRecord(P->done, P->out)) != cudaSuccess) return cuda_fail(e, "record done");
+  if ((e = cudaStreamWaitEvent(user, P->done, 0)) != cudaSuccess) return cuda_fail(e, "wait done");
+  return ATTN_OK;
+}
+
+// ---------------------------------------------------------------------------
+// attn_bwd_host_varlen: the same pipeline for packed [total, H, D] tensors.
+// A chunk is a run of whole sequences (all heads), the runs cut so that each
+// holds about an equal share of the attention work (query rows x key rows per
+// sequence); its rows are contiguous, so each tensor moves in one pitched copy.
+// The chunk's LSE rows, which are strided in [H_q, total_q], land in a compact
+// [H_q, rows] block of their own, and its cu_seqlens are rebased to start at 0
+// (all chunks' arrays go to the device in one small copy before the first).
+
+namespace attn {
+namespace {
+
+struct VarlenChunk {
+  int b0, nb;          // sequences [b0, b0 + nb)
+  int q0, nq, k0, nk;  // packed rows [q0, q0 + nq) and [k0, k0 + nk)
+  int max_q, max_k;    // longest query / key sequence of the chunk
+  int cu_off;          // offset (in ints) of the chunk's rebased cu_q; cu_k follows
+};
+
+int plan_varlen(const int* cu_q, const int* cu_k, int batch, int total_q, int total_k, int want,
+                VarlenChunk* out, int* n_out) {
+  if (cu_q == nullptr || cu_k == nullptr) return fail(ATTN_ERR_NULL, "cu_seqlens is NULL");
+  if (cu_q[0] != 0 || cu_k[0] != 0 || cu_q[batch] != total_q || cu_k[batch] != total_k)
+    return fail(ATTN_ERR_ARG, "cu_seqlens must start at 0 and end at the total row counts");
+  double work = 0;
+  for (int b = 0; b < batch; ++b) {
+    const int lq = cu_q[b + 1] - cu_q[b], lk = cu_k[b + 1] - cu_k[b];
+    if (lq < 0 || lk < 0) return fail(ATTN_ERR_ARG, "cu_seqlens must be nondecreasing");
+    work += static_cast<double>(lq) * lk + lq + lk;
+  }
+  if (want <= 0) want = 8;
+  if (want > kMaxChunks) want = kMaxChunks;
+  const double share = work / want;
+  int n = 0, b = 0, cu_off = 0;
+  while (b < batch) {
+    VarlenChunk c{b, 0, cu_q[b], 0, cu_k[b], 0, 0, 0, cu_off};
+    double w = 0;
+    // take sequences until the share is reached; the last chunk takes the rest
+    while (b < batch && (c.nb == 0 || w < share || n == want - 1)) {
+      const int lq = cu_q[b + 1] - cu_q[b], lk = cu_k[b + 1] - cu_k[b];
+      w += static_cast<double>(lq) * lk + lq + lk;
+      c.max_q = lq > c.max_q ? lq : c.max_q;
+      c.max_k = lk > c.max_k ? lk : c.max_k;
+      ++c.nb;
+      ++b;
+    }
+    c.nq = cu_q[b] - c.q0;
+    c.nk = cu_k[b] - c.k0;
+    cu_off += 2 * (c.nb + 1);
+    out[n++] = c;
+  }
+  *n_out = n;
+  return ATTN_OK;
+}
+
+struct VarlenLayout {
+  size_t q, k, v, o, dout, dq, dk, dv, lse, cu, ws[kSlots], ws_bytes, total;
+};
+
+VarlenLayout varlen_layout(int batch, int total_q, int total_k, int h_q, int h_k, int head_dim,
+                           const VarlenChunk* ch, int n) {
+  const size_t e = 2;
+  const size_t nq = static_cast<size_t>(total_q) * h_q * head_dim * e;
+  const size_t nk = static_cast<size_t>(total_k) * h_k * head_dim * e;
+  VarlenLayout L;
+  size_t at = 0;
+  auto take = [&](size_t bytes) {
+    const size_t off = at;
+    at = align256(at + bytes);
+    return off;
+  };
+  L.q = take(nq);
+  L.o = take(nq);
+  L.dout = take(nq);
+  L.dq = take(nq);
+  L.k = take(nk);
+  L.v = take(nk);
+  L.dk = take(nk);
+  L.dv = take(nk);
+  L.lse = take(static_cast<size_t>(h_q) * total_q * 4);
+  L.cu = take(static_cast<size_t>(2) * (batch + n) * 4);
+  L.ws_bytes = 0;
+  for (int c = 0; c < n; ++c) {
+    const size_t w = ws_layout(ch[c].nb, ch[c].nq, h_q, head_dim, 1).total;
+    L.ws_bytes = w > L.ws_bytes ? w : L.ws_bytes;
+  }
+  for (int i = 0; i < kSlots; ++i) L.ws[i] = take(L.ws_bytes);
+  L.total = at;
+  return L;
+}
+
+// rows [r0, r0 + n) of a packed host tensor <-> the same rows of its compact
+// device copy, all heads, one pitched copy
+cudaError_t copy_rows(const attn_tensor& host, char* dev, int r0, int n, int heads, int head_dim,
+                      bool to_device, cudaStream_t st) {
+  if (n == 0) return cudaSuccess;
+  const size_t e = 2;
+  const size_t width = static_cast<size_t>(heads) * head_dim * e;
+  const size_t hpitch = static_cast<size_t>(host.stride_s) * e;
+  char* h = static_cast<char*>(host.ptr) + static_cast<int64_t>(r0) * host.stride_s * e;
+  char* d = dev + static_cast<size_t>(r0) * width;
+  return to_device ? cudaMemcpy2DAsync(d, width, h, hpitch, width, n, cudaMemcpyDefault, st)
+                   : cudaMemcpy2DAsync(h, hpitch, d, width, width, n, cudaMemcpyDefault, st);
+}
+
+int check_packed_host_tensor(const attn_tensor* t, const char* name, int heads, int head_dim,
+                             bool need) {
+  if (t == nullptr) return fail(ATTN_ERR_NULL, "%s: descriptor is NULL", name);
+  if (!need) return ATTN_OK;
+  if (t->ptr == nullptr) return fail(ATTN_ERR_NULL, "%s: pointer is NULL", name);
+  if (t->stride_h != head_dim)
+    return fail(ATTN_ERR_STRIDE,
+                "%s: host tensors need adjacent heads (stride_h == D = %d, got %lld)", name,
+                head_dim, static_cast<long long>(t->stride_h));
+  if (t->stride_s < static_cast<int64_t>(heads) * head_dim)
+    return fail(ATTN_ERR_STRIDE, "%s: rows overlap (stride_s=%lld)", name,
+                static_cast<long long>(t->stride_s));
+  return ATTN_OK;
+}
+
+}  // namespace
+}  // namespace attn
+
+extern "C" size_t attn_bwd_host_varlen_buffer_size(const int* cu_seqlens_q,
+                                                   const int* cu_seqlens_k, int batch,
+                                                   int total_q, int total_k, int h_q, int h_k,
+                                                   int head_dim, int chunks) {
+  if (batch <= 0 || total_q < 0 || total_k < 0 || h_q <= 0 || h_k <= 0 || h_q % h_k != 0 ||
+      head_dim <= 0)
+    return 0;
+  VarlenChunk ch[kMaxChunks];
+  int n = 0;
+  if (plan_varlen(cu_seqlens_q, cu_seqlens_k, batch, total_q, total_k, chunks, ch, &n))
+    return 0;  // invalid cu_seqlens (the message stays in attn_last_error)
+  return varlen_layout(batch, total_q, total_k, h_q, h_k, head_dim, ch, n).total;
+}
+
+extern "C" int attn_bwd_host_varlen(const attn_tensor* q, const attn_tensor* k,
+                                    const attn_tensor* v, const attn_tensor* o, const float* lse,
+                                    const attn_tensor* dout, const attn_tensor* dq,
+                                    const attn_tensor* dk, const attn_tensor* dv, int dtype,
+                                    int batch, int total_q, int total_k, int h_q, int h_k,
+                                    int head_dim, float scale, int causal,
+                                    const int* cu_seqlens_q, const int* cu_seqlens_k,
+                                    int deterministic, const attn_opts* opts, int chunks,
+                                    void* device_buffer, size_t device_buffer_bytes,
+                                    attn_stream_t stream) {
+  clear_error();
+  int rc = check_common(dtype, batch, total_q, total_k, h_q, h_k, head_dim, scale, nullptr,
+                        nullptr, 0, 0);
+  if (rc) return rc;
+  const bool hq = total_q > 0, hk = total_k > 0;
+  if ((rc = check_packed_host_tensor(q, "q", h_q, head_dim, hq && hk))) return rc;
+  if ((rc = check_packed_host_tensor(k, "k", h_k, head_dim, hq && hk))) return rc;
+  if ((rc = check_packed_host_tensor(v, "v", h_k, head_dim, hq && hk))) return rc;
+  if ((rc = check_packed_host_tensor(o, "o", h_q, head_dim, hq && hk))) return rc;
+  if ((rc = check_packed_host_tensor(dout, "dout", h_q, head_dim, hq && hk))) return rc;
+  if ((rc = check_packed_host_tensor(dq, "dq", h_q, head_dim, hq))) return rc;
+  if ((rc = check_packed_host_tensor(dk, "dk", h_k, head_dim, hk))) return rc;
+  if ((rc = check_packed_host_tensor(dv, "dv", h_k, head_dim, hk))) return rc;
+  if (hq && hk && lse == nullptr) return fail(ATTN_ERR_NULL, "lse is NULL");
+  attn_opts checked;
+  if ((rc = resolve_opts(opts, &checked))) return rc;
+  VarlenChunk ch[kMaxChunks];
+  int n = 0;
+  if ((rc = plan_varlen(cu_seqlens_q, cu_seqlens_k, batch, total_q, total_k, chunks, ch, &n)))
+    return rc;
+  const VarlenLayout L = varlen_layout(batch, total_q, total_k, h_q, h_k, head_dim, ch, n);
+  if (device_buffer == nullptr) return fail(ATTN_ERR_WORKSPACE, "device_buffer is NULL");
+  if (reinterpret_cast<uintptr_t>(device_buffer) % 256 != 0)
+    return fail(ATTN_ERR_WORKSPACE, "device_buffer must be 256-byte aligned");
+  if (device_buffer_bytes < L.total)
+    return fail(ATTN_ERR_WORKSPACE, "device_buffer too small: %zu bytes given, %zu needed",
+                device_buffer_bytes, L.total);
+  // every chunk's rebased cu_seqlens_q then cu_seqlens_k
+  std::vector<int> cu_all(static_cast<size_t>(2) * (batch + n));
+  for (int c = 0; c < n; ++c) {
+    int* dst = cu_all.data() + ch[c].cu_off;
+    for (int i = 0; i <= ch[c].nb; ++i) {
+      dst[i] = cu_seqlens_q[ch[c].b0 + i] - ch[c].q0;
+      dst[ch[c].nb + 1 + i] = cu_seqlens_k[ch[c].b0 + i] - ch[c].k0;
+    }
+  }
+
+  std::lock_guard<std::mutex> lock(g_pool_mu);
+  Pool* P = nullptr;
+  if ((rc = get_pool(&P))) return rc;
+  cudaStream_t user = reinterpret_cast<cudaStream_t>(stream);
+  char* buf = static_cast<char*>(device_buffer);
+  cudaError_t e;
+  if ((e = cudaEventRecord(P->start, user)) != cudaSuccess) return cuda_fail(e, "record start");
+  cudaStream_t all[2 + kSlots];
+  all[0] = P->in;
+  all[1] = P->out;
+  for (int i = 0; i < kSlots; ++i) all[2 + i] = P->comp[i];
+  for (cudaStream_t s : all)
+    if ((e = cudaStreamWaitEvent(s, P->start, 0)) != cudaSuccess) return cuda_fail(e, "wait start");
+  // pageable source: the call returns once the data sit in the driver's staging memory
+  if ((e = cudaMemcpyAsync(buf + L.cu, cu_all.data(), cu_all.size() * sizeof(int),
+                           cudaMemcpyHostToDevice, P->in)) != cudaSuccess)
+    return cuda_fail(e, "copy cu_seqlens to the device");
+
+  for (int c = 0; c < n; ++c) {
+    const VarlenChunk& C = ch[c];
+    float* lse_dev = reinterpret_cast<float*>(buf + L.lse) + static_cast<size_t>(h_q) * C.q0;
+    if (hq && hk) {
+      if ((e = copy_rows(*q, buf + L.q, C.q0, C.nq, h_q, head_dim, true, P->in)) ||
+          (e = copy_rows(*o, buf + L.o, C.q0, C.nq, h_q, head_dim, true, P->in)) ||
+          (e = copy_rows(*dout, buf + L.dout, C.q0, C.nq, h_q, head_dim, true, P->in)) ||
+          (e = copy_rows(*k, buf + L.k, C.k0, C.nk, h_k, head_dim, true, P->in)) ||
+          (e = copy_rows(*v, buf + L.v, C.k0, C.nk, h_k, head_dim, true, P->in)))
+        return cuda_fail(e, "copy inputs to the device");
+      // LSE [H_q, total_q]: the chunk's columns of every head, into a compact [H_q, nq]
+      if (C.nq > 0 &&
+          (e = cudaMemcpy2DAsync(lse_dev, static_cast<size_t>(C.nq) * 4, lse + C.q0,
+                                 static_cast<size_t>(total_q) * 4, static_cast<size_t>(C.nq) * 4,
+                                 h_q, cudaMemcpyDefault, P->in)) != cudaSuccess)
+        return cuda_fail(e, "copy lse to the device");
+    }
+    if ((e = cudaEventRecord(P->in_done[c], P->in)) != cudaSuccess) return cuda_fail(e, "record");
+
+    cudaStream_t cs = P->comp[c % kSlots];
+    if ((e = cudaStreamWaitEvent(cs, P->in_done[c], 0)) != cudaSuccess)
+      return cuda_fail(e, "wait copy-in");
+    const size_t qoff = static_cast<size_t>(C.q0) * h_q * head_dim * 2;
+    const size_t koff = static_cast<size_t>(C.k0) * h_k * head_dim * 2;
+    const int64_t sq = static_cast<int64_t>(h_q) * head_dim;
+    const int64_t sk = static_cast<int64_t>(h_k) * head_dim;
+    const attn_tensor tq{buf + L.q + qoff, 0, sq, head_dim}, to{buf + L.o + qoff, 0, sq, head_dim};
+    const attn_tensor tdo{buf + L.dout + qoff, 0, sq, head_dim};
+    const attn_tensor tdq{buf + L.dq + qoff, 0, sq, head_dim};
+    const attn_tensor tk{buf + L.k + koff, 0, sk, head_dim}, tv{buf + L.v + koff, 0, sk, head_dim};
+    const attn_tensor tdk{buf + L.dk + koff, 0, sk, head_dim};
+    const attn_tensor tdv{buf + L.dv + koff, 0, sk, head_dim};
+    const int* cuq = reinterpret_cast<const int*>(buf + L.cu) + C.cu_off;
+    const int* cuk = cuq + C.nb + 1;
+    attn_opts co = checked;  // used lengths of this chunk's sequences
+    if (co.seqused_q != nullptr) co.seqused_q += C.b0;
+    if (co.seqused_k != nullptr) co.seqused_k += C.b0;
+    Prepared pr;
+    rc = prepare_bwd(&tq, &tk, &tv, &to, lse_dev, &tdo, &tdq, &tdk, &tdv, dtype, C.nb, C.nq,
+                     C.nk, h_q, h_k, head_dim, scale, causal, cuq, cuk, C.max_q, C.max_k,
+                     deterministic, &co, buf + L.ws[c % kSlots], L.ws_bytes, &pr);
+    if (rc) return rc;
+    if ((rc = run_stages(kPre | kMain | kPost, pr, cs))) return rc;
+    if ((e = cudaEventRecord(P->comp_done[c], cs)) != cudaSuccess) return cuda_fail(e, "record");
+
+    if ((e = cudaStreamWaitEvent(P->out, P->comp_done[c], 0)) != cudaSuccess)
+      return cuda_fail(e, "wait compute");
+    if ((e = copy_rows(*dq, buf + L.dq, C.q0, C.nq, h_q, head_dim, false, P->out)) ||
+        (e = copy_rows(*dk, buf + L.dk, C.k0, C.nk, h_k, head_dim, false, P->out)) ||
+        (e = copy_rows(*dv, buf + L.dv, C.k0, C.nk, h_k, head_dim, false, P->out)))
       return cuda_fail(e, "copy results to the host");
   }
   if ((e = cudaEventRecord(P->done, P->out)) != cudaSuccess) return cuda_fail(e, "record done");

@@ -245,9 +245,9 @@ def run_ours(args):
     t_main = statistics.mean(e[1].elapsed_time(e[2]) for e in evs)
     t_post = statistics.mean(e[2].elapsed_time(e[3]) for e in evs)
 
-    # --- end to end: pinned host inputs -> device -> backward -> pinned host results.
-    # Padded workloads go through attn_bwd_host (chunks whose copies overlap the
-    # kernels of other chunks); varlen ones copy in, call attn_bwd, copy out.
+    # --- end to end: pinned host inputs -> device -> backward -> pinned host results,
+    # through attn_bwd_host (padded) or attn_bwd_host_varlen (packed): chunks whose
+    # copies overlap the kernels of other chunks.
     hq_ = [t.cpu().pin_memory() for t in (q, k, v, o, do, lse)]
     host_out = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in (dq, dk, dv)]
     h2d = sum(t.numel() * t.element_size() for t in hq_)
@@ -264,16 +264,18 @@ def run_ours(args):
                              device_buffer=hbuf, stream=stream, window=window,
                              softcap=w.softcap)
     else:
-        dev_in = [torch.empty_like(t) for t in (q, k, v, o, do, lse)]
-        e2e_path = "copies + attn_bwd"
+        cu_q_h, cu_k_h = x.cu_seqlens_q.cpu(), x.cu_seqlens_k.cpu()
+        need = int(ab.lib().attn_bwd_host_varlen_buffer_size(
+            cu_q_h.data_ptr(), cu_k_h.data_ptr(), len(x.lengths), q.shape[0], k.shape[0],
+            q.shape[1], k.shape[1], q.shape[2], args.chunks))
+        hbuf = torch.empty(need, dtype=torch.uint8, device=dev)
+        e2e_path = f"attn_bwd_host_varlen, chunks={args.chunks or 'auto'}"
 
         def e2e_step():
-            for dst, src in zip(dev_in, hq_):
-                dst.copy_(src, non_blocking=True)
-            ab.attn_bwd(dev_in[0], dev_in[1], dev_in[2], dev_in[3], dev_in[5], dev_in[4],
-                        stream=stream, **kw)
-            for dst, src in zip(host_out, (dq, dk, dv)):
-                dst.copy_(src, non_blocking=True)
+            ab.attn_bwd_host_varlen(hq_[0], hq_[1], hq_[2], hq_[3], hq_[5], hq_[4], cu_q_h,
+                                    cu_k_h, *host_out, causal=w.causal, deterministic=det,
+                                    chunks=args.chunks, device_buffer=hbuf, stream=stream,
+                                    window=window, softcap=w.softcap)
 
     for _ in range(2):
         e2e_step()

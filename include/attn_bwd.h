@@ -264,6 +264,29 @@ int attn_bwd_host(const attn_tensor* q, const attn_tensor* k, const attn_tensor*
                   void* device_buffer, size_t device_buffer_bytes, attn_stream_t stream);
 
 /*
+ * attn_bwd_host_varlen -- attn_bwd_host for packed [total, H, D] tensors with
+ * cu_seqlens_q / cu_seqlens_k in HOST memory (int32 [batch + 1], starting at
+ * 0, nondecreasing, ending at total_q / total_k; checked on the host:
+ * ATTN_ERR_ARG).  A chunk is a run of whole sequences holding about an equal
+ * share of the attention work; each tensor's rows of a chunk move in one
+ * pitched copy.  lse is [H_q, total_q] in host memory.  Host tensors need
+ * adjacent heads (stride_h == D) and stride_s >= H * D.  device_buffer: at
+ * least attn_bwd_host_varlen_buffer_size(...) bytes (0 means invalid
+ * arguments or cu_seqlens).  Everything else as attn_bwd_host.
+ */
+size_t attn_bwd_host_varlen_buffer_size(const int* cu_seqlens_q, const int* cu_seqlens_k,
+                                        int batch, int total_q, int total_k, int h_q, int h_k,
+                                        int head_dim, int chunks);
+int attn_bwd_host_varlen(const attn_tensor* q, const attn_tensor* k, const attn_tensor* v,
+                         const attn_tensor* o, const float* lse, const attn_tensor* dout,
+                         const attn_tensor* dq, const attn_tensor* dk, const attn_tensor* dv,
+                         int dtype, int batch, int total_q, int total_k, int h_q, int h_k,
+                         int head_dim, float scale, int causal, const int* cu_seqlens_q,
+                         const int* cu_seqlens_k, int deterministic, const attn_opts* opts,
+                         int chunks, void* device_buffer, size_t device_buffer_bytes,
+                         attn_stream_t stream);
+
+/*
  * The three stages of attn_bwd, callable one by one (same arguments, same
  * checks) so that each kernel can be timed on its own.  They must run in this
  * order on one stream with the same workspace.

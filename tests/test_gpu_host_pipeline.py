@@ -152,3 +152,25 @@ def test_host_with_window_and_softcap():
     torch.cuda.synchronize()
     ab.check_device_status()
     _compare(dev, got, True, "host window softcap")
+
+
+@pytest.mark.parametrize("det,window,chunks", [(False, None, 0), (True, None, 3),
+                                               (False, (64, 16), 2)])
+def test_host_varlen_matches_device(det, window, chunks):
+    """Packed sequences (empty ones, cross attention with cu_seqlens_q !=
+    cu_seqlens_k) through attn_bwd_host_varlen: equal to attn_bwd's results."""
+    lq, lk = [300, 0, 17, 640, 129, 5], [200, 150, 0, 513, 129, 5]
+    w = synth.Workload("hostvl", 0, 8, 2, 0, 0, 128, "bf16", window is None, 71, n_seqs=len(lq),
+                       len_lo=0, len_hi=700)
+    x = synth.make_inputs(w, lengths=lq, lengths_k=lk)
+    q, k, v, do = (t.cuda() for t in (x.q, x.k, x.v, x.do))
+    kw = dict(cu_seqlens_q=x.cu_seqlens_q.cuda(), cu_seqlens_k=x.cu_seqlens_k.cuda(),
+              max_seqlen_q=max(lq), max_seqlen_k=max(lk), causal=w.causal, window=window)
+    o, lse = ab.attn_fwd(q, k, v, **kw)
+    dev = ab.attn_bwd(q, k, v, o, lse, do, deterministic=det, **kw)
+    host_in = [_pinned(t.cpu()) for t in (q, k, v, o, lse, do)]
+    got = ab.attn_bwd_host_varlen(*host_in, x.cu_seqlens_q, x.cu_seqlens_k, causal=w.causal,
+                                  deterministic=det, chunks=chunks, window=window)
+    torch.cuda.synchronize()
+    ab.check_device_status()
+    _compare(dev, got, det, "host varlen")

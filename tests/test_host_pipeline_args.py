@@ -88,3 +88,19 @@ def test_bad_options_rejected(lib):
                            ctypes.byref(k), 1, 2, 256, 256, 8, 2, 128, 0.1, 1, 0,
                            ctypes.byref(opts), 0, 1 << 24, size, None)
     assert rc == -9 and b"window" in lib.attn_last_error()
+
+
+def test_varlen_buffer_size_and_bad_cu(lib):
+    import numpy as np
+    cu = np.array([0, 300, 300, 1000, 1500], dtype=np.int32)
+    size = lib.attn_bwd_host_varlen_buffer_size(cu.ctypes.data, cu.ctypes.data, 4, 1500, 1500, 8,
+                                                2, 128, 0)
+    tensors = 4 * 1500 * 8 * 128 * 2 + 4 * 1500 * 2 * 128 * 2 + 8 * 1500 * 4
+    assert size > tensors and size % 256 == 0
+    for bad, msg in (([0, 300, 200, 1000, 1500], b"nondecreasing"),
+                     ([1, 300, 300, 1000, 1500], b"start at 0"),
+                     ([0, 300, 300, 1000, 1499], b"end at")):
+        arr = np.array(bad, dtype=np.int32)
+        assert lib.attn_bwd_host_varlen_buffer_size(arr.ctypes.data, cu.ctypes.data, 4, 1500, 1500,
+                                                    8, 2, 128, 0) == 0
+        assert msg in lib.attn_last_error()
