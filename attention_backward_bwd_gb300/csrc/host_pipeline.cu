@@ -191,6 +191,46 @@ cudaError_t copy_heads(const attn_tensor& host, char* dev, int b0, int nb, int h
   return cudaSuccess;
 }
 
+// The stream and event choreography shared by both entry points: every
+// internal stream waits for the caller's stream; `prologue` runs first on the
+// copy-in stream; chunk c's copies in run on the copy-in stream, its kernels on
+// compute stream c % kSlots (workspace slot c % kSlots) after them, and its
+// copies out on the copy-out stream after the kernels; the caller's stream
+// then waits for the copy-out stream.  Each callback returns ATTN_OK or an
+// error code (with the message already set).
+template <typename Prologue, typename CopyIn, typename Compute, typename CopyOut>
+int run_chunks(cudaStream_t user, int n, Prologue prologue, CopyIn copy_in, Compute compute,
+               CopyOut copy_out) {
+  std::lock_guard<std::mutex> lock(g_pool_mu);
+  Pool* P = nullptr;
+  int rc = get_pool(&P);
+  if (rc) return rc;
+  cudaError_t e;
+  if ((e = cudaEventRecord(P->start, user)) != cudaSuccess) return cuda_fail(e, "record start");
+  cudaStream_t all[2 + kSlots];
+  all[0] = P->in;
+  all[1] = P->out;
+  for (int i = 0; i < kSlots; ++i) all[2 + i] = P->comp[i];
+  for (cudaStream_t s : all)
+    if ((e = cudaStreamWaitEvent(s, P->start, 0)) != cudaSuccess) return cuda_fail(e, "wait start");
+  if ((rc = prologue(P->in))) return rc;
+  for (int c = 0; c < n; ++c) {
+    if ((rc = copy_in(c, P->in))) return rc;
+    if ((e = cudaEventRecord(P->in_done[c], P->in)) != cudaSuccess) return cuda_fail(e, "record");
+    cudaStream_t cs = P->comp[c % kSlots];
+    if ((e = cudaStreamWaitEvent(cs, P->in_done[c], 0)) != cudaSuccess)
+      return cuda_fail(e, "wait copy-in");
+    if ((rc = compute(c, c % kSlots, cs))) return rc;
+    if ((e = cudaEventRecord(P->comp_done[c], cs)) != cudaSuccess) return cuda_fail(e, "record");
+    if ((e = cudaStreamWaitEvent(P->out, P->comp_done[c], 0)) != cudaSuccess)
+      return cuda_fail(e, "wait compute");
+    if ((rc = copy_out(c, P->out))) return rc;
+  }
+  if ((e = cudaEventRecord(P->done, P->out)) != cudaSuccess) return cuda_fail(e, "record done");
+  if ((e = cudaStreamWaitEvent(user, P->done, 0)) != cudaSuccess) return cuda_fail(e, "wait done");
+  return ATTN_OK;
+}
+
 }  // namespace
 
 }  // namespace attn
@@ -238,48 +278,40 @@ extern "C" int attn_bwd_host(const attn_tensor* q, const attn_tensor* k, const a
     return fail(ATTN_ERR_WORKSPACE, "device_buffer too small: %zu bytes given, %zu needed",
                 device_buffer_bytes, L.total);
 
-  std::lock_guard<std::mutex> lock(g_pool_mu);
-  Pool* P = nullptr;
-  if ((rc = get_pool(&P))) return rc;
-  cudaStream_t user = reinterpret_cast<cudaStream_t>(stream);
   char* buf = static_cast<char*>(device_buffer);
   const int g = h_q / h_k;
-  cudaError_t e;
-  if ((e = cudaEventRecord(P->start, user)) != cudaSuccess) return cuda_fail(e, "record start");
-  cudaStream_t all[2 + kSlots];
-  all[0] = P->in;
-  all[1] = P->out;
-  for (int i = 0; i < kSlots; ++i) all[2 + i] = P->comp[i];
-  for (cudaStream_t s : all)
-    if ((e = cudaStreamWaitEvent(s, P->start, 0)) != cudaSuccess) return cuda_fail(e, "wait start");
-
-  for (int c = 0; c < ch.n; ++c) {
-    const int b0 = (ch.kv_heads == h_k) ? c * ch.seqs : c / (h_k / ch.kv_heads);
-    const int nb = (ch.kv_heads == h_k) ? (b0 + ch.seqs <= batch ? ch.seqs : batch - b0) : 1;
-    const int j0 = (ch.kv_heads == h_k) ? 0 : (c % (h_k / ch.kv_heads)) * ch.kv_heads;
-    const int nj = ch.kv_heads, i0 = j0 * g, ni = nj * g;
-
-    // copy in: Q, O, dO, K, V slices and the chunk's LSE rows (contiguous in [B, H_q, Sq])
-    if (hq && hk) {
-      if ((e = copy_heads(*q, buf + L.q, b0, nb, i0, ni, seqlen_q, h_q, head_dim, true, P->in)) ||
-          (e = copy_heads(*o, buf + L.o, b0, nb, i0, ni, seqlen_q, h_q, head_dim, true, P->in)) ||
-          (e = copy_heads(*dout, buf + L.dout, b0, nb, i0, ni, seqlen_q, h_q, head_dim, true,
-                          P->in)) ||
-          (e = copy_heads(*k, buf + L.k, b0, nb, j0, nj, seqlen_k, h_k, head_dim, true, P->in)) ||
-          (e = copy_heads(*v, buf + L.v, b0, nb, j0, nj, seqlen_k, h_k, head_dim, true, P->in)))
-        return cuda_fail(e, "copy inputs to the device");
-      const size_t lse_off = (static_cast<size_t>(b0) * h_q + i0) * seqlen_q;
-      const size_t lse_n = static_cast<size_t>(nb) * ni * seqlen_q;
-      if ((e = cudaMemcpyAsync(buf + L.lse + lse_off * 4, lse + lse_off, lse_n * 4,
-                               cudaMemcpyDefault, P->in)) != cudaSuccess)
-        return cuda_fail(e, "copy lse to the device");
-    }
-    if ((e = cudaEventRecord(P->in_done[c], P->in)) != cudaSuccess) return cuda_fail(e, "record");
-
-    // compute: the chunk is a backward problem of nb sequences and ni / nj heads
-    cudaStream_t cs = P->comp[c % kSlots];
-    if ((e = cudaStreamWaitEvent(cs, P->in_done[c], 0)) != cudaSuccess)
-      return cuda_fail(e, "wait copy-in");
+  // chunk c: sequences [b0, b0 + nb), kv heads [j0, j0 + nj), query heads [i0, i0 + ni)
+  auto geom = [&](int c, int& b0, int& nb, int& j0, int& nj, int& i0, int& ni) {
+    b0 = (ch.kv_heads == h_k) ? c * ch.seqs : c / (h_k / ch.kv_heads);
+    nb = (ch.kv_heads == h_k) ? (b0 + ch.seqs <= batch ? ch.seqs : batch - b0) : 1;
+    j0 = (ch.kv_heads == h_k) ? 0 : (c % (h_k / ch.kv_heads)) * ch.kv_heads;
+    nj = ch.kv_heads;
+    i0 = j0 * g;
+    ni = nj * g;
+  };
+  auto copy_in = [&](int c, cudaStream_t st) -> int {
+    if (!(hq && hk)) return ATTN_OK;
+    int b0, nb, j0, nj, i0, ni;
+    geom(c, b0, nb, j0, nj, i0, ni);
+    cudaError_t e;
+    // Q, O, dO, K, V slices and the chunk's LSE rows (contiguous in [B, H_q, Sq])
+    if ((e = copy_heads(*q, buf + L.q, b0, nb, i0, ni, seqlen_q, h_q, head_dim, true, st)) ||
+        (e = copy_heads(*o, buf + L.o, b0, nb, i0, ni, seqlen_q, h_q, head_dim, true, st)) ||
+        (e = copy_heads(*dout, buf + L.dout, b0, nb, i0, ni, seqlen_q, h_q, head_dim, true, st)) ||
+        (e = copy_heads(*k, buf + L.k, b0, nb, j0, nj, seqlen_k, h_k, head_dim, true, st)) ||
+        (e = copy_heads(*v, buf + L.v, b0, nb, j0, nj, seqlen_k, h_k, head_dim, true, st)))
+      return cuda_fail(e, "copy inputs to the device");
+    const size_t lse_off = (static_cast<size_t>(b0) * h_q + i0) * seqlen_q;
+    const size_t lse_n = static_cast<size_t>(nb) * ni * seqlen_q;
+    if ((e = cudaMemcpyAsync(buf + L.lse + lse_off * 4, lse + lse_off, lse_n * 4,
+                             cudaMemcpyDefault, st)) != cudaSuccess)
+      return cuda_fail(e, "copy lse to the device");
+    return ATTN_OK;
+  };
+  auto compute = [&](int c, int slot, cudaStream_t cs) -> int {
+    // the chunk is a backward problem of nb sequences and ni / nj heads
+    int b0, nb, j0, nj, i0, ni;
+    geom(c, b0, nb, j0, nj, i0, ni);
     const size_t qoff = (static_cast<size_t>(b0) * seqlen_q * h_q + i0) * head_dim * 2;
     const size_t koff = (static_cast<size_t>(b0) * seqlen_k * h_k + j0) * head_dim * 2;
     const attn_tensor tq = compact_view(buf + L.q + qoff, seqlen_q, h_q, head_dim);
@@ -292,30 +324,28 @@ extern "C" int attn_bwd_host(const attn_tensor* q, const attn_tensor* k, const a
     const attn_tensor tdv = compact_view(buf + L.dv + koff, seqlen_k, h_k, head_dim);
     const float* tlse = reinterpret_cast<const float*>(buf + L.lse) +
                         (static_cast<size_t>(b0) * h_q + i0) * seqlen_q;
-    Prepared pr;
     attn_opts co = checked;  // used lengths of this chunk's sequences
     if (co.seqused_q != nullptr) co.seqused_q += b0;
     if (co.seqused_k != nullptr) co.seqused_k += b0;
-    rc = prepare_bwd(&tq, &tk, &tv, &to, tlse, &tdo, &tdq, &tdk, &tdv, dtype, nb, seqlen_q,
-                     seqlen_k, ni, nj, head_dim, scale, causal, nullptr, nullptr, seqlen_q,
-                     seqlen_k, deterministic, &co, buf + L.ws[c % kSlots], L.ws_bytes, &pr);
-    if (rc) return rc;
-    if ((rc = run_stages(kPre | kMain | kPost, pr, cs))) return rc;
-    if ((e = cudaEventRecord(P->comp_done[c], cs)) != cudaSuccess) return cuda_fail(e, "record");
-
-    // copy out: dQ, dK, dV slices
-    if ((e = cudaStreamWaitEvent(P->out, P->comp_done[c], 0)) != cudaSuccess)
-      return cuda_fail(e, "wait compute");
-    if ((e = copy_heads(*dq, buf + L.dq, b0, nb, i0, ni, seqlen_q, h_q, head_dim, false,
-                        P->out)) ||
-        (e = copy_heads(*dk, buf + L.dk, b0, nb, j0, nj, seqlen_k, h_k, head_dim, false,
-                        P->out)) ||
-        (e = copy_heads(*dv, buf + L.dv, b0, nb, j0, nj, seqlen_k, h_k, head_dim, false, P->out)))
+    Prepared pr;
+    int r = prepare_bwd(&tq, &tk, &tv, &to, tlse, &tdo, &tdq, &tdk, &tdv, dtype, nb, seqlen_q,
+                        seqlen_k, ni, nj, head_dim, scale, causal, nullptr, nullptr, seqlen_q,
+                        seqlen_k, deterministic, &co, buf + L.ws[slot], L.ws_bytes, &pr);
+    return r ? r : run_stages(kPre | kMain | kPost, pr, cs);
+  };
+  auto copy_out = [&](int c, cudaStream_t st) -> int {
+    int b0, nb, j0, nj, i0, ni;
+    geom(c, b0, nb, j0, nj, i0, ni);
+    cudaError_t e;
+    if ((e = copy_heads(*dq, buf + L.dq, b0, nb, i0, ni, seqlen_q, h_q, head_dim, false, st)) ||
+        (e = copy_heads(*dk, buf + L.dk, b0, nb, j0, nj, seqlen_k, h_k, head_dim, false, st)) ||
+        (e = copy_heads(*dv, buf + L.dv, b0, nb, j0, nj, seqlen_k, h_k, head_dim, false, st)))
       return cuda_fail(e, "copy results to the host");
-  }
-  if ((e = cudaEventRecord(P->done, P->out)) != cudaSuccess) return cuda_fail(e, "record done");
-  if ((e = cudaStreamWaitEvent(user, P->done, 0)) != cudaSuccess) return cuda_fail(e, "wait done");
-  return ATTN_OK;
+    return ATTN_OK;
+  };
+  return run_chunks(reinterpret_cast<cudaStream_t>(stream), ch.n,
+                    [](cudaStream_t) { return static_cast<int>(ATTN_OK); }, copy_in, compute,
+                    copy_out);
 }
 
 // ---------------------------------------------------------------------------
@@ -502,46 +532,37 @@ extern "C" int attn_bwd_host_varlen(const attn_tensor* q, const attn_tensor* k,
     }
   }
 
-  std::lock_guard<std::mutex> lock(g_pool_mu);
-  Pool* P = nullptr;
-  if ((rc = get_pool(&P))) return rc;
-  cudaStream_t user = reinterpret_cast<cudaStream_t>(stream);
   char* buf = static_cast<char*>(device_buffer);
-  cudaError_t e;
-  if ((e = cudaEventRecord(P->start, user)) != cudaSuccess) return cuda_fail(e, "record start");
-  cudaStream_t all[2 + kSlots];
-  all[0] = P->in;
-  all[1] = P->out;
-  for (int i = 0; i < kSlots; ++i) all[2 + i] = P->comp[i];
-  for (cudaStream_t s : all)
-    if ((e = cudaStreamWaitEvent(s, P->start, 0)) != cudaSuccess) return cuda_fail(e, "wait start");
-  // pageable source: the call returns once the data sit in the driver's staging memory
-  if ((e = cudaMemcpyAsync(buf + L.cu, cu_all.data(), cu_all.size() * sizeof(int),
-                           cudaMemcpyHostToDevice, P->in)) != cudaSuccess)
-    return cuda_fail(e, "copy cu_seqlens to the device");
-
-  for (int c = 0; c < n; ++c) {
+  auto prologue = [&](cudaStream_t st) -> int {
+    // pageable source: the call returns once the data sit in the driver's staging memory
+    const cudaError_t e = cudaMemcpyAsync(buf + L.cu, cu_all.data(), cu_all.size() * sizeof(int),
+                                          cudaMemcpyHostToDevice, st);
+    return e == cudaSuccess ? static_cast<int>(ATTN_OK)
+                            : cuda_fail(e, "copy cu_seqlens to the device");
+  };
+  auto lse_dev = [&](const VarlenChunk& C) {
+    return reinterpret_cast<float*>(buf + L.lse) + static_cast<size_t>(h_q) * C.q0;
+  };
+  auto copy_in = [&](int c, cudaStream_t st) -> int {
     const VarlenChunk& C = ch[c];
-    float* lse_dev = reinterpret_cast<float*>(buf + L.lse) + static_cast<size_t>(h_q) * C.q0;
-    if (hq && hk) {
-      if ((e = copy_rows(*q, buf + L.q, C.q0, C.nq, h_q, head_dim, true, P->in)) ||
-          (e = copy_rows(*o, buf + L.o, C.q0, C.nq, h_q, head_dim, true, P->in)) ||
-          (e = copy_rows(*dout, buf + L.dout, C.q0, C.nq, h_q, head_dim, true, P->in)) ||
-          (e = copy_rows(*k, buf + L.k, C.k0, C.nk, h_k, head_dim, true, P->in)) ||
-          (e = copy_rows(*v, buf + L.v, C.k0, C.nk, h_k, head_dim, true, P->in)))
-        return cuda_fail(e, "copy inputs to the device");
-      // LSE [H_q, total_q]: the chunk's columns of every head, into a compact [H_q, nq]
-      if (C.nq > 0 &&
-          (e = cudaMemcpy2DAsync(lse_dev, static_cast<size_t>(C.nq) * 4, lse + C.q0,
-                                 static_cast<size_t>(total_q) * 4, static_cast<size_t>(C.nq) * 4,
-                                 h_q, cudaMemcpyDefault, P->in)) != cudaSuccess)
-        return cuda_fail(e, "copy lse to the device");
-    }
-    if ((e = cudaEventRecord(P->in_done[c], P->in)) != cudaSuccess) return cuda_fail(e, "record");
-
-    cudaStream_t cs = P->comp[c % kSlots];
-    if ((e = cudaStreamWaitEvent(cs, P->in_done[c], 0)) != cudaSuccess)
-      return cuda_fail(e, "wait copy-in");
+    if (!(hq && hk)) return ATTN_OK;
+    cudaError_t e;
+    if ((e = copy_rows(*q, buf + L.q, C.q0, C.nq, h_q, head_dim, true, st)) ||
+        (e = copy_rows(*o, buf + L.o, C.q0, C.nq, h_q, head_dim, true, st)) ||
+        (e = copy_rows(*dout, buf + L.dout, C.q0, C.nq, h_q, head_dim, true, st)) ||
+        (e = copy_rows(*k, buf + L.k, C.k0, C.nk, h_k, head_dim, true, st)) ||
+        (e = copy_rows(*v, buf + L.v, C.k0, C.nk, h_k, head_dim, true, st)))
+      return cuda_fail(e, "copy inputs to the device");
+    // LSE [H_q, total_q]: the chunk's columns of every head, into a compact [H_q, nq]
+    if (C.nq > 0 &&
+        (e = cudaMemcpy2DAsync(lse_dev(C), static_cast<size_t>(C.nq) * 4, lse + C.q0,
+                               static_cast<size_t>(total_q) * 4, static_cast<size_t>(C.nq) * 4,
+                               h_q, cudaMemcpyDefault, st)) != cudaSuccess)
+      return cuda_fail(e, "copy lse to the device");
+    return ATTN_OK;
+  };
+  auto compute = [&](int c, int slot, cudaStream_t cs) -> int {
+    const VarlenChunk& C = ch[c];
     const size_t qoff = static_cast<size_t>(C.q0) * h_q * head_dim * 2;
     const size_t koff = static_cast<size_t>(C.k0) * h_k * head_dim * 2;
     const int64_t sq = static_cast<int64_t>(h_q) * head_dim;
@@ -558,21 +579,20 @@ extern "C" int attn_bwd_host_varlen(const attn_tensor* q, const attn_tensor* k,
     if (co.seqused_q != nullptr) co.seqused_q += C.b0;
     if (co.seqused_k != nullptr) co.seqused_k += C.b0;
     Prepared pr;
-    rc = prepare_bwd(&tq, &tk, &tv, &to, lse_dev, &tdo, &tdq, &tdk, &tdv, dtype, C.nb, C.nq,
-                     C.nk, h_q, h_k, head_dim, scale, causal, cuq, cuk, C.max_q, C.max_k,
-                     deterministic, &co, buf + L.ws[c % kSlots], L.ws_bytes, &pr);
-    if (rc) return rc;
-    if ((rc = run_stages(kPre | kMain | kPost, pr, cs))) return rc;
-    if ((e = cudaEventRecord(P->comp_done[c], cs)) != cudaSuccess) return cuda_fail(e, "record");
-
-    if ((e = cudaStreamWaitEvent(P->out, P->comp_done[c], 0)) != cudaSuccess)
-      return cuda_fail(e, "wait compute");
-    if ((e = copy_rows(*dq, buf + L.dq, C.q0, C.nq, h_q, head_dim, false, P->out)) ||
-        (e = copy_rows(*dk, buf + L.dk, C.k0, C.nk, h_k, head_dim, false, P->out)) ||
-        (e = copy_rows(*dv, buf + L.dv, C.k0, C.nk, h_k, head_dim, false, P->out)))
+    int r = prepare_bwd(&tq, &tk, &tv, &to, lse_dev(C), &tdo, &tdq, &tdk, &tdv, dtype, C.nb, C.nq,
+                        C.nk, h_q, h_k, head_dim, scale, causal, cuq, cuk, C.max_q, C.max_k,
+                        deterministic, &co, buf + L.ws[slot], L.ws_bytes, &pr);
+    return r ? r : run_stages(kPre | kMain | kPost, pr, cs);
+  };
+  auto copy_out = [&](int c, cudaStream_t st) -> int {
+    const VarlenChunk& C = ch[c];
+    cudaError_t e;
+    if ((e = copy_rows(*dq, buf + L.dq, C.q0, C.nq, h_q, head_dim, false, st)) ||
+        (e = copy_rows(*dk, buf + L.dk, C.k0, C.nk, h_k, head_dim, false, st)) ||
+        (e = copy_rows(*dv, buf + L.dv, C.k0, C.nk, h_k, head_dim, false, st)))
       return cuda_fail(e, "copy results to the host");
-  }
-  if ((e = cudaEventRecord(P->done, P->out)) != cudaSuccess) return cuda_fail(e, "record done");
-  if ((e = cudaStreamWaitEvent(user, P->done, 0)) != cudaSuccess) return cuda_fail(e, "wait done");
-  return ATTN_OK;
+    return ATTN_OK;
+  };
+  return run_chunks(reinterpret_cast<cudaStream_t>(stream), n, prologue, copy_in, compute,
+                    copy_out);
 }
