@@ -178,6 +178,66 @@ def _dims(q: torch.Tensor, k: torch.Tensor, cu_q, cu_k, max_q, max_k):
     return q.shape[0], q.shape[1], k.shape[1], q.shape[2], k.shape[2], q.shape[3], q.shape[1], k.shape[1]
 
 
+def _placed(t, q, on_device: bool) -> bool:
+    """On q's CUDA device (device entry points), or in host memory."""
+    if on_device:
+        return t.is_cuda and t.device == q.device
+    return t.device.type == "cpu"
+
+
+def _check_tensors(q, k, like_q, like_k, lse, ints, on_device: bool, varlen: bool):
+    """Checks the library cannot make from raw pointers, made before any call:
+    where each tensor lives (device memory for the device entry points, host
+    memory for the host-buffer ones), that the attention tensors share q's
+    dtype and have a unit stride over the head dimension, that o, dO, dQ have
+    q's shape and v, dK, dV k's, that LSE is a contiguous fp32 tensor of the
+    documented shape, and that the int32 arrays (cu_seqlens, seqused) are
+    contiguous with an entry per sequence.  A tensor smaller than its
+    arguments imply would otherwise be read or written past its end.
+
+    ``like_q`` / ``like_k``: dicts name -> tensor or None; ``ints``: dict
+    name -> (tensor or None, minimum entries)."""
+    where = "CUDA tensors" if on_device else "host (CPU) tensors"
+    nd = 3 if varlen else 4
+    if q.dim() != nd or k.dim() != nd:
+        raise AttnError(-2, f"q and k must be {'packed [total, H, D]' if varlen else '[B, S, H, D]'}"
+                            f" tensors, got {tuple(q.shape)} and {tuple(k.shape)}")
+    if q.shape[-1] != k.shape[-1] or (not varlen and q.shape[0] != k.shape[0]):
+        raise AttnError(-2, f"q {tuple(q.shape)} and k {tuple(k.shape)} disagree on batch or D")
+    named = {"q": q, "k": k, **like_q, **like_k}
+    for name, t in named.items():
+        if t is None:
+            continue
+        if not _placed(t, q, on_device):
+            raise AttnError(-9, f"{name} must be {where}"
+                                f"{' on ' + str(q.device) if on_device else ''}, got {t.device}")
+        if t.dtype != q.dtype:
+            raise AttnError(-1, f"{name} has dtype {t.dtype}, q has {q.dtype}")
+        if t.numel() > 0 and t.stride(-1) != 1:
+            raise AttnError(-3, f"{name} must have unit stride over the head dimension")
+    for name, t in like_q.items():
+        if t is not None and t.shape != q.shape:
+            raise AttnError(-2, f"{name} has shape {tuple(t.shape)}, q has {tuple(q.shape)}")
+    for name, t in like_k.items():
+        if t is not None and t.shape != k.shape:
+            raise AttnError(-2, f"{name} has shape {tuple(t.shape)}, k has {tuple(k.shape)}")
+    if lse is not None:
+        want = (q.shape[1], q.shape[0]) if varlen else (q.shape[0], q.shape[2], q.shape[1])
+        if not _placed(lse, q, on_device):
+            raise AttnError(-9, f"lse must be {where}, got {lse.device}")
+        if lse.dtype != torch.float32 or tuple(lse.shape) != want or not lse.is_contiguous():
+            raise AttnError(-2, f"lse must be a contiguous float32 tensor of shape {want}, got "
+                                f"{lse.dtype} {tuple(lse.shape)}")
+    for name, (t, n) in ints.items():
+        if t is None:
+            continue
+        if not t.is_cuda or t.device != q.device:
+            raise AttnError(-9, f"{name} must be a CUDA tensor on {q.device}, got {t.device}")
+        if t.dtype != torch.int32 or not t.is_contiguous() or t.dim() != 1 or t.numel() < n:
+            raise AttnError(-9, f"{name} must be a contiguous 1-D int32 tensor of at least {n} "
+                                f"entries, got {t.dtype} {tuple(t.shape)}")
+
+
 def version() -> str:
     return lib().attn_version().decode()
 
@@ -194,10 +254,14 @@ def attn_fwd(q, k, v, causal: bool = False, scale: Optional[float] = None, cu_se
     L = lib()
     b, sq, sk, hq, hk, d, mq, mk = _dims(q, k, cu_seqlens_q, cu_seqlens_k, max_seqlen_q,
                                          max_seqlen_k)
+    varlen = cu_seqlens_q is not None
+    _check_tensors(q, k, {"out": out}, {"v": v}, lse,
+                   {"cu_seqlens_q": (cu_seqlens_q, b + 1), "cu_seqlens_k": (cu_seqlens_k, b + 1),
+                    "seqused_q": (seqused_q, b), "seqused_k": (seqused_k, b)}, True, varlen)
     scale = d ** -0.5 if scale is None else float(scale)
     o = torch.empty_like(q) if out is None else out
     if lse is None:
-        shape = (hq, sq) if cu_seqlens_q is not None else (b, hq, sq)
+        shape = (hq, sq) if varlen else (b, hq, sq)
         lse = torch.empty(shape, dtype=torch.float32, device=q.device)
     dq_, dk_, dv_, do_ = _desc(q), _desc(k), _desc(v), _desc(o)
     args = [ctypes.byref(dq_), ctypes.byref(dk_), ctypes.byref(dv_), ctypes.byref(do_), _ptr(lse),
@@ -259,6 +323,12 @@ def attn_bwd(q, k, v, o, lse, do, causal: bool = False, scale: Optional[float] =
     L = lib()
     b, sq, sk, hq, hk, d, mq, mk = _dims(q, k, cu_seqlens_q, cu_seqlens_k, max_seqlen_q,
                                          max_seqlen_k)
+    _check_tensors(q, k, {"o": o, "do": do, "dq": dq}, {"v": v, "dk": dk, "dv": dv}, lse,
+                   {"cu_seqlens_q": (cu_seqlens_q, b + 1), "cu_seqlens_k": (cu_seqlens_k, b + 1),
+                    "seqused_q": (seqused_q, b), "seqused_k": (seqused_k, b)}, True,
+                   cu_seqlens_q is not None)
+    if workspace is not None and not (workspace.is_cuda and workspace.device == q.device):
+        raise AttnError(-9, f"workspace must be a CUDA tensor on {q.device}")
     scale = d ** -0.5 if scale is None else float(scale)
     dq = torch.empty_like(q) if dq is None else dq
     dk = torch.empty_like(k) if dk is None else dk
@@ -301,6 +371,10 @@ def attn_bwd_host(q, k, v, o, lse, do, dq=None, dk=None, dv=None, causal: bool =
     allocated on ``device`` if not given.  Returns (dq, dk, dv).
     """
     L = lib()
+    _check_tensors(q, k, {"o": o, "do": do, "dq": dq}, {"v": v, "dk": dk, "dv": dv}, lse, {},
+                   False, False)
+    if device_buffer is not None and not device_buffer.is_cuda:
+        raise AttnError(-9, "device_buffer must be a CUDA tensor")
     b, sq, sk, hq, hk, d = q.shape[0], q.shape[1], k.shape[1], q.shape[2], k.shape[2], q.shape[3]
     scale = d ** -0.5 if scale is None else float(scale)
     pin = torch.cuda.is_available()
@@ -333,6 +407,10 @@ def attn_bwd_host_varlen(q, k, v, o, lse, do, cu_seqlens_q, cu_seqlens_k, dq=Non
     [H_q, total_q]) with host int32 cu_seqlens; results in host tensors (pinned,
     allocated here if not given), valid once ``stream`` has passed the call."""
     L = lib()
+    _check_tensors(q, k, {"o": o, "do": do, "dq": dq}, {"v": v, "dk": dk, "dv": dv}, lse, {},
+                   False, True)
+    if device_buffer is not None and not device_buffer.is_cuda:
+        raise AttnError(-9, "device_buffer must be a CUDA tensor")
     b = int(cu_seqlens_q.numel()) - 1
     tq, tk, hq, hk, d = q.shape[0], k.shape[0], q.shape[1], k.shape[1], q.shape[2]
     scale = d ** -0.5 if scale is None else float(scale)

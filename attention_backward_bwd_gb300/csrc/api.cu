@@ -481,8 +481,13 @@ int attn_check_device_status(attn_stream_t stream) {
     const unsigned int zero[2] = {0u, 0u};
     e = cudaMemcpyToSymbol(g_device_status, zero, sizeof(zero));
     if (e != cudaSuccess) return cuda_fail(e, "clear device status");
-    if (v[1] != 0)
-      return fail(ATTN_ERR_ARG, "cu_seqlens failed device-side validation (code 0x%08x)", v[1]);
+    if (v[1] != 0) {
+      // codes 0xB0000001..4: cu_seqlens; 0xB0000005 / 6: seqused_q / seqused_k
+      const char* what = v[1] == 0xB0000005u   ? "seqused_q"
+                         : v[1] == 0xB0000006u ? "seqused_k"
+                                               : "cu_seqlens";
+      return fail(ATTN_ERR_ARG, "%s failed device-side validation (code 0x%08x)", what, v[1]);
+    }
     return fail(ATTN_ERR_DEVICE_TIMEOUT, "a bounded device wait gave up (site 0x%08x)", v[0]);
   }
   return ATTN_OK;

@@ -62,7 +62,7 @@ enum attn_dtype { ATTN_FP16 = 0, ATTN_BF16 = 1 };
 enum attn_status {
   ATTN_OK = 0,
   ATTN_ERR_DTYPE = -1,          /* dtype not fp16/bf16 */
-  ATTN_ERR_SHAPE = -2,          /* bad sizes: B<=0, H_q%H_k, D not 64/128, ... */
+  ATTN_ERR_SHAPE = -2,          /* bad sizes: B<=0, H_q%H_k, D not 8..128 by 8 */
   ATTN_ERR_STRIDE = -3,         /* stride not a multiple of 8 elements or negative */
   ATTN_ERR_ALIGN = -4,          /* base pointer not 16-byte aligned */
   ATTN_ERR_NULL = -5,           /* required pointer is NULL */
@@ -327,8 +327,9 @@ int attn_bwd_postprocess(const attn_tensor* q, const attn_tensor* k, const attn_
 /*
  * attn_check_device_status -- synchronises `stream`, then reads and clears the
  * device status word.  Returns ATTN_OK, ATTN_ERR_DEVICE_TIMEOUT (a bounded
- * wait inside a kernel gave up; attn_last_error names the wait site) or
- * ATTN_ERR_CUDA (the stream reported an error).
+ * wait inside a kernel gave up; attn_last_error names the wait site),
+ * ATTN_ERR_ARG (cu_seqlens or seqused_q/k failed the device-side check;
+ * attn_last_error names which) or ATTN_ERR_CUDA (the stream reported an error).
  */
 int attn_check_device_status(attn_stream_t stream);
 

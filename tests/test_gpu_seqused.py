@@ -108,5 +108,5 @@ def test_seqused_beyond_rows_is_reported():
     ab.attn_bwd(q, q, q, o, lse, q, seqused_q=bad)
     with pytest.raises(ab.AttnError) as e:
         ab.check_device_status()
-    assert e.value.code == -9
+    assert e.value.code == -9 and "seqused_q" in str(e.value)
     ab.check_device_status()  # the status was cleared by the report
