@@ -227,6 +227,10 @@ int prepare_bwd(const attn_tensor* q, const attn_tensor* k, const attn_tensor* v
   if (hq && hk && reinterpret_cast<uintptr_t>(lse) % 4 != 0)
     return fail(ATTN_ERR_ALIGN, "lse must be 4-byte aligned");
   const WsLayout w = ws_layout(batch, seqlen_q, h_q, head_dim, varlen ? 1 : 0);
+  // the dQ accumulator's rows of all heads are one TMA dimension (32-bit coordinates)
+  if (w.rows * h_q > INT32_MAX)
+    return fail(ATTN_ERR_SHAPE, "too many query rows: %lld accumulator rows x %d heads >= 2^31",
+                static_cast<long long>(w.rows), h_q);
   if (hq && hk) {
     if (workspace == nullptr) return fail(ATTN_ERR_WORKSPACE, "workspace is NULL");
     if (reinterpret_cast<uintptr_t>(workspace) % 256 != 0)

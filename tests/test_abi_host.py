@@ -143,6 +143,13 @@ def test_argument_errors(lib, case, code):
     assert lib.attn_last_error()  # a message is set
 
 
+def test_too_many_query_rows_is_a_shape_error(lib):
+    # 2^26 query rows x 32 heads: the dQ accumulator's row coordinate would pass 2^31
+    q, k, v, o, do = shapes(sq=1 << 26, sk=64, hq=32, hk=8)
+    assert call_bwd(lib, q, k, v, o, do) == -2
+    assert b"too many query rows" in lib.attn_last_error()
+
+
 def test_error_message_names_the_problem(lib):
     q, k, v, o, do = shapes(hq=3, hk=2)
     assert call_bwd(lib, q, k, v, o, do) == -2
