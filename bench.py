@@ -81,7 +81,7 @@ def kernel_traffic():
     """DRAM bytes per launch of the main kernel from the committed ncu summary,
     valid only while the kernel source still hashes to the profiled version."""
     src = os.path.join(ROOT, "attention_backward_bwd_gb300", "csrc", "bwd_main.cu")
-    prof = os.path.join(ROOT, "profiles", "bwd_main_traffic.txt")
+    prof = os.path.join(ROOT, "profiles", "bwd_main_traffic_gqa_b2_hq32_hk8_s8192_d128_causal.txt")
     try:
         h = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
         kv = dict(line.strip().split("=", 1) for line in open(prof) if "=" in line)
