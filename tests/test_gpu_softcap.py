@@ -69,3 +69,27 @@ def test_softcap_varlen():
     floor = float(np.abs(ref["dV"]).max())
     for name, got in (("dQ", dq), ("dK", dk), ("dV", dv)):
         assert_close(f"softcap varlen {name}", got, ref[name], floor=floor)
+
+
+INSTANCES = [(dt, d, cap, left) for dt in ("bf16", "fp16") for d in (64, 128)
+             for cap in (0.0, 2.0) for left in (-1, 150)]
+
+
+@pytest.mark.parametrize("dt,d,cap,left", INSTANCES,
+                         ids=[f"{c[0]}_d{c[1]}_cap{c[2]:g}_left{c[3]}" for c in INSTANCES])
+def test_every_main_kernel_instance(dt, d, cap, left):
+    """The main kernel is instantiated per dtype, head dim, logit cap on/off and
+    left window side present/absent: each of the sixteen against the oracle on
+    a causal problem whose window edge and diagonal cut through tiles."""
+    w = synth.small("inst", 1, 4, 2, 401, 401, d, dt, True, 500 + d + int(cap) + (left > 0))
+    x = synth.make_inputs(w)
+    q = (x.q.float() * 2).to(x.q.dtype) if cap else x.q
+    window = (left, -1) if left >= 0 else None
+    qd, k, v, do = (t.cuda() for t in (q, x.k, x.v, x.do))
+    o, lse = ab.attn_fwd(qd, k, v, causal=True, window=window, softcap=cap)
+    got = ab.attn_bwd(qd, k, v, o, lse, do, causal=True, window=window, softcap=cap)
+    ab.check_device_status()
+    ref = attn_oracle.mha_backward(q, x.k, x.v, x.do, w.scale, True, window=window, softcap=cap)
+    floor = float(np.abs(ref["dV"]).max())
+    for name, t in zip(("dQ", "dK", "dV"), got):
+        assert_close(f"instance {name}", t, ref[name], floor=floor)
