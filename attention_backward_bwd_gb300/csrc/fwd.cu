@@ -11,6 +11,8 @@
 //
 // Design: 4 warps per CTA, 64 query rows (16 per warp), 64-key tiles,
 // mma.sync m16n8k16 with fp32 accumulation, cp.async double-buffered K/V.
+#include <atomic>
+
 #include "common.cuh"
 
 namespace attn {
@@ -276,13 +278,18 @@ template <typename T, int D>
 cudaError_t launch_fwd_t(const FwdParams& p, cudaStream_t stream) {
   constexpr int LD = D + 8;
   const size_t smem = static_cast<size_t>(5) * kBM * LD * sizeof(T);
-  static bool attr_done = false;
-  if (!attr_done) {
+  // Kernel attributes are per device: set them once on each.
+  constexpr int kMaxDevices = 64;
+  static std::atomic<bool> attr_done[kMaxDevices];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
+    return cudaErrorInvalidDevice;
+  if (!attr_done[dev].load(std::memory_order_acquire)) {
     cudaError_t e = cudaFuncSetAttribute(fwd_kernel<T, D>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
     if (e != cudaSuccess) return e;
-    attr_done = true;
+    attr_done[dev].store(true, std::memory_order_release);
   }
   dim3 grid(ceil_div(p.max_seqlen_q, kBM), p.h_q, p.seq.batch);
   fwd_kernel<T, D><<<grid, kFwdThreads, smem, stream>>>(p);
