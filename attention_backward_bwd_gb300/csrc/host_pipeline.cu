@@ -51,6 +51,20 @@ struct Pool {
 Pool g_pool[kMaxDevices];
 std::mutex g_pool_mu;
 
+void destroy_pool(Pool& t) {
+  cudaStream_t streams[2 + kSlots] = {t.in, t.out};
+  for (int i = 0; i < kSlots; ++i) streams[2 + i] = t.comp[i];
+  for (cudaStream_t st : streams)
+    if (st != nullptr) cudaStreamDestroy(st);
+  cudaEvent_t single[2] = {t.start, t.done};
+  for (cudaEvent_t ev : single)
+    if (ev != nullptr) cudaEventDestroy(ev);
+  for (int i = 0; i < kMaxChunks; ++i) {
+    if (t.in_done[i] != nullptr) cudaEventDestroy(t.in_done[i]);
+    if (t.comp_done[i] != nullptr) cudaEventDestroy(t.comp_done[i]);
+  }
+}
+
 int get_pool(Pool** out) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -59,22 +73,27 @@ int get_pool(Pool** out) {
     return fail(ATTN_ERR_CUDA, "device index %d not supported", dev);
   Pool& P = g_pool[dev];
   if (!P.ready) {
+    // build into a zeroed pool; on a failure destroy what was made, so a later
+    // call starts again from nothing
+    Pool t = {};
     const unsigned sflags = cudaStreamNonBlocking;
     const unsigned eflags = cudaEventDisableTiming;
-    if ((e = cudaStreamCreateWithFlags(&P.in, sflags)) != cudaSuccess ||
-        (e = cudaStreamCreateWithFlags(&P.out, sflags)) != cudaSuccess)
-      return cuda_fail(e, "create copy streams");
-    for (int i = 0; i < kSlots; ++i)
-      if ((e = cudaStreamCreateWithFlags(&P.comp[i], sflags)) != cudaSuccess)
-        return cuda_fail(e, "create compute streams");
-    if ((e = cudaEventCreateWithFlags(&P.start, eflags)) != cudaSuccess ||
-        (e = cudaEventCreateWithFlags(&P.done, eflags)) != cudaSuccess)
-      return cuda_fail(e, "create events");
-    for (int i = 0; i < kMaxChunks; ++i)
-      if ((e = cudaEventCreateWithFlags(&P.in_done[i], eflags)) != cudaSuccess ||
-          (e = cudaEventCreateWithFlags(&P.comp_done[i], eflags)) != cudaSuccess)
-        return cuda_fail(e, "create events");
-    P.ready = true;
+    e = cudaStreamCreateWithFlags(&t.in, sflags);
+    if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&t.out, sflags);
+    for (int i = 0; i < kSlots && e == cudaSuccess; ++i)
+      e = cudaStreamCreateWithFlags(&t.comp[i], sflags);
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&t.start, eflags);
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&t.done, eflags);
+    for (int i = 0; i < kMaxChunks && e == cudaSuccess; ++i) {
+      e = cudaEventCreateWithFlags(&t.in_done[i], eflags);
+      if (e == cudaSuccess) e = cudaEventCreateWithFlags(&t.comp_done[i], eflags);
+    }
+    if (e != cudaSuccess) {
+      destroy_pool(t);
+      return cuda_fail(e, "create the internal streams and events");
+    }
+    t.ready = true;
+    P = t;
   }
   *out = &P;
   return ATTN_OK;
