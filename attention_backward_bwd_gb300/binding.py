@@ -92,6 +92,9 @@ def lib() -> ctypes.CDLL:
             f = getattr(L, name)
             f.argtypes = _BWD_ARGS
             f.restype = _I
+        # attn_bwd's arguments without the workspace and its size
+        L.attn_bwd_noalloc.argtypes = _BWD_ARGS[:23] + _BWD_ARGS[25:]
+        L.attn_bwd_noalloc.restype = _I
         L.attn_bwd_host.argtypes = [_T, _T, _T, _T, _P, _T, _T, _T, _T, _I, _I, _I, _I, _I, _I,
                                     _I, ctypes.c_float, _I, _I, ctypes.POINTER(AttnOpts), _I, _P,
                                     ctypes.c_size_t, _P]

@@ -189,3 +189,55 @@ def test_extended_options_argument_errors(lib):
     rc = lib.attn_fwd_ex(*(ctypes.byref(x) for x in ds), 1 << 21, 1, 1, 64, 64, 2, 2, 64, 0.125,
                          0, None, None, 64, 64, ctypes.byref(bad), None)
     assert rc == -9 and b"window" in lib.attn_last_error()
+
+
+def declared_signatures():
+    """name -> (return kind, [parameter kinds]) for every function in include/."""
+    sigs = {}
+    for h in ("attn_bwd.h", "attn_diag.h"):
+        text = open(os.path.join(ROOT, "include", h)).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        for ret, name, params in re.findall(
+                r"([A-Za-z_][\w \t]*?\**)\s*\b(attn_[a-z0-9_]+)\s*\(([^()]*)\)\s*;", text):
+            params = " ".join(params.split())
+            kinds = [] if params in ("", "void") else [_c_kind(p) for p in params.split(",")]
+            sigs[name] = (_c_kind(ret.strip() + " r"), kinds)
+    return sigs
+
+
+def _c_kind(decl):
+    """Kind of a C declaration 'type name' (name may carry an array suffix)."""
+    decl = decl.strip()
+    typ = re.sub(r"\s*\b\w+\s*(\[\s*\d*\s*\])?$", "", decl)
+    if "*" in typ or "[" in decl or typ.endswith("attn_stream_t"):
+        return "ptr"
+    for key, kind in (("size_t", "size"), ("int64_t", "i64"), ("float", "float"),
+                      ("int", "int"), ("void", "void")):
+        if re.search(rf"\b{key}\b", typ):
+            return kind
+    raise AssertionError(f"unclassified C type in {decl!r}")
+
+
+def _ctypes_kind(t):
+    if t is None:
+        return "void"
+    if t in (ctypes.c_void_p, ctypes.c_char_p) or issubclass(t, ctypes._Pointer):
+        return "ptr"
+    for c, kind in ((ctypes.c_size_t, "size"), (ctypes.c_int64, "i64"),
+                    (ctypes.c_float, "float"), (ctypes.c_int, "int")):
+        if t is c:
+            return kind
+    raise AssertionError(f"unclassified ctypes type {t}")
+
+
+def test_binding_signatures_match_the_headers(lib):
+    """Every argtypes / restype the binding sets agrees with the header's
+    declaration in count and kind (pointer, int, float, size_t, int64_t): a
+    drift here would pass wrong values through the ABI without any error."""
+    sigs = declared_signatures()
+    assert set(sigs) == set(declared_functions())
+    for name, (ret, params) in sigs.items():
+        f = getattr(lib, name)
+        got = [_ctypes_kind(t) for t in f.argtypes]
+        assert got == params, f"{name}: binding {got} vs header {params}"
+        assert _ctypes_kind(f.restype) == ret, f"{name}: restype vs header {ret}"
