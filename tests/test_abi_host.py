@@ -241,3 +241,36 @@ def test_binding_signatures_match_the_headers(lib):
         got = [_ctypes_kind(t) for t in f.argtypes]
         assert got == params, f"{name}: binding {got} vs header {params}"
         assert _ctypes_kind(f.restype) == ret, f"{name}: restype vs header {ret}"
+
+
+def test_struct_layouts_match_the_headers(tmp_path):
+    """attn_tensor and attn_opts as a C compiler lays them out (sizes and field
+    offsets, from a small program built with gcc against include/attn_bwd.h)
+    equal the binding's ctypes structures."""
+    import shutil
+    import subprocess
+    from attention_backward_bwd_gb300 import binding
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    fields = {"attn_tensor": ("ptr", "stride_b", "stride_s", "stride_h"),
+              "attn_opts": ("window_left", "window_right", "softcap", "seqused_q", "seqused_k")}
+    lines = ['#include <stdio.h>', '#include <stddef.h>', '#include "attn_bwd.h"',
+             "int main(void) {"]
+    for st, fs in fields.items():
+        lines.append(f'  printf("{st} size %zu\\n", sizeof({st}));')
+        for f in fs:
+            lines.append(f'  printf("{st} {f} %zu\\n", offsetof({st}, {f}));')
+    lines += ["  return 0;", "}"]
+    src = tmp_path / "layout.c"
+    src.write_text("\n".join(lines) + "\n")
+    exe = tmp_path / "layout"
+    subprocess.run([cc, "-std=c11", "-I", os.path.join(ROOT, "include"), str(src), "-o", str(exe)],
+                   check=True)
+    out = subprocess.run([str(exe)], check=True, capture_output=True, text=True).stdout
+    c = {tuple(line.split()[:2]): int(line.split()[2]) for line in out.splitlines()}
+    for st, cls in (("attn_tensor", binding.AttnTensor), ("attn_opts", binding.AttnOpts)):
+        assert c[(st, "size")] == ctypes.sizeof(cls), st
+        for f in fields[st]:
+            assert c[(st, f)] == getattr(cls, f).offset, f"{st}.{f}"
+        assert [n for n, _ in cls._fields_] == list(fields[st])
