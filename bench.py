@@ -350,37 +350,40 @@ def _cores():
         return os.cpu_count() or 1
 
 
-def oracle_sample(w, x, n_heads=1):
-    """A bounded slice of the workload for the CPU oracle: the first n_heads
-    query heads (one GQA group member each) of sequence 0, full length."""
+def oracle_sample(w, x, n_rows=None):
+    """A bounded slice of the workload for the CPU oracle: one query head of
+    sequence 0 (one GQA group member), its last ``n_rows`` query rows (all rows
+    if None) against every key they see.  With the bottom-right aligned masks
+    the last n rows of a sequence are an exact sub-problem (Sq = n, Sk = L), so
+    the oracle runs on it unchanged; FLOPs are 10 D per allowed pair of the
+    slice (for whole causal heads without a window: the 2.5 x 4 L^2 D / 2
+    convention of the GPU line)."""
     from oracle import attn_oracle
     if w.varlen:
-        n = x.lengths[0]
-        q, k, v, do = x.q[:n], x.k[:n], x.v[:n], x.do[:n]
-        sl = lambda t, h: t[:, h]  # noqa: E731
-        L = n
+        L = x.lengths[0]
+        q, k, v, do = x.q[:L], x.k[:L], x.v[:L], x.do[:L]
     else:
         q, k, v, do = x.q[0], x.k[0], x.v[0], x.do[0]
-        sl = lambda t, h: t[:, h]  # noqa: E731
         L = w.seqlen_q
+    n = L if n_rows is None else max(1, min(L, int(n_rows)))
     g = w.h_q // w.h_k
-
     window = tuple(w.window) if w.windowed else None
 
     def run(h):
-        return attn_oracle.head_backward(sl(q, h).double().numpy(), sl(k, h // g).double().numpy(),
-                                         sl(v, h // g).double().numpy(),
-                                         sl(do, h).double().numpy(), w.scale, w.causal, window,
-                                         w.softcap)
-    if w.windowed:
-        f_one = 10.0 * w.head_dim * window_pairs(L, L, w.causal, w.window)
+        return attn_oracle.head_backward(q[L - n:, h].double().numpy(),
+                                         k[:, h // g].double().numpy(),
+                                         v[:, h // g].double().numpy(),
+                                         do[L - n:, h].double().numpy(), w.scale, w.causal,
+                                         window, w.softcap)
+    if w.windowed or n < L:
+        f_one = 10.0 * w.head_dim * window_pairs(n, L, w.causal, window or (-1, -1))
     else:
         f_one = 2.5 * 4.0 * L * L * w.head_dim / (2 if w.causal else 1)
-    return run, f_one, L
+    return run, f_one, L, n
 
 
 def cpu_baseline(w, x, budget_s=20.0):
-    run, f_one, L = oracle_sample(w, x)
+    run, f_one, L, _ = oracle_sample(w, x)
     t0 = time.perf_counter()
     n = 0
     while True:
@@ -395,13 +398,25 @@ def cpu_baseline(w, x, budget_s=20.0):
                       f"{dt:.1f} s"}
 
 
-def run_reference(args):
+def run_reference(args, budget_s=120.0):
+    """The oracle on the host cores, each step the same bounded slice of the
+    workload (one query head's last n query rows), n sized from one timed
+    calibration call so that the warm-up and timed steps take about
+    ``budget_s`` together."""
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return
     w = synth.WORKLOADS[args.workload]
     x = synth.make_inputs(w)
-    run, f_one, L = oracle_sample(w, x)
+    L = x.lengths[0] if w.varlen else w.seqlen_q
+    n0 = min(L, 256)
+    run0, _, _, _ = oracle_sample(w, x, n0)
+    t0 = time.perf_counter()
+    run0(0)
+    per_row = (time.perf_counter() - t0) / n0
+    want = budget_s / (args.steps + args.warmup) / max(per_row, 1e-9)
+    n = L if want >= L else max(64, int(want) // 64 * 64)
+    run, f_one, L, n = oracle_sample(w, x, n)
     for i in range(args.warmup):
         run(i % w.h_q)
     times = []
@@ -411,7 +426,8 @@ def run_reference(args):
         times.append(time.perf_counter() - t0)
     ms = 1e3 * statistics.mean(times)
     val = f_one / (ms * 1e-3) / 1e12
-    sample = f"one query head of sequence 0 per step (length {L}), fp64 numpy oracle"
+    sample = (f"one query head of sequence 0 per step: its last {n} of {L} query rows against "
+              f"every key they see, fp64 numpy oracle")
     out = {"impl": "reference", "metric": METRIC, "value": round(val, 6), "unit": "TFLOP/s",
            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
            "ms_per_step": round(ms, 2), "higher_is_better": True, "scaling": "weak",
