@@ -288,6 +288,8 @@ extern "C" int attn_bwd_host(const attn_tensor* q, const attn_tensor* k, const a
   if (hq && hk && lse == nullptr) return fail(ATTN_ERR_NULL, "lse is NULL");
   attn_opts checked;
   if ((rc = resolve_opts(opts, &checked))) return rc;
+  if (checked.seqused_q != nullptr || checked.seqused_k != nullptr)
+    return fail(ATTN_ERR_ARG, "seqused_q/k are not taken by the host-buffer calls");
   const Chunking ch = chunking(batch, h_k, chunks);
   const BufLayout L = buf_layout(batch, seqlen_q, seqlen_k, h_q, h_k, head_dim, ch);
   if (device_buffer == nullptr) return fail(ATTN_ERR_WORKSPACE, "device_buffer is NULL");
@@ -343,13 +345,10 @@ extern "C" int attn_bwd_host(const attn_tensor* q, const attn_tensor* k, const a
     const attn_tensor tdv = compact_view(buf + L.dv + koff, seqlen_k, h_k, head_dim);
     const float* tlse = reinterpret_cast<const float*>(buf + L.lse) +
                         (static_cast<size_t>(b0) * h_q + i0) * seqlen_q;
-    attn_opts co = checked;  // used lengths of this chunk's sequences
-    if (co.seqused_q != nullptr) co.seqused_q += b0;
-    if (co.seqused_k != nullptr) co.seqused_k += b0;
     Prepared pr;
     int r = prepare_bwd(&tq, &tk, &tv, &to, tlse, &tdo, &tdq, &tdk, &tdv, dtype, nb, seqlen_q,
                         seqlen_k, ni, nj, head_dim, scale, causal, nullptr, nullptr, seqlen_q,
-                        seqlen_k, deterministic, &co, buf + L.ws[slot], L.ws_bytes, &pr);
+                        seqlen_k, deterministic, &checked, buf + L.ws[slot], L.ws_bytes, &pr);
     return r ? r : run_stages(kPre | kMain | kPost, pr, cs);
   };
   auto copy_out = [&](int c, cudaStream_t st) -> int {
@@ -530,6 +529,8 @@ extern "C" int attn_bwd_host_varlen(const attn_tensor* q, const attn_tensor* k,
   if (hq && hk && lse == nullptr) return fail(ATTN_ERR_NULL, "lse is NULL");
   attn_opts checked;
   if ((rc = resolve_opts(opts, &checked))) return rc;
+  if (checked.seqused_q != nullptr || checked.seqused_k != nullptr)
+    return fail(ATTN_ERR_ARG, "seqused_q/k are not taken by the host-buffer calls");
   VarlenChunk ch[kMaxChunks];
   int n = 0;
   if ((rc = plan_varlen(cu_seqlens_q, cu_seqlens_k, batch, total_q, total_k, chunks, ch, &n)))
@@ -594,13 +595,10 @@ extern "C" int attn_bwd_host_varlen(const attn_tensor* q, const attn_tensor* k,
     const attn_tensor tdv{buf + L.dv + koff, 0, sk, head_dim};
     const int* cuq = reinterpret_cast<const int*>(buf + L.cu) + C.cu_off;
     const int* cuk = cuq + C.nb + 1;
-    attn_opts co = checked;  // used lengths of this chunk's sequences
-    if (co.seqused_q != nullptr) co.seqused_q += C.b0;
-    if (co.seqused_k != nullptr) co.seqused_k += C.b0;
     Prepared pr;
     int r = prepare_bwd(&tq, &tk, &tv, &to, lse_dev(C), &tdo, &tdq, &tdk, &tdv, dtype, C.nb, C.nq,
                         C.nk, h_q, h_k, head_dim, scale, causal, cuq, cuk, C.max_q, C.max_k,
-                        deterministic, &co, buf + L.ws[slot], L.ws_bytes, &pr);
+                        deterministic, &checked, buf + L.ws[slot], L.ws_bytes, &pr);
     return r ? r : run_stages(kPre | kMain | kPost, pr, cs);
   };
   auto copy_out = [&](int c, cudaStream_t st) -> int {

@@ -248,7 +248,8 @@ int attn_bwd_noalloc(const attn_tensor* q, const attn_tensor* k, const attn_tens
  * chunks) bytes, 256-byte aligned, owned by the caller, not used by any other
  * call while this one runs.  It holds device copies of all eight tensors and
  * of lse plus three chunk-sized workspaces (one per internal compute stream).
- * opts: a local window and a logit cap as for attn_bwd_ex (NULL: none).
+ * opts: a local window and a logit cap as for attn_bwd_ex (NULL: none);
+ * seqused_q/k must be NULL here (ATTN_ERR_ARG otherwise).
  * Errors as attn_bwd (argument errors before anything is enqueued; a
  * stride_h other than D is ATTN_ERR_STRIDE).  The first call on a device
  * creates the library's internal streams and events for that device; make

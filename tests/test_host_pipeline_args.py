@@ -104,3 +104,33 @@ def test_varlen_buffer_size_and_bad_cu(lib):
         assert lib.attn_bwd_host_varlen_buffer_size(arr.ctypes.data, cu.ctypes.data, 4, 1500, 1500,
                                                     8, 2, 128, 0) == 0
         assert msg in lib.attn_last_error()
+
+
+def test_seqused_refused_by_the_host_calls(lib):
+    """Used lengths are device arrays read by the kernels; the host-buffer calls
+    take host tensors, so they refuse seqused_q/k rather than hand a kernel a
+    pointer of the wrong kind."""
+    import numpy as np
+    from attention_backward_bwd_gb300.binding import AttnOpts
+    used = np.array([100, 200], dtype=np.int32)
+    q = _t(1 << 20, 2, 256, 8, 128)
+    k = _t(1 << 20, 2, 256, 2, 128)
+    for opts in (AttnOpts(-1, -1, 0.0, used.ctypes.data, None),
+                 AttnOpts(-1, -1, 0.0, None, used.ctypes.data)):
+        size = lib.attn_bwd_host_buffer_size(2, 256, 256, 8, 2, 128, 0)
+        rc = lib.attn_bwd_host(ctypes.byref(q), ctypes.byref(k), ctypes.byref(k),
+                               ctypes.byref(q), 1 << 21, ctypes.byref(q), ctypes.byref(q),
+                               ctypes.byref(k), ctypes.byref(k), 1, 2, 256, 256, 8, 2, 128, 0.1,
+                               1, 0, ctypes.byref(opts), 0, 1 << 24, size, None)
+        assert rc == -9 and b"seqused" in lib.attn_last_error()
+        cu = np.array([0, 200, 512], dtype=np.int32)
+        pq = _t(1 << 20, 1, 512, 8, 128)
+        pk = _t(1 << 20, 1, 512, 2, 128)
+        vsize = lib.attn_bwd_host_varlen_buffer_size(cu.ctypes.data, cu.ctypes.data, 2, 512, 512,
+                                                     8, 2, 128, 0)
+        rc = lib.attn_bwd_host_varlen(ctypes.byref(pq), ctypes.byref(pk), ctypes.byref(pk),
+                                      ctypes.byref(pq), 1 << 21, ctypes.byref(pq),
+                                      ctypes.byref(pq), ctypes.byref(pk), ctypes.byref(pk), 1, 2,
+                                      512, 512, 8, 2, 128, 0.1, 1, cu.ctypes.data, cu.ctypes.data,
+                                      0, ctypes.byref(opts), 0, 1 << 24, vsize, None)
+        assert rc == -9 and b"seqused" in lib.attn_last_error()
