@@ -6,12 +6,12 @@ builds and binds it.  PyTorch provides device memory and streams.
 """
 from .binding import (AttnError, alloc_workspace, attn_bwd, attn_bwd_host, attn_bwd_host_varlen,
                       attn_fwd,
-                      check_device_status, diag_exp2, diag_mma, diag_tanh, diag_wait_timeout,
+                      check_device_status, diag_mma, diag_tanh, diag_wait_timeout,
                       host_buffer_size, lib, set_wait_timeout_ns, version, workspace_layout,
                       workspace_size)
 
 __all__ = ["AttnError", "alloc_workspace", "attn_bwd", "attn_bwd_host", "attn_bwd_host_varlen",
            "attn_fwd",
-           "check_device_status", "diag_exp2", "diag_mma", "diag_tanh", "diag_wait_timeout",
+           "check_device_status", "diag_mma", "diag_tanh", "diag_wait_timeout",
            "host_buffer_size", "lib", "set_wait_timeout_ns", "version", "workspace_layout",
            "workspace_size"]

@@ -65,7 +65,7 @@ EXPORTS = ("attn_fwd", "attn_bwd", "attn_bwd_preprocess", "attn_bwd_main", "attn
            "attn_bwd_host_varlen_buffer_size", "attn_bwd_ex", "attn_fwd_ex",
            "attn_check_device_status",
            "attn_set_wait_timeout_ns", "attn_last_error", "attn_version", "attn_diag_mma",
-           "attn_diag_wait_timeout", "attn_diag_exp2", "attn_diag_tanh")
+           "attn_diag_wait_timeout", "attn_diag_tanh")
 
 
 def lib() -> ctypes.CDLL:
@@ -123,8 +123,6 @@ def lib() -> ctypes.CDLL:
         L.attn_version.restype = ctypes.c_char_p
         L.attn_diag_mma.argtypes = [_I, _I, _I, _P, _P, _P, _P]
         L.attn_diag_mma.restype = _I
-        L.attn_diag_exp2.argtypes = [_P, _P, _I, _P]
-        L.attn_diag_exp2.restype = _I
         L.attn_diag_tanh.argtypes = [_P, _P, _I, _P]
         L.attn_diag_tanh.restype = _I
         L.attn_diag_wait_timeout.argtypes = [ctypes.c_int64, _P]
@@ -460,13 +458,6 @@ def diag_mma(mode: int, a: torch.Tensor, b: torch.Tensor) -> torch.Tensor:
     _check(lib().attn_diag_mma(mode, _dtype_code(a), d, a.data_ptr(), b.data_ptr(), c.data_ptr(),
                                _stream(None)))
     return c
-
-
-def diag_exp2(x: torch.Tensor) -> torch.Tensor:
-    """The kernel's polynomial 2^x on a device fp32 tensor (see include/attn_diag.h)."""
-    y = torch.empty_like(x)
-    _check(lib().attn_diag_exp2(x.data_ptr(), y.data_ptr(), x.numel(), _stream(None)))
-    return y
 
 
 def diag_tanh(x: torch.Tensor) -> torch.Tensor:

@@ -312,24 +312,6 @@ __device__ __forceinline__ float tanh_exp(float x) {
   return 1.f - 2.f * rcp_approx(ex2(x * 2.8853900817779268f) + 1.f);
 }
 
-// 2^x on the FMA/ALU pipes (no MUFU), for x in [-125, 1].  Range reduction
-// x = j + f with j = round(x) (the 1.5 * 2^23 rounding trick) and f in
-// [-0.5, 0.5]; 2^f by a degree-3 polynomial whose coefficients were fitted for
-// minimax relative error on that interval (max relative error 7.5e-5, about
-// 2^-13.7, below the 2^-9 / 2^-11 rounding of the bf16 / fp16 P it feeds);
-// 2^j is added to the exponent field.
-__device__ __forceinline__ float ex2_poly(float x) {
-  x = fmaxf(x, -125.0f);
-  const float t = x + 12582912.0f;
-  const float j = t - 12582912.0f;
-  const float f = x - j;
-  float p = fmaf(0.0551716685295105f, f, 0.2426111251115799f);
-  p = fmaf(p, f, 0.6932609677314758f);
-  p = fmaf(p, f, 0.9999280571937561f);
-  const int ji = __float_as_int(t) - 0x4B400000;
-  return __int_as_float(__float_as_int(p) + (ji << 23));
-}
-
 template <typename T>
 struct Pack;
 template <>

@@ -146,11 +146,6 @@ __global__ void diag_wait_kernel(unsigned int* status, unsigned long long timeou
   __syncthreads();
 }
 
-__global__ void diag_exp2_kernel(const float* x, float* y, int n) {
-  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x)
-    y[i] = ex2_poly(x[i]);
-}
-
 __global__ void diag_tanh_kernel(const float* x, float* y, int n) {
   for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x)
     y[i] = tanh_exp(x[i]);
@@ -196,13 +191,6 @@ int attn_diag_mma(int mode, int dtype, int head_dim, const void* a, const void* 
     return head_dim == 64 ? diag_mma_t<__half, 64>(mode, a, b, c, s, st, to)
                           : diag_mma_t<__half, 128>(mode, a, b, c, s, st, to);
   return ATTN_ERR_DTYPE;
-}
-
-int attn_diag_exp2(const float* x, float* y, int n, attn_stream_t stream) {
-  if (x == nullptr || y == nullptr) return ATTN_ERR_NULL;
-  if (n <= 0) return ATTN_ERR_ARG;
-  diag_exp2_kernel<<<64, 256, 0, reinterpret_cast<cudaStream_t>(stream)>>>(x, y, n);
-  return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
 int attn_diag_tanh(const float* x, float* y, int n, attn_stream_t stream) {

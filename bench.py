@@ -93,7 +93,7 @@ def kernel_traffic():
 
 
 class ClockSampler:
-    """nvidia-smi sampling (200 ms) of SM clock and throttle reasons."""
+    """nvidia-smi sampling (every 50 ms) of SM clock and throttle reasons."""
 
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
@@ -109,7 +109,7 @@ class ClockSampler:
             self.f = open(self.path, "w")
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "200"], stdout=self.f,
+                 "--format=csv,noheader,nounits", "-lms", "50"], stdout=self.f,
                 stderr=subprocess.DEVNULL)
         except Exception:
             self.proc = None
@@ -295,7 +295,12 @@ def run_ours(args):
         return
     peaks = measured_peaks()
     achieved = flops / (t_main * 1e-3) / 1e12
-    peak = peaks["bf16_tflops_sustained"]
+    # The main kernel is timed on its own, a few milliseconds per launch at the
+    # clocks recorded below, so its denominator is the burst bf16 GEMM figure
+    # (measured the same way); the sustained figure was taken over seconds of
+    # back-to-back GEMMs at power-capped clocks and is printed for comparison.
+    peak = peaks["bf16_tflops"]
+    peak_sus = peaks["bf16_tflops_sustained"]
     traffic = kernel_traffic()
     rows_heads = (sum(x.lengths) if w.varlen else w.batch * w.seqlen_q) * w.h_q
     esz = 2
@@ -322,7 +327,8 @@ def run_ours(args):
         "pct_of_peak": round(100.0 * value / world / peak, 2),
         "roofline": {"bound": "tensor", "kernel": "bwd_main_kernel", "achieved": round(achieved, 2),
                      "peak": peak, "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
-                     "peak_src": peaks["src"] + " bf16 sustained",
+                     "peak_src": "bf16 burst, of " + peaks["src"],
+                     "frac_of_sustained": round(achieved / peak_sus, 4),
                      "traffic": traffic},
         "kernels_ms": {"preprocess": round(t_pre, 4), "main": round(t_main, 4),
                        "postprocess": round(t_post, 4)},

@@ -331,6 +331,13 @@ int attn_bwd_postprocess(const attn_tensor* q, const attn_tensor* k, const attn_
  * wait inside a kernel gave up; attn_last_error names the wait site),
  * ATTN_ERR_ARG (cu_seqlens or seqused_q/k failed the device-side check;
  * attn_last_error names which) or ATTN_ERR_CUDA (the stream reported an error).
+ * The status word is one per device and stays set until this call clears it.
+ * While a failed cu_seqlens / seqused check is recorded there, the kernels of
+ * EVERY later varlen or seqused call on that device (any stream, any host
+ * thread, valid arrays or not) return at once without writing their outputs,
+ * and those calls still return ATTN_OK on the host.  A caller that passes
+ * device offsets it has not validated itself should therefore call this
+ * function after such a call, before relying on any later varlen result.
  */
 int attn_check_device_status(attn_stream_t stream);
 

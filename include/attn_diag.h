@@ -34,14 +34,6 @@ int attn_diag_mma(int mode, int dtype, int head_dim, const void* a, const void* 
                   attn_stream_t stream);
 
 /*
- * attn_diag_exp2 -- y[i] = 2^x[i] computed with the polynomial (FMA-pipe)
- * exponential the backward kernel uses for half of its P entries, so its
- * accuracy can be checked against a reference.  Valid for x in [-125, 1].
- * x, y: device fp32 arrays of n elements.
- */
-int attn_diag_exp2(const float* x, float* y, int n, attn_stream_t stream);
-
-/*
  * attn_diag_tanh -- y[i] = tanh(x[i]) computed as the logit cap of the
  * kernels does (1 - 2 / (e^{2x} + 1) from the hardware exponential and
  * reciprocal), so its error can be checked against a reference.

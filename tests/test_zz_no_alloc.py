@@ -59,6 +59,41 @@ def test_noalloc_matches_attn_bwd_on_two_calls(deterministic):
                 assert torch.equal(g, r), name
 
 
+@pytest.mark.parametrize("deterministic", [False, True])
+def test_noalloc_varlen_matches_attn_bwd_on_two_calls(deterministic):
+    """Packed sequences (cu_seqlens) through the static scratch: ragged lengths,
+    an empty sequence, and a GQA group, compared with attn_bwd's results."""
+    lens = [300, 0, 129, 77]
+    w = synth.Workload("noalloc_vl", 0, 4, 2, 0, 0, 128, "bf16", True, 124, n_seqs=len(lens),
+                       len_lo=0, len_hi=300)
+    x = synth.make_inputs(w, lengths=lens)
+    q, k, v, do = (t.cuda() for t in (x.q, x.k, x.v, x.do))
+    cu = x.cu_seqlens_q.cuda()
+    mx = max(lens)
+    o, lse = ab.attn_fwd(q, k, v, causal=True, cu_seqlens_q=cu, cu_seqlens_k=cu,
+                         max_seqlen_q=mx, max_seqlen_k=mx)
+    ref = ab.attn_bwd(q, k, v, o, lse, do, causal=True, cu_seqlens_q=cu, cu_seqlens_k=cu,
+                      max_seqlen_q=mx, max_seqlen_k=mx, deterministic=deterministic)
+    ab.check_device_status()
+    f = _entry()
+    total, hq, d = q.shape
+    hk = k.shape[1]
+    for _ in range(2):
+        got = [torch.full_like(t, float("nan")) for t in (q, k, v)]
+        descs = [binding._desc(t) for t in (q, k, v, o)]
+        rest = [binding._desc(t) for t in (do, *got)]
+        rc = f(*(ctypes.byref(t) for t in descs), lse.data_ptr(),
+               *(ctypes.byref(t) for t in rest), binding._dtype_code(q), len(lens), total, total,
+               hq, hk, d, d ** -0.5, 1, cu.data_ptr(), cu.data_ptr(), mx, mx, int(deterministic),
+               torch.cuda.current_stream().cuda_stream)
+        assert rc == 0, binding.lib().attn_last_error()
+        ab.check_device_status()
+        for name, g, r in zip(("dQ", "dK", "dV"), got, ref):
+            assert_close(f"noalloc varlen {name}", g, r.float().cpu().double().numpy())
+            if deterministic:
+                assert torch.equal(g, r), name
+
+
 def test_noalloc_rejects_problems_beyond_its_scratch():
     q = torch.zeros(1, 64, 2, 128, dtype=torch.bfloat16, device="cuda")
     lse = torch.zeros(1, 2, 64, device="cuda")
