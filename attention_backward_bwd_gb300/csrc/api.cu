@@ -449,6 +449,8 @@ int attn_fwd_ex(const attn_tensor* q, const attn_tensor* k, const attn_tensor* v
   if (p.max_seqlen_q == 0) return ATTN_OK;
   unsigned int* st = status_word();
   if (st == nullptr) return fail(ATTN_ERR_CUDA, "cannot resolve the device status word");
+  p.status = st;
+  p.timeout_ns = static_cast<unsigned long long>(g_timeout_ns.load());
   cudaError_t e;
   if (varlen) {
     p.input_bad = st + 1;

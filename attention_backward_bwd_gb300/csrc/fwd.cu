@@ -1,16 +1,35 @@
-// Attention forward (supporting kernel): produces O and the natural-log LSE
-// that the backward consumes.  Not on the timed path.
+// Attention forward for sm_103a: produces O and the natural-log LSE that the
+// backward consumes.  tcgen05 MMAs with TMEM accumulators, TMA tile loads,
+// warp-specialised, persistent over work units.
 //
-// Online-softmax forward as in TileLang test_tilelang_kernel_mha_bwd.py,
-// flashattn_fwd: scores in base 2 (scale * log2 e folded in), running row max
-// and sum, causal loop stopped at the diagonal tile with an elementwise mask
-// there.  Differences from that page: LSE is returned in natural log (the
-// FlashAttention convention the backward API takes), causal uses bottom-right
-// alignment (key j allowed iff j <= i + Sk - Sq), GQA and varlen are handled,
-// and rows with no allowed key give O = 0, LSE = +inf.
+// Algorithm (TileLang test_tilelang_kernel_mha_bwd.py, flashattn_fwd): online
+// softmax over key tiles in base 2 (scale * log2 e folded into the exponent),
+// the causal / window range of key tiles only, with an element mask on the
+// tiles a mask cuts.  Differences from that page: LSE is returned in natural
+// log (the FlashAttention convention the backward API takes), masks are
+// bottom-right aligned (key j allowed for query i iff j <= i + Sk - Sq, plus a
+// left window side), GQA, varlen, used lengths and a logit cap are handled, and
+// rows with no allowed key give O = 0, LSE = +inf.
 //
-// Design: 4 warps per CTA, 64 query rows (16 per warp), 64-key tiles,
-// mma.sync m16n8k16 with fp32 accumulation, cp.async double-buffered K/V.
+// One work unit = (query tile m of BM = 128 rows, query head h, sequence b).
+// For each key tile n of BN = 128 keys in the unit's range:
+//   S = Q K_n^T                     (TMEM fp32, one of three S buffers)
+//   P = exp2(S * scale * log2 e - m_ref)     (bf16/fp16, written over S)
+//   O += P V_n                      (TMEM fp32; A = P from TMEM, B = V in smem)
+// The reference maximum m_ref of a row only moves when the row's running
+// maximum exceeds it by more than 2^8 (then O and the row sum are rescaled);
+// otherwise P is at most 2^8 and O, the row sum and the LSE stay consistent
+// with the stale reference, so the result is the same softmax.
+//
+// Warp roles (256 threads): warp 0 TMA producer, warp 1 MMA issuer (one
+// thread), warp 2 TMEM allocator, warps 4-7 softmax and epilogue (thread =
+// query row = TMEM lane).  The MMA thread issues S of tile t before O += P V
+// of tile t - 1, so the tensor pipe computes S of the next tile while the
+// softmax warps work on the current one; three S buffers keep S of tile t
+// from waiting on O += P V of tile t - 2.
+//
+// TMEM columns (512 allocated): S buffers [0,128), [128,256), [256,384);
+// O [384, 384 + D).  Shared memory: 2 Q stages, 3 K stages, 2 V stages.
 #include <atomic>
 
 #include "common.cuh"
@@ -19,265 +38,435 @@ namespace attn {
 
 namespace {
 
-constexpr int kBM = 64, kBN = 64, kFwdThreads = 128;
+constexpr int FBM = 128;  // query tile
+constexpr int FBN = 128;  // key tile
+constexpr int kFThreads = 256;
+constexpr int kQSt = 2, kKSt = 3, kVSt = 2;
+constexpr int kSBufs = 3;
+constexpr uint32_t kFChunk = 128 * 128;  // one 64-column (128-byte) slice of a 128-row tile
+constexpr uint32_t kFTmemCols = 512;
+constexpr uint32_t TF_S = 0, TF_O = 384;
+constexpr float kRescaleLog2 = 8.f;  // P stays below 2^8 between rescales
 
-template <typename T>
-struct MmaOp;
-template <>
-struct MmaOp<__nv_bfloat16> {
-  static __device__ __forceinline__ void run(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
-                                             uint32_t b1) {
-    asm volatile(
-        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
-        "{%8,%9}, {%0,%1,%2,%3};"
-        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
-  }
-};
-template <>
-struct MmaOp<__half> {
-  static __device__ __forceinline__ void run(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
-                                             uint32_t b1) {
-    asm volatile(
-        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
-        "{%8,%9}, {%0,%1,%2,%3};"
-        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
-  }
+enum FBar : uint32_t {
+  F_QFULL = 0,
+  F_QEMPTY = F_QFULL + kQSt,
+  F_KFULL = F_QEMPTY + kQSt,
+  F_KEMPTY = F_KFULL + kKSt,
+  F_VFULL = F_KEMPTY + kKSt,
+  F_VEMPTY = F_VFULL + kVSt,
+  F_SFULL = F_VEMPTY + kVSt,    // per S buffer: S computed
+  F_PREADY = F_SFULL + kSBufs,  // per S buffer: P written over it (4 softmax warps)
+  F_PVDONE = F_PREADY + kSBufs, // per S buffer: O += P V has read it
+  F_OFULL = F_PVDONE + kSBufs,  // the unit's last O += P V done
+  F_FINAL,
+  F_COUNT
 };
 
-__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
-                                        uint32_t& r3) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
-               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
-               : "r"(addr));
-}
-__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
-                                          uint32_t& r3) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
-               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
-               : "r"(addr));
-}
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, bool ok) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src),
-               "r"(ok ? 16 : 0)
-               : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() {
-  asm volatile("cp.async.commit_group;" ::: "memory");
-}
-__device__ __forceinline__ void cp_async_wait_all() {
-  asm volatile("cp.async.wait_group 0;" ::: "memory");
-}
+template <int D>
+struct FSmem {
+  static constexpr uint32_t kTile = (D / 64) * kFChunk;
+  static constexpr uint32_t kQ = 0;
+  static constexpr uint32_t kK = kQ + kQSt * kTile;
+  static constexpr uint32_t kV = kK + kKSt * kTile;
+  static constexpr uint32_t kBar = kV + kVSt * kTile;
+  static constexpr uint32_t kTmemSlot = kBar + F_COUNT * 8;
+  static constexpr uint32_t kAbort = kTmemSlot + 4;
+  static constexpr uint32_t kTotal = kAbort + 4;
+};
+static_assert(FSmem<128>::kTotal <= 232448, "shared memory budget");
 
-// Copy rows [row0, row0 + 64) of a (rows x D) head slice into smem (row stride LD),
-// zero-filling rows at or beyond `valid_rows`.
-template <typename T, int D, int LD>
-__device__ __forceinline__ void load_tile(T* dst, const T* src, int64_t row_stride, int row0,
-                                          int valid_rows, int valid_cols) {
-  constexpr int kChunks = kBN * D / 8;
-  for (int c = threadIdx.x; c < kChunks; c += kFwdThreads) {
-    const int r = c / (D / 8);
-    const int col = (c % (D / 8)) * 8;
-    const int gr = row0 + r;
-    // rows past the sequence and columns past a padded head dimension read as 0
-    const bool ok = gr < valid_rows && col < valid_cols;
-    const T* g = ok ? src + static_cast<int64_t>(gr) * row_stride + col : src;  // no read if !ok
-    cp_async16(smem_u32(dst + r * LD + col), g, ok);
-  }
-}
+struct FUnit {
+  int m, h, b;
+  SeqInfo si;
+  bool active;         // the query tile holds rows of the sequence
+  int n_start, n_end;  // key tiles [n_start, n_end) seen by some query of the tile
+};
 
-template <typename T, int D>
-__global__ void __launch_bounds__(kFwdThreads) fwd_kernel(FwdParams p) {
-  constexpr int LD = D + 8;  // padded row stride (elements) keeps ldmatrix conflict-free
-  extern __shared__ __align__(128) unsigned char smem_raw[];
-  T* sQ = reinterpret_cast<T*>(smem_raw);
-  T* sK = sQ + kBM * LD;       // [2][kBN][LD]
-  T* sV = sK + 2 * kBN * LD;   // [2][kBN][LD]
-  if (p.input_bad != nullptr && *p.input_bad) return;
-
-  const int b = blockIdx.z, h = blockIdx.y;
-  const SeqInfo si = seq_info(p.seq, b);
-  const int m0 = blockIdx.x * kBM;
-  if (m0 >= si.sq) return;
-  const bool varlen = p.seq.cu_q != nullptr;
-  const int hk = h / (p.h_q / p.h_k);
-  const T* qg = static_cast<const T*>(p.q.ptr) + (varlen ? 0 : b * p.q.sb) +
-                static_cast<int64_t>(si.q_start) * p.q.ss + static_cast<int64_t>(h) * p.q.sh;
-  const T* kg = static_cast<const T*>(p.k.ptr) + (varlen ? 0 : b * p.k.sb) +
-                static_cast<int64_t>(si.k_start) * p.k.ss + static_cast<int64_t>(hk) * p.k.sh;
-  const T* vg = static_cast<const T*>(p.v.ptr) + (varlen ? 0 : b * p.v.sb) +
-                static_cast<int64_t>(si.k_start) * p.v.ss + static_cast<int64_t>(hk) * p.v.sh;
-  T* og = const_cast<T*>(static_cast<const T*>(p.o.ptr)) + (varlen ? 0 : b * p.o.sb) +
-          static_cast<int64_t>(si.q_start) * p.o.ss + static_cast<int64_t>(h) * p.o.sh;
-
-  const int off = si.sk - si.sq;  // bottom-right alignment of causal / window masks
-  // key tiles holding a key that some query of this tile sees
-  const int n_start = window_first_key(m0, si.sq, si.sk, p.win_left) / kBN;
-  int n_end = ceil_div(si.sk, kBN);
+// Unit u -> (query tile m, sequence b, head h): query tiles from the last to the
+// first (causal units are longest first), heads fastest so that CTAs running at
+// the same time share the K/V tiles of a group in L2.
+__device__ __forceinline__ FUnit fwd_unit(const FwdParams& p, int u, int n_mt) {
+  FUnit r;
+  const int per_m = p.seq.batch * p.h_q;
+  const int mr = u / per_m;
+  const int rem = u - mr * per_m;
+  r.b = rem / p.h_q;
+  r.h = rem - r.b * p.h_q;
+  r.m = n_mt - 1 - mr;
+  r.si = seq_info(p.seq, r.b);
+  const int m0 = r.m * FBM;
+  r.active = m0 < r.si.sq;
+  r.n_start = r.n_end = 0;
+  if (!r.active) return r;
+  const int off = r.si.sk - r.si.sq;
+  r.n_start = window_first_key(m0, r.si.sq, r.si.sk, p.win_left) / FBN;
+  int n_end = ceil_div(r.si.sk, FBN);
   if (p.win_right >= 0) {
-    const int last_key = m0 + kBM - 1 + off + p.win_right;
-    n_end = min(n_end, last_key < 0 ? 0 : last_key / kBN + 1);
+    const int last_key = min(m0 + FBM, r.si.sq) - 1 + off + p.win_right;
+    n_end = min(n_end, last_key < 0 ? 0 : last_key / FBN + 1);
   }
-
-  load_tile<T, D, LD>(sQ, qg, p.q.ss, m0, si.sq, p.head_dim);
-  cp_async_commit();
-  if (n_end > n_start) {
-    load_tile<T, D, LD>(sK, kg, p.k.ss, n_start * kBN, si.sk, p.head_dim);
-    load_tile<T, D, LD>(sV, vg, p.v.ss, n_start * kBN, si.sk, p.head_dim);
-  }
-  cp_async_commit();
-  cp_async_wait_all();
-  __syncthreads();
-
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int g = lane >> 2, t = lane & 3;
-  uint32_t qf[D / 16][4];
-#pragma unroll
-  for (int kk = 0; kk < D / 16; ++kk) {
-    const uint32_t a = smem_u32(sQ + (warp * 16 + (lane & 15)) * LD + kk * 16 + (lane >> 4) * 8);
-    ldsm_x4(a, qf[kk][0], qf[kk][1], qf[kk][2], qf[kk][3]);
-  }
-
-  float o[D / 8][4];
-#pragma unroll
-  for (int i = 0; i < D / 8; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
-  float mrow[2] = {-INFINITY, -INFINITY};
-  float lpart[2] = {0.f, 0.f};
-  const int row_lo = m0 + warp * 16 + g;
-
-  for (int n = n_start; n < n_end; ++n) {
-    const int buf = (n - n_start) & 1;
-    if (n + 1 < n_end) {
-      load_tile<T, D, LD>(sK + (buf ^ 1) * kBN * LD, kg, p.k.ss, (n + 1) * kBN, si.sk,
-                          p.head_dim);
-      load_tile<T, D, LD>(sV + (buf ^ 1) * kBN * LD, vg, p.v.ss, (n + 1) * kBN, si.sk,
-                          p.head_dim);
-    }
-    cp_async_commit();
-    const T* cK = sK + buf * kBN * LD;
-    const T* cV = sV + buf * kBN * LD;
-
-    float s[8][4];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) s[i][0] = s[i][1] = s[i][2] = s[i][3] = 0.f;
-#pragma unroll
-    for (int kk = 0; kk < D / 16; ++kk) {
-#pragma unroll
-      for (int np = 0; np < 4; ++np) {
-        uint32_t r0, r1, r2, r3;
-        const int key = np * 16 + (lane >> 4) * 8 + (lane & 7);
-        const int col = kk * 16 + ((lane >> 3) & 1) * 8;
-        ldsm_x4(smem_u32(cK + key * LD + col), r0, r1, r2, r3);
-        MmaOp<T>::run(s[2 * np], qf[kk], r0, r1);
-        MmaOp<T>::run(s[2 * np + 1], qf[kk], r2, r3);
-      }
-    }
-
-    const bool need_mask = (n * kBN + kBN > si.sk) ||
-                           (p.win_right >= 0 && n * kBN + kBN - 1 > m0 + off + p.win_right) ||
-                           (p.win_left >= 0 && n * kBN < m0 + kBM - 1 + off - p.win_left);
-    float tmax[2] = {-INFINITY, -INFINITY};
-#pragma unroll
-    for (int nt = 0; nt < 8; ++nt) {
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        // logit in log2 units; with a cap c: c tanh(S scale / c) log2 e
-        float x = p.softcap > 0.f ? tanh_exp(s[nt][e] * p.cap_in) * p.cap_out
-                                  : s[nt][e] * p.scale_log2;
-        if (need_mask) {
-          const int key = n * kBN + nt * 8 + 2 * t + (e & 1);
-          const int row = row_lo + (e >> 1) * 8;
-          const bool ok = key < si.sk && (p.win_right < 0 || key <= row + off + p.win_right) &&
-                          (p.win_left < 0 || key >= row + off - p.win_left);
-          x = ok ? x : -INFINITY;
-        }
-        s[nt][e] = x;
-        tmax[e >> 1] = fmaxf(tmax[e >> 1], x);
-      }
-    }
-    float alpha[2], muse[2];
-#pragma unroll
-    for (int r = 0; r < 2; ++r) {
-      tmax[r] = fmaxf(tmax[r], __shfl_xor_sync(0xffffffffu, tmax[r], 1));
-      tmax[r] = fmaxf(tmax[r], __shfl_xor_sync(0xffffffffu, tmax[r], 2));
-      const float mnew = fmaxf(mrow[r], tmax[r]);
-      muse[r] = (mnew == -INFINITY) ? 0.f : mnew;
-      alpha[r] = ex2(mrow[r] - muse[r]);
-      mrow[r] = mnew;
-      lpart[r] *= alpha[r];
-    }
-#pragma unroll
-    for (int nt = 0; nt < 8; ++nt) {
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const float pv = ex2(s[nt][e] - muse[e >> 1]);
-        s[nt][e] = pv;
-        lpart[e >> 1] += pv;
-      }
-    }
-#pragma unroll
-    for (int dn = 0; dn < D / 8; ++dn) {
-      o[dn][0] *= alpha[0];
-      o[dn][1] *= alpha[0];
-      o[dn][2] *= alpha[1];
-      o[dn][3] *= alpha[1];
-    }
-#pragma unroll
-    for (int kk = 0; kk < 4; ++kk) {
-      uint32_t a[4];
-      a[0] = Pack<T>::two(s[2 * kk][0], s[2 * kk][1]);
-      a[1] = Pack<T>::two(s[2 * kk][2], s[2 * kk][3]);
-      a[2] = Pack<T>::two(s[2 * kk + 1][0], s[2 * kk + 1][1]);
-      a[3] = Pack<T>::two(s[2 * kk + 1][2], s[2 * kk + 1][3]);
-#pragma unroll
-      for (int dp = 0; dp < D / 16; ++dp) {
-        uint32_t r0, r1, r2, r3;
-        const int key = kk * 16 + ((lane >> 3) & 1) * 8 + (lane & 7);
-        const int col = dp * 16 + (lane >> 4) * 8;
-        ldsm_x4_t(smem_u32(cV + key * LD + col), r0, r1, r2, r3);
-        MmaOp<T>::run(o[2 * dp], a, r0, r1);
-        MmaOp<T>::run(o[2 * dp + 1], a, r2, r3);
-      }
-    }
-    cp_async_wait_all();
-    __syncthreads();
-  }
-
-  float inv[2], lse[2];
-#pragma unroll
-  for (int r = 0; r < 2; ++r) {
-    float l = lpart[r];
-    l += __shfl_xor_sync(0xffffffffu, l, 1);
-    l += __shfl_xor_sync(0xffffffffu, l, 2);
-    inv[r] = l > 0.f ? 1.f / l : 0.f;
-    // natural log: (m + log2 l) * ln 2
-    lse[r] = l > 0.f ? (mrow[r] + __log2f(l)) * 0.6931471805599453f : INFINITY;
-  }
-#pragma unroll
-  for (int r = 0; r < 2; ++r) {
-    const int row = row_lo + r * 8;
-    if (row < si.sq) {
-      T* orow = og + static_cast<int64_t>(row) * p.o.ss;
-#pragma unroll
-      for (int dn = 0; dn < D / 8; ++dn) {
-        const uint32_t v = Pack<T>::two(o[dn][2 * r] * inv[r], o[dn][2 * r + 1] * inv[r]);
-        if (dn * 8 < p.head_dim)  // a padded head dimension stops early
-          *reinterpret_cast<uint32_t*>(orow + dn * 8 + 2 * t) = v;
-      }
-      if (t == 0) {
-        const int64_t li = varlen ? static_cast<int64_t>(h) * p.seq.seqlen_q + si.q_start + row
-                                  : (static_cast<int64_t>(b) * p.h_q + h) * p.seq.seqlen_q + row;
-        p.lse[li] = lse[r];
-      }
-    }
-  }
+  r.n_end = max(n_end, r.n_start);
+  return r;
 }
 
-template <typename T, int D>
-cudaError_t launch_fwd_t(const FwdParams& p, cudaStream_t stream) {
-  constexpr int LD = D + 8;
-  const size_t smem = static_cast<size_t>(5) * kBM * LD * sizeof(T);
+template <typename T, int D, bool kCap>
+__global__ void __launch_bounds__(kFThreads, 1)
+    fwd_kernel(const FwdParams p, const __grid_constant__ CUtensorMap tmQ,
+               const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV) {
+  using L = FSmem<D>;
+  extern __shared__ __align__(1024) unsigned char smem[];
+  if (p.input_bad != nullptr && *p.input_bad) return;
+  const uint32_t sb = smem_u32(smem);
+  if (sb & 1023u) {  // 128-byte swizzled tiles need a 1024-byte aligned base
+    if (threadIdx.x == 0) atomicCAS(p.status, 0u, 0xA2100000u);
+    return;
+  }
+  auto bar = [&](uint32_t i) -> uint32_t { return sb + L::kBar + i * 8; };
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kAbort);
+  const WaitCtl ctl{abort_flag, p.status, p.timeout_ns};
+  const uint32_t warp = warp_id();
+  const uint32_t lane = lane_id();
+  const int G = p.h_q / p.h_k;
+  const bool varlen = p.seq.cu_q != nullptr;
+  const int n_mt = ceil_div(p.max_seqlen_q, FBM);
+  const int num_units = n_mt * p.seq.batch * p.h_q;
+  constexpr int kIsBf16 = Pack<T>::kIsBf16;
+
+  if (threadIdx.x == 0) {
+    *abort_flag = 0;
+    for (int s = 0; s < kQSt; ++s) {
+      mbar_init(bar(F_QFULL + s), 1);
+      mbar_init(bar(F_QEMPTY + s), 1);
+    }
+    for (int s = 0; s < kKSt; ++s) {
+      mbar_init(bar(F_KFULL + s), 1);
+      mbar_init(bar(F_KEMPTY + s), 1);
+    }
+    for (int s = 0; s < kVSt; ++s) {
+      mbar_init(bar(F_VFULL + s), 1);
+      mbar_init(bar(F_VEMPTY + s), 1);
+    }
+    for (int s = 0; s < kSBufs; ++s) {
+      mbar_init(bar(F_SFULL + s), 1);
+      mbar_init(bar(F_PREADY + s), 4);
+      mbar_init(bar(F_PVDONE + s), 1);
+    }
+    mbar_init(bar(F_OFULL), 1);
+    mbar_init(bar(F_FINAL), 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    fence_proxy_async_smem();
+  }
+  if (warp == 2) {
+    tmem_alloc(sb + L::kTmemSlot, kFTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + L::kTmemSlot);
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      prefetch_tmap(&tmQ);
+      prefetch_tmap(&tmK);
+      prefetch_tmap(&tmV);
+      uint32_t qc = 0, kc = 0, vc = 0;  // Q, K and V tiles whose loads were issued
+      bool stop = false;
+      for (int u = blockIdx.x; u < num_units && !stop; u += gridDim.x) {
+        const FUnit un = fwd_unit(p, u, n_mt);
+        if (!un.active || un.n_end == un.n_start) continue;
+        const int bq = varlen ? 0 : un.b;
+        const int hk = un.h / G;
+        {
+          const uint32_t s = qc % kQSt, use = qc / kQSt;
+          if (use > 0 && !wait1(bar(F_QEMPTY + s), (use - 1) & 1, ctl, 0xA2000001u)) break;
+          mbar_expect_tx(bar(F_QFULL + s), L::kTile);
+#pragma unroll
+          for (int c = 0; c < D / 64; ++c)
+            tma_load_4d(sb + L::kQ + s * L::kTile + c * kFChunk, &tmQ, bar(F_QFULL + s), c * 64,
+                        un.si.q_start + un.m * FBM, un.h, bq);
+          ++qc;
+        }
+        for (int n = un.n_start; n < un.n_end; ++n) {
+          const int krow = un.si.k_start + n * FBN;
+          const uint32_t ks = kc % kKSt, kuse = kc / kKSt;
+          if (kuse > 0 && !wait1(bar(F_KEMPTY + ks), (kuse - 1) & 1, ctl, 0xA2000002u)) {
+            stop = true;
+            break;
+          }
+          mbar_expect_tx(bar(F_KFULL + ks), L::kTile);
+#pragma unroll
+          for (int c = 0; c < D / 64; ++c)
+            tma_load_4d(sb + L::kK + ks * L::kTile + c * kFChunk, &tmK, bar(F_KFULL + ks), c * 64,
+                        krow, hk, bq);
+          ++kc;
+          const uint32_t vs = vc % kVSt, vuse = vc / kVSt;
+          if (vuse > 0 && !wait1(bar(F_VEMPTY + vs), (vuse - 1) & 1, ctl, 0xA2000003u)) {
+            stop = true;
+            break;
+          }
+          mbar_expect_tx(bar(F_VFULL + vs), L::kTile);
+#pragma unroll
+          for (int c = 0; c < D / 64; ++c)
+            tma_load_4d(sb + L::kV + vs * L::kTile + c * kFChunk, &tmV, bar(F_VFULL + vs), c * 64,
+                        krow, hk, bq);
+          ++vc;
+        }
+        if (*abort_flag) break;
+      }
+      // Before exit, wait (bounded, ignoring the abort flag) until every copy this
+      // thread issued has landed, so no TMA write targets a finished CTA.  Only the
+      // last issue into each stage can be outstanding: an earlier one was consumed
+      // (its stage released) before the stage was refilled.
+      for (uint32_t i = qc > kQSt ? qc - kQSt : 0; i < qc; ++i)
+        wait1(bar(F_QFULL + i % kQSt), (i / kQSt) & 1, ctl, 0xA2000004u, false);
+      for (uint32_t i = kc > kKSt ? kc - kKSt : 0; i < kc; ++i)
+        wait1(bar(F_KFULL + i % kKSt), (i / kKSt) & 1, ctl, 0xA2000005u, false);
+      for (uint32_t i = vc > kVSt ? vc - kVSt : 0; i < vc; ++i)
+        wait1(bar(F_VFULL + i % kVSt), (i / kVSt) & 1, ctl, 0xA2000006u, false);
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t kIdS = idesc_f16(kIsBf16, 0, 0, FBM, FBN);  // Q, K both K-major
+      constexpr uint32_t kIdPV = idesc_f16(kIsBf16, 0, 1, FBM, D);   // P from TMEM, V MN-major
+      uint32_t qc = 0, kc = 0, it = 0;  // Q tiles, K/V tiles, S tiles (= P tiles)
+      // O += P V of tile `t` (global S-tile index), whose V is K/V tile `kt`
+      auto issue_pv = [&](uint32_t t, uint32_t kt, bool first) -> bool {
+        const uint32_t buf = t % kSBufs;
+        const uint32_t vs = kt % kVSt;
+        if (!wait1(bar(F_PREADY + buf), (t / kSBufs) & 1, ctl, 0xA2000011u)) return false;
+        if (!wait1(bar(F_VFULL + vs), (kt / kVSt) & 1, ctl, 0xA2000012u)) return false;
+        tc_fence_after();
+        const uint32_t sV = sb + L::kV + vs * L::kTile;
+#pragma unroll
+        for (int kk = 0; kk < FBN / 16; ++kk)
+          mma_ts(tmem + TF_O, tmem + TF_S + buf * 128 + kk * 8,
+                 sdesc_sw128(sV + kk * 2048, kFChunk, 1024), kIdPV, (!first || kk > 0) ? 1u : 0u);
+        tc_commit(bar(F_PVDONE + buf));
+        tc_commit(bar(F_VEMPTY + vs));
+        return true;
+      };
+      for (int u = blockIdx.x; u < num_units; u += gridDim.x) {
+        const FUnit un = fwd_unit(p, u, n_mt);
+        if (!un.active || un.n_end == un.n_start) continue;
+        const int nt = un.n_end - un.n_start;
+        const uint32_t qs = qc % kQSt;
+        if (!wait1(bar(F_QFULL + qs), (qc / kQSt) & 1, ctl, 0xA2000013u)) goto mma_exit;
+        const uint32_t sQ = sb + L::kQ + qs * L::kTile;
+        for (int j = 0; j < nt; ++j) {
+          const uint32_t t = it + j, kt = kc + j;
+          const uint32_t buf = t % kSBufs, ks = kt % kKSt;
+          // S buffer `buf` last held tile t - 3, whose O += P V must have read its P
+          if (t >= kSBufs &&
+              !wait1(bar(F_PVDONE + buf), ((t - kSBufs) / kSBufs) & 1, ctl, 0xA2000014u))
+            goto mma_exit;
+          if (!wait1(bar(F_KFULL + ks), (kt / kKSt) & 1, ctl, 0xA2000015u)) goto mma_exit;
+          tc_fence_after();
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t koff = (kk >> 2) * kFChunk + (kk & 3) * 32;
+            mma_ss(tmem + TF_S + buf * 128, sdesc_sw128(sQ + koff, 16, 1024),
+                   sdesc_sw128(sb + L::kK + ks * L::kTile + koff, 16, 1024), kIdS, kk > 0);
+          }
+          tc_commit(bar(F_SFULL + buf));
+          tc_commit(bar(F_KEMPTY + ks));
+          if (j == nt - 1) tc_commit(bar(F_QEMPTY + qs));
+          if (j > 0 && !issue_pv(t - 1, kt - 1, j == 1)) goto mma_exit;
+        }
+        if (!issue_pv(it + nt - 1, kc + nt - 1, nt == 1)) goto mma_exit;
+        tc_commit(bar(F_OFULL));
+        it += nt;
+        kc += nt;
+        ++qc;
+      }
+    mma_exit:
+      // make sure no MMA is still running before TMEM is released
+      tc_commit(bar(F_FINAL));
+      wait1(bar(F_FINAL), 0, ctl, 0xA200001Fu, false);
+    }
+  } else if (warp >= 4) {
+    // ------------------------------------------------------- softmax / epilogue
+    const uint32_t quad = warp & 3;
+    const int row = static_cast<int>(quad * 32 + lane);  // query row within the tile
+    const uint32_t tl = tmem + ((quad * 32) << 16);     // this warp's TMEM lanes
+    // logits in log2 units: x * mul with x the raw score (kCap: already in log2 units).
+    // A nonpositive scale is multiplied in first, so the running maximum is taken
+    // over the final logits either way.
+    const bool pre_scale = !kCap && !(p.scale_log2 > 0.f);
+    const float mul = (kCap || pre_scale) ? 1.f : p.scale_log2;
+    uint32_t it = 0, uc = 0;
+    for (int u = blockIdx.x; u < num_units; u += gridDim.x) {
+      const FUnit un = fwd_unit(p, u, n_mt);
+      if (!un.active) continue;
+      const int m0 = un.m * FBM;
+      const int qi = m0 + row;  // query index within the sequence
+      const bool row_ok = qi < un.si.sq;
+      const int off = un.si.sk - un.si.sq;
+      const int nt = un.n_end - un.n_start;
+      float m_ref = -INFINITY, lsum = 0.f;
+      for (int j = 0; j < nt; ++j, ++it) {
+        const int n = un.n_start + j;
+        const uint32_t buf = it % kSBufs;
+        const uint32_t sbase = TF_S + buf * 128;
+        const int k0 = n * FBN;
+        const bool need_mask =
+            (k0 + FBN > un.si.sk) ||
+            (p.win_right >= 0 && k0 + FBN - 1 > m0 + off + p.win_right) ||
+            (p.win_left >= 0 && k0 < m0 + FBM - 1 + off - p.win_left);
+        // allowed keys of this row, in tile column coordinates: lo <= c < hi
+        int lo = 0, hi = min(FBN, un.si.sk - k0);
+        if (p.win_right >= 0) hi = min(hi, qi + off + p.win_right - k0 + 1);
+        if (p.win_left >= 0) lo = max(0, qi + off - p.win_left - k0);
+        if (!wait_warp(bar(F_SFULL + buf), (it / kSBufs) & 1, ctl, 0xA2000021u)) goto done;
+        tc_fence_after();
+        float x[FBN];
+        {
+          uint32_t sv[FBN];
+#pragma unroll
+          for (int c = 0; c < FBN / 32; ++c) tmem_ld32p(tl + sbase + 32 * c, sv + 32 * c);
+          tmem_wait_ld();
+#pragma unroll
+          for (int c = 0; c < FBN; ++c) x[c] = __uint_as_float(sv[c]);
+        }
+        if (kCap) {
+#pragma unroll
+          for (int c = 0; c < FBN; ++c) x[c] = tanh_exp(x[c] * p.cap_in) * p.cap_out;
+        } else if (pre_scale) {
+#pragma unroll
+          for (int c = 0; c < FBN; ++c) x[c] *= p.scale_log2;
+        }
+        if (need_mask) {
+#pragma unroll
+          for (int c = 0; c < FBN; ++c) x[c] = (c >= lo && c < hi) ? x[c] : -INFINITY;
+        }
+        float mx[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) mx[e] = x[e];
+#pragma unroll
+        for (int c = 8; c < FBN; ++c) mx[c & 7] = fmaxf(mx[c & 7], x[c]);
+        const float tmax =
+            fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                  fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7]))) * mul;
+        // move the reference only when the maximum rose by more than 2^8
+        const bool grow = tmax > m_ref + kRescaleLog2;  // false for tmax = -inf
+        const bool had_ref = m_ref != -INFINITY;
+        const float alpha = grow ? (had_ref ? ex2(m_ref - tmax) : 0.f) : 1.f;
+        if (grow) m_ref = tmax;
+        lsum *= alpha;
+        // O holds earlier tiles' P V under the old reference: rescale it (rare)
+        const bool rescale = grow && had_ref && j > 0;
+        if (__any_sync(0xffffffffu, rescale)) {
+          const uint32_t pt = it - 1;  // the previous tile's O += P V must have landed
+          if (!wait_warp(bar(F_PVDONE + pt % kSBufs), (pt / kSBufs) & 1, ctl, 0xA2000022u))
+            goto done;
+          tc_fence_after();
+#pragma unroll 1
+          for (int c = 0; c < D / 32; ++c) {
+            uint32_t o[32];
+            tmem_ld32(tl + TF_O + 32 * c, o);
+            tmem_wait_ld();
+#pragma unroll
+            for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+            tmem_st16(tl + TF_O + 32 * c, *reinterpret_cast<uint32_t(*)[16]>(o));
+            tmem_st16(tl + TF_O + 32 * c + 16, *reinterpret_cast<uint32_t(*)[16]>(o + 16));
+          }
+          tmem_wait_st();
+        }
+        const float m_use = m_ref == -INFINITY ? 0.f : m_ref;
+        float ls[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int c16 = 0; c16 < FBN / 32; ++c16) {
+          uint32_t pk[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            const float p0 = ex2(fmaf(x[32 * c16 + 2 * e], mul, -m_use));
+            const float p1 = ex2(fmaf(x[32 * c16 + 2 * e + 1], mul, -m_use));
+            ls[e & 3] += p0 + p1;
+            pk[e] = Pack<T>::two(p0, p1);
+          }
+          tmem_st16(tl + sbase + 16 * c16, pk);
+        }
+        lsum += (ls[0] + ls[1]) + (ls[2] + ls[3]);
+        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(F_PREADY + buf));
+      }
+      // ---- epilogue: O / l and the LSE of this row
+      {
+        T* orow = static_cast<T*>(const_cast<void*>(p.o.ptr)) + (varlen ? 0 : un.b * p.o.sb) +
+                  static_cast<int64_t>(un.si.q_start + qi) * p.o.ss +
+                  static_cast<int64_t>(un.h) * p.o.sh;
+        const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
+        if (nt > 0) {
+          if (!wait_warp(bar(F_OFULL), uc & 1, ctl, 0xA2000023u)) goto done;
+          tc_fence_after();
+#pragma unroll 1
+          for (int c = 0; c < D / 32; ++c) {
+            uint32_t o[32];
+            tmem_ld32(tl + TF_O + 32 * c, o);
+            tmem_wait_ld();
+            if (row_ok) {
+#pragma unroll
+              for (int q = 0; q < 4; ++q) {
+                uint4 v;
+                v.x = Pack<T>::two(__uint_as_float(o[8 * q + 0]) * inv,
+                                   __uint_as_float(o[8 * q + 1]) * inv);
+                v.y = Pack<T>::two(__uint_as_float(o[8 * q + 2]) * inv,
+                                   __uint_as_float(o[8 * q + 3]) * inv);
+                v.z = Pack<T>::two(__uint_as_float(o[8 * q + 4]) * inv,
+                                   __uint_as_float(o[8 * q + 5]) * inv);
+                v.w = Pack<T>::two(__uint_as_float(o[8 * q + 6]) * inv,
+                                   __uint_as_float(o[8 * q + 7]) * inv);
+                if (32 * c + 8 * q < p.head_dim)  // a padded head dimension stops early
+                  reinterpret_cast<uint4*>(orow + 32 * c)[q] = v;
+              }
+            }
+          }
+          tc_fence_before();
+          ++uc;
+        } else if (row_ok) {  // no key tile at all: O = 0
+#pragma unroll
+          for (int c = 0; c < D / 8; ++c)
+            if (8 * c < p.head_dim) reinterpret_cast<uint4*>(orow)[c] = make_uint4(0, 0, 0, 0);
+        }
+        if (row_ok) {
+          const int64_t li =
+              varlen ? static_cast<int64_t>(un.h) * p.seq.seqlen_q + un.si.q_start + qi
+                      : (static_cast<int64_t>(un.b) * p.h_q + un.h) * p.seq.seqlen_q + qi;
+          // natural log: (m_ref + log2 l) * ln 2; a row without an allowed key: +inf
+          p.lse[li] = lsum > 0.f ? (m_ref + __log2f(lsum)) * 0.6931471805599453f : INFINITY;
+        }
+      }
+    }
+  }
+
+done:
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 2) tmem_dealloc(tmem, kFTmemCols);
+}
+
+template <typename T, int D, bool kCap>
+cudaError_t launch_fwd_t(const FwdParams& p, int dtype, cudaStream_t stream) {
+  const bool varlen = p.seq.cu_q != nullptr;
+  const int nb = varlen ? 1 : p.seq.batch;
+  CUtensorMap tq, tk, tv;
+  // the maps span the logical head dimension: columns up to D read as zero
+  const int d = p.head_dim;
+  if (!encode_tmap_bshd(&tq, p.q, dtype, p.seq.seqlen_q, p.h_q, nb, d, FBM) ||
+      !encode_tmap_bshd(&tk, p.k, dtype, p.seq.seqlen_k, p.h_k, nb, d, FBN) ||
+      !encode_tmap_bshd(&tv, p.v, dtype, p.seq.seqlen_k, p.h_k, nb, d, FBN))
+    return cudaErrorInvalidValue;
+  // Every CTA allocates all 512 TMEM columns, so two CTAs on one SM would
+  // serialise in the allocator: the launch reserves enough shared memory (the
+  // D = 128 layout's) to keep one CTA per SM at any head dimension.
+  constexpr uint32_t smem =
+      FSmem<D>::kTotal > FSmem<128>::kTotal ? FSmem<D>::kTotal : FSmem<128>::kTotal;
   // Kernel attributes are per device: set them once on each.
   constexpr int kMaxDevices = 64;
   static std::atomic<bool> attr_done[kMaxDevices];
@@ -285,26 +474,33 @@ cudaError_t launch_fwd_t(const FwdParams& p, cudaStream_t stream) {
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
     return cudaErrorInvalidDevice;
   if (!attr_done[dev].load(std::memory_order_acquire)) {
-    cudaError_t e = cudaFuncSetAttribute(fwd_kernel<T, D>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(smem));
+    const cudaError_t e = cudaFuncSetAttribute(fwd_kernel<T, D, kCap>,
+                                               cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     attr_done[dev].store(true, std::memory_order_release);
   }
-  dim3 grid(ceil_div(p.max_seqlen_q, kBM), p.h_q, p.seq.batch);
-  fwd_kernel<T, D><<<grid, kFwdThreads, smem, stream>>>(p);
+  const int units = ceil_div(p.max_seqlen_q, FBM) * p.seq.batch * p.h_q;
+  if (units <= 0) return cudaSuccess;
+  const int grid = units < num_sms() ? units : num_sms();
+  fwd_kernel<T, D, kCap><<<grid, kFThreads, smem, stream>>>(p, tq, tk, tv);
   return cudaGetLastError();
+}
+
+template <bool kCap>
+cudaError_t launch_fwd_cap(const FwdParams& p, int dtype, cudaStream_t stream) {
+  const bool d64 = pad_head_dim(p.head_dim) == 64;
+  if (dtype == 1)
+    return d64 ? launch_fwd_t<__nv_bfloat16, 64, kCap>(p, dtype, stream)
+               : launch_fwd_t<__nv_bfloat16, 128, kCap>(p, dtype, stream);
+  return d64 ? launch_fwd_t<__half, 64, kCap>(p, dtype, stream)
+             : launch_fwd_t<__half, 128, kCap>(p, dtype, stream);
 }
 
 }  // namespace
 
 cudaError_t launch_fwd(const FwdParams& p, int dtype, cudaStream_t stream) {
-  if (dtype == 1) {
-    return pad_head_dim(p.head_dim) == 64 ? launch_fwd_t<__nv_bfloat16, 64>(p, stream)
-                                          : launch_fwd_t<__nv_bfloat16, 128>(p, stream);
-  }
-  return pad_head_dim(p.head_dim) == 64 ? launch_fwd_t<__half, 64>(p, stream)
-                                        : launch_fwd_t<__half, 128>(p, stream);
+  return p.softcap > 0.f ? launch_fwd_cap<true>(p, dtype, stream)
+                         : launch_fwd_cap<false>(p, dtype, stream);
 }
 
 }  // namespace attn

@@ -67,6 +67,8 @@ struct FwdParams {
   float softcap, cap_in, cap_out;  // logit cap as in BwdParams (0 = off)
   int max_seqlen_q;
   const unsigned int* input_bad;
+  unsigned int* status;            // device status word (bounded waits that gave up)
+  unsigned long long timeout_ns;   // limit of every device-side wait
 };
 
 // Workspace layout (byte offsets), identical on host and device.

@@ -6,10 +6,12 @@ O and LSE come from this library's forward.  One step = one attn_bwd call
 (preprocess + main + postprocess kernels) over that batch.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                  [--workload NAME] [--deterministic]
+                  [--workload NAME] [--deterministic] [--pass bwd|fwd]
 
 Metric: backward TFLOPS = 2.5 * 4 * B * H_q * Sq * Sk * D / t, halved for
-causal.  Prints one JSON line (rank 0).  Multi-GPU runs (torchrun) are
+causal.  ``--pass fwd`` times the forward (attn_fwd: O and LSE) on the same
+workload instead, at 4 * B * H_q * Sq * Sk * D FLOPs (halved for causal).
+Prints one JSON line (rank 0).  Multi-GPU runs (torchrun) are
 independent replicas, one per GPU; value = total FLOPs of all ranks / the
 slowest rank's time.  `--impl reference` times the fp64 CPU oracle on a
 bounded sample of the same workload on this host's cores.
@@ -35,6 +37,7 @@ from attention_backward_bwd_gb300 import synth  # noqa: E402
 
 DEFAULT_WORKLOAD = "gqa_b2_hq32_hk8_s8192_d128_bf16_causal"
 METRIC = "attention-backward TFLOPS (bf16, 1xGB300) and % of dense tensor-core peak"
+METRIC_FWD = "attention-forward TFLOPS (bf16, 1xGB300) and % of dense tensor-core peak"
 L2_BYTES = 129 * 2 ** 20
 
 
@@ -349,6 +352,111 @@ def run_ours(args):
         dist.destroy_process_group()
 
 
+def run_ours_fwd(args):
+    """The forward (attn_fwd) of the workload: O and the natural-log LSE."""
+    import attention_backward_bwd_gb300 as ab
+    rank, world, local, dist = dist_setup(args.gpus)
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    w = synth.WORKLOADS[args.workload]
+    x = synth.make_inputs(w)
+    mq = mk = max(x.lengths) if w.varlen else None
+    cu_q = x.cu_seqlens_q.to(dev) if w.varlen else None
+    cu_k = x.cu_seqlens_k.to(dev) if w.varlen else None
+    q, k, v = (t.to(dev) for t in (x.q, x.k, x.v))
+    window = tuple(w.window) if w.windowed else None
+    o = torch.empty_like(q)
+    lse_shape = (q.shape[1], q.shape[0]) if w.varlen else (q.shape[0], q.shape[2], q.shape[1])
+    lse = torch.empty(lse_shape, dtype=torch.float32, device=dev)
+    kw = dict(causal=w.causal, cu_seqlens_q=cu_q, cu_seqlens_k=cu_k, max_seqlen_q=mq,
+              max_seqlen_k=mk, window=window, softcap=w.softcap, out=o, lse=lse)
+    stream = torch.cuda.current_stream()
+    flops = bwd_flops(w, x.lengths) / 2.5
+    in_bytes = sum(t.numel() * t.element_size() for t in (q, k, v))
+
+    def step():
+        ab.attn_fwd(q, k, v, stream=stream, **kw)
+
+    for _ in range(args.warmup):
+        step()
+    ab.check_device_status()
+    barrier(dist)
+    with ClockSampler(local) as clk:
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.steps):
+            step()
+        e1.record(stream)
+        barrier(dist)
+    ab.check_device_status()
+    ms = e0.elapsed_time(e1) / args.steps
+    ms_max = max_over_ranks(ms, dist)
+
+    # end to end: pinned host Q, K, V -> device -> attn_fwd -> pinned host O, LSE
+    hq_ = [t.cpu().pin_memory() for t in (q, k, v)]
+    ho, hl = torch.empty(o.shape, dtype=o.dtype, pin_memory=True), torch.empty(
+        lse.shape, dtype=lse.dtype, pin_memory=True)
+    dq_, dk_, dv_ = (torch.empty_like(t) for t in (q, k, v))
+    h2d = sum(t.numel() * t.element_size() for t in hq_)
+    d2h = ho.numel() * ho.element_size() + hl.numel() * hl.element_size()
+
+    def e2e_step():
+        for dst, src in zip((dq_, dk_, dv_), hq_):
+            dst.copy_(src, non_blocking=True)
+        ab.attn_fwd(dq_, dk_, dv_, stream=stream, **kw)
+        ho.copy_(o, non_blocking=True)
+        hl.copy_(lse, non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    barrier(dist)
+    n_e2e = max(2, args.steps // 2)
+    a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a0.record(stream)
+    for _ in range(n_e2e):
+        e2e_step()
+    a1.record(stream)
+    barrier(dist)
+    e2e_ms = max_over_ranks(a0.elapsed_time(a1) / n_e2e, dist)
+    if rank != 0:
+        if dist is not None:
+            dist.destroy_process_group()
+        return
+    peaks = measured_peaks()
+    achieved = flops / (ms * 1e-3) / 1e12
+    peak = peaks["bf16_tflops"]
+    value = replica_value(flops, ms_max, world)
+    cfg = {"workload": w.name, "pass": "forward", "batch": w.batch if not w.varlen else len(x.lengths),
+           "h_q": w.h_q, "h_k": w.h_k, "seqlen": w.seqlen_q if not w.varlen else "varlen",
+           "head_dim": w.head_dim, "causal": w.causal,
+           "l2": "inputs larger than L2 (%.0f MB resident per step)" % (in_bytes / 1e6),
+           "parallelism": f"replicas x{world}" if world > 1 else "single GPU"}
+    if w.varlen:
+        cfg["lengths"] = x.lengths
+    if w.softcap:
+        cfg["softcap"] = w.softcap
+    if w.windowed:
+        cfg["window"] = list(w.window)
+    out = {
+        "metric": METRIC_FWD, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_max, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": w.dtype,
+        "data": "synthetic N(0,1), seeded", "config": cfg,
+        "pct_of_peak": round(100.0 * value / world / peak, 2),
+        "roofline": {"bound": "tensor", "kernel": "fwd_kernel", "achieved": round(achieved, 2),
+                     "peak": peak, "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
+                     "peak_src": "bf16 burst, of " + peaks["src"], "traffic": None},
+        "e2e": {"value": round(world * flops / (e2e_ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
+                "ms_per_step": round(e2e_ms, 3), "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "path": "pinned copies + attn_fwd"},
+        "gpu_launches": (2 if w.varlen else 1) * args.steps,
+        "clocks": clk.summary(),
+    }
+    print(json.dumps(out))
+    if dist is not None:
+        dist.destroy_process_group()
+
+
 def _cores():
     try:
         return len(os.sched_getaffinity(0))
@@ -454,6 +562,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(synth.WORKLOADS))
     ap.add_argument("--deterministic", action="store_true")
+    ap.add_argument("--pass", dest="pass_", default="bwd", choices=["bwd", "fwd"],
+                    help="bwd: the backward (default); fwd: the forward that makes O and LSE")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=20.0)
     ap.add_argument("--chunks", type=int, default=0,
@@ -462,6 +572,8 @@ def main():
     args.warmup = max(args.warmup, 3)
     if args.impl == "reference":
         run_reference(args)
+    elif args.pass_ == "fwd":
+        run_ours_fwd(args)
     else:
         run_ours(args)
 
