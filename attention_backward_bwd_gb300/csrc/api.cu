@@ -169,8 +169,8 @@ int check_common(int dtype, int batch, int seqlen_q, int seqlen_k, int h_q, int 
                  int max_seqlen_q, int max_seqlen_k) {
   if (dtype != ATTN_FP16 && dtype != ATTN_BF16)
     return fail(ATTN_ERR_DTYPE, "dtype must be ATTN_FP16 (0) or ATTN_BF16 (1), got %d", dtype);
-  if (head_dim < 8 || head_dim > 128 || head_dim % 8 != 0)
-    return fail(ATTN_ERR_SHAPE, "head_dim must be a multiple of 8 in [8, 128], got %d", head_dim);
+  if (head_dim < 8 || head_dim > 256 || head_dim % 8 != 0)
+    return fail(ATTN_ERR_SHAPE, "head_dim must be a multiple of 8 in [8, 256], got %d", head_dim);
   if (batch <= 0) return fail(ATTN_ERR_SHAPE, "batch must be positive, got %d", batch);
   if (h_q <= 0 || h_k <= 0 || h_q % h_k != 0)
     return fail(ATTN_ERR_SHAPE, "h_q (%d) must be a positive multiple of h_k (%d)", h_q, h_k);
@@ -323,7 +323,8 @@ int run_stages(int stages, const Prepared& pr, cudaStream_t stream) {
     if (e != cudaSuccess) return cuda_fail(e, "preprocess launch");
   }
   if (stages & kMain) {
-    e = launch_bwd_main(p, pr.dtype, stream);
+    e = pad_head_dim(p.head_dim) > 128 ? launch_bwd_wide(p, pr.dtype, stream)
+                                       : launch_bwd_main(p, pr.dtype, stream);
     if (e == cudaErrorInvalidValue)
       return fail(ATTN_ERR_CUDA, "main kernel: TMA descriptor encoding or launch failed");
     if (e != cudaSuccess) return cuda_fail(e, "main kernel launch");

@@ -44,6 +44,7 @@
 // the site in the status word and unwinds.
 #include <atomic>
 
+#include "bwd_units.cuh"
 #include "common.cuh"
 
 namespace attn {
@@ -122,51 +123,6 @@ struct Smem {
   static constexpr uint32_t kTotal = kAbort + 4;
 };
 static_assert(Smem<128>::kTotal <= 232448, "shared memory budget");
-
-struct Unit {
-  int n, g, b;
-  SeqInfo si;
-  int m_start, m_count, n_iters;
-  bool has_keys;
-};
-
-// win_left: the left window side (-1 = none; a compile-time -1 in the
-// instantiation without a left window), win_right: p.win_right.
-__device__ __forceinline__ Unit get_unit(const BwdParams& p, int u, int G, int win_left) {
-  Unit r;
-  const int per_n = p.seq.batch * p.h_k;
-  r.n = u / per_n;
-  const int rem = u - r.n * per_n;
-  r.b = rem / p.h_k;
-  r.g = rem - r.b * p.h_k;
-  r.si = seq_info(p.seq, r.b);
-  r.has_keys = r.n * BN < r.si.sk;
-  // query tiles holding a query that sees a key of this tile (all of them
-  // without a mask; causal or a window narrows the range)
-  const int k1 = min(r.n * BN + BN, r.si.sk);
-  int lo, hi;
-  window_queries(r.n * BN, k1, r.si.sq, r.si.sk, win_left, p.win_right, lo, hi);
-  r.m_start = lo / BM;
-  r.m_count = lo < hi ? ceil_div(hi, BM) - r.m_start : 0;
-  r.n_iters = r.has_keys ? G * r.m_count : 0;
-  return r;
-}
-
-// Iteration j of a unit -> (query head h, query tile m), heads of the group
-// innermost.  Query tiles run from the last to the first, so every CTA working
-// on the same (sequence, kv head) reads the same Q/dO tile at about the same
-// time (the causal start tile only shortens the tail) and those tiles are
-// served from L2 instead of being streamed from HBM once per key tile.  The
-// same order serves deterministic mode: key tiles that start together meet
-// each query tile together, so key tile n trails key tile n-1 only by the
-// latency of one ordered add.  (First to last would put key tile n one query
-// tile ahead of key tile n-1 from the start, a wait of G tiles per link of the
-// chain; measured 10 % slower.)
-__device__ __forceinline__ void iter_hm(const Unit& un, int j, int G, int& h, int& m) {
-  const int jm = j / G;
-  h = un.g * G + (j - jm * G);
-  m = un.m_start + un.m_count - 1 - jm;
-}
 
 template <typename T, int D, bool kCap, bool kLeft>
 __global__ void __launch_bounds__(kThreads, 1)

@@ -30,6 +30,10 @@
 //
 // TMEM columns (512 allocated): S buffers [0,128), [128,256), [256,384);
 // O [384, 384 + D).  Shared memory: 2 Q stages, 3 K stages, 2 V stages.
+// Head dimensions above 128 run on D = 256 tiles (extra columns zero): O takes
+// TMEM [256,512) next to two S buffers, the unit's Q tile (64 KiB) stays in
+// shared memory, and K and V stream through a ring of ten 64-column chunks
+// (K_t for S_t, then V_{t-1} for O += P V_{t-1}, in the MMA thread's order).
 #include <atomic>
 
 #include "common.cuh"
@@ -42,10 +46,19 @@ constexpr int FBM = 128;  // query tile
 constexpr int FBN = 128;  // key tile
 constexpr int kFThreads = 256;
 constexpr int kQSt = 2, kKSt = 3, kVSt = 2;
-constexpr int kSBufs = 3;
 constexpr uint32_t kFChunk = 128 * 128;  // one 64-column (128-byte) slice of a 128-row tile
 constexpr uint32_t kFTmemCols = 512;
-constexpr uint32_t TF_S = 0, TF_O = 384;
+constexpr uint32_t TF_S = 0;
+constexpr int kFRing = 10;  // chunk slots of the D = 256 layout (even: chunk pairs never wrap)
+
+// Per head-dimension layout: three S buffers and O at column 384 up to D = 128;
+// two S buffers and O at column 256 for the D = 256 tiles.
+template <int D>
+struct FCfg {
+  static constexpr bool kWide = D > 128;
+  static constexpr int kSBufs = kWide ? 2 : 3;
+  static constexpr uint32_t kO = kWide ? 256 : 384;
+};
 constexpr float kRescaleLog2 = 8.f;  // P stays below 2^8 between rescales
 
 enum FBar : uint32_t {
@@ -55,26 +68,30 @@ enum FBar : uint32_t {
   F_KEMPTY = F_KFULL + kKSt,
   F_VFULL = F_KEMPTY + kKSt,
   F_VEMPTY = F_VFULL + kVSt,
-  F_SFULL = F_VEMPTY + kVSt,    // per S buffer: S computed
-  F_PREADY = F_SFULL + kSBufs,  // per S buffer: P written over it (4 softmax warps)
-  F_PVDONE = F_PREADY + kSBufs, // per S buffer: O += P V has read it
-  F_OFULL = F_PVDONE + kSBufs,  // the unit's last O += P V done
+  F_SFULL = F_VEMPTY + kVSt,    // per S buffer (up to 3): S computed
+  F_PREADY = F_SFULL + 3,       // per S buffer: P written over it (4 softmax warps)
+  F_PVDONE = F_PREADY + 3,      // per S buffer: O += P V has read it
+  F_OFULL = F_PVDONE + 3,       // the unit's last O += P V done
   F_FINAL,
-  F_COUNT
+  F_RFULL,                      // D = 256: chunk ring slots
+  F_REMPTY = F_RFULL + kFRing,
+  F_COUNT = F_REMPTY + kFRing
 };
 
 template <int D>
 struct FSmem {
   static constexpr uint32_t kTile = (D / 64) * kFChunk;
   static constexpr uint32_t kQ = 0;
-  static constexpr uint32_t kK = kQ + kQSt * kTile;
+  // up to D = 128: Q, K and V stages; D = 256: one Q tile and the chunk ring at kK
+  static constexpr uint32_t kK = kQ + (FCfg<D>::kWide ? 1 : kQSt) * kTile;
   static constexpr uint32_t kV = kK + kKSt * kTile;
-  static constexpr uint32_t kBar = kV + kVSt * kTile;
+  static constexpr uint32_t kBar = FCfg<D>::kWide ? kK + kFRing * kFChunk : kV + kVSt * kTile;
   static constexpr uint32_t kTmemSlot = kBar + F_COUNT * 8;
   static constexpr uint32_t kAbort = kTmemSlot + 4;
   static constexpr uint32_t kTotal = kAbort + 4;
 };
 static_assert(FSmem<128>::kTotal <= 232448, "shared memory budget");
+static_assert(FSmem<256>::kTotal <= 232448, "shared memory budget (D = 256)");
 
 struct FUnit {
   int m, h, b;
@@ -115,6 +132,9 @@ __global__ void __launch_bounds__(kFThreads, 1)
     fwd_kernel(const FwdParams p, const __grid_constant__ CUtensorMap tmQ,
                const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV) {
   using L = FSmem<D>;
+  constexpr bool kWide = FCfg<D>::kWide;
+  constexpr int kSBufs = FCfg<D>::kSBufs;
+  constexpr uint32_t TF_O = FCfg<D>::kO;
   extern __shared__ __align__(1024) unsigned char smem[];
   if (p.input_bad != nullptr && *p.input_bad) return;
   const uint32_t sb = smem_u32(smem);
@@ -154,6 +174,10 @@ __global__ void __launch_bounds__(kFThreads, 1)
     }
     mbar_init(bar(F_OFULL), 1);
     mbar_init(bar(F_FINAL), 1);
+    for (int r = 0; r < kFRing; ++r) {
+      mbar_init(bar(F_RFULL + r), 1);
+      mbar_init(bar(F_REMPTY + r), 1);
+    }
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     fence_proxy_async_smem();
   }
@@ -168,7 +192,50 @@ __global__ void __launch_bounds__(kFThreads, 1)
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
-    if (lane == 0) {
+    if (lane == 0 && kWide) {
+      prefetch_tmap(&tmQ);
+      prefetch_tmap(&tmK);
+      prefetch_tmap(&tmV);
+      uint32_t qc = 0, q = 0;  // Q tiles and ring chunks whose loads were issued
+      bool stop = false;
+      // one 64-column chunk into the next ring slot
+      auto ring_load = [&](const CUtensorMap* map, int col, int row, int head, int bb) -> bool {
+        const uint32_t r = q % kFRing, use = q / kFRing;
+        if (use > 0 && !wait1(bar(F_REMPTY + r), (use - 1) & 1, ctl, 0xA2000007u)) return false;
+        mbar_expect_tx(bar(F_RFULL + r), kFChunk);
+        tma_load_4d(sb + L::kK + r * kFChunk, map, bar(F_RFULL + r), col, row, head, bb);
+        ++q;
+        return true;
+      };
+      for (int u = blockIdx.x; u < num_units && !stop; u += gridDim.x) {
+        const FUnit un = fwd_unit(p, u, n_mt);
+        if (!un.active || un.n_end == un.n_start) continue;
+        const int bq = varlen ? 0 : un.b;
+        const int hk = un.h / G;
+        if (qc > 0 && !wait1(bar(F_QEMPTY), (qc - 1) & 1, ctl, 0xA2000001u)) break;
+        mbar_expect_tx(bar(F_QFULL), L::kTile);
+#pragma unroll
+        for (int c = 0; c < D / 64; ++c)
+          tma_load_4d(sb + L::kQ + c * kFChunk, &tmQ, bar(F_QFULL), c * 64,
+                      un.si.q_start + un.m * FBM, un.h, bq);
+        ++qc;
+        // K_n for S_n, then V_{n-1} for O += P V_{n-1}: the MMA thread's order
+        for (int n = un.n_start; n < un.n_end && !stop; ++n) {
+          const int krow = un.si.k_start + n * FBN;
+          for (int c = 0; c < D / 64 && !stop; ++c) stop = !ring_load(&tmK, c * 64, krow, hk, bq);
+          for (int c = 0; c < D / 64 && !stop && n > un.n_start; ++c)
+            stop = !ring_load(&tmV, c * 64, krow - FBN, hk, bq);
+        }
+        const int klast = un.si.k_start + (un.n_end - 1) * FBN;
+        for (int c = 0; c < D / 64 && !stop; ++c) stop = !ring_load(&tmV, c * 64, klast, hk, bq);
+        if (*abort_flag) break;
+      }
+      // Before exit, wait (bounded, ignoring the abort flag) for the copies that may
+      // still be in flight: the last Q tile and the last issue into each ring slot.
+      if (qc > 0) wait1(bar(F_QFULL), (qc - 1) & 1, ctl, 0xA2000004u, false);
+      for (uint32_t i = q > static_cast<uint32_t>(kFRing) ? q - kFRing : 0; i < q; ++i)
+        wait1(bar(F_RFULL + i % kFRing), (i / kFRing) & 1, ctl, 0xA2000005u, false);
+    } else if (lane == 0) {
       prefetch_tmap(&tmQ);
       prefetch_tmap(&tmK);
       prefetch_tmap(&tmV);
@@ -229,9 +296,70 @@ __global__ void __launch_bounds__(kFThreads, 1)
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
+    if (lane == 0 && kWide) {
       constexpr uint32_t kIdS = idesc_f16(kIsBf16, 0, 0, FBM, FBN);  // Q, K both K-major
-      constexpr uint32_t kIdPV = idesc_f16(kIsBf16, 0, 1, FBM, D);   // P from TMEM, V MN-major
+      constexpr uint32_t kIdPV = idesc_f16(kIsBf16, 0, 1, FBM, 128);  // P from TMEM, V halves
+      uint32_t qc = 0, q = 0, it = 0;  // Q tiles, ring chunks consumed, S tiles
+      auto ring_wait = [&](uint32_t qq) -> bool {
+        return wait1(bar(F_RFULL + qq % kFRing), (qq / kFRing) & 1, ctl, 0xA2000016u);
+      };
+      auto slot = [&](uint32_t qq) -> uint32_t { return sb + L::kK + (qq % kFRing) * kFChunk; };
+      // O += P V of tile t: two N = 128 halves, B = V chunk pairs of the ring
+      auto issue_pv = [&](uint32_t t, bool first) -> bool {
+        const uint32_t buf = t % kSBufs;
+        if (!wait1(bar(F_PREADY + buf), (t / kSBufs) & 1, ctl, 0xA2000011u)) return false;
+        for (int pr = 0; pr < D / 128; ++pr) {
+          const uint32_t q0 = q + 2 * pr;
+          if (!ring_wait(q0) || !ring_wait(q0 + 1)) return false;
+          tc_fence_after();
+#pragma unroll
+          for (int kk = 0; kk < FBN / 16; ++kk)
+            mma_ts(tmem + TF_O + 128 * pr, tmem + TF_S + buf * 128 + kk * 8,
+                   sdesc_sw128(slot(q0) + kk * 2048, kFChunk, 1024), kIdPV,
+                   (!first || kk > 0) ? 1u : 0u);
+          tc_commit(bar(F_REMPTY + q0 % kFRing));
+          tc_commit(bar(F_REMPTY + (q0 + 1) % kFRing));
+        }
+        q += D / 64;
+        tc_commit(bar(F_PVDONE + buf));
+        return true;
+      };
+      for (int u = blockIdx.x; u < num_units; u += gridDim.x) {
+        const FUnit un = fwd_unit(p, u, n_mt);
+        if (!un.active || un.n_end == un.n_start) continue;
+        const int nt = un.n_end - un.n_start;
+        if (!wait1(bar(F_QFULL), qc & 1, ctl, 0xA2000013u)) goto mma_exit_w;
+        for (int j = 0; j < nt; ++j) {
+          const uint32_t t = it + j, buf = t % kSBufs;
+          // S buffer `buf` last held tile t - 2, whose O += P V must have read its P
+          if (t >= kSBufs &&
+              !wait1(bar(F_PVDONE + buf), ((t - kSBufs) / kSBufs) & 1, ctl, 0xA2000014u))
+            goto mma_exit_w;
+          for (int c = 0; c < D / 64; ++c, ++q) {
+            if (!ring_wait(q)) goto mma_exit_w;
+            tc_fence_after();
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+              mma_ss(tmem + TF_S + buf * 128, sdesc_sw128(sb + L::kQ + c * kFChunk + kk * 32, 16, 1024),
+                     sdesc_sw128(slot(q) + kk * 32, 16, 1024), kIdS, (c > 0 || kk > 0) ? 1u : 0u);
+            tc_commit(bar(F_REMPTY + q % kFRing));
+          }
+          tc_commit(bar(F_SFULL + buf));
+          if (j == nt - 1) tc_commit(bar(F_QEMPTY));
+          if (j > 0 && !issue_pv(t - 1, j == 1)) goto mma_exit_w;
+        }
+        if (!issue_pv(it + nt - 1, nt == 1)) goto mma_exit_w;
+        tc_commit(bar(F_OFULL));
+        it += nt;
+        ++qc;
+      }
+    mma_exit_w:
+      // make sure no MMA is still running before TMEM is released
+      tc_commit(bar(F_FINAL));
+      wait1(bar(F_FINAL), 0, ctl, 0xA200001Fu, false);
+    } else if (lane == 0) {
+      constexpr uint32_t kIdS = idesc_f16(kIsBf16, 0, 0, FBM, FBN);  // Q, K both K-major
+      constexpr uint32_t kIdPV = idesc_f16(kIsBf16, 0, 1, FBM, kWide ? 128 : D);  // P from TMEM, V MN-major
       uint32_t qc = 0, kc = 0, it = 0;  // Q tiles, K/V tiles, S tiles (= P tiles)
       // O += P V of tile `t` (global S-tile index), whose V is K/V tile `kt`
       auto issue_pv = [&](uint32_t t, uint32_t kt, bool first) -> bool {
@@ -488,12 +616,14 @@ cudaError_t launch_fwd_t(const FwdParams& p, int dtype, cudaStream_t stream) {
 
 template <bool kCap>
 cudaError_t launch_fwd_cap(const FwdParams& p, int dtype, cudaStream_t stream) {
-  const bool d64 = pad_head_dim(p.head_dim) == 64;
+  const int dp = pad_head_dim(p.head_dim);
   if (dtype == 1)
-    return d64 ? launch_fwd_t<__nv_bfloat16, 64, kCap>(p, dtype, stream)
-               : launch_fwd_t<__nv_bfloat16, 128, kCap>(p, dtype, stream);
-  return d64 ? launch_fwd_t<__half, 64, kCap>(p, dtype, stream)
-             : launch_fwd_t<__half, 128, kCap>(p, dtype, stream);
+    return dp == 64    ? launch_fwd_t<__nv_bfloat16, 64, kCap>(p, dtype, stream)
+           : dp == 128 ? launch_fwd_t<__nv_bfloat16, 128, kCap>(p, dtype, stream)
+                       : launch_fwd_t<__nv_bfloat16, 256, kCap>(p, dtype, stream);
+  return dp == 64    ? launch_fwd_t<__half, 64, kCap>(p, dtype, stream)
+         : dp == 128 ? launch_fwd_t<__half, 128, kCap>(p, dtype, stream)
+                     : launch_fwd_t<__half, 256, kCap>(p, dtype, stream);
 }
 
 }  // namespace

@@ -42,7 +42,7 @@ struct BwdParams {
   float* delta;  // [Hq][ws_rows]
   float* dqacc;  // [Hq][ws_rows][D]
   int* sem;      // [Hq][ws_rows / kTileRows]
-  int* sched;    // work counter of the persistent main kernel (after the semaphores)
+  int* sched;    // work counters of the persistent main kernel(s) (after the semaphores)
   int64_t ws_rows;
   int h_q, h_k, head_dim;
   int win_left, win_right;  // local mask sides, -1 = unbounded; causal is (-1, 0)
@@ -79,11 +79,15 @@ struct WsLayout {
 
 inline size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
-// The kernels run D = 64 or 128; a head dimension that is a multiple of 8 below
-// either runs on the next one with the extra columns zero (TMA's out-of-bounds
-// fill on loads, masked stores), and the fp32 dQ accumulator is laid out at
-// the padded width.
-__host__ __device__ inline int pad_head_dim(int d) { return d <= 64 ? 64 : 128; }
+// The kernels run D = 64, 128 or 256; a head dimension that is a multiple of 8
+// below one of those runs on the next with the extra columns zero (TMA's
+// out-of-bounds fill on loads, masked stores), and the fp32 dQ accumulator is
+// laid out at the padded width.
+__host__ __device__ inline int pad_head_dim(int d) { return d <= 64 ? 64 : (d <= 128 ? 128 : 256); }
+
+// Work counters after the semaphores: one per launch of the persistent
+// backward kernels (the D = 256 backward runs two passes).
+constexpr int kSchedCounters = 2;
 
 inline WsLayout ws_layout(int batch, int seqlen_q, int h_q, int head_dim, int varlen) {
   WsLayout w;
@@ -97,8 +101,9 @@ inline WsLayout ws_layout(int batch, int seqlen_q, int h_q, int head_dim, int va
   w.off_delta = align256(w.off_lse2 + per_row * 4);
   w.off_dqacc = align256(w.off_delta + per_row * 4);
   w.off_sem = align256(w.off_dqacc + per_row * static_cast<size_t>(pad_head_dim(head_dim)) * 4);
-  // semaphores, then one int32 work counter for the persistent scheduler
-  w.total = align256(w.off_sem + (static_cast<size_t>(h_q) * (w.rows / kTileRows) + 1) * 4);
+  // semaphores, then the int32 work counters of the persistent scheduler
+  w.total = align256(w.off_sem +
+                     (static_cast<size_t>(h_q) * (w.rows / kTileRows) + kSchedCounters) * 4);
   return w;
 }
 
@@ -106,6 +111,8 @@ inline WsLayout ws_layout(int batch, int seqlen_q, int h_q, int head_dim, int va
 cudaError_t launch_preprocess(const BwdParams& p, int dtype, cudaStream_t stream);
 cudaError_t launch_postprocess(const BwdParams& p, int dtype, cudaStream_t stream);
 cudaError_t launch_bwd_main(const BwdParams& p, int dtype, cudaStream_t stream);
+// Head dimensions above 128: the two-pass D = 256 backward (bwd_wide.cu).
+cudaError_t launch_bwd_wide(const BwdParams& p, int dtype, cudaStream_t stream);
 cudaError_t launch_fwd(const FwdParams& p, int dtype, cudaStream_t stream);
 cudaError_t launch_zero_rows(const TensorArg& t, int dtype, int nseq, int rows_per_seq,
                              const int* cu, int total_rows, int heads, int head_dim,

@@ -117,8 +117,8 @@ __global__ void __launch_bounds__(kThreads, 8) preprocess_kernel(BwdParams p) {
     }
   }
 
-  // Phase 2: clear the deterministic-mode semaphores and the work counter after them.
-  const int64_t ns = p.ws_rows / kTileRows * p.h_q + 1;
+  // Phase 2: clear the deterministic-mode semaphores and the work counters after them.
+  const int64_t ns = p.ws_rows / kTileRows * p.h_q + kSchedCounters;
   for (int64_t e = gtid; e < ns; e += nthreads) p.sem[e] = 0;
 }
 
@@ -249,13 +249,16 @@ inline int grid_for(int64_t work_threads, K kernel, Occupancy& occ) {
 template <typename T>
 static cudaError_t launch_pre_t(const BwdParams& p, cudaStream_t stream) {
   const int64_t work = p.ws_rows * p.h_q * (pad_head_dim(p.head_dim) / 8);
-  static Occupancy occ64, occ128;
+  static Occupancy occ64, occ128, occ256;
   if (pad_head_dim(p.head_dim) == 64)
     preprocess_kernel<T, 64>
         <<<grid_for(work, preprocess_kernel<T, 64>, occ64), kThreads, 0, stream>>>(p);
-  else
+  else if (pad_head_dim(p.head_dim) == 128)
     preprocess_kernel<T, 128>
         <<<grid_for(work, preprocess_kernel<T, 128>, occ128), kThreads, 0, stream>>>(p);
+  else
+    preprocess_kernel<T, 256>
+        <<<grid_for(work, preprocess_kernel<T, 256>, occ256), kThreads, 0, stream>>>(p);
   return cudaGetLastError();
 }
 
@@ -270,13 +273,16 @@ static cudaError_t launch_post_t(const BwdParams& p, cudaStream_t stream) {
                              : static_cast<int64_t>(p.seq.seqlen_q);
   const int64_t work = tokens * p.h_q * (pad_head_dim(p.head_dim) / 8);
   if (work == 0) return cudaSuccess;
-  static Occupancy occ64, occ128;
+  static Occupancy occ64, occ128, occ256;
   if (pad_head_dim(p.head_dim) == 64)
     postprocess_kernel<T, 64>
         <<<grid_for(work, postprocess_kernel<T, 64>, occ64), kThreads, 0, stream>>>(p);
-  else
+  else if (pad_head_dim(p.head_dim) == 128)
     postprocess_kernel<T, 128>
         <<<grid_for(work, postprocess_kernel<T, 128>, occ128), kThreads, 0, stream>>>(p);
+  else
+    postprocess_kernel<T, 256>
+        <<<grid_for(work, postprocess_kernel<T, 256>, occ256), kThreads, 0, stream>>>(p);
   return cudaGetLastError();
 }
 
@@ -290,12 +296,15 @@ static cudaError_t launch_zero_t(const TensorArg& t, int nseq, int rows_per_seq,
   const int64_t rows = (cu == nullptr) ? static_cast<int64_t>(nseq) * rows_per_seq : total_rows;
   const int64_t work = rows * heads * (pad_head_dim(head_dim) / 8);
   if (work == 0) return cudaSuccess;
-  static Occupancy occ64, occ128;
+  static Occupancy occ64, occ128, occ256;
   if (pad_head_dim(head_dim) == 64)
     zero_rows_kernel<T, 64><<<grid_for(work, zero_rows_kernel<T, 64>, occ64), kThreads, 0,
                               stream>>>(t, nseq, rows_per_seq, cu, total_rows, heads, head_dim);
-  else
+  else if (pad_head_dim(head_dim) == 128)
     zero_rows_kernel<T, 128><<<grid_for(work, zero_rows_kernel<T, 128>, occ128), kThreads, 0,
+                               stream>>>(t, nseq, rows_per_seq, cu, total_rows, heads, head_dim);
+  else
+    zero_rows_kernel<T, 256><<<grid_for(work, zero_rows_kernel<T, 256>, occ256), kThreads, 0,
                                stream>>>(t, nseq, rows_per_seq, cu, total_rows, heads, head_dim);
   return cudaGetLastError();
 }

@@ -58,7 +58,8 @@ class Workload:
         return self.head_dim ** -0.5
 
 
-# The five problem shapes the attention-backward benchmark is quoted on.
+# The five problem shapes the attention-backward benchmark is quoted on, and extensions
+# of them (deterministic, window, logit cap, head dims above 128).
 WORKLOADS = {
     "mha_b1_h2_s128_d64_fp16": Workload(
         "mha_b1_h2_s128_d64_fp16", 1, 2, 2, 128, 128, 64, "fp16", False, 0),
@@ -80,6 +81,11 @@ WORKLOADS = {
     "gqa_b2_hq32_hk8_s8192_d128_bf16_causal_cap30": Workload(
         "gqa_b2_hq32_hk8_s8192_d128_bf16_causal_cap30", 2, 32, 8, 8192, 8192, 128, "bf16", True,
         3, softcap=30.0),
+    # head dimensions above 128 (the wide kernels), same shape as the MHA S=4096 workload
+    "mha_b2_h16_s4096_d256_bf16_causal": Workload(
+        "mha_b2_h16_s4096_d256_bf16_causal", 2, 16, 16, 4096, 4096, 256, "bf16", True, 2),
+    "mha_b2_h16_s4096_d192_bf16_causal": Workload(
+        "mha_b2_h16_s4096_d192_bf16_causal", 2, 16, 16, 4096, 4096, 192, "bf16", True, 2),
     "varlen16_h16_d128_bf16_causal": Workload(
         "varlen16_h16_d128_bf16_causal", 0, 16, 16, 0, 0, 128, "bf16", True, 4,
         n_seqs=16, len_lo=128, len_hi=8192),

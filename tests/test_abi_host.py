@@ -117,7 +117,7 @@ def test_argument_errors(lib, case, code):
     elif case == "head_dim":
         q, k, v, o, do = shapes(d=100)  # not a multiple of 8
     elif case == "head_dim_large":
-        q, k, v, o, do = shapes(d=136)  # above 128
+        q, k, v, o, do = shapes(d=264)  # above 256
     elif case == "gqa_ratio":
         q, k, v, o, do = shapes(hq=3, hk=2)
     elif case == "align":
