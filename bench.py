@@ -328,7 +328,10 @@ def run_ours(args):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": w.dtype,
         "data": "synthetic N(0,1), seeded; O and LSE from attn_fwd", "config": cfg,
         "pct_of_peak": round(100.0 * value / world / peak, 2),
-        "roofline": {"bound": "tensor", "kernel": "bwd_main_kernel", "achieved": round(achieved, 2),
+        "roofline": {"bound": "tensor",
+                     "kernel": "bwd_main_kernel" if w.head_dim <= 128 else
+                               "bwd_wide_kernel (dK/dQ pass + dV pass)",
+                     "achieved": round(achieved, 2),
                      "peak": peak, "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
                      "peak_src": "bf16 burst, of " + peaks["src"],
                      "frac_of_sustained": round(achieved / peak_sus, 4),

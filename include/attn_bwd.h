@@ -28,9 +28,11 @@
  * varlen mode (flash-attention's softmax_lse).
  *
  * Supported: dtype fp16 or bf16 (all of Q,K,V,O,dO,dQ,dK,dV share it), D a
- * multiple of 8 in [8, 128] (64 and 128 run natively; any other D runs on the
- * next of those with the extra head-dimension columns zero), H_q % H_k == 0,
- * base pointers and strides 16-byte aligned (strides multiples of 8 elements).
+ * multiple of 8 in [8, 256] (the head sizes the CK wrapper's mha_bwd accepts;
+ * 64, 128 and 256 run natively, any other D runs on the next of those with the
+ * extra head-dimension columns zero; above 128 the backward runs as two
+ * passes, one for dV and one for dK and dQ), H_q % H_k == 0, base pointers and
+ * strides 16-byte aligned (strides multiples of 8 elements).
  *
  * Ownership.  The caller owns every buffer, including the workspace; the
  * library allocates nothing per call and keeps no state across calls except
@@ -62,7 +64,7 @@ enum attn_dtype { ATTN_FP16 = 0, ATTN_BF16 = 1 };
 enum attn_status {
   ATTN_OK = 0,
   ATTN_ERR_DTYPE = -1,          /* dtype not fp16/bf16 */
-  ATTN_ERR_SHAPE = -2,          /* bad sizes: B<=0, H_q%H_k, D not 8..128 by 8 */
+  ATTN_ERR_SHAPE = -2,          /* bad sizes: B<=0, H_q%H_k, D not 8..256 by 8 */
   ATTN_ERR_STRIDE = -3,         /* stride not a multiple of 8 elements or negative */
   ATTN_ERR_ALIGN = -4,          /* base pointer not 16-byte aligned */
   ATTN_ERR_NULL = -5,           /* required pointer is NULL */
@@ -105,8 +107,9 @@ size_t attn_bwd_workspace_size(int batch, int seqlen_q, int h_q, int head_dim,
  * attn_bwd_workspace_layout -- where the pieces of the workspace live, for
  * callers that inspect them.  Writes byte offsets of LSE2 (fp32
  * [H_q][rows]), Delta (fp32 [H_q][rows]), dQaccum (fp32 [H_q][rows][D]) and
- * the semaphores (int32 [H_q][rows/128], followed by one int32 work counter of
- * the main kernel's scheduler) into offsets[0..3], and `rows`.
+ * the semaphores (int32 [H_q][rows/128], followed by two int32 work counters
+ * of the main kernels' schedulers) into offsets[0..3], and `rows`.  dQaccum's
+ * row width D is the head dimension padded to 64, 128 or 256.
  * Row of query i of sequence b: padded mode b*round_up(Sq,128) + i; varlen
  * 128*(cu_seqlens_q[b]/128 + b) + i.  Returns ATTN_OK or ATTN_ERR_NULL.
  */
