@@ -257,7 +257,7 @@ int prepare_bwd(const attn_tensor* q, const attn_tensor* k, const attn_tensor* v
   p.delta = reinterpret_cast<float*>(ws + w.off_delta);
   p.dqacc = reinterpret_cast<float*>(ws + w.off_dqacc);
   p.sem = reinterpret_cast<int*>(ws + w.off_sem);
-  p.sched = p.sem + static_cast<int64_t>(h_q) * (w.rows / kTileRows);
+  p.sched = p.sem + static_cast<int64_t>(h_q) * (w.rows / kTileRows) * 4;
   p.ws_rows = w.rows;
   p.h_q = h_q;
   p.h_k = h_k;

@@ -18,8 +18,9 @@
 // summed in TMEM over the group's query heads (the group sum of
 // flash-attention csrc/flash_attn_ck/mha_bwd.cpp, done without extra memory).
 // dQaccum is reduced with TMA tensor reduce-adds (fp32), or, in deterministic
-// mode, in ascending KV-tile order behind a per-(head, query tile) semaphore
-// (the dq_semaphore of flash-attention hopper/flash_bwd_launch_template.h).
+// mode, in ascending KV-tile order behind per-(head, query tile, 32-row quarter)
+// semaphores (the dq_semaphore of flash-attention
+// hopper/flash_bwd_launch_template.h).
 // D is 64 or 128 here; smaller head dims (multiples of 8) run zero-padded to
 // the next of those.  Template switches: kCap (logit cap), kLeft (a left
 // window side); the default instantiation has neither.
@@ -647,8 +648,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     // rows, so they need no mask.
     // In deterministic mode a warp waits until the key tiles before n that see
     // this query tile (0..n-1, or from the first one inside a left window) have
-    // completed their adds (4 arrivals each, one per drain warp) and releases
-    // once its own adds have completed.
+    // completed their adds to the warp's 32 rows (one arrival each on the
+    // semaphore of those rows) and releases once its own adds have completed.
     const uint32_t quad = warp & 3;
     const uint32_t tl = tmem + ((quad * 32) << 16);
     // Per warp and pass: kBoxes boxes of 32 rows x 32 fp32 columns (4 KB each);
@@ -669,8 +670,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         iter_hm(un, j, G, h, m);
         const int row0 = static_cast<int>(static_cast<int64_t>(h) * p.ws_rows + un.si.ws_row0 +
                                           m * BM + quad * 32);
-        int* sem = p.sem + static_cast<int64_t>(h) * (p.ws_rows / kTileRows) +
-                   un.si.ws_row0 / kTileRows + m;
+        // one semaphore per (head, query tile, drain warp): the 32 rows of warp
+        // `quad` take their adds in key-tile order, independently of the others
+        int* sem = p.sem + (static_cast<int64_t>(h) * (p.ws_rows / kTileRows) +
+                            un.si.ws_row0 / kTileRows + m) * 4 + quad;
         const uint32_t s = it % kStages;
         const uint32_t stage_off = L::kDO + s * L::kTile + quad * (kBoxes * 4096);
         if (!wait_warp(bar(B_DQFULL), it & 1, ctl, 0xA0000031u)) goto done;
@@ -692,8 +695,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (lane == 0) {
             // key tiles before this one that see query tile m (all of them
             // unless a left window starts the range later)
-            const int want =
-                4 * (un.n - window_first_key(m * BM, un.si.sq, un.si.sk, wleft) / BN);
+            const int want = un.n - window_first_key(m * BM, un.si.sq, un.si.sk, wleft) / BN;
             const uint64_t t0 = globaltimer_ns();
             for (uint32_t spin = 0;; ++spin) {
               if (ld_acquire(sem) >= want) break;

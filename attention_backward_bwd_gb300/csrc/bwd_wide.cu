@@ -22,8 +22,8 @@
 //   pass dK/dQ, per query tile: Q chunks (S^T), V and dO chunk pairs (dP^T),
 //     Q chunks again (dK).
 // dQ is drained in four 64-column passes through a 32 KiB staging buffer with
-// TMA reduce-adds (in deterministic mode ordered by the per-(head, query tile)
-// semaphore, as in the D <= 128 kernel).
+// TMA reduce-adds (in deterministic mode ordered by the per-(head, query tile,
+// 32-row quarter) semaphore, as in the D <= 128 kernel).
 //
 // Warp roles (768 threads): warp 0 TMA producer, warp 1 MMA issuer, warp 2
 // TMEM allocator, warps 4-19 softmax / dS / epilogue (thread = key row; warp
@@ -610,8 +610,9 @@ __global__ void __launch_bounds__(kWThreads, 1)
         iter_hm(un, j, G, h, m);
         const int row0 = static_cast<int>(static_cast<int64_t>(h) * p.ws_rows + un.si.ws_row0 +
                                           m * kTileRows + quad * 32);
-        int* sem = p.sem + static_cast<int64_t>(h) * (p.ws_rows / kTileRows) +
-                   un.si.ws_row0 / kTileRows + m;
+        // one semaphore per (head, query tile, drain warp), as in the D <= 128 kernel
+        int* sem = p.sem + (static_cast<int64_t>(h) * (p.ws_rows / kTileRows) +
+                            un.si.ws_row0 / kTileRows + m) * 4 + quad;
         if (!wait_warp(bar(W_DQFULL), it & 1, ctl, 0xA3000031u)) goto done;
         tc_fence_after();
         uint32_t a[64];
@@ -623,8 +624,7 @@ __global__ void __launch_bounds__(kWThreads, 1)
           if (lane == 0) {
             // key tiles before this one that see query tile m
             const int want =
-                4 * (un.n - window_first_key(m * kTileRows, un.si.sq, un.si.sk, p.win_left) /
-                                kTileRows);
+                un.n - window_first_key(m * kTileRows, un.si.sq, un.si.sk, p.win_left) / kTileRows;
             const uint64_t t0 = globaltimer_ns();
             for (uint32_t spin = 0;; ++spin) {
               if (ld_acquire(sem) >= want) break;

@@ -41,7 +41,7 @@ struct BwdParams {
   float* lse2;   // [Hq][ws_rows]
   float* delta;  // [Hq][ws_rows]
   float* dqacc;  // [Hq][ws_rows][D]
-  int* sem;      // [Hq][ws_rows / kTileRows]
+  int* sem;      // [Hq][ws_rows / kTileRows][4]: one per (query tile, 32-row quarter)
   int* sched;    // work counters of the persistent main kernel(s) (after the semaphores)
   int64_t ws_rows;
   int h_q, h_k, head_dim;
@@ -101,9 +101,10 @@ inline WsLayout ws_layout(int batch, int seqlen_q, int h_q, int head_dim, int va
   w.off_delta = align256(w.off_lse2 + per_row * 4);
   w.off_dqacc = align256(w.off_delta + per_row * 4);
   w.off_sem = align256(w.off_dqacc + per_row * static_cast<size_t>(pad_head_dim(head_dim)) * 4);
-  // semaphores, then the int32 work counters of the persistent scheduler
+  // semaphores (one per 32-row quarter of each query tile), then the int32 work
+  // counters of the persistent scheduler
   w.total = align256(w.off_sem +
-                     (static_cast<size_t>(h_q) * (w.rows / kTileRows) + kSchedCounters) * 4);
+                     (static_cast<size_t>(h_q) * (w.rows / kTileRows) * 4 + kSchedCounters) * 4);
   return w;
 }
 

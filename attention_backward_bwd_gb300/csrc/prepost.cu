@@ -118,7 +118,7 @@ __global__ void __launch_bounds__(kThreads, 8) preprocess_kernel(BwdParams p) {
   }
 
   // Phase 2: clear the deterministic-mode semaphores and the work counters after them.
-  const int64_t ns = p.ws_rows / kTileRows * p.h_q + kSchedCounters;
+  const int64_t ns = p.ws_rows / kTileRows * p.h_q * 4 + kSchedCounters;
   for (int64_t e = gtid; e < ns; e += nthreads) p.sem[e] = 0;
 }
 

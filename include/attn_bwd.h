@@ -107,8 +107,9 @@ size_t attn_bwd_workspace_size(int batch, int seqlen_q, int h_q, int head_dim,
  * attn_bwd_workspace_layout -- where the pieces of the workspace live, for
  * callers that inspect them.  Writes byte offsets of LSE2 (fp32
  * [H_q][rows]), Delta (fp32 [H_q][rows]), dQaccum (fp32 [H_q][rows][D]) and
- * the semaphores (int32 [H_q][rows/128], followed by two int32 work counters
- * of the main kernels' schedulers) into offsets[0..3], and `rows`.  dQaccum's
+ * the semaphores (int32 [H_q][rows/128][4], one per 32-row quarter of a
+ * query tile, followed by two int32 work counters of the main kernels'
+ * schedulers) into offsets[0..3], and `rows`.  dQaccum's
  * row width D is the head dimension padded to 64, 128 or 256.
  * Row of query i of sequence b: padded mode b*round_up(Sq,128) + i; varlen
  * 128*(cu_seqlens_q[b]/128 + b) + i.  Returns ATTN_OK or ATTN_ERR_NULL.

@@ -46,7 +46,11 @@ def test_workspace_size_and_layout(lib):
     assert offs["dqaccum"] >= offs["delta"] + 4 * rows * 4
     assert offs["sem"] >= offs["dqaccum"] + 4 * rows * 128 * 4
     size = binding.workspace_size(2, 300, 4, 128)
-    assert size >= offs["sem"] + 4 * (rows // 128) * 4 and size % 256 == 0
+    # 4 heads x (rows / 128) query tiles x 4 row quarters of semaphores, 2 work counters
+    assert size >= offs["sem"] + (4 * (rows // 128) * 4 + 2) * 4 and size % 256 == 0
+    # head dims above 128 lay dQaccum out at width 256
+    offs256, _ = binding.workspace_layout(2, 300, 4, 192)
+    assert offs256["sem"] >= offs256["dqaccum"] + 4 * rows * 256 * 4
     # varlen: total rows + one padding tile per sequence
     _, vrows = binding.workspace_layout(3, 1000, 4, 64, varlen=True)
     assert vrows == ((1000 + 3 * 128 + 127) // 128) * 128
