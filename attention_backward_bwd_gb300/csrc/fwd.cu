@@ -21,12 +21,13 @@
 // otherwise P is at most 2^8 and O, the row sum and the LSE stay consistent
 // with the stale reference, so the result is the same softmax.
 //
-// Warp roles (256 threads): warp 0 TMA producer, warp 1 MMA issuer (one
-// thread), warp 2 TMEM allocator, warps 4-7 softmax and epilogue (thread =
-// query row = TMEM lane).  The MMA thread issues S of tile t before O += P V
-// of tile t - 1, so the tensor pipe computes S of the next tile while the
-// softmax warps work on the current one; three S buffers keep S of tile t
-// from waiting on O += P V of tile t - 2.
+// Warp roles (256 threads): warp 0 TMA producer (Q and K), warp 3 V producer,
+// warp 1 issues S = Q K^T, warp 2 allocates TMEM and issues O += P V (one
+// thread each), warps 4-7 softmax and epilogue (thread = query row = TMEM
+// lane).  S runs up to two tiles ahead of the softmax (three S buffers), so
+// the tensor pipe computes S of the next tile while the softmax warps work on
+// the current one.  (At D = 256 warp 0 alone fills the chunk ring and warp 1
+// alone issues both products.)
 //
 // TMEM columns (512 allocated): S buffers [0,128), [128,256), [256,384);
 // O [384, 384 + D).  Shared memory: 2 Q stages, 3 K stages, 2 V stages.
@@ -64,15 +65,14 @@ constexpr float kRescaleLog2 = 8.f;  // P stays below 2^8 between rescales
 enum FBar : uint32_t {
   F_QFULL = 0,
   F_QEMPTY = F_QFULL + kQSt,
-  F_KFULL = F_QEMPTY + kQSt,
-  F_KEMPTY = F_KFULL + kKSt,
-  F_VFULL = F_KEMPTY + kKSt,
-  F_VEMPTY = F_VFULL + kVSt,
-  F_SFULL = F_VEMPTY + kVSt,    // per S buffer (up to 3): S computed
+  F_KFULL = F_QEMPTY + kQSt,    // K and V stages are released by SFULL / PVDONE
+  F_VFULL = F_KFULL + kKSt,
+  F_SFULL = F_VFULL + kVSt,     // per S buffer (up to 3): S computed
   F_PREADY = F_SFULL + 3,       // per S buffer: P written over it (4 softmax warps)
   F_PVDONE = F_PREADY + 3,      // per S buffer: O += P V has read it
   F_OFULL = F_PVDONE + 3,       // the unit's last O += P V done
   F_FINAL,
+  F_FINAL2,                     // the O += P V issuer's own drain before TMEM is released
   F_RFULL,                      // D = 256: chunk ring slots
   F_REMPTY = F_RFULL + kFRing,
   F_COUNT = F_REMPTY + kFRing
@@ -159,14 +159,8 @@ __global__ void __launch_bounds__(kFThreads, 1)
       mbar_init(bar(F_QFULL + s), 1);
       mbar_init(bar(F_QEMPTY + s), 1);
     }
-    for (int s = 0; s < kKSt; ++s) {
-      mbar_init(bar(F_KFULL + s), 1);
-      mbar_init(bar(F_KEMPTY + s), 1);
-    }
-    for (int s = 0; s < kVSt; ++s) {
-      mbar_init(bar(F_VFULL + s), 1);
-      mbar_init(bar(F_VEMPTY + s), 1);
-    }
+    for (int s = 0; s < kKSt; ++s) mbar_init(bar(F_KFULL + s), 1);
+    for (int s = 0; s < kVSt; ++s) mbar_init(bar(F_VFULL + s), 1);
     for (int s = 0; s < kSBufs; ++s) {
       mbar_init(bar(F_SFULL + s), 1);
       mbar_init(bar(F_PREADY + s), 4);
@@ -174,6 +168,7 @@ __global__ void __launch_bounds__(kFThreads, 1)
     }
     mbar_init(bar(F_OFULL), 1);
     mbar_init(bar(F_FINAL), 1);
+    mbar_init(bar(F_FINAL2), 1);
     for (int r = 0; r < kFRing; ++r) {
       mbar_init(bar(F_RFULL + r), 1);
       mbar_init(bar(F_REMPTY + r), 1);
@@ -190,9 +185,12 @@ __global__ void __launch_bounds__(kFThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + L::kTmemSlot);
 
-  if (warp == 0) {
-    // ------------------------------------------------------------ TMA producer
-    if (lane == 0 && kWide) {
+  if (warp == 0 || warp == 3) {
+    // ------------------------------------------------------------ TMA producers
+    // D = 256: warp 0 fills the chunk ring.  Up to D = 128: warp 0 loads Q and K,
+    // warp 3 loads V, so that a K load never waits behind the release of a V
+    // stage (which comes one tile later, after O += P V).
+    if (lane == 0 && kWide && warp == 0) {
       prefetch_tmap(&tmQ);
       prefetch_tmap(&tmK);
       prefetch_tmap(&tmV);
@@ -235,10 +233,10 @@ __global__ void __launch_bounds__(kFThreads, 1)
       if (qc > 0) wait1(bar(F_QFULL), (qc - 1) & 1, ctl, 0xA2000004u, false);
       for (uint32_t i = q > static_cast<uint32_t>(kFRing) ? q - kFRing : 0; i < q; ++i)
         wait1(bar(F_RFULL + i % kFRing), (i / kFRing) & 1, ctl, 0xA2000005u, false);
-    } else if (lane == 0) {
-      prefetch_tmap(&tmQ);
-      prefetch_tmap(&tmK);
-      prefetch_tmap(&tmV);
+    } else if (lane == 0 && !kWide) {
+      const bool loads_v = warp == 3;
+      prefetch_tmap(loads_v ? &tmV : &tmQ);
+      if (!loads_v) prefetch_tmap(&tmK);
       uint32_t qc = 0, kc = 0, vc = 0;  // Q, K and V tiles whose loads were issued
       bool stop = false;
       for (int u = blockIdx.x; u < num_units && !stop; u += gridDim.x) {
@@ -246,7 +244,7 @@ __global__ void __launch_bounds__(kFThreads, 1)
         if (!un.active || un.n_end == un.n_start) continue;
         const int bq = varlen ? 0 : un.b;
         const int hk = un.h / G;
-        {
+        if (!loads_v) {
           const uint32_t s = qc % kQSt, use = qc / kQSt;
           if (use > 0 && !wait1(bar(F_QEMPTY + s), (use - 1) & 1, ctl, 0xA2000001u)) break;
           mbar_expect_tx(bar(F_QFULL + s), L::kTile);
@@ -258,8 +256,34 @@ __global__ void __launch_bounds__(kFThreads, 1)
         }
         for (int n = un.n_start; n < un.n_end; ++n) {
           const int krow = un.si.k_start + n * FBN;
-          const uint32_t ks = kc % kKSt, kuse = kc / kKSt;
-          if (kuse > 0 && !wait1(bar(F_KEMPTY + ks), (kuse - 1) & 1, ctl, 0xA2000002u)) {
+          if (loads_v) {
+            // V stage vc % kVSt last held V of tile vc - kVSt: free once that tile's
+            // O += P V is done (the MMA thread's PVDONE of its S buffer; K/V tile and
+            // S tile counters coincide).  That barrier cannot have moved on by a
+            // further phase: that would need the V this thread has not loaded yet.
+            const uint32_t vs = vc % kVSt;
+            if (vc >= static_cast<uint32_t>(kVSt)) {
+              const uint32_t pt = vc - kVSt;
+              if (!wait1(bar(F_PVDONE + pt % kSBufs), (pt / kSBufs) & 1, ctl, 0xA2000003u)) {
+                stop = true;
+                break;
+              }
+            }
+            mbar_expect_tx(bar(F_VFULL + vs), L::kTile);
+#pragma unroll
+            for (int c = 0; c < D / 64; ++c)
+              tma_load_4d(sb + L::kV + vs * L::kTile + c * kFChunk, &tmV, bar(F_VFULL + vs),
+                          c * 64, krow, hk, bq);
+            ++vc;
+            continue;
+          }
+          // K stage kc % kKSt (= S buffer kc % kSBufs) last held K of tile kc - kKSt:
+          // free once that tile's S is done (its SFULL), which cannot have moved on
+          // by a further phase before this K is loaded.
+          static_assert(kKSt == 3 && FCfg<128>::kSBufs == 3, "K stages follow the S buffers");
+          const uint32_t ks = kc % kKSt;
+          if (kc >= static_cast<uint32_t>(kKSt) &&
+              !wait1(bar(F_SFULL + ks), ((kc - kKSt) / kKSt) & 1, ctl, 0xA2000002u)) {
             stop = true;
             break;
           }
@@ -269,17 +293,6 @@ __global__ void __launch_bounds__(kFThreads, 1)
             tma_load_4d(sb + L::kK + ks * L::kTile + c * kFChunk, &tmK, bar(F_KFULL + ks), c * 64,
                         krow, hk, bq);
           ++kc;
-          const uint32_t vs = vc % kVSt, vuse = vc / kVSt;
-          if (vuse > 0 && !wait1(bar(F_VEMPTY + vs), (vuse - 1) & 1, ctl, 0xA2000003u)) {
-            stop = true;
-            break;
-          }
-          mbar_expect_tx(bar(F_VFULL + vs), L::kTile);
-#pragma unroll
-          for (int c = 0; c < D / 64; ++c)
-            tma_load_4d(sb + L::kV + vs * L::kTile + c * kFChunk, &tmV, bar(F_VFULL + vs), c * 64,
-                        krow, hk, bq);
-          ++vc;
         }
         if (*abort_flag) break;
       }
@@ -357,41 +370,30 @@ __global__ void __launch_bounds__(kFThreads, 1)
       // make sure no MMA is still running before TMEM is released
       tc_commit(bar(F_FINAL));
       wait1(bar(F_FINAL), 0, ctl, 0xA200001Fu, false);
-    } else if (lane == 0) {
+    } else if (lane == 0 && !kWide) {
+      // Up to D = 128 this thread issues the S = Q K^T products and warp 2 the
+      // O += P V products: each tcgen05.mma blocks its issuing thread for about
+      // its own execution time, so with one issuer every wait and commit between
+      // the two kinds of product left the tensor pipe idle.  The barriers order
+      // what the two threads share: S of tile t waits for O += P V of tile t - 3
+      // (the S buffer's previous P), O += P V of tile t for P of tile t.
       constexpr uint32_t kIdS = idesc_f16(kIsBf16, 0, 0, FBM, FBN);  // Q, K both K-major
-      constexpr uint32_t kIdPV = idesc_f16(kIsBf16, 0, 1, FBM, kWide ? 128 : D);  // P from TMEM, V MN-major
-      uint32_t qc = 0, kc = 0, it = 0;  // Q tiles, K/V tiles, S tiles (= P tiles)
-      // O += P V of tile `t` (global S-tile index), whose V is K/V tile `kt`
-      auto issue_pv = [&](uint32_t t, uint32_t kt, bool first) -> bool {
-        const uint32_t buf = t % kSBufs;
-        const uint32_t vs = kt % kVSt;
-        if (!wait1(bar(F_PREADY + buf), (t / kSBufs) & 1, ctl, 0xA2000011u)) return false;
-        if (!wait1(bar(F_VFULL + vs), (kt / kVSt) & 1, ctl, 0xA2000012u)) return false;
-        tc_fence_after();
-        const uint32_t sV = sb + L::kV + vs * L::kTile;
-#pragma unroll
-        for (int kk = 0; kk < FBN / 16; ++kk)
-          mma_ts(tmem + TF_O, tmem + TF_S + buf * 128 + kk * 8,
-                 sdesc_sw128(sV + kk * 2048, kFChunk, 1024), kIdPV, (!first || kk > 0) ? 1u : 0u);
-        tc_commit(bar(F_PVDONE + buf));
-        tc_commit(bar(F_VEMPTY + vs));
-        return true;
-      };
+      uint32_t qc = 0, it = 0;  // Q tiles, S tiles
       for (int u = blockIdx.x; u < num_units; u += gridDim.x) {
         const FUnit un = fwd_unit(p, u, n_mt);
         if (!un.active || un.n_end == un.n_start) continue;
         const int nt = un.n_end - un.n_start;
         const uint32_t qs = qc % kQSt;
-        if (!wait1(bar(F_QFULL + qs), (qc / kQSt) & 1, ctl, 0xA2000013u)) goto mma_exit;
+        if (!wait1(bar(F_QFULL + qs), (qc / kQSt) & 1, ctl, 0xA2000013u)) goto s_exit;
         const uint32_t sQ = sb + L::kQ + qs * L::kTile;
         for (int j = 0; j < nt; ++j) {
-          const uint32_t t = it + j, kt = kc + j;
-          const uint32_t buf = t % kSBufs, ks = kt % kKSt;
+          const uint32_t t = it + j;
+          const uint32_t buf = t % kSBufs, ks = t % kKSt;  // K/V and S tile counters coincide
           // S buffer `buf` last held tile t - 3, whose O += P V must have read its P
           if (t >= kSBufs &&
               !wait1(bar(F_PVDONE + buf), ((t - kSBufs) / kSBufs) & 1, ctl, 0xA2000014u))
-            goto mma_exit;
-          if (!wait1(bar(F_KFULL + ks), (kt / kKSt) & 1, ctl, 0xA2000015u)) goto mma_exit;
+            goto s_exit;
+          if (!wait1(bar(F_KFULL + ks), (t / kKSt) & 1, ctl, 0xA2000015u)) goto s_exit;
           tc_fence_after();
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
@@ -399,21 +401,45 @@ __global__ void __launch_bounds__(kFThreads, 1)
             mma_ss(tmem + TF_S + buf * 128, sdesc_sw128(sQ + koff, 16, 1024),
                    sdesc_sw128(sb + L::kK + ks * L::kTile + koff, 16, 1024), kIdS, kk > 0);
           }
-          tc_commit(bar(F_SFULL + buf));
-          tc_commit(bar(F_KEMPTY + ks));
+          tc_commit(bar(F_SFULL + buf));  // also frees K stage ks for the producer
           if (j == nt - 1) tc_commit(bar(F_QEMPTY + qs));
-          if (j > 0 && !issue_pv(t - 1, kt - 1, j == 1)) goto mma_exit;
         }
-        if (!issue_pv(it + nt - 1, kc + nt - 1, nt == 1)) goto mma_exit;
-        tc_commit(bar(F_OFULL));
         it += nt;
-        kc += nt;
         ++qc;
       }
-    mma_exit:
+    s_exit:
       // make sure no MMA is still running before TMEM is released
       tc_commit(bar(F_FINAL));
       wait1(bar(F_FINAL), 0, ctl, 0xA200001Fu, false);
+    }
+  } else if (warp == 2 && !kWide) {
+    if (lane == 0) {
+      // ---------------------------------------------------- O += P V issuer
+      constexpr uint32_t kIdPV = idesc_f16(kIsBf16, 0, 1, FBM, kWide ? 128 : D);  // P from TMEM, V MN-major
+      uint32_t it = 0;
+      for (int u = blockIdx.x; u < num_units; u += gridDim.x) {
+        const FUnit un = fwd_unit(p, u, n_mt);
+        if (!un.active || un.n_end == un.n_start) continue;
+        const int nt = un.n_end - un.n_start;
+        for (int j = 0; j < nt; ++j) {
+          const uint32_t t = it + j;
+          const uint32_t buf = t % kSBufs, vs = t % kVSt;
+          if (!wait1(bar(F_PREADY + buf), (t / kSBufs) & 1, ctl, 0xA2000011u)) goto pv_exit;
+          if (!wait1(bar(F_VFULL + vs), (t / kVSt) & 1, ctl, 0xA2000012u)) goto pv_exit;
+          tc_fence_after();
+          const uint32_t sV = sb + L::kV + vs * L::kTile;
+#pragma unroll
+          for (int kk = 0; kk < FBN / 16; ++kk)
+            mma_ts(tmem + TF_O, tmem + TF_S + buf * 128 + kk * 8,
+                   sdesc_sw128(sV + kk * 2048, kFChunk, 1024), kIdPV, (j > 0 || kk > 0) ? 1u : 0u);
+          tc_commit(bar(F_PVDONE + buf));  // also frees V stage vs for the V producer
+        }
+        tc_commit(bar(F_OFULL));
+        it += nt;
+      }
+    pv_exit:
+      tc_commit(bar(F_FINAL2));
+      wait1(bar(F_FINAL2), 0, ctl, 0xA200002Fu, false);
     }
   } else if (warp >= 4) {
     // ------------------------------------------------------- softmax / epilogue
