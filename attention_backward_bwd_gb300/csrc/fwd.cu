@@ -26,15 +26,14 @@
 // thread each), warps 4-7 softmax and epilogue (thread = query row = TMEM
 // lane).  S runs up to two tiles ahead of the softmax (three S buffers), so
 // the tensor pipe computes S of the next tile while the softmax warps work on
-// the current one.  (At D = 256 warp 0 alone fills the chunk ring and warp 1
-// alone issues both products.)
+// the current one.  (At D = 256 the same roles work on the chunk rings.)
 //
 // TMEM columns (512 allocated): S buffers [0,128), [128,256), [256,384);
 // O [384, 384 + D).  Shared memory: 2 Q stages, 3 K stages, 2 V stages.
 // Head dimensions above 128 run on D = 256 tiles (extra columns zero): O takes
 // TMEM [256,512) next to two S buffers, the unit's Q tile (64 KiB) stays in
-// shared memory, and K and V stream through a ring of ten 64-column chunks
-// (K_t for S_t, then V_{t-1} for O += P V_{t-1}, in the MMA thread's order).
+// shared memory, and K and V stream through rings of 64-column chunks (six for
+// K, four for V), filled by the two producer threads in their consumers' order.
 #include <atomic>
 
 #include "common.cuh"
@@ -50,7 +49,9 @@ constexpr int kQSt = 2, kKSt = 3, kVSt = 2;
 constexpr uint32_t kFChunk = 128 * 128;  // one 64-column (128-byte) slice of a 128-row tile
 constexpr uint32_t kFTmemCols = 512;
 constexpr uint32_t TF_S = 0;
-constexpr int kFRing = 10;  // chunk slots of the D = 256 layout (even: chunk pairs never wrap)
+// D = 256: K and V stream through rings of 64-column chunks (K: six slots, a
+// tile and a half; V: four slots, one tile, so a tile's chunk pairs never wrap)
+constexpr int kFKRing = 6, kFVRing = 4;
 
 // Per head-dimension layout: three S buffers and O at column 384 up to D = 128;
 // two S buffers and O at column 256 for the D = 256 tiles.
@@ -73,19 +74,18 @@ enum FBar : uint32_t {
   F_OFULL = F_PVDONE + 3,       // the unit's last O += P V done
   F_FINAL,
   F_FINAL2,                     // the O += P V issuer's own drain before TMEM is released
-  F_RFULL,                      // D = 256: chunk ring slots
-  F_REMPTY = F_RFULL + kFRing,
-  F_COUNT = F_REMPTY + kFRing
+  F_RFULL,                      // D = 256: K ring slots, then V ring slots (released by SFULL / PVDONE)
+  F_COUNT = F_RFULL + kFKRing + kFVRing
 };
 
 template <int D>
 struct FSmem {
   static constexpr uint32_t kTile = (D / 64) * kFChunk;
   static constexpr uint32_t kQ = 0;
-  // up to D = 128: Q, K and V stages; D = 256: one Q tile and the chunk ring at kK
+  // up to D = 128: Q, K and V tile stages; D = 256: one Q tile, the K and V chunk rings
   static constexpr uint32_t kK = kQ + (FCfg<D>::kWide ? 1 : kQSt) * kTile;
-  static constexpr uint32_t kV = kK + kKSt * kTile;
-  static constexpr uint32_t kBar = FCfg<D>::kWide ? kK + kFRing * kFChunk : kV + kVSt * kTile;
+  static constexpr uint32_t kV = kK + (FCfg<D>::kWide ? kFKRing * kFChunk : kKSt * kTile);
+  static constexpr uint32_t kBar = kV + (FCfg<D>::kWide ? kFVRing * kFChunk : kVSt * kTile);
   static constexpr uint32_t kTmemSlot = kBar + F_COUNT * 8;
   static constexpr uint32_t kAbort = kTmemSlot + 4;
   static constexpr uint32_t kTotal = kAbort + 4;
@@ -169,10 +169,7 @@ __global__ void __launch_bounds__(kFThreads, 1)
     mbar_init(bar(F_OFULL), 1);
     mbar_init(bar(F_FINAL), 1);
     mbar_init(bar(F_FINAL2), 1);
-    for (int r = 0; r < kFRing; ++r) {
-      mbar_init(bar(F_RFULL + r), 1);
-      mbar_init(bar(F_REMPTY + r), 1);
-    }
+    for (int r = 0; r < kFKRing + kFVRing; ++r) mbar_init(bar(F_RFULL + r), 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     fence_proxy_async_smem();
   }
@@ -190,49 +187,56 @@ __global__ void __launch_bounds__(kFThreads, 1)
     // D = 256: warp 0 fills the chunk ring.  Up to D = 128: warp 0 loads Q and K,
     // warp 3 loads V, so that a K load never waits behind the release of a V
     // stage (which comes one tile later, after O += P V).
-    if (lane == 0 && kWide && warp == 0) {
-      prefetch_tmap(&tmQ);
-      prefetch_tmap(&tmK);
-      prefetch_tmap(&tmV);
-      uint32_t qc = 0, q = 0;  // Q tiles and ring chunks whose loads were issued
+    if (lane == 0 && kWide) {
+      const bool loads_v = warp == 3;
+      prefetch_tmap(loads_v ? &tmV : &tmQ);
+      if (!loads_v) prefetch_tmap(&tmK);
+      uint32_t qc = 0, q = 0;  // Q tiles and chunks (K or V) whose loads were issued
+      const int ring = loads_v ? kFVRing : kFKRing;
+      const uint32_t base = loads_v ? L::kV : L::kK;
+      const uint32_t fbar = loads_v ? F_RFULL + kFKRing : F_RFULL;
       bool stop = false;
-      // one 64-column chunk into the next ring slot
-      auto ring_load = [&](const CUtensorMap* map, int col, int row, int head, int bb) -> bool {
-        const uint32_t r = q % kFRing, use = q / kFRing;
-        if (use > 0 && !wait1(bar(F_REMPTY + r), (use - 1) & 1, ctl, 0xA2000007u)) return false;
-        mbar_expect_tx(bar(F_RFULL + r), kFChunk);
-        tma_load_4d(sb + L::kK + r * kFChunk, map, bar(F_RFULL + r), col, row, head, bb);
-        ++q;
-        return true;
-      };
       for (int u = blockIdx.x; u < num_units && !stop; u += gridDim.x) {
         const FUnit un = fwd_unit(p, u, n_mt);
         if (!un.active || un.n_end == un.n_start) continue;
         const int bq = varlen ? 0 : un.b;
         const int hk = un.h / G;
-        if (qc > 0 && !wait1(bar(F_QEMPTY), (qc - 1) & 1, ctl, 0xA2000001u)) break;
-        mbar_expect_tx(bar(F_QFULL), L::kTile);
+        if (!loads_v) {
+          if (qc > 0 && !wait1(bar(F_QEMPTY), (qc - 1) & 1, ctl, 0xA2000001u)) break;
+          mbar_expect_tx(bar(F_QFULL), L::kTile);
 #pragma unroll
-        for (int c = 0; c < D / 64; ++c)
-          tma_load_4d(sb + L::kQ + c * kFChunk, &tmQ, bar(F_QFULL), c * 64,
-                      un.si.q_start + un.m * FBM, un.h, bq);
-        ++qc;
-        // K_n for S_n, then V_{n-1} for O += P V_{n-1}: the MMA thread's order
+          for (int c = 0; c < D / 64; ++c)
+            tma_load_4d(sb + L::kQ + c * kFChunk, &tmQ, bar(F_QFULL), c * 64,
+                        un.si.q_start + un.m * FBM, un.h, bq);
+          ++qc;
+        }
         for (int n = un.n_start; n < un.n_end && !stop; ++n) {
           const int krow = un.si.k_start + n * FBN;
-          for (int c = 0; c < D / 64 && !stop; ++c) stop = !ring_load(&tmK, c * 64, krow, hk, bq);
-          for (int c = 0; c < D / 64 && !stop && n > un.n_start; ++c)
-            stop = !ring_load(&tmV, c * 64, krow - FBN, hk, bq);
+          for (int c = 0; c < D / 64; ++c, ++q) {
+            const uint32_t r = q % ring;
+            if (q >= static_cast<uint32_t>(ring)) {
+              // the slot's previous chunk belonged to tile tp: free once S (K) or
+              // O += P V (V) of that tile is done.  Neither barrier can have moved
+              // on by a further phase: that would need chunks not yet loaded.
+              const uint32_t tp = (q - ring) / (D / 64);
+              const uint32_t rel = loads_v ? F_PVDONE : F_SFULL;
+              if (!wait1(bar(rel + tp % kSBufs), (tp / kSBufs) & 1, ctl, 0xA2000002u)) {
+                stop = true;
+                break;
+              }
+            }
+            mbar_expect_tx(bar(fbar + r), kFChunk);
+            tma_load_4d(sb + base + r * kFChunk, loads_v ? &tmV : &tmK, bar(fbar + r), c * 64,
+                        krow, hk, bq);
+          }
         }
-        const int klast = un.si.k_start + (un.n_end - 1) * FBN;
-        for (int c = 0; c < D / 64 && !stop; ++c) stop = !ring_load(&tmV, c * 64, klast, hk, bq);
         if (*abort_flag) break;
       }
       // Before exit, wait (bounded, ignoring the abort flag) for the copies that may
       // still be in flight: the last Q tile and the last issue into each ring slot.
       if (qc > 0) wait1(bar(F_QFULL), (qc - 1) & 1, ctl, 0xA2000004u, false);
-      for (uint32_t i = q > static_cast<uint32_t>(kFRing) ? q - kFRing : 0; i < q; ++i)
-        wait1(bar(F_RFULL + i % kFRing), (i / kFRing) & 1, ctl, 0xA2000005u, false);
+      for (uint32_t i = q > static_cast<uint32_t>(ring) ? q - ring : 0; i < q; ++i)
+        wait1(bar(fbar + i % ring), (i / ring) & 1, ctl, 0xA2000005u, false);
     } else if (lane == 0 && !kWide) {
       const bool loads_v = warp == 3;
       prefetch_tmap(loads_v ? &tmV : &tmQ);
@@ -310,33 +314,9 @@ __global__ void __launch_bounds__(kFThreads, 1)
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0 && kWide) {
+      // D = 256: S = Q K^T from the unit's Q tile and the K ring
       constexpr uint32_t kIdS = idesc_f16(kIsBf16, 0, 0, FBM, FBN);  // Q, K both K-major
-      constexpr uint32_t kIdPV = idesc_f16(kIsBf16, 0, 1, FBM, 128);  // P from TMEM, V halves
-      uint32_t qc = 0, q = 0, it = 0;  // Q tiles, ring chunks consumed, S tiles
-      auto ring_wait = [&](uint32_t qq) -> bool {
-        return wait1(bar(F_RFULL + qq % kFRing), (qq / kFRing) & 1, ctl, 0xA2000016u);
-      };
-      auto slot = [&](uint32_t qq) -> uint32_t { return sb + L::kK + (qq % kFRing) * kFChunk; };
-      // O += P V of tile t: two N = 128 halves, B = V chunk pairs of the ring
-      auto issue_pv = [&](uint32_t t, bool first) -> bool {
-        const uint32_t buf = t % kSBufs;
-        if (!wait1(bar(F_PREADY + buf), (t / kSBufs) & 1, ctl, 0xA2000011u)) return false;
-        for (int pr = 0; pr < D / 128; ++pr) {
-          const uint32_t q0 = q + 2 * pr;
-          if (!ring_wait(q0) || !ring_wait(q0 + 1)) return false;
-          tc_fence_after();
-#pragma unroll
-          for (int kk = 0; kk < FBN / 16; ++kk)
-            mma_ts(tmem + TF_O + 128 * pr, tmem + TF_S + buf * 128 + kk * 8,
-                   sdesc_sw128(slot(q0) + kk * 2048, kFChunk, 1024), kIdPV,
-                   (!first || kk > 0) ? 1u : 0u);
-          tc_commit(bar(F_REMPTY + q0 % kFRing));
-          tc_commit(bar(F_REMPTY + (q0 + 1) % kFRing));
-        }
-        q += D / 64;
-        tc_commit(bar(F_PVDONE + buf));
-        return true;
-      };
+      uint32_t qc = 0, it = 0, q = 0;  // Q tiles, S tiles, K ring chunks consumed
       for (int u = blockIdx.x; u < num_units; u += gridDim.x) {
         const FUnit un = fwd_unit(p, u, n_mt);
         if (!un.active || un.n_end == un.n_start) continue;
@@ -349,20 +329,18 @@ __global__ void __launch_bounds__(kFThreads, 1)
               !wait1(bar(F_PVDONE + buf), ((t - kSBufs) / kSBufs) & 1, ctl, 0xA2000014u))
             goto mma_exit_w;
           for (int c = 0; c < D / 64; ++c, ++q) {
-            if (!ring_wait(q)) goto mma_exit_w;
+            if (!wait1(bar(F_RFULL + q % kFKRing), (q / kFKRing) & 1, ctl, 0xA2000016u))
+              goto mma_exit_w;
             tc_fence_after();
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk)
               mma_ss(tmem + TF_S + buf * 128, sdesc_sw128(sb + L::kQ + c * kFChunk + kk * 32, 16, 1024),
-                     sdesc_sw128(slot(q) + kk * 32, 16, 1024), kIdS, (c > 0 || kk > 0) ? 1u : 0u);
-            tc_commit(bar(F_REMPTY + q % kFRing));
+                     sdesc_sw128(sb + L::kK + (q % kFKRing) * kFChunk + kk * 32, 16, 1024), kIdS,
+                     (c > 0 || kk > 0) ? 1u : 0u);
           }
-          tc_commit(bar(F_SFULL + buf));
+          tc_commit(bar(F_SFULL + buf));  // also frees the tile's K ring slots
           if (j == nt - 1) tc_commit(bar(F_QEMPTY));
-          if (j > 0 && !issue_pv(t - 1, j == 1)) goto mma_exit_w;
         }
-        if (!issue_pv(it + nt - 1, nt == 1)) goto mma_exit_w;
-        tc_commit(bar(F_OFULL));
         it += nt;
         ++qc;
       }
@@ -412,11 +390,13 @@ __global__ void __launch_bounds__(kFThreads, 1)
       tc_commit(bar(F_FINAL));
       wait1(bar(F_FINAL), 0, ctl, 0xA200001Fu, false);
     }
-  } else if (warp == 2 && !kWide) {
+  } else if (warp == 2) {
     if (lane == 0) {
       // ---------------------------------------------------- O += P V issuer
-      constexpr uint32_t kIdPV = idesc_f16(kIsBf16, 0, 1, FBM, kWide ? 128 : D);  // P from TMEM, V MN-major
-      uint32_t it = 0;
+      // (D = 256: O in two N = 128 halves, V chunk pairs from the V ring)
+      constexpr uint32_t kIdPV =
+          idesc_f16(kIsBf16, 0, 1, FBM, kWide ? 128 : D);  // P from TMEM, V MN-major
+      uint32_t it = 0, q = 0;  // P tiles; D = 256: V ring chunks consumed
       for (int u = blockIdx.x; u < num_units; u += gridDim.x) {
         const FUnit un = fwd_unit(p, u, n_mt);
         if (!un.active || un.n_end == un.n_start) continue;
@@ -425,14 +405,32 @@ __global__ void __launch_bounds__(kFThreads, 1)
           const uint32_t t = it + j;
           const uint32_t buf = t % kSBufs, vs = t % kVSt;
           if (!wait1(bar(F_PREADY + buf), (t / kSBufs) & 1, ctl, 0xA2000011u)) goto pv_exit;
-          if (!wait1(bar(F_VFULL + vs), (t / kVSt) & 1, ctl, 0xA2000012u)) goto pv_exit;
-          tc_fence_after();
-          const uint32_t sV = sb + L::kV + vs * L::kTile;
+          if (kWide) {
+#pragma unroll 1
+            for (int pr = 0; pr < D / 128; ++pr, q += 2) {
+              const uint32_t r0 = kFKRing + q % kFVRing;
+              if (!wait1(bar(F_RFULL + r0), (q / kFVRing) & 1, ctl, 0xA2000012u) ||
+                  !wait1(bar(F_RFULL + r0 + 1), ((q + 1) / kFVRing) & 1, ctl, 0xA2000012u))
+                goto pv_exit;
+              tc_fence_after();
+              const uint32_t sV = sb + L::kV + (q % kFVRing) * kFChunk;
 #pragma unroll
-          for (int kk = 0; kk < FBN / 16; ++kk)
-            mma_ts(tmem + TF_O, tmem + TF_S + buf * 128 + kk * 8,
-                   sdesc_sw128(sV + kk * 2048, kFChunk, 1024), kIdPV, (j > 0 || kk > 0) ? 1u : 0u);
-          tc_commit(bar(F_PVDONE + buf));  // also frees V stage vs for the V producer
+              for (int kk = 0; kk < FBN / 16; ++kk)
+                mma_ts(tmem + TF_O + 128 * pr, tmem + TF_S + buf * 128 + kk * 8,
+                       sdesc_sw128(sV + kk * 2048, kFChunk, 1024), kIdPV,
+                       (j > 0 || kk > 0) ? 1u : 0u);
+            }
+          } else {
+            if (!wait1(bar(F_VFULL + vs), (t / kVSt) & 1, ctl, 0xA2000012u)) goto pv_exit;
+            tc_fence_after();
+            const uint32_t sV = sb + L::kV + vs * L::kTile;
+#pragma unroll
+            for (int kk = 0; kk < FBN / 16; ++kk)
+              mma_ts(tmem + TF_O, tmem + TF_S + buf * 128 + kk * 8,
+                     sdesc_sw128(sV + kk * 2048, kFChunk, 1024), kIdPV,
+                     (j > 0 || kk > 0) ? 1u : 0u);
+          }
+          tc_commit(bar(F_PVDONE + buf));  // also frees the tile's V stage / V ring slots
         }
         tc_commit(bar(F_OFULL));
         it += nt;
