@@ -154,6 +154,58 @@ class ClockSampler:
                 "samples": len(rows), "power_w_max": max(pw) if pw else None}
 
 
+class DeviceRounds:
+    """Device time of rounds of work enqueued from the host.
+
+    Each chunk of rounds is queued behind a device-side sleep that outlasts the
+    host's enqueue time for that chunk, so no launch waits for the host and the
+    events bracket device time only (on small problems a Python-level call takes
+    longer than the kernels it launches).  Chunks keep the launch queue short.
+    When the step's resident data would fit in L2 (under twice its size), every
+    round first overwrites a buffer of twice the L2 size, outside the events, so
+    each timed round starts with a cold L2.
+    """
+
+    CHUNK = 32
+    SLEEP_HZ = 2.2e9  # cycles per second of the device sleep: at most the SM clock
+
+    def __init__(self, stream, one_round, resident_bytes: int, dev):
+        self.stream = stream
+        self.flush = (torch.empty(2 * L2_BYTES, dtype=torch.uint8, device=dev)
+                      if resident_bytes < 2 * L2_BYTES else None)
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        for _ in range(3):
+            if self.flush is not None:
+                self.flush.zero_()
+            one_round()
+        self.host_s = (time.perf_counter() - t0) / 3
+        torch.cuda.synchronize()
+
+    def l2_note(self, resident_bytes: int) -> str:
+        if self.flush is None:
+            return "inputs larger than L2 (%.0f MB resident per step)" % (resident_bytes / 1e6)
+        return ("L2 flushed before every timed step (%.0f MB resident per step, %d MB written)"
+                % (resident_bytes / 1e6, 2 * L2_BYTES // 2 ** 20))
+
+    def run(self, n: int, body, n_events: int):
+        """Runs body(events) n times; `events` holds n_events timing events that
+        body records around its stages.  Returns the per-round event lists."""
+        rounds = []
+        i = 0
+        while i < n:
+            m = min(self.CHUNK, n - i)
+            torch.cuda._sleep(int((1.5 * m * self.host_s + 5e-4) * self.SLEEP_HZ))
+            for _ in range(m):
+                ev = [torch.cuda.Event(enable_timing=True) for _ in range(n_events)]
+                if self.flush is not None:
+                    self.flush.zero_()
+                body(ev)
+                rounds.append(ev)
+            i += m
+        return rounds
+
+
 def dist_setup(n_gpus: int):
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -219,30 +271,37 @@ def run_ours(args):
     for _ in range(args.warmup):
         step()
     ab.check_device_status()
+    resident = in_bytes + sum(t.numel() * t.element_size() for t in (dq, dk, dv)) + \
+        ws.numel() * ws.element_size()
+    timer = DeviceRounds(stream, step, resident, dev)
 
-    # --- timed region: K steps, device-resident inputs
+    def whole(ev):
+        ev[0].record(stream)
+        step()
+        ev[1].record(stream)
+
+    def staged(ev):
+        ev[0].record(stream)
+        ab.attn_bwd(q, k, v, o, lse, do, stream=stream, stage="pre", **kw)
+        ev[1].record(stream)
+        ab.attn_bwd(q, k, v, o, lse, do, stream=stream, stage="main", **kw)
+        ev[2].record(stream)
+        ab.attn_bwd(q, k, v, o, lse, do, stream=stream, stage="post", **kw)
+        ev[3].record(stream)
+
+    # --- timed region: K steps, device-resident inputs, device time of each step
+    torch.cuda.synchronize()
     barrier(dist)
     with ClockSampler(local) as clk:
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        for _ in range(args.steps):
-            step()
-        e1.record(stream)
+        steps_ev = timer.run(args.steps, whole, 2)
+        torch.cuda.synchronize()
         barrier(dist)
         # per-kernel times over the same number of steps (events on the launch stream)
-        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
-        for i in range(args.steps):
-            ev = evs[i]
-            ev[0].record(stream)
-            ab.attn_bwd(q, k, v, o, lse, do, stream=stream, stage="pre", **kw)
-            ev[1].record(stream)
-            ab.attn_bwd(q, k, v, o, lse, do, stream=stream, stage="main", **kw)
-            ev[2].record(stream)
-            ab.attn_bwd(q, k, v, o, lse, do, stream=stream, stage="post", **kw)
-            ev[3].record(stream)
+        evs = timer.run(args.steps, staged, 4)
+        torch.cuda.synchronize()
         barrier(dist)
     ab.check_device_status()
-    ms = e0.elapsed_time(e1) / args.steps
+    ms = statistics.mean(e[0].elapsed_time(e[1]) for e in steps_ev)
     ms_max = max_over_ranks(ms, dist)
     t_pre = statistics.mean(e[0].elapsed_time(e[1]) for e in evs)
     t_main = statistics.mean(e[1].elapsed_time(e[2]) for e in evs)
@@ -313,7 +372,8 @@ def run_ours(args):
     cfg = {"workload": w.name, "batch": w.batch if not w.varlen else len(x.lengths),
            "h_q": w.h_q, "h_k": w.h_k, "seqlen": w.seqlen_q if not w.varlen else "varlen",
            "head_dim": w.head_dim, "causal": w.causal, "deterministic": det,
-           "l2": "inputs larger than L2 (%.0f MB resident per step)" % (in_bytes / 1e6),
+           "l2": timer.l2_note(resident),
+           "timing": "device time per step (CUDA events; launches queued ahead of the device)",
            "parallelism": f"replicas x{world}" if world > 1 else "single GPU"}
     if w.varlen:
         cfg["lengths"] = x.lengths
@@ -383,16 +443,22 @@ def run_ours_fwd(args):
     for _ in range(args.warmup):
         step()
     ab.check_device_status()
+    resident = in_bytes + o.numel() * o.element_size() + lse.numel() * lse.element_size()
+    timer = DeviceRounds(stream, step, resident, dev)
+
+    def whole(ev):
+        ev[0].record(stream)
+        step()
+        ev[1].record(stream)
+
+    torch.cuda.synchronize()
     barrier(dist)
     with ClockSampler(local) as clk:
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        for _ in range(args.steps):
-            step()
-        e1.record(stream)
+        steps_ev = timer.run(args.steps, whole, 2)
+        torch.cuda.synchronize()
         barrier(dist)
     ab.check_device_status()
-    ms = e0.elapsed_time(e1) / args.steps
+    ms = statistics.mean(e[0].elapsed_time(e[1]) for e in steps_ev)
     ms_max = max_over_ranks(ms, dist)
 
     # end to end: pinned host Q, K, V -> device -> attn_fwd -> pinned host O, LSE
@@ -432,7 +498,8 @@ def run_ours_fwd(args):
     cfg = {"workload": w.name, "pass": "forward", "batch": w.batch if not w.varlen else len(x.lengths),
            "h_q": w.h_q, "h_k": w.h_k, "seqlen": w.seqlen_q if not w.varlen else "varlen",
            "head_dim": w.head_dim, "causal": w.causal,
-           "l2": "inputs larger than L2 (%.0f MB resident per step)" % (in_bytes / 1e6),
+           "l2": timer.l2_note(resident),
+           "timing": "device time per step (CUDA events; launches queued ahead of the device)",
            "parallelism": f"replicas x{world}" if world > 1 else "single GPU"}
     if w.varlen:
         cfg["lengths"] = x.lengths
