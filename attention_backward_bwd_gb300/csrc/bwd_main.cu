@@ -36,11 +36,14 @@
 //   [  0,128) S^T fp32; each column group keeps its packed P^T in the first half
 //             of the S^T columns it has read itself
 //   [128,256) dP^T fp32, then dQ in [128,128+D)
-//   [256,256+D) dK, [384,384+D) dV
+//   [256,256+D) dK, [384,384+D) dV; at D = 64 a second pair at [320,384) and
+//   [448,512) for every other unit
 // dS^T goes to a swizzled shared-memory tile read by both the dQ and dK MMAs.
 // The tensor pipe runs dP, dV, then the next tile's S (as soon as dV and the
 // dS phase have read P^T), then dQ and dK; dP of the next tile waits for the dQ
-// drain to have read dQ out of TMEM.
+// drain to have read dQ out of TMEM.  At D = 64 the K/V tiles and dK/dV are
+// double-buffered across units, so the next unit's K/V load during this one
+// and the last tile of a unit issues the next unit's first S like any other.
 // Every mbarrier wait is bounded (see WaitCtl): on timeout the kernel records
 // the site in the status word and unwinds.
 #include <atomic>
@@ -104,7 +107,11 @@ enum Bar : uint32_t {
   B_UNITEMPTY = B_UNITFULL + 2,    // 2 slots: every consumer role has read it
   B_FINAL = B_UNITEMPTY + 2,
   B_FULLQ2,                        // 2 slots: second head-dim chunk of the Q tile (D = 128)
-  B_COUNT = B_FULLQ2 + kStages
+  B_KVFULL1 = B_FULLQ2 + kStages,  // second K/V slot and dK/dV buffer (D = 64)
+  B_KVEMPTY1,
+  B_DKDVFULL1,
+  B_DKDVFREE1,
+  B_COUNT
 };
 
 template <int D>
@@ -121,16 +128,26 @@ struct Smem {
   static constexpr uint32_t kRing = kBar + B_COUNT * 8;  // 2 x int32 unit ring
   static constexpr uint32_t kTmemSlot = kRing + 8;
   static constexpr uint32_t kAbort = kTmemSlot + 4;
-  static constexpr uint32_t kTotal = kAbort + 4;
+  // D = 64: a second K/V slot, so that the next unit's K/V load while this unit
+  // runs (its dK/dV accumulate in a second TMEM range meanwhile)
+  static constexpr uint32_t kKVSlots = D == 64 ? 2 : 1;
+  static constexpr uint32_t kK1 = (kAbort + 4 + 1023) / 1024 * 1024;
+  static constexpr uint32_t kV1 = kK1 + kTile;
+  // D = 64: the dQ drain warps also write dK/dV, staged here as 32-row boxes
+  static constexpr uint32_t kEpi = kV1 + kTile;
+  static constexpr uint32_t kTotal = kKVSlots == 2 ? kEpi + 2 * 128 * D * 2 : kAbort + 4;
 };
 static_assert(Smem<128>::kTotal <= 232448, "shared memory budget");
+static_assert(Smem<64>::kTotal <= 232448, "shared memory budget");
 
 template <typename T, int D, bool kCap, bool kLeft>
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_main_kernel(const BwdParams p, const __grid_constant__ CUtensorMap tmQ,
                     const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                     const __grid_constant__ CUtensorMap tmDO,
-                    const __grid_constant__ CUtensorMap tmDQ) {
+                    const __grid_constant__ CUtensorMap tmDQ,
+                    const __grid_constant__ CUtensorMap tmDK,
+                    const __grid_constant__ CUtensorMap tmDV) {
   using L = Smem<D>;
   extern __shared__ __align__(1024) unsigned char smem[];
   if (p.input_bad != nullptr && *p.input_bad) return;
@@ -176,12 +193,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(bar(B_DQFREE), 4);
     mbar_init(bar(B_DKDONE), 1);
     mbar_init(bar(B_DKDVFULL), 1);
-    mbar_init(bar(B_DKDVFREE), kSoftmaxWarps);
+    // the dK/dV epilogue: the softmax warps, or at D = 64 the 4 dQ drain warps
+    mbar_init(bar(B_DKDVFREE), L::kKVSlots == 2 ? 4 : kSoftmaxWarps);
     for (int k = 0; k < 2; ++k) {
       mbar_init(bar(B_UNITFULL + k), 1);
       mbar_init(bar(B_UNITEMPTY + k), 1 + kSoftmaxWarps + 4);  // MMA + softmax + drain warps
     }
     mbar_init(bar(B_FINAL), 1);
+    if (L::kKVSlots == 2) {
+      mbar_init(bar(B_KVFULL1), 1);
+      mbar_init(bar(B_KVEMPTY1), 1);
+      mbar_init(bar(B_DKDVFULL1), 1);
+      mbar_init(bar(B_DKDVFREE1), 4);
+    }
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     fence_proxy_async_smem();
   }
@@ -240,16 +264,22 @@ __global__ void __launch_bounds__(kThreads, 1)
         const Unit un = get_unit(p, u, G, wleft);
         u = u_next;
         if (un.n_iters == 0) continue;
-        if (uc > 0 && !wait1(bar(B_KVEMPTY), (uc - 1) & 1, ctl, 0xA0000001u)) break;
+        // unit uc takes K/V slot uc % kKVSlots, freed by the unit kKVSlots before it
+        const uint32_t kvs = uc % L::kKVSlots, kvuse = uc / L::kKVSlots;
+        if (kvuse > 0 &&
+            !wait1(bar(kvs ? B_KVEMPTY1 : B_KVEMPTY), (kvuse - 1) & 1, ctl, 0xA0000001u))
+          break;
         ++uc;
         {
           const int krow = un.si.k_start + un.n * BN;
           const int bk = varlen ? 0 : un.b;
-          mbar_expect_tx(bar(B_KVFULL), 2 * L::kTile);
+          const uint32_t kvfull = bar(kvs ? B_KVFULL1 : B_KVFULL);
+          const uint32_t sK = sb + (kvs ? L::kK1 : L::kK), sV = sb + (kvs ? L::kV1 : L::kV);
+          mbar_expect_tx(kvfull, 2 * L::kTile);
 #pragma unroll
           for (int c = 0; c < D / 64; ++c) {
-            tma_load_4d(sb + L::kK + c * kChunk, &tmK, bar(B_KVFULL), c * 64, krow, un.g, bk);
-            tma_load_4d(sb + L::kV + c * kChunk, &tmV, bar(B_KVFULL), c * 64, krow, un.g, bk);
+            tma_load_4d(sK + c * kChunk, &tmK, kvfull, c * 64, krow, un.g, bk);
+            tma_load_4d(sV + c * kChunk, &tmV, kvfull, c * 64, krow, un.g, bk);
           }
         }
         for (int j = 0; j < un.n_iters; ++j, ++it) {
@@ -296,7 +326,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       // Before exit, wait (bounded, ignoring the abort flag) until every copy this
       // thread issued has landed, so no TMA write targets a finished CTA.
-      if (uc > 0) wait1(bar(B_KVFULL), (uc - 1) & 1, ctl, 0xA0000003u, false);
+      for (uint32_t d = 1; d <= L::kKVSlots && d <= uc; ++d) {  // the last K/V loads of each slot
+        const uint32_t v = uc - d;
+        wait1(bar(v % L::kKVSlots ? B_KVFULL1 : B_KVFULL), (v / L::kKVSlots) & 1, ctl, 0xA0000003u,
+              false);
+      }
       for (uint32_t s = 0; s < kStages && s < it; ++s) {
         const uint32_t last = (it - 1 - s) / kStages;  // uses of stage (it-1-s) % kStages
         const uint32_t st = (it - 1 - s) % kStages;
@@ -317,7 +351,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr uint32_t kIdKV = idesc_f16(kIsBf16, 0, 1, BN, D);
       constexpr uint32_t kIdDQ = idesc_f16(kIsBf16, 1, 1, BM, D);
       // S^T = K Q^T   (M = keys, N = queries, K = head dim; both K-major)
-      auto issue_s = [&](uint32_t sQ, uint32_t st, uint32_t ph) -> bool {
+      auto issue_s = [&](uint32_t sK, uint32_t sQ, uint32_t st, uint32_t ph) -> bool {
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           if (kSplitQ && kk == 4) {  // the second head-dim chunk of Q lands separately
@@ -325,8 +359,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_after();
           }
           const uint32_t koff = (kk >> 2) * kChunk + (kk & 3) * 32;
-          mma_ss(tmem + TM_S, sdesc_sw128(sb + L::kK + koff, 16, 1024),
-                 sdesc_sw128(sQ + koff, 16, 1024), kIdS, kk > 0);
+          mma_ss(tmem + TM_S, sdesc_sw128(sK + koff, 16, 1024), sdesc_sw128(sQ + koff, 16, 1024),
+                 kIdS, kk > 0);
         }
         tc_commit(bar(B_SFULL));
         return true;
@@ -338,20 +372,35 @@ __global__ void __launch_bounds__(kThreads, 1)
                wait1(bar(B_PREAD), prev & 1, ctl, 0xA0000019u);
       };
       uint32_t it = 0, uc = 0;
+      // With two K/V slots the last tile of a unit also issues the next unit's
+      // first S^T (its K is already in the other slot): that unit is then taken
+      // early (pk) and its S^T not issued again (s_pre).
+      int u_pk = 0;
+      bool pk = false, s_pre = false;
       for (uint32_t k = 0;; ++k) {
         int u;
-        if (!take_unit(k, false, u)) goto mma_exit;
+        if (pk) {
+          u = u_pk;
+          pk = false;
+        } else if (!take_unit(k, false, u)) {
+          goto mma_exit;
+        }
         if (u >= num_units) break;
         const Unit un = get_unit(p, u, G, wleft);
         if (un.n_iters == 0) continue;
-        if (!wait1(bar(B_KVFULL), uc & 1, ctl, 0xA0000011u)) goto mma_exit;
-        {
+        const uint32_t kvs = uc % L::kKVSlots;
+        const uint32_t sK = sb + (kvs ? L::kK1 : L::kK), sV = sb + (kvs ? L::kV1 : L::kV);
+        const uint32_t tDK = tmem + TM_DK + kvs * 64, tDV = tmem + TM_DV + kvs * 64;
+        if (!s_pre) {
+          if (!wait1(bar(kvs ? B_KVFULL1 : B_KVFULL), (uc / L::kKVSlots) & 1, ctl, 0xA0000011u))
+            goto mma_exit;
           const uint32_t s = it % kStages;
           if (!wait1(bar(B_FULLQ + s), (it / kStages) & 1, ctl, 0xA0000013u)) goto mma_exit;
           if (it > 0 && !wait_p_consumed(it - 1)) goto mma_exit;
           tc_fence_after();
-          if (!issue_s(sb + L::kQ + s * L::kTile, s, (it / kStages) & 1)) goto mma_exit;
+          if (!issue_s(sK, sb + L::kQ + s * L::kTile, s, (it / kStages) & 1)) goto mma_exit;
         }
+        s_pre = false;
         for (int j = 0; j < un.n_iters; ++j, ++it) {
           const uint32_t s = it % kStages;
           const uint32_t ph = (it / kStages) & 1;
@@ -365,19 +414,21 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
             const uint32_t koff = (kk >> 2) * kChunk + (kk & 3) * 32;
-            mma_ss(tmem + TM_DP, sdesc_sw128(sb + L::kV + koff, 16, 1024),
-                   sdesc_sw128(sDO + koff, 16, 1024), kIdS, kk > 0);
+            mma_ss(tmem + TM_DP, sdesc_sw128(sV + koff, 16, 1024), sdesc_sw128(sDO + koff, 16, 1024),
+                   kIdS, kk > 0);
           }
           tc_commit(bar(B_DPFULL));
           // dV += P^T dO   (A = P^T from TMEM, B = dO MN-major, K = queries)
           if (!wait1(bar(B_PREADY), it & 1, ctl, 0xA0000017u)) goto mma_exit;
           // the previous unit's epilogue must have read dK/dV before they restart
-          if (j == 0 && uc > 0 && !wait1(bar(B_DKDVFREE), (uc - 1) & 1, ctl, 0xA0000012u))
+          if (j == 0 && uc >= L::kKVSlots &&
+              !wait1(bar(kvs ? B_DKDVFREE1 : B_DKDVFREE), ((uc / L::kKVSlots) - 1) & 1, ctl,
+                     0xA0000012u))
             goto mma_exit;
           tc_fence_after();
 #pragma unroll
           for (int kk = 0; kk < BM / 16; ++kk)
-            mma_ts(tmem + TM_DV, tmem + TM_P + (16 * kk / kCols) * kCols + (16 * kk % kCols) / 2,
+            mma_ts(tDV, tmem + TM_P + (16 * kk / kCols) * kCols + (16 * kk % kCols) / 2,
                    sdesc_sw128(sDO + kk * 2048, kChunk, 1024),
                    kIdKV, (j > 0 || kk > 0) ? 1u : 0u);
           tc_commit(bar(B_PVDONE));
@@ -390,7 +441,26 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!wait1(bar(B_FULLQ + s1), ((it + 1) / kStages) & 1, ctl, 0xA000001Au))
               goto mma_exit;
             tc_fence_after();
-            if (!issue_s(sb + L::kQ + s1 * L::kTile, s1, ((it + 1) / kStages) & 1)) goto mma_exit;
+            if (!issue_s(sK, sb + L::kQ + s1 * L::kTile, s1, ((it + 1) / kStages) & 1))
+              goto mma_exit;
+          } else if constexpr (L::kKVSlots == 2) {
+            // the next unit's first S^T, from the other K/V slot
+            if (!take_unit(k + 1, false, u_pk)) goto mma_exit;
+            pk = true;
+            if (u_pk < num_units && get_unit(p, u_pk, G, wleft).n_iters > 0) {
+              const uint32_t kvs2 = (uc + 1) % 2;
+              const uint32_t s1 = (it + 1) % kStages;
+              if (!wait1(bar(kvs2 ? B_KVFULL1 : B_KVFULL), ((uc + 1) / 2) & 1, ctl, 0xA000001Cu))
+                goto mma_exit;
+              if (!wait_p_consumed(it)) goto mma_exit;
+              if (!wait1(bar(B_FULLQ + s1), ((it + 1) / kStages) & 1, ctl, 0xA000001Du))
+                goto mma_exit;
+              tc_fence_after();
+              if (!issue_s(sb + (kvs2 ? L::kK1 : L::kK), sb + L::kQ + s1 * L::kTile, s1,
+                           ((it + 1) / kStages) & 1))
+                goto mma_exit;
+              s_pre = true;
+            }
           }
           if (!wait1(bar(B_DSREADY), it & 1, ctl, 0xA0000018u)) goto mma_exit;
           tc_fence_after();
@@ -398,20 +468,20 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int kk = 0; kk < BN / 16; ++kk)
             mma_ss(tmem + TM_DQ, sdesc_sw128(sb + L::kDS + kk * 2048, kChunk, 1024),
-                   sdesc_sw128(sb + L::kK + kk * 2048, kChunk, 1024), kIdDQ, kk > 0);
+                   sdesc_sw128(sK + kk * 2048, kChunk, 1024), kIdDQ, kk > 0);
           tc_commit(bar(B_DQFULL));
           // dK += dS^T Q   (A = dS^T K-major from the dS^T tile, B = Q MN-major)
 #pragma unroll
           for (int kk = 0; kk < BM / 16; ++kk) {
             const uint32_t koff = (kk >> 2) * kChunk + (kk & 3) * 32;
-            mma_ss(tmem + TM_DK, sdesc_sw128(sb + L::kDS + koff, 16, 1024),
+            mma_ss(tDK, sdesc_sw128(sb + L::kDS + koff, 16, 1024),
                    sdesc_sw128(sQ + kk * 2048, kChunk, 1024), kIdKV, (j > 0 || kk > 0) ? 1u : 0u);
           }
           tc_commit(bar(B_DKDONE));
           tc_commit(bar(B_EMPTY + s));
         }
-        tc_commit(bar(B_DKDVFULL));
-        tc_commit(bar(B_KVEMPTY));
+        tc_commit(bar(kvs ? B_DKDVFULL1 : B_DKDVFULL));
+        tc_commit(bar(kvs ? B_KVEMPTY1 : B_KVEMPTY));
         ++uc;
       }
     mma_exit:
@@ -605,34 +675,37 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
         if (lane == 0) mbar_arrive(bar(B_DSREADY));
       }
-      // ---- epilogue: this group's columns of dK = scale * acc or dV = acc
-      if (!wait_warp(bar(B_DKDVFULL), uc & 1, ctl, 0xA0000025u)) goto done;
-      tc_fence_after();
-      {
-        const uint32_t src = (writes_dk ? TM_DK : TM_DV) + e0;
-        const float mul = writes_dk ? p.scale : 1.0f;
+      // ---- epilogue: this group's columns of dK = scale * acc or dV = acc (with
+      // two K/V slots the dQ drain warps write dK/dV instead)
+      if constexpr (L::kKVSlots == 1) {
+        if (!wait_warp(bar(B_DKDVFULL), uc & 1, ctl, 0xA0000025u)) goto done;
+        tc_fence_after();
+        {
+          const uint32_t src = (writes_dk ? TM_DK : TM_DV) + e0;
+          const float mul = writes_dk ? p.scale : 1.0f;
 #pragma unroll 1
-        for (int c = 0; c < eCols / 32; ++c) {
-          uint32_t a[32];
-          tmem_ld32(tl + src + c * 32, a);
-          tmem_wait_ld();
-          if (key_ok) {
+          for (int c = 0; c < eCols / 32; ++c) {
+            uint32_t a[32];
+            tmem_ld32(tl + src + c * 32, a);
+            tmem_wait_ld();
+            if (key_ok) {
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-              uint4 o;
-              o.x = Pack<T>::two(__uint_as_float(a[8 * q + 0]) * mul, __uint_as_float(a[8 * q + 1]) * mul);
-              o.y = Pack<T>::two(__uint_as_float(a[8 * q + 2]) * mul, __uint_as_float(a[8 * q + 3]) * mul);
-              o.z = Pack<T>::two(__uint_as_float(a[8 * q + 4]) * mul, __uint_as_float(a[8 * q + 5]) * mul);
-              o.w = Pack<T>::two(__uint_as_float(a[8 * q + 6]) * mul, __uint_as_float(a[8 * q + 7]) * mul);
-              if (e0 + c * 32 + 8 * q < p.head_dim)  // a padded head dimension stops early
-                reinterpret_cast<uint4*>(out_row + c * 32)[q] = o;
+              for (int q = 0; q < 4; ++q) {
+                uint4 o;
+                o.x = Pack<T>::two(__uint_as_float(a[8 * q + 0]) * mul, __uint_as_float(a[8 * q + 1]) * mul);
+                o.y = Pack<T>::two(__uint_as_float(a[8 * q + 2]) * mul, __uint_as_float(a[8 * q + 3]) * mul);
+                o.z = Pack<T>::two(__uint_as_float(a[8 * q + 4]) * mul, __uint_as_float(a[8 * q + 5]) * mul);
+                o.w = Pack<T>::two(__uint_as_float(a[8 * q + 6]) * mul, __uint_as_float(a[8 * q + 7]) * mul);
+                if (e0 + c * 32 + 8 * q < p.head_dim)  // a padded head dimension stops early
+                  reinterpret_cast<uint4*>(out_row + c * 32)[q] = o;
+              }
             }
           }
         }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(B_DKDVFREE));
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar(B_DKDVFREE));
       ++uc;
     }
   } else {
@@ -650,6 +723,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     // this query tile (0..n-1, or from the first one inside a left window) have
     // completed their adds to the warp's 32 rows (one arrival each on the
     // semaphore of those rows) and releases once its own adds have completed.
+    // With two K/V slots (D = 64) these warps also write each unit's dK and dV
+    // once its last tile is drained (the epilogue below), so that the softmax
+    // warps go straight on to the next unit.
     const uint32_t quad = warp & 3;
     const uint32_t tl = tmem + ((quad * 32) << 16);
     // Per warp and pass: kBoxes boxes of 32 rows x 32 fp32 columns (4 KB each);
@@ -658,7 +734,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     constexpr int kPassCols = 32 * kBoxes;
     constexpr int kPasses = D / kPassCols;
     static_assert(4 * kBoxes * 4096 == L::kTile, "dQ staging must fit the dO stage");
-    uint32_t it = 0;
+    uint32_t it = 0, uc = 0;
     for (uint32_t k = 0;; ++k) {
       int u;
       if (!take_unit(k, true, u)) goto done;
@@ -761,11 +837,80 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
         if (lane == 0) mbar_arrive(bar(B_EMPTYDO + s));
       }
+      if constexpr (L::kKVSlots == 2) {
+        // ---- epilogue: rows [32 quad, +32) of dK = scale * acc and dV = acc from
+        // the unit's TMEM buffer.  A key tile wholly inside the sequence is staged
+        // as two 32-row x 64-column boxes (128-byte rows, 128-byte swizzle) and
+        // leaves through TMA tile stores (whole lines, and no per-row stores in
+        // the load/store pipe every warp's barrier operations use); a ragged tile
+        // stores per row and stops at the sequence end.
+        const uint32_t kvs = uc % 2;
+        const uint32_t stg = L::kEpi + quad * 8192;  // dK box, then dV box
+        const int key = un.n * BN + static_cast<int>(quad) * 32 + static_cast<int>(lane);
+        const bool tile_store = un.n * BN + BN <= un.si.sk;
+        if (!wait_warp(bar(kvs ? B_DKDVFULL1 : B_DKDVFULL), (uc / 2) & 1, ctl, 0xA0000035u))
+          goto done;
+        tc_fence_after();
+        if (lane == 0) bulk_wait_read_all();  // the previous unit's stores have read the staging
+        __syncwarp();
+#pragma unroll 1
+        for (int t = 0; t < 2; ++t) {
+          const TensorArg& outp = t == 0 ? p.dk : p.dv;
+          const float mul = t == 0 ? p.scale : 1.0f;
+#pragma unroll 1
+          for (int c = 0; c < D / 32; ++c) {
+            uint32_t a[32];
+            tmem_ld32(tl + (t == 0 ? TM_DK : TM_DV) + kvs * 64 + c * 32, a);
+            tmem_wait_ld();
+            uint32_t o[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i)
+              o[i] = Pack<T>::two(__uint_as_float(a[2 * i]) * mul,
+                                  __uint_as_float(a[2 * i + 1]) * mul);
+            if (tile_store) {
+              // columns [32 c, 32 c + 32): 16-byte units 4 c .. 4 c + 3 of the row
+              const uint32_t row = stg + t * 4096 + lane * 128;
+#pragma unroll
+              for (int q = 0; q < 4; ++q)
+                *reinterpret_cast<uint4*>(smem + row + (((c * 4 + q) ^ (lane & 7)) << 4)) =
+                    make_uint4(o[4 * q], o[4 * q + 1], o[4 * q + 2], o[4 * q + 3]);
+            } else if (key < un.si.sk) {
+              T* out_row = static_cast<T*>(const_cast<void*>(outp.ptr)) +
+                           (varlen ? 0 : un.b * outp.sb) +
+                           static_cast<int64_t>(un.si.k_start + key) * outp.ss +
+                           static_cast<int64_t>(un.g) * outp.sh + c * 32;
+#pragma unroll
+              for (int q = 0; q < 4; ++q)
+                if (c * 32 + 8 * q < p.head_dim)  // a padded head dimension stops early
+                  reinterpret_cast<uint4*>(out_row)[q] =
+                      make_uint4(o[4 * q], o[4 * q + 1], o[4 * q + 2], o[4 * q + 3]);
+            }
+          }
+        }
+        // dK and dV have left TMEM: the unit two ahead may restart this buffer
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(kvs ? B_DKDVFREE1 : B_DKDVFREE));
+        if (tile_store) {
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            const int row0 = un.si.k_start + un.n * BN + static_cast<int>(quad) * 32;
+            tma_store_4d(&tmDK, sb + stg, 0, row0, un.g, varlen ? 0 : un.b);
+            tma_store_4d(&tmDV, sb + stg + 4096, 0, row0, un.g, varlen ? 0 : un.b);
+            bulk_commit();
+          }
+        }
+        ++uc;
+      }
     }
     if (lane == 0) bulk_wait_all();
   }
 
 done:
+  if constexpr (L::kKVSlots == 2) {
+    if (lane == 0) bulk_wait_all();  // no store may still read this CTA's shared memory
+  }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -786,6 +931,10 @@ cudaError_t launch_t(const BwdParams& p, int dtype, cudaStream_t stream) {
     return cudaErrorInvalidValue;
   CUtensorMap tdq;
   if (!encode_tmap_f32_2d(&tdq, p.dqacc, p.ws_rows * p.h_q, D)) return cudaErrorInvalidValue;
+  CUtensorMap tdk, tdv;  // dK/dV tile stores (D = 64), 32-row boxes
+  if (!encode_tmap_bshd(&tdk, p.dk, dtype, p.seq.seqlen_k, p.h_k, nb, d, 32) ||
+      !encode_tmap_bshd(&tdv, p.dv, dtype, p.seq.seqlen_k, p.h_k, nb, d, 32))
+    return cudaErrorInvalidValue;
   constexpr uint32_t smem = Smem<D>::kTotal;
   // Kernel attributes are per device: set (and check) them once on each.
   constexpr int kMaxDevices = 64;
@@ -809,7 +958,8 @@ cudaError_t launch_t(const BwdParams& p, int dtype, cudaStream_t stream) {
   const int units = n_tiles * p.seq.batch * p.h_k;
   if (units <= 0) return cudaSuccess;
   const int grid = units < num_sms() ? units : num_sms();
-  bwd_main_kernel<T, D, kCap, kLeft><<<grid, kThreads, smem, stream>>>(p, tq, tk, tv, tdo, tdq);
+  bwd_main_kernel<T, D, kCap, kLeft><<<grid, kThreads, smem, stream>>>(p, tq, tk, tv, tdo, tdq,
+                                                                        tdk, tdv);
   return cudaGetLastError();
 }
 
