@@ -21,8 +21,10 @@
 // mode, in ascending KV-tile order behind per-(head, query tile, 32-row quarter)
 // semaphores (the dq_semaphore of flash-attention
 // hopper/flash_bwd_launch_template.h).
-// D is 64 or 128 here; smaller head dims (multiples of 8) run zero-padded to
-// the next of those.  Template switches: kCap (logit cap), kLeft (a left
+// D is 64, 96 or 128 here (96: the D = 128 shared-memory layout, whose second
+// 64-column chunk the TMA loads zero-fill past column 96, with 6 instead of 8
+// head-dim steps for S^T and dP^T and N = 96 products for dV, dK and dQ);
+// other head dims (multiples of 8) run zero-padded to the next of those.  Template switches: kCap (logit cap), kLeft (a left
 // window side); the default instantiation has neither.
 //
 // Warp roles (768 threads = 6 warpgroups): warp 0 TMA producer, warp 1 MMA
@@ -116,7 +118,7 @@ enum Bar : uint32_t {
 
 template <int D>
 struct Smem {
-  static constexpr uint32_t kTile = (D / 64) * kChunk;
+  static constexpr uint32_t kTile = ((D + 63) / 64) * kChunk;  // 64-column chunks (D = 96: 2)
   static constexpr uint32_t kK = 0;
   static constexpr uint32_t kV = kK + kTile;
   static constexpr uint32_t kQ = kV + kTile;
@@ -139,6 +141,7 @@ struct Smem {
 };
 static_assert(Smem<128>::kTotal <= 232448, "shared memory budget");
 static_assert(Smem<64>::kTotal <= 232448, "shared memory budget");
+static_assert(Smem<96>::kTotal == Smem<128>::kTotal, "D = 96 uses the D = 128 layout");
 
 template <typename T, int D, bool kCap, bool kLeft>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -167,7 +170,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int n_tiles = ceil_div(p.max_seqlen_k, BN);
   const int num_units = n_tiles * p.seq.batch * p.h_k;
   constexpr int kIsBf16 = Pack<T>::kIsBf16;
-  constexpr bool kSplitQ = D == 128;
+  constexpr int kDC = (D + 63) / 64;  // 64-column chunks of a tile row (the last one zero-filled
+                                      // past D by the TMA loads at D = 96)
+  constexpr bool kSplitQ = kDC == 2;
   // the left side of a local window; without one (the usual case) a constant,
   // so the unmasked and causal schedules carry none of its arithmetic
   const int wleft = kLeft ? p.win_left : -1;
@@ -277,7 +282,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t sK = sb + (kvs ? L::kK1 : L::kK), sV = sb + (kvs ? L::kV1 : L::kV);
           mbar_expect_tx(kvfull, 2 * L::kTile);
 #pragma unroll
-          for (int c = 0; c < D / 64; ++c) {
+          for (int c = 0; c < kDC; ++c) {
             tma_load_4d(sK + c * kChunk, &tmK, kvfull, c * 64, krow, un.g, bk);
             tma_load_4d(sV + c * kChunk, &tmV, kvfull, c * 64, krow, un.g, bk);
           }
@@ -305,7 +310,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           } else {
             mbar_expect_tx(bar(B_FULLQ + s), L::kTile + BM * 4);
 #pragma unroll
-            for (int c = 0; c < D / 64; ++c)
+            for (int c = 0; c < kDC; ++c)
               tma_load_4d(sb + L::kQ + s * L::kTile + c * kChunk, &tmQ, bar(B_FULLQ + s), c * 64,
                           qrow, h, bq);
             bulk_load(sb + L::kLSE + s * BM * 4, p.lse2 + ws, BM * 4, bar(B_FULLQ + s));
@@ -317,7 +322,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           mbar_expect_tx(bar(B_FULLDO + s), L::kTile + BM * 4);
 #pragma unroll
-          for (int c = 0; c < D / 64; ++c)
+          for (int c = 0; c < kDC; ++c)
             tma_load_4d(sb + L::kDO + s * L::kTile + c * kChunk, &tmDO, bar(B_FULLDO + s), c * 64,
                         qrow, h, bq);
           bulk_load(sb + L::kDelta + s * BM * 4, p.delta + ws, BM * 4, bar(B_FULLDO + s));
@@ -356,7 +361,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // descriptor built from the address, in fewer instructions of this one
       // issuing thread (measured +2.2 to +2.9 % at D = 128; the D = 64
       // instantiations, 4 % slower that way, build each from its address).
-      constexpr bool kBaseDesc = D == 128;
+      constexpr bool kBaseDesc = D != 64;
       const uint64_t dKM = sdesc_sw128(sb, 16, 1024);      // K-major (LBO unused)
       const uint64_t dMN = sdesc_sw128(sb, kChunk, 1024);  // MN-major
       auto dk_at = [&](uint32_t a) -> uint64_t {
@@ -698,21 +703,26 @@ __global__ void __launch_bounds__(kThreads, 1)
         {
           const uint32_t src = (writes_dk ? TM_DK : TM_DV) + e0;
           const float mul = writes_dk ? p.scale : 1.0f;
+          constexpr int kEStep = eCols % 32 == 0 ? 32 : 16;  // TMEM columns per load
 #pragma unroll 1
-          for (int c = 0; c < eCols / 32; ++c) {
-            uint32_t a[32];
-            tmem_ld32(tl + src + c * 32, a);
+          for (int c = 0; c < eCols / kEStep; ++c) {
+            uint32_t a[kEStep];
+            if constexpr (kEStep == 32) {
+              tmem_ld32(tl + src + c * 32, a);
+            } else {
+              tmem_ld16(tl + src + c * 16, a);
+            }
             tmem_wait_ld();
             if (key_ok) {
 #pragma unroll
-              for (int q = 0; q < 4; ++q) {
+              for (int q = 0; q < kEStep / 8; ++q) {
                 uint4 o;
                 o.x = Pack<T>::two(__uint_as_float(a[8 * q + 0]) * mul, __uint_as_float(a[8 * q + 1]) * mul);
                 o.y = Pack<T>::two(__uint_as_float(a[8 * q + 2]) * mul, __uint_as_float(a[8 * q + 3]) * mul);
                 o.z = Pack<T>::two(__uint_as_float(a[8 * q + 4]) * mul, __uint_as_float(a[8 * q + 5]) * mul);
                 o.w = Pack<T>::two(__uint_as_float(a[8 * q + 6]) * mul, __uint_as_float(a[8 * q + 7]) * mul);
-                if (e0 + c * 32 + 8 * q < p.head_dim)  // a padded head dimension stops early
-                  reinterpret_cast<uint4*>(out_row + c * 32)[q] = o;
+                if (e0 + c * kEStep + 8 * q < p.head_dim)  // a padded head dimension stops early
+                  reinterpret_cast<uint4*>(out_row + c * kEStep)[q] = o;
               }
             }
           }
@@ -743,12 +753,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     // warps go straight on to the next unit.
     const uint32_t quad = warp & 3;
     const uint32_t tl = tmem + ((quad * 32) << 16);
-    // Per warp and pass: kBoxes boxes of 32 rows x 32 fp32 columns (4 KB each);
-    // the 4 warps' staging fills the dO stage exactly (kTile bytes).
-    constexpr int kBoxes = D / 64;
+    // Per warp and pass: up to kBoxes boxes of 32 rows x 32 fp32 columns (4 KB
+    // each); the 4 warps' staging fills the dO stage exactly (kTile bytes).  At
+    // D = 96 the second pass has one box.
+    constexpr int kBoxes = static_cast<int>(L::kTile / (4 * 4096));
     constexpr int kPassCols = 32 * kBoxes;
-    constexpr int kPasses = D / kPassCols;
+    constexpr int kPasses = (D + kPassCols - 1) / kPassCols;
     static_assert(4 * kBoxes * 4096 == L::kTile, "dQ staging must fit the dO stage");
+    constexpr int kLastBoxes = D / 32 - (kPasses - 1) * kBoxes;  // kBoxes unless D = 96
     uint32_t it = 0, uc = 0;
     for (uint32_t k = 0;; ++k) {
       int u;
@@ -774,7 +786,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         constexpr int kHeld = kDrainWholeRow ? D : kPassCols;
         uint32_t a[kHeld];
 #pragma unroll
-        for (int c = 0; c < kHeld / 32; ++c) tmem_ld32p(tl + TM_DQ + c * 32, a + c * 32);
+        for (int c = 0; c < (kDrainWholeRow ? D : (kPasses == 1 ? 32 * kLastBoxes : kPassCols)) / 32; ++c)
+          tmem_ld32p(tl + TM_DQ + c * 32, a + c * 32);
         tmem_wait_ld();
         if (kDrainWholeRow) {
           tc_fence_before();
@@ -807,7 +820,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int pass = 0; pass < kPasses; ++pass) {
           if (!kDrainWholeRow && pass > 0) {
 #pragma unroll
-            for (int c = 0; c < kPassCols / 32; ++c)
+            for (int c = 0; c < (pass == kPasses - 1 ? kLastBoxes : kBoxes); ++c)
               tmem_ld32p(tl + TM_DQ + pass * kPassCols + c * 32, a + c * 32);
             tmem_wait_ld();
             if (pass == kPasses - 1) {
@@ -821,7 +834,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             __syncwarp();
           }
 #pragma unroll
-          for (int bx = 0; bx < kBoxes; ++bx) {
+          for (int bx = 0; bx < (pass == kPasses - 1 ? kLastBoxes : kBoxes); ++bx) {
             const uint32_t box = stage_off + bx * 4096;
 #pragma unroll
             for (int q = 0; q < 8; ++q) {
@@ -834,7 +847,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           __syncwarp();
           if (lane == 0) {
 #pragma unroll
-            for (int bx = 0; bx < kBoxes; ++bx)
+            for (int bx = 0; bx < (pass == kPasses - 1 ? kLastBoxes : kBoxes); ++bx)
               tma_reduce_add_2d(&tmDQ, sb + stage_off + bx * 4096, pass * kPassCols + bx * 32, row0);
             bulk_commit();
           }
@@ -945,7 +958,9 @@ cudaError_t launch_t(const BwdParams& p, int dtype, cudaStream_t stream) {
       !encode_tmap_bshd(&tdo, p.dout, dtype, p.seq.seqlen_q, p.h_q, nb, d, BM))
     return cudaErrorInvalidValue;
   CUtensorMap tdq;
-  if (!encode_tmap_f32_2d(&tdq, p.dqacc, p.ws_rows * p.h_q, D)) return cudaErrorInvalidValue;
+  // the accumulator rows are pad_head_dim wide (128 for the D = 96 kernel)
+  if (!encode_tmap_f32_2d(&tdq, p.dqacc, p.ws_rows * p.h_q, pad_head_dim(p.head_dim)))
+    return cudaErrorInvalidValue;
   CUtensorMap tdk, tdv;  // dK/dV tile stores (D = 64), 32-row boxes
   if (!encode_tmap_bshd(&tdk, p.dk, dtype, p.seq.seqlen_k, p.h_k, nb, d, 32) ||
       !encode_tmap_bshd(&tdv, p.dv, dtype, p.seq.seqlen_k, p.h_k, nb, d, 32))
@@ -981,6 +996,13 @@ cudaError_t launch_t(const BwdParams& p, int dtype, cudaStream_t stream) {
 template <bool kCap, bool kLeft>
 cudaError_t launch_cap(const BwdParams& p, int dtype, cudaStream_t stream) {
   const bool d64 = pad_head_dim(p.head_dim) == 64;
+  // head dims in (64, 96] have a native D = 96 kernel without a cap or a left
+  // window side; with either they run zero-padded on the D = 128 one
+  if constexpr (!kCap && !kLeft) {
+    if (p.head_dim > 64 && p.head_dim <= 96)
+      return dtype == 1 ? launch_t<__nv_bfloat16, 96, false, false>(p, dtype, stream)
+                        : launch_t<__half, 96, false, false>(p, dtype, stream);
+  }
   if (dtype == 1) {
     return d64 ? launch_t<__nv_bfloat16, 64, kCap, kLeft>(p, dtype, stream)
                : launch_t<__nv_bfloat16, 128, kCap, kLeft>(p, dtype, stream);

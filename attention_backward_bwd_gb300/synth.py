@@ -81,7 +81,10 @@ WORKLOADS = {
     "gqa_b2_hq32_hk8_s8192_d128_bf16_causal_cap30": Workload(
         "gqa_b2_hq32_hk8_s8192_d128_bf16_causal_cap30", 2, 32, 8, 8192, 8192, 128, "bf16", True,
         3, softcap=30.0),
-    # head dimensions above 128 (the wide kernels), same shape as the MHA S=4096 workload
+    # other head dimensions, same shape as the MHA S=4096 workload: 96 (its own kernel),
+    # above 128 (the wide kernels)
+    "mha_b2_h16_s4096_d96_bf16_causal": Workload(
+        "mha_b2_h16_s4096_d96_bf16_causal", 2, 16, 16, 4096, 4096, 96, "bf16", True, 2),
     "mha_b2_h16_s4096_d256_bf16_causal": Workload(
         "mha_b2_h16_s4096_d256_bf16_causal", 2, 16, 16, 4096, 4096, 256, "bf16", True, 2),
     "mha_b2_h16_s4096_d192_bf16_causal": Workload(

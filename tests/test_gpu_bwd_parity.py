@@ -166,12 +166,15 @@ def test_cross_attention_varlen(case):
 
 
 HEAD_DIMS = [
-    # B, Hq, Hk, Sq, Sk, D, dtype, causal: D below 64 or between 64 and 128 runs on the
-    # D = 64 / 128 kernels with the extra head-dimension columns zero
+    # B, Hq, Hk, Sq, Sk, D, dtype, causal: D below 64 runs on the D = 64 kernel, in
+    # (64, 96] on the D = 96 kernel, in (96, 128) on the D = 128 one, with the extra
+    # head-dimension columns zero
     (1, 4, 2, 300, 300, 32, "bf16", True),
     (2, 2, 2, 257, 257, 48, "fp16", False),
     (1, 4, 4, 513, 513, 80, "bf16", True),
     (1, 8, 2, 700, 700, 96, "bf16", True),
+    (2, 2, 2, 257, 257, 88, "fp16", False),
+    (1, 2, 2, 1000, 1000, 96, "fp16", True),
     (1, 2, 1, 200, 333, 112, "bf16", False),
     (1, 2, 2, 129, 129, 8, "bf16", True),
 ]

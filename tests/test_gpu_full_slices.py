@@ -11,8 +11,8 @@ Slices:
   * GQA B=2, Hq=32, Hk=8, S=8192, D=128, bf16, causal, deterministic off and on:
     the (sequence, kv head) groups (0, 0) and (1, 7), all four query heads each;
     deterministic mode is also compared bit for bit with a second run.
-  * MHA B=2, H=16, S=4096, D=128, bf16, causal and not: heads (0, 0), (0, 9),
-    (1, 4), (1, 15).
+  * MHA B=2, H=16, S=4096, D=128, bf16, causal and not, and D=96 causal (its own
+    kernel): heads (0, 0), (0, 9), (1, 4), (1, 15).
   * varlen, 16 packed sequences of lengths drawn from [128, 8192]: the
     shortest and the longest sequence, two heads each.
 And the properties that hold at any size, on every head of the GQA workload:
@@ -104,7 +104,8 @@ def test_gqa_s8192_whole_groups(deterministic):
 
 
 @pytest.mark.parametrize("name", ["mha_b2_h16_s4096_d128_bf16",
-                                  "mha_b2_h16_s4096_d128_bf16_causal"])
+                                  "mha_b2_h16_s4096_d128_bf16_causal",
+                                  "mha_b2_h16_s4096_d96_bf16_causal"])
 def test_mha_s4096_whole_heads(name):
     w = synth.WORKLOADS[name]
     x = _inputs(name)

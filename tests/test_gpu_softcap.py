@@ -72,15 +72,17 @@ def test_softcap_varlen():
 
 
 INSTANCES = [(dt, d, cap, left) for dt in ("bf16", "fp16") for d in (64, 128)
-             for cap in (0.0, 2.0) for left in (-1, 150)]
+             for cap in (0.0, 2.0) for left in (-1, 150)] + \
+    [(dt, 96, 0.0, -1) for dt in ("bf16", "fp16")]  # the D = 96 kernel: no cap, no left side
 
 
 @pytest.mark.parametrize("dt,d,cap,left", INSTANCES,
                          ids=[f"{c[0]}_d{c[1]}_cap{c[2]:g}_left{c[3]}" for c in INSTANCES])
 def test_every_main_kernel_instance(dt, d, cap, left):
     """The main kernel is instantiated per dtype, head dim, logit cap on/off and
-    left window side present/absent: each of the sixteen against the oracle on
-    a causal problem whose window edge and diagonal cut through tiles."""
+    left window side present/absent (D = 96 without either): each of the eighteen
+    against the oracle on a causal problem whose window edge and diagonal cut
+    through tiles."""
     w = synth.small("inst", 1, 4, 2, 401, 401, d, dt, True, 500 + d + int(cap) + (left > 0))
     x = synth.make_inputs(w)
     q = (x.q.float() * 2).to(x.q.dtype) if cap else x.q
