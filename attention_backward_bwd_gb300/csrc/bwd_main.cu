@@ -232,7 +232,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   volatile int* ring = reinterpret_cast<volatile int*>(smem + L::kRing);
   // Work units come from a persistent scheduler: the first unit of CTA c is c,
   // later ones are taken by the producer from a global counter in
-  // longest-first order (key tile major) and published through a 2-slot ring
+  // unit order of get_unit (longest first) and published through a 2-slot ring
   // that every role reads.  A published index >= num_units means "done".
   // Consumer side (single thread when `warp_wide` is false):
   auto take_unit = [&](uint32_t k, bool warp_wide, int& u) -> bool {
