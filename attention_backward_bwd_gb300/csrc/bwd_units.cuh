@@ -23,12 +23,18 @@ struct Unit {
 // L2 (measured: 41 GB of DRAM traffic per launch for 16 sequences of up to 8192,
 // 84 % of the DRAM peak); sequence major keeps them on one sequence's groups,
 // each group's key tiles still in ascending order (longest first, and the order
-// the deterministic mode's semaphores expect).
+// the deterministic mode's semaphores expect).  With seq_major_mha (the D = 128
+// main kernel) padded MHA batches (one query head per group) outside
+// deterministic mode take the sequence-major order too: it shares each head's
+// tiles among ~10 running CTAs instead of ~5 (MHA S = 4096 non-causal +3.4 %);
+// GQA groups are already shared enough, and the longer deterministic chains and
+// the other kernels lose by it.
 // win_left: the left window side (-1 = none; a compile-time -1 in the
 // instantiation without a left window), win_right: p.win_right.
-__device__ __forceinline__ Unit get_unit(const BwdParams& p, int u, int G, int win_left) {
+__device__ __forceinline__ Unit get_unit(const BwdParams& p, int u, int G, int win_left,
+                                         bool seq_major_mha) {
   Unit r;
-  if (p.seq.cu_q != nullptr) {
+  if (p.seq.cu_q != nullptr || (seq_major_mha && G == 1 && !p.deterministic)) {
     const int per_b = (p.max_seqlen_k + kTileRows - 1) / kTileRows * p.h_k;
     r.b = u / per_b;
     const int rem = u - r.b * per_b;
