@@ -266,7 +266,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (u >= num_units) break;
         // fetch the next unit now; the atomic's latency overlaps this unit's loads
         const int u_next = static_cast<int>(gridDim.x) + atomicAdd(p.sched, 1);
-        const Unit un = get_unit(p, u, G, wleft, D == 128);
+        const Unit un = get_unit(p, u, G, wleft);
         u = u_next;
         if (un.n_iters == 0) continue;
         // unit uc takes K/V slot uc % kKVSlots, freed by the unit kKVSlots before it
@@ -406,7 +406,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           goto mma_exit;
         }
         if (u >= num_units) break;
-        const Unit un = get_unit(p, u, G, wleft, D == 128);
+        const Unit un = get_unit(p, u, G, wleft);
         if (un.n_iters == 0) continue;
         const uint32_t kvs = uc % L::kKVSlots;
         const uint32_t sK = sb + (kvs ? L::kK1 : L::kK), sV = sb + (kvs ? L::kV1 : L::kV);
@@ -467,7 +467,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             // the next unit's first S^T, from the other K/V slot
             if (!take_unit(k + 1, false, u_pk)) goto mma_exit;
             pk = true;
-            if (u_pk < num_units && get_unit(p, u_pk, G, wleft, D == 128).n_iters > 0) {
+            if (u_pk < num_units && get_unit(p, u_pk, G, wleft).n_iters > 0) {
               const uint32_t kvs2 = (uc + 1) % 2;
               const uint32_t s1 = (it + 1) % kStages;
               if (!wait1(bar(kvs2 ? B_KVFULL1 : B_KVFULL), ((uc + 1) / 2) & 1, ctl, 0xA000001Cu))
@@ -533,7 +533,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       int u;
       if (!take_unit(k, true, u)) goto done;
       if (u >= num_units) break;
-      const Unit un = get_unit(p, u, G, wleft, D == 128);
+      const Unit un = get_unit(p, u, G, wleft);
       if (!un.has_keys) continue;
       const int key = un.n * BN + jl;
       const bool key_ok = key < un.si.sk;
@@ -766,7 +766,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       int u;
       if (!take_unit(k, true, u)) goto done;
       if (u >= num_units) break;
-      const Unit un = get_unit(p, u, G, wleft, D == 128);
+      const Unit un = get_unit(p, u, G, wleft);
       if (un.n_iters == 0) continue;
       for (int j = 0; j < un.n_iters; ++j, ++it) {
         int h, m;
@@ -946,8 +946,13 @@ done:
 }
 
 template <typename T, int D, bool kCap, bool kLeft>
-cudaError_t launch_t(const BwdParams& p, int dtype, cudaStream_t stream) {
-  const bool varlen = p.seq.cu_q != nullptr;
+cudaError_t launch_t(const BwdParams& p_in, int dtype, cudaStream_t stream) {
+  const bool varlen = p_in.seq.cu_q != nullptr;
+  // unit order (see get_unit): sequence major for packed batches and, at D = 128,
+  // for padded MHA outside deterministic mode; key-tile major otherwise
+  BwdParams p = p_in;
+  p.unit_seq_major = varlen || (D == 128 && p.h_q == p.h_k && !p.deterministic);
+  p.unit_per = p.unit_seq_major ? ceil_div(p.max_seqlen_k, BN) * p.h_k : p.seq.batch * p.h_k;
   const int nb = varlen ? 1 : p.seq.batch;
   CUtensorMap tq, tk, tv, tdo;
   // the maps span the logical head dimension: columns up to D read as zero

@@ -14,39 +14,32 @@ struct Unit {
   bool has_keys;
 };
 
-// Unit order (the scheduler hands units out in index order): padded batches are
-// key-tile major, (n, b, g) with g innermost, so the CTAs running at once are
-// the first key tiles (the longest units under a causal mask) of every
-// (sequence, kv head) group.  Packed varlen batches are sequence major, (b, n,
-// g): with many sequences, key-tile major would spread the running CTAs over
-// every group, and their Q/dO tiles and dQ accumulator rows would not stay in
-// L2 (measured: 41 GB of DRAM traffic per launch for 16 sequences of up to 8192,
-// 84 % of the DRAM peak); sequence major keeps them on one sequence's groups,
-// each group's key tiles still in ascending order (longest first, and the order
-// the deterministic mode's semaphores expect).  With seq_major_mha (the D = 128
-// main kernel) padded MHA batches (one query head per group) outside
-// deterministic mode take the sequence-major order too: it shares each head's
-// tiles among ~10 running CTAs instead of ~5 (MHA S = 4096 non-causal +3.4 %);
-// GQA groups are already shared enough, and the longer deterministic chains and
-// the other kernels lose by it.
+// Unit order (the scheduler hands units out in index order; the launch sets
+// p.unit_seq_major and p.unit_per).  Key-tile major, (n, b, g) with g innermost:
+// the CTAs running at once hold the first key tiles (the longest units under a
+// causal mask) of every (sequence, kv head) group, ~10 CTAs per group on the
+// bench workload (GQA, 16 groups), sharing each group's Q/dO tiles and dQ
+// accumulator rows in L2.  Sequence major, (b, n, g): packed (varlen) batches,
+// where key-tile major spread the running CTAs over every group of 16 sequences
+// x 16 heads and moved 41 GB of DRAM per launch (84 % of the DRAM peak; 5.5 GB
+// sequence major), and, in the D = 128 main kernel, padded MHA batches outside
+// deterministic mode (~10 CTAs per head instead of ~5: MHA S = 4096 non-causal
+// +3.4 %; GQA groups are shared enough already, and deterministic mode's longer
+// chains and the other kernels lose by it).  Either way each group's key tiles
+// come in ascending order: longest first, and the order the deterministic
+// mode's semaphores expect.  The decode has no branch on the order: an earlier
+// form that chose it by a branch on the sequence layout slowed the short-unit
+// D = 64 kernel by 12 %.
 // win_left: the left window side (-1 = none; a compile-time -1 in the
 // instantiation without a left window), win_right: p.win_right.
-__device__ __forceinline__ Unit get_unit(const BwdParams& p, int u, int G, int win_left,
-                                         bool seq_major_mha) {
+__device__ __forceinline__ Unit get_unit(const BwdParams& p, int u, int G, int win_left) {
   Unit r;
-  if (p.seq.cu_q != nullptr || (seq_major_mha && G == 1 && !p.deterministic)) {
-    const int per_b = (p.max_seqlen_k + kTileRows - 1) / kTileRows * p.h_k;
-    r.b = u / per_b;
-    const int rem = u - r.b * per_b;
-    r.n = rem / p.h_k;
-    r.g = rem - r.n * p.h_k;
-  } else {
-    const int per_n = p.seq.batch * p.h_k;
-    r.n = u / per_n;
-    const int rem = u - r.n * per_n;
-    r.b = rem / p.h_k;
-    r.g = rem - r.b * p.h_k;
-  }
+  const int outer = u / p.unit_per;
+  const int rem = u - outer * p.unit_per;
+  const int mid = rem / p.h_k;
+  r.g = rem - mid * p.h_k;
+  r.n = p.unit_seq_major ? mid : outer;
+  r.b = p.unit_seq_major ? outer : mid;
   r.si = seq_info(p.seq, r.b);
   r.has_keys = r.n * kTileRows < r.si.sk;
   // query tiles holding a query that sees a key of this tile (all of them

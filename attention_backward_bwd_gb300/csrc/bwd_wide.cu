@@ -209,7 +209,7 @@ __global__ void __launch_bounds__(kWThreads, 1)
           mbar_arrive(bar(W_UNITFULL + (k & 1)));
           if (u >= num_units) break;
           const int u_next = static_cast<int>(gridDim.x) + atomicAdd(sched, 1);
-          const Unit un = get_unit(p, u, G, p.win_left, false);
+          const Unit un = get_unit(p, u, G, p.win_left);
           u = u_next;
           if (un.n_iters == 0) continue;
           const int bk = varlen ? 0 : un.b;
@@ -305,7 +305,7 @@ __global__ void __launch_bounds__(kWThreads, 1)
           int u;
           if (!take_unit(k, false, u)) goto mma_exit;
           if (u >= num_units) break;
-          const Unit un = get_unit(p, u, G, p.win_left, false);
+          const Unit un = get_unit(p, u, G, p.win_left);
           if (un.n_iters == 0) continue;
           if (!wait1(bar(W_KFULL), uc & 1, ctl, 0xA3000012u)) goto mma_exit;
           tc_fence_after();
@@ -423,7 +423,7 @@ __global__ void __launch_bounds__(kWThreads, 1)
       int u;
       if (!take_unit(k, true, u)) goto done;
       if (u >= num_units) break;
-      const Unit un = get_unit(p, u, G, p.win_left, false);
+      const Unit un = get_unit(p, u, G, p.win_left);
       if (!un.has_keys) continue;
       const int key = un.n * kTileRows + jl;
       const bool key_ok = key < un.si.sk;
@@ -603,7 +603,7 @@ __global__ void __launch_bounds__(kWThreads, 1)
       int u;
       if (!take_unit(k, true, u)) goto done;
       if (u >= num_units) break;
-      const Unit un = get_unit(p, u, G, p.win_left, false);
+      const Unit un = get_unit(p, u, G, p.win_left);
       if (un.n_iters == 0) continue;
       for (int j = 0; j < un.n_iters; ++j, ++it) {
         int h, m;
@@ -723,8 +723,12 @@ cudaError_t launch_wide_t(const BwdParams& p, int dtype, cudaStream_t stream,
 }
 
 template <typename T, bool kCap>
-cudaError_t launch_wide_passes(const BwdParams& p, int dtype, cudaStream_t stream) {
-  const bool varlen = p.seq.cu_q != nullptr;
+cudaError_t launch_wide_passes(const BwdParams& p_in, int dtype, cudaStream_t stream) {
+  const bool varlen = p_in.seq.cu_q != nullptr;
+  // unit order (see get_unit): sequence major for packed batches only
+  BwdParams p = p_in;
+  p.unit_seq_major = varlen;
+  p.unit_per = varlen ? ceil_div(p.max_seqlen_k, kTileRows) * p.h_k : p.seq.batch * p.h_k;
   const int nb = varlen ? 1 : p.seq.batch;
   const int d = p.head_dim;
   CUtensorMap tq, tk, tv, tdo, tdq;

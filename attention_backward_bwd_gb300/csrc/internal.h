@@ -55,6 +55,10 @@ struct BwdParams {
   unsigned int* status;
   const unsigned int* input_bad;  // nonzero after cu_seqlens failed validation (varlen)
   unsigned long long timeout_ns;
+  // Work-unit order of the KV-stationary kernels, chosen by each kernel's launch:
+  // u = outer * unit_per + mid * h_k + g, with (outer, mid) = (b, n) when
+  // unit_seq_major, else (n, b); unit_per = the units of one outer index.
+  int unit_seq_major, unit_per;
 };
 
 struct FwdParams {
