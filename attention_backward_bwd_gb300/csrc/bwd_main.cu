@@ -24,8 +24,9 @@
 // D is 64, 96 or 128 here (96: the D = 128 shared-memory layout, whose second
 // 64-column chunk the TMA loads zero-fill past column 96, with 6 instead of 8
 // head-dim steps for S^T and dP^T and N = 96 products for dV, dK and dQ);
-// other head dims (multiples of 8) run zero-padded to the next of those.  Template switches: kCap (logit cap), kLeft (a left
-// window side); the default instantiation has neither.
+// other head dims (multiples of 8) run zero-padded to the next of those.
+// Template switches: kCap (logit cap), kLeft (a left window side); the default
+// instantiation has neither.
 //
 // Warp roles (768 threads = 6 warpgroups): warp 0 TMA producer, warp 1 MMA
 // issuer (one thread), warp 2 TMEM allocator, warps 4-19 softmax / dS / dK-dV
@@ -789,9 +790,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         // these TMEM columns); otherwise one pass at a time.
         constexpr int kHeld = kDrainWholeRow ? D : kPassCols;
         uint32_t a[kHeld];
+        // columns read before the first pass: the whole row, or the first pass's
+        constexpr int kFirstCols =
+            kDrainWholeRow ? D : (kPasses == 1 ? 32 * kLastBoxes : kPassCols);
 #pragma unroll
-        for (int c = 0; c < (kDrainWholeRow ? D : (kPasses == 1 ? 32 * kLastBoxes : kPassCols)) / 32; ++c)
-          tmem_ld32p(tl + TM_DQ + c * 32, a + c * 32);
+        for (int c = 0; c < kFirstCols / 32; ++c) tmem_ld32p(tl + TM_DQ + c * 32, a + c * 32);
         tmem_wait_ld();
         if (kDrainWholeRow) {
           tc_fence_before();
@@ -852,7 +855,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (lane == 0) {
 #pragma unroll
             for (int bx = 0; bx < (pass == kPasses - 1 ? kLastBoxes : kBoxes); ++bx)
-              tma_reduce_add_2d(&tmDQ, sb + stage_off + bx * 4096, pass * kPassCols + bx * 32, row0);
+              tma_reduce_add_2d(&tmDQ, sb + stage_off + bx * 4096, pass * kPassCols + bx * 32,
+                                row0);
             bulk_commit();
           }
         }
