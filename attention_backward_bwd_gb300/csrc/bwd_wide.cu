@@ -1,7 +1,8 @@
 // Attention backward for head dimensions above 128 (sm_103a): tcgen05 MMAs
-// with TMEM accumulators, TMA loads, warp-specialised, persistent.  The tiles
-// are D = 256 wide; head dimensions in (128, 256) run on them with the extra
-// columns zero (TMA out-of-bounds fill, masked stores).
+// with TMEM accumulators, TMA loads, warp-specialised, persistent.  A tile row
+// is kNC chunks of 64 head-dim columns: four (256 wide) for D in (192, 256],
+// three (192 wide) for D in (128, 192]; the columns past D are zero (TMA
+// out-of-bounds fill, masked stores).
 //
 // Same mathematics and work units as the D <= 128 kernel (TileLang
 // test_tilelang_kernel_mha_bwd.py, flashattn_bwd; KV stationary, one unit =
@@ -16,12 +17,12 @@
 // in shared memory for the whole unit; the other operands stream through a
 // ring of 64-column chunks (128 rows x 128 bytes, 128-byte swizzle), loaded in
 // exactly the order the MMA thread consumes them:
-//   pass dV, per query tile j: Q_j chunks 0-3 (S^T_j), then dO_{j-1} chunks
-//     0-3 (dV_{j-1}), since S^T of the next tile is issued before dV of this
+//   pass dV, per query tile j: Q_j's kNC chunks (S^T_j), then dO_{j-1}'s kNC
+//     chunks (dV_{j-1}), since S^T of the next tile is issued before dV of this
 //     one so that it runs while the softmax warps compute P;
 //   pass dK/dQ, per query tile: Q chunks (S^T), V and dO chunk pairs (dP^T),
 //     Q chunks again (dK).
-// dQ is drained in four 64-column passes through a 32 KiB staging buffer with
+// dQ is drained in kNC 64-column passes through a 32 KiB staging buffer with
 // TMA reduce-adds (in deterministic mode ordered by the per-(head, query tile,
 // 32-row quarter) semaphore, as in the D <= 128 kernel).
 //
@@ -31,8 +32,10 @@
 // dQ drain (pass dK/dQ only; thread = query row).
 //
 // TMEM columns (512): pass dV: S^T buffers [0,128) and [128,256), dV
-// [256,512).  Pass dK/dQ: S^T [0,128), dP^T [128,256), then dQ [0,256) once
-// the dS phase has read both; dK [256,512).
+// [256,512).  Pass dK/dQ: S^T [0,128), dP^T [128,256), then dQ [0,64 kNC) once
+// the dS phase has read both; dK [256,512).  dV and dK are accumulated as
+// N = 128 products over chunk pairs (and an N = 64 product for an odd last
+// chunk).
 #include <atomic>
 
 #include "bwd_units.cuh"
@@ -42,8 +45,7 @@ namespace attn {
 
 namespace {
 
-constexpr int WD = 256;                 // tile width (head dimension)
-constexpr int kNC = WD / 64;            // 64-column chunks per tile row block
+constexpr int WD = 256;                 // accumulator width (head dimension padded to 256)
 constexpr uint32_t kWChunk = 128 * 128; // bytes of one chunk
 constexpr int kWSoftWarps = 16;
 constexpr int kWCols = 32;              // query columns per softmax warp
@@ -70,7 +72,7 @@ enum WBar : uint32_t {
   W_DSREADY,
   W_DQFULL,
   W_DQFREE0,                   // drain read dQ columns [0,128)
-  W_DQFREE1,                   // drain read dQ columns [128,256)
+  W_DQFREE1,                   // drain read dQ columns [128,64 kNC)
   W_DKDONE,                    // dK (and dQ) MMAs of a tile done: dS^T tile free
   W_ACCFULL,                   // the unit's dV (pass dV) / dK (pass dK/dQ) complete
   W_ACCFREE,                   // the epilogue read it
@@ -80,9 +82,15 @@ enum WBar : uint32_t {
   W_COUNT
 };
 
-template <int kPass>
+// kNC: 64-column chunks per tile row (4 at D in (192, 256], 3 at D in (128, 192]).
+template <int kPass, int kNC>
 struct WSmem {
-  static constexpr int kRing = kPass == kPassDV ? 10 : 6;  // even: chunk pairs never wrap
+  // ring slots.  The chunks of a tile arrive in groups of kNC (Q, dO, or
+  // V/dO interleaved); an N = 128 product reads a pair of chunks starting at
+  // an even offset of its group as one operand, so both must sit in adjacent
+  // slots: the ring is even (four chunks) or a multiple of three (three).
+  static constexpr int kRing = kPass == kPassDV ? (kNC == 4 ? 10 : 9) : 6;
+  static_assert(kRing % (kNC == 4 ? 2 : 3) == 0, "chunk pairs must not wrap the ring");
   static constexpr uint32_t kK = 0;
   static constexpr uint32_t kDS = kK + kNC * kWChunk;                         // pass dK/dQ
   static constexpr uint32_t kStage = kDS + (kPass == kPassDKDQ ? 2 * kWChunk : 0);
@@ -95,16 +103,18 @@ struct WSmem {
   static constexpr uint32_t kAbort = kTmemSlot + 4;
   static constexpr uint32_t kTotal = kAbort + 4;
 };
-static_assert(WSmem<kPassDV>::kTotal <= 232448, "shared memory budget (pass dV)");
-static_assert(WSmem<kPassDKDQ>::kTotal <= 232448, "shared memory budget (pass dK/dQ)");
+static_assert(WSmem<kPassDV, 4>::kTotal <= 232448, "shared memory budget (pass dV)");
+static_assert(WSmem<kPassDKDQ, 4>::kTotal <= 232448, "shared memory budget (pass dK/dQ)");
+static_assert(WSmem<kPassDV, 3>::kTotal <= 232448, "shared memory budget (pass dV, D <= 192)");
+static_assert(WSmem<kPassDKDQ, 3>::kTotal <= 232448, "shared memory budget (pass dK/dQ, D <= 192)");
 
-template <typename T, int kPass, bool kCap>
+template <typename T, int kPass, bool kCap, int kNC>
 __global__ void __launch_bounds__(kWThreads, 1)
     bwd_wide_kernel(const BwdParams p, const __grid_constant__ CUtensorMap tmQ,
                     const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                     const __grid_constant__ CUtensorMap tmDO,
                     const __grid_constant__ CUtensorMap tmDQ) {
-  using L = WSmem<kPass>;
+  using L = WSmem<kPass, kNC>;
   constexpr int R = L::kRing;
   constexpr bool kKQ = kPass == kPassDKDQ;
   extern __shared__ __align__(1024) unsigned char smem[];
@@ -283,7 +293,8 @@ __global__ void __launch_bounds__(kWThreads, 1)
       if (lane == 0) {
         constexpr uint32_t kIdS = idesc_f16(kIsBf16, 0, 0, 128, 128);     // K, Q K-major
         constexpr uint32_t kIdN128 = idesc_f16(kIsBf16, 0, 1, 128, 128);  // B MN-major, N = 128
-        constexpr uint32_t kIdDQ = idesc_f16(kIsBf16, 1, 1, 128, WD);     // dS, K MN-major
+        constexpr uint32_t kIdN64 = idesc_f16(kIsBf16, 0, 1, 128, 64);    // B MN-major, N = 64
+        constexpr uint32_t kIdDQ = idesc_f16(kIsBf16, 1, 1, 128, 64 * kNC);  // dS, K MN-major
         uint32_t q = 0, it = 0, uc = 0;
         auto ring_wait = [&](uint32_t qq) -> bool {
           return wait1(bar(W_RFULL + qq % R), (qq / R) & 1, ctl, 0xA3000011u);
@@ -317,18 +328,20 @@ __global__ void __launch_bounds__(kWThreads, 1)
               // the previous unit's epilogue must have read dV before it restarts
               if (first && uc > 0 && !wait1(bar(W_ACCFREE), (uc - 1) & 1, ctl, 0xA3000014u))
                 return false;
-              for (int pr = 0; pr < kNC / 2; ++pr) {
+              // chunk pairs as N = 128 products, an odd last chunk as N = 64
+              for (int pr = 0; pr < (kNC + 1) / 2; ++pr) {
                 const uint32_t q0 = q + 2 * pr;
-                if (!ring_wait(q0) || !ring_wait(q0 + 1)) return false;
+                const bool pair = 2 * pr + 1 < kNC;
+                if (!ring_wait(q0) || (pair && !ring_wait(q0 + 1))) return false;
                 tc_fence_after();
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk)
                   mma_ts(tmem + 256 + 128 * pr, tmem + buf * 128 + (16 * kk / kWCols) * kWCols +
                                                     (16 * kk % kWCols) / 2,
-                         sdesc_sw128(slot(q0) + kk * 2048, kWChunk, 1024), kIdN128,
+                         sdesc_sw128(slot(q0) + kk * 2048, kWChunk, 1024), pair ? kIdN128 : kIdN64,
                          (!first || kk > 0) ? 1u : 0u);
                 tc_commit(bar(W_REMPTY + q0 % R));
-                tc_commit(bar(W_REMPTY + (q0 + 1) % R));
+                if (pair) tc_commit(bar(W_REMPTY + (q0 + 1) % R));
               }
               q += kNC;
               tc_commit(bar(W_PVDONE + buf));
@@ -354,7 +367,7 @@ __global__ void __launch_bounds__(kWThreads, 1)
               if (t > 0 && !wait1(bar(W_DQFREE0), (t - 1) & 1, ctl, 0xA3000016u)) goto mma_exit;
               if (!issue_s(0)) goto mma_exit;
               tc_commit(bar(W_SFULL));
-              // dP^T = V dO^T over chunk pairs (V chunk, dO chunk); overwrites dQ [128,256)
+              // dP^T = V dO^T over chunk pairs (V chunk, dO chunk); overwrites dQ [128,64 kNC)
               if (t > 0 && !wait1(bar(W_DQFREE1), (t - 1) & 1, ctl, 0xA3000017u)) goto mma_exit;
               for (int c = 0; c < kNC; ++c, q += 2) {
                 if (!ring_wait(q) || !ring_wait(q + 1)) goto mma_exit;
@@ -370,7 +383,7 @@ __global__ void __launch_bounds__(kWThreads, 1)
               tc_commit(bar(W_DPFULL));
               if (!wait1(bar(W_DSREADY), t & 1, ctl, 0xA3000018u)) goto mma_exit;
               tc_fence_after();
-              // dQ = dS K   (A = dS MN-major from the dS^T tile, B = K MN-major, N = 256)
+              // dQ = dS K   (A = dS MN-major from the dS^T tile, B = K MN-major, N = 64 kNC)
 #pragma unroll
               for (int kk = 0; kk < 8; ++kk)
                 mma_ss(tmem + 0, sdesc_sw128(sb + L::kDS + kk * 2048, kWChunk, 1024),
@@ -380,19 +393,20 @@ __global__ void __launch_bounds__(kWThreads, 1)
               // dK += dS^T Q   (A = dS^T K-major, B = Q chunk pairs MN-major)
               if (j == 0 && uc > 0 && !wait1(bar(W_ACCFREE), (uc - 1) & 1, ctl, 0xA3000019u))
                 goto mma_exit;
-              for (int pr = 0; pr < kNC / 2; ++pr) {
+              for (int pr = 0; pr < (kNC + 1) / 2; ++pr) {
                 const uint32_t q0 = q + 2 * pr;
-                if (!ring_wait(q0) || !ring_wait(q0 + 1)) goto mma_exit;
+                const bool pair = 2 * pr + 1 < kNC;  // an odd last chunk: N = 64
+                if (!ring_wait(q0) || (pair && !ring_wait(q0 + 1))) goto mma_exit;
                 tc_fence_after();
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk) {
                   const uint32_t koff = (kk >> 2) * kWChunk + (kk & 3) * 32;
                   mma_ss(tmem + 256 + 128 * pr, sdesc_sw128(sb + L::kDS + koff, 16, 1024),
-                         sdesc_sw128(slot(q0) + kk * 2048, kWChunk, 1024), kIdN128,
-                         (j > 0 || kk > 0) ? 1u : 0u);
+                         sdesc_sw128(slot(q0) + kk * 2048, kWChunk, 1024),
+                         pair ? kIdN128 : kIdN64, (j > 0 || kk > 0) ? 1u : 0u);
                 }
                 tc_commit(bar(W_REMPTY + q0 % R));
-                tc_commit(bar(W_REMPTY + (q0 + 1) % R));
+                if (pair) tc_commit(bar(W_REMPTY + (q0 + 1) % R));
               }
               q += kNC;
               tc_commit(bar(W_DKDONE));
@@ -559,9 +573,10 @@ __global__ void __launch_bounds__(kWThreads, 1)
         }
       }
       // ---- epilogue: this group's 64 columns of dK = scale * acc (pass dK/dQ) or dV = acc
+      // (with three chunks the fourth group has none)
       if (!wait_warp(bar(W_ACCFULL), uc & 1, ctl, 0xA3000025u)) goto done;
       tc_fence_after();
-      {
+      if (e0 < 64 * kNC) {
         const float mul = kKQ ? p.scale : 1.0f;
 #pragma unroll 1
         for (int c = 0; c < eCols / 32; ++c) {
@@ -590,11 +605,11 @@ __global__ void __launch_bounds__(kWThreads, 1)
   } else if (kKQ) {
     setmaxnreg_inc<kWRegDrain>();
     // ------------------------------------------------------------ dQ drain
-    // Thread = query row (TMEM lane); warp q owns rows [32 q, 32 q + 32).  Four
+    // Thread = query row (TMEM lane); warp q owns rows [32 q, 32 q + 32).  kNC
     // passes of 64 columns, each staged as two 32x32 fp32 boxes per warp (the
     // 128-byte swizzle) in the staging buffer and added to dQaccum by TMA
     // reduces; after the first two passes the S^T columns are free again, after
-    // the last two the dP^T columns.
+    // the last one the dP^T columns.
     const uint32_t quad = warp & 3;
     const uint32_t tl = tmem + ((quad * 32) << 16);
     const uint32_t stage_off = L::kStage + quad * 8192;
@@ -642,13 +657,13 @@ __global__ void __launch_bounds__(kWThreads, 1)
           if (__shfl_sync(0xffffffffu, stop, 0)) goto done;
         }
 #pragma unroll 1
-        for (int pass = 0; pass < 4; ++pass) {
+        for (int pass = 0; pass < kNC; ++pass) {
           if (pass > 0) {
             tmem_ld32p(tl + pass * 64, a);
             tmem_ld32p(tl + pass * 64 + 32, a + 32);
             tmem_wait_ld();
           }
-          if (pass == 1 || pass == 3) {  // columns [0,128) resp. [128,256) have been read
+          if (pass == 1 || pass == kNC - 1) {  // columns [0,128) resp. [128,64 kNC) read
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(bar(pass == 1 ? W_DQFREE0 : W_DQFREE1));
@@ -694,23 +709,23 @@ done:
   if (warp == 2) tmem_dealloc(tmem, kWTmemCols);
 }
 
-template <typename T, int kPass, bool kCap>
+template <typename T, int kPass, bool kCap, int kNC>
 cudaError_t launch_wide_t(const BwdParams& p, int dtype, cudaStream_t stream,
                           const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                           const CUtensorMap& tdo, const CUtensorMap& tdq) {
-  constexpr uint32_t smem = WSmem<kPass>::kTotal;
+  constexpr uint32_t smem = WSmem<kPass, kNC>::kTotal;
   constexpr int kMaxDevices = 64;
   static std::atomic<bool> attr_done[kMaxDevices];
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
     return cudaErrorInvalidDevice;
   if (!attr_done[dev].load(std::memory_order_acquire)) {
-    cudaError_t e = cudaFuncSetAttribute(bwd_wide_kernel<T, kPass, kCap>,
+    cudaError_t e = cudaFuncSetAttribute(bwd_wide_kernel<T, kPass, kCap, kNC>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     // the warpgroup register split assumes exactly kWRegLaunch registers at launch
     cudaFuncAttributes fa;
-    e = cudaFuncGetAttributes(&fa, bwd_wide_kernel<T, kPass, kCap>);
+    e = cudaFuncGetAttributes(&fa, bwd_wide_kernel<T, kPass, kCap, kNC>);
     if (e != cudaSuccess) return e;
     if (fa.numRegs != static_cast<int>(kWRegLaunch)) return cudaErrorInvalidConfiguration;
     attr_done[dev].store(true, std::memory_order_release);
@@ -718,11 +733,11 @@ cudaError_t launch_wide_t(const BwdParams& p, int dtype, cudaStream_t stream,
   const int units = ceil_div(p.max_seqlen_k, kTileRows) * p.seq.batch * p.h_k;
   if (units <= 0) return cudaSuccess;
   const int grid = units < num_sms() ? units : num_sms();
-  bwd_wide_kernel<T, kPass, kCap><<<grid, kWThreads, smem, stream>>>(p, tq, tk, tv, tdo, tdq);
+  bwd_wide_kernel<T, kPass, kCap, kNC><<<grid, kWThreads, smem, stream>>>(p, tq, tk, tv, tdo, tdq);
   return cudaGetLastError();
 }
 
-template <typename T, bool kCap>
+template <typename T, bool kCap, int kNC>
 cudaError_t launch_wide_passes(const BwdParams& p_in, int dtype, cudaStream_t stream) {
   const bool varlen = p_in.seq.cu_q != nullptr;
   // unit order (see get_unit): sequence major for packed batches only
@@ -738,9 +753,16 @@ cudaError_t launch_wide_passes(const BwdParams& p_in, int dtype, cudaStream_t st
       !encode_tmap_bshd(&tdo, p.dout, dtype, p.seq.seqlen_q, p.h_q, nb, d, kTileRows))
     return cudaErrorInvalidValue;
   if (!encode_tmap_f32_2d(&tdq, p.dqacc, p.ws_rows * p.h_q, WD)) return cudaErrorInvalidValue;
-  cudaError_t e = launch_wide_t<T, kPassDKDQ, kCap>(p, dtype, stream, tq, tk, tv, tdo, tdq);
+  cudaError_t e = launch_wide_t<T, kPassDKDQ, kCap, kNC>(p, dtype, stream, tq, tk, tv, tdo, tdq);
   if (e != cudaSuccess) return e;
-  return launch_wide_t<T, kPassDV, kCap>(p, dtype, stream, tq, tk, tv, tdo, tdq);
+  return launch_wide_t<T, kPassDV, kCap, kNC>(p, dtype, stream, tq, tk, tv, tdo, tdq);
+}
+
+// three 64-column chunks per row up to D = 192, four above
+template <typename T, bool kCap>
+cudaError_t launch_wide_width(const BwdParams& p, int dtype, cudaStream_t stream) {
+  return p.head_dim <= 192 ? launch_wide_passes<T, kCap, 3>(p, dtype, stream)
+                           : launch_wide_passes<T, kCap, 4>(p, dtype, stream);
 }
 
 }  // namespace
@@ -748,10 +770,10 @@ cudaError_t launch_wide_passes(const BwdParams& p_in, int dtype, cudaStream_t st
 cudaError_t launch_bwd_wide(const BwdParams& p, int dtype, cudaStream_t stream) {
   const bool cap = p.softcap > 0.f;
   if (dtype == 1)
-    return cap ? launch_wide_passes<__nv_bfloat16, true>(p, dtype, stream)
-               : launch_wide_passes<__nv_bfloat16, false>(p, dtype, stream);
-  return cap ? launch_wide_passes<__half, true>(p, dtype, stream)
-             : launch_wide_passes<__half, false>(p, dtype, stream);
+    return cap ? launch_wide_width<__nv_bfloat16, true>(p, dtype, stream)
+               : launch_wide_width<__nv_bfloat16, false>(p, dtype, stream);
+  return cap ? launch_wide_width<__half, true>(p, dtype, stream)
+             : launch_wide_width<__half, false>(p, dtype, stream);
 }
 
 }  // namespace attn

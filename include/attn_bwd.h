@@ -29,10 +29,10 @@
  *
  * Supported: dtype fp16 or bf16 (all of Q,K,V,O,dO,dQ,dK,dV share it), D a
  * multiple of 8 in [8, 256] (the head sizes the CK wrapper's mha_bwd accepts;
- * 64, 96, 128 and 256 run natively (96 without a logit cap or a left window
- * side), any other D runs on the next of those with the extra head-dimension
- * columns zero; above 128 the backward runs as two passes, one for dV and one
- * for dK and dQ), H_q % H_k == 0, base pointers and
+ * 64, 96, 128, 192 and 256 run natively (96 without a logit cap or a left
+ * window side), any other D runs on the next of those with the extra
+ * head-dimension columns zero; above 128 the backward runs as two passes, one
+ * for dV and one for dK and dQ), H_q % H_k == 0, base pointers and
  * strides 16-byte aligned (strides multiples of 8 elements).
  *
  * Ownership.  The caller owns every buffer, including the workspace; the

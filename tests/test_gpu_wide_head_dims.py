@@ -3,10 +3,11 @@
 The CK wrapper's argument checks (flash-attention csrc/flash_attn_ck/mha_bwd.cpp,
 mha_bwd) accept head_size % 8 == 0 and head_size <= 256, and the FA3 launcher
 (hopper/flash_bwd_launch_template.h) dispatches backward kernels for 192 and
-256.  Here D = 256 runs on its own kernels (the backward in two passes, dV and
-dK/dQ, the forward with K and V streamed in 64-column chunks); D in (128, 256)
-runs on them with the extra columns zero.  Tolerance as everywhere: rel-L2 <=
-1e-2, max-abs <= 2e-2 * max|ref| per gradient; O and LSE as in the forward test.
+256.  Here the backward for D in (128, 256] runs in two passes (dV and dK/dQ)
+on tiles of 64-column chunks: three chunks for D <= 192, four above, with the
+columns past D zero; the forward streams K and V in 64-column chunks.
+Tolerance as everywhere: rel-L2 <= 1e-2, max-abs <= 2e-2 * max|ref| per
+gradient; O and LSE as in the forward test.
 """
 import numpy as np
 import pytest
@@ -59,8 +60,11 @@ CASES = [
     (1, 2, 1, 1, 1, 256, "bf16", False),
     (1, 2, 2, 100, 300, 256, "bf16", True),     # Sq < Sk, bottom-right causal
     (1, 2, 2, 300, 100, 256, "fp16", True),     # Sq > Sk: leading rows see no key
-    (1, 4, 2, 384, 384, 192, "bf16", True),     # D = 192 (zero-padded to 256)
+    (1, 4, 2, 384, 384, 192, "bf16", True),     # D = 192: three chunks, none padded
     (2, 2, 2, 257, 257, 192, "fp16", False),
+    (1, 4, 2, 300, 100, 192, "bf16", True),     # Sq > Sk at three chunks
+    (1, 8, 2, 520, 520, 160, "bf16", True),     # three chunks, the last half zero
+    (1, 2, 2, 200, 200, 200, "fp16", False),    # just above 192: four chunks
     (1, 2, 2, 200, 200, 136, "bf16", True),     # just above 128
     (1, 2, 1, 333, 333, 248, "bf16", False),
 ]
@@ -89,8 +93,10 @@ def test_wide_backward_alone(d):
     _check(w, x, outs, tag=f"secondary d={d}")
 
 
-def test_wide_deterministic_bitwise():
-    w = synth.small("wide_det", 1, 8, 2, 1000, 1000, 256, "bf16", True, 821, deterministic=True)
+@pytest.mark.parametrize("d", [256, 192])
+def test_wide_deterministic_bitwise(d):
+    w = synth.small("wide_det", 1, 8, 2, 1000, 1000, d, "bf16", True, 821 + d,
+                    deterministic=True)
     x = synth.make_inputs(w)
     runs = [_run(w, x, deterministic=True)[0] for _ in range(3)]
     for r in runs[1:]:
@@ -99,29 +105,33 @@ def test_wide_deterministic_bitwise():
     _check(w, x, runs[0], tag="det")
 
 
-def test_wide_varlen_cross_attention():
+@pytest.mark.parametrize("d", [256, 192])
+def test_wide_varlen_cross_attention(d):
     lq, lk = [300, 0, 17, 129, 640], [200, 150, 0, 513, 64]
-    w = synth.Workload("wide_vl", 0, 4, 2, 0, 0, 256, "bf16", True, 831, n_seqs=len(lq),
+    w = synth.Workload("wide_vl", 0, 4, 2, 0, 0, d, "bf16", True, 831 + d, n_seqs=len(lq),
                        len_lo=0, len_hi=700)
     x = synth.make_inputs(w, lengths=lq, lengths_k=lk)
     outs, _, _ = _run(w, x)
     _check(w, x, outs, tag="varlen cross")
 
 
-@pytest.mark.parametrize("window,cap", [((200, -1), 0.0), (None, 4.0), ((64, 64), 3.0)],
-                         ids=["window", "softcap", "band+cap"])
-def test_wide_window_and_softcap(window, cap):
+@pytest.mark.parametrize("window,cap,d", [((200, -1), 0.0, 256), (None, 4.0, 256),
+                                         ((64, 64), 3.0, 256), ((64, 64), 3.0, 176)],
+                         ids=["window", "softcap", "band+cap", "band+cap-d176"])
+def test_wide_window_and_softcap(window, cap, d):
     causal = window is None or window[1] < 0
-    w = synth.small("wide_wc", 1, 4, 2, 600, 600, 256, "bf16", causal, 841)
+    w = synth.small("wide_wc", 1, 4, 2, 600, 600, d, "bf16", causal, 841 + d)
     x = synth.make_inputs(w)
     outs, _, _ = _run(w, x, window=window, softcap=cap)
     _check(w, x, outs, window=window, softcap=cap, tag=f"window={window} cap={cap}")
 
 
-def test_wide_full_size_whole_heads():
-    """MHA B=2, H=16, S=4096, D=256, bf16, causal at full size: every row of two
-    whole heads against the fp64 oracle, and sum_j dV_j = sum_i dO_i on every head."""
-    w = synth.WORKLOADS["mha_b2_h16_s4096_d256_bf16_causal"]
+@pytest.mark.parametrize("d", [256, 192])
+def test_wide_full_size_whole_heads(d):
+    """MHA B=2, H=16, S=4096, D=256 and 192, bf16, causal at full size: every row
+    of two whole heads against the fp64 oracle, and sum_j dV_j = sum_i dO_i on
+    every head."""
+    w = synth.WORKLOADS[f"mha_b2_h16_s4096_d{d}_bf16_causal"]
     x = synth.make_inputs(w)
     (dq, dk, dv), _, _ = _run(w, x)
     for b, h in ((0, 3), (1, 15)):
@@ -129,7 +139,7 @@ def test_wide_full_size_whole_heads():
                                       x.v[b, :, h].double().numpy(), x.do[b, :, h].double().numpy(),
                                       w.scale, w.causal)
         for name, got in (("dQ", dq[b, :, h]), ("dK", dk[b, :, h]), ("dV", dv[b, :, h])):
-            assert_close(f"d256 full {name} b={b} h={h}", got, r[name])
+            assert_close(f"d{d} full {name} b={b} h={h}", got, r[name])
     sdv = dv.double().sum(dim=1)
     sdo = x.do.cuda().double().sum(dim=1)
     assert ((sdv - sdo).abs() <= 2e-2 * sdo.abs().amax(dim=-1, keepdim=True)).all()
