@@ -5,6 +5,8 @@ oracle gradients of the same rounded inputs.  Secondary check: the oracle's
 O (rounded to the dtype) and LSE are fed to the GPU backward, isolating the
 backward's own error.  Tolerance: rel-L2 <= 1e-2, max-abs <= 2e-2 * max|ref|.
 """
+import functools
+
 import numpy as np
 import pytest
 import torch
@@ -363,3 +365,35 @@ def test_full_size_varlen_sampled_rows():
         assert_close(f"varlen seq {bsel} dQ", dq[idx, h].unsqueeze(0), dq_ref)
         assert_close(f"varlen seq {bsel} dK", dk[idx, h], dk_ref)
         assert_close(f"varlen seq {bsel} dV", dv[idx, h], dv_ref)
+
+
+_LONG = synth.small("long", 1, 2, 1, 32768, 32768, 128, "bf16", True, 4242)
+
+
+@functools.lru_cache(maxsize=1)
+def _long_case():
+    """Inputs and row-wise oracle gradients of the long-sequence case, computed
+    once for both of its tests (the oracle takes about a minute on the host)."""
+    x = synth.make_inputs(_LONG)
+    rng = np.random.default_rng(5)
+    rows = sorted(set(_sampled_rows(_LONG.seqlen_q, rng) + [16383, 16384, 32640]))
+    refs = attn_oracle.group_backward_rows(x.q, x.k, x.v, x.do, 0, 0, rows, rows, _LONG.scale,
+                                           _LONG.causal)
+    return x, rows, refs
+
+
+@pytest.mark.parametrize("deterministic", [False, True], ids=["nondet", "det"])
+def test_long_sequence_sampled_rows(deterministic):
+    """One long sequence, S = 32768 (256 key tiles; the unit of key tile 0 runs
+    512 tiles, and in deterministic mode a query tile's adds form a chain of up
+    to 256 key tiles), GQA 2:1, D = 128, bf16, causal: sampled rows against the
+    row-wise fp64 oracle; deterministic mode also bit for bit against a second
+    run."""
+    x, rows, (dq_ref, dk_ref, dv_ref) = _long_case()
+    dq, dk, dv = run_gpu(_LONG, x, deterministic)
+    assert_close("long dQ", dq[0, rows, 0:2].transpose(0, 1), dq_ref)
+    assert_close("long dK", dk[0, rows, 0], dk_ref)
+    assert_close("long dV", dv[0, rows, 0], dv_ref)
+    if deterministic:
+        dq2, dk2, dv2 = run_gpu(_LONG, x, deterministic)
+        assert torch.equal(dq, dq2) and torch.equal(dk, dk2) and torch.equal(dv, dv2)
