@@ -174,6 +174,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   constexpr int kDC = (D + 63) / 64;  // 64-column chunks of a tile row (the last one zero-filled
                                       // past D by the TMA loads at D = 96)
   constexpr bool kSplitQ = kDC == 2;
+  // Who writes a unit's dK/dV: the softmax warps, or the dQ drain warps once the
+  // unit's last tile is drained (so the softmax warps go straight on to the next
+  // unit): with two K/V slots (D = 64), and in the left-window instantiation
+  // without a logit cap (its units are short: +0.8 %; the default and the
+  // logit-cap instantiations measured 0 and -3 % that way)
+  constexpr bool kDrainEpi = L::kKVSlots == 2 || (kLeft && !kCap);
   // the left side of a local window; without one (the usual case) a constant,
   // so the unmasked and causal schedules carry none of its arithmetic
   const int wleft = kLeft ? p.win_left : -1;
@@ -199,8 +205,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(bar(B_DQFREE), 4);
     mbar_init(bar(B_DKDONE), 1);
     mbar_init(bar(B_DKDVFULL), 1);
-    // the dK/dV epilogue: the softmax warps, or at D = 64 the 4 dQ drain warps
-    mbar_init(bar(B_DKDVFREE), L::kKVSlots == 2 ? 4 : kSoftmaxWarps);
+    // the dK/dV epilogue: the softmax warps, or the 4 dQ drain warps
+    mbar_init(bar(B_DKDVFREE), kDrainEpi ? 4 : kSoftmaxWarps);
     for (int k = 0; k < 2; ++k) {
       mbar_init(bar(B_UNITFULL + k), 1);
       mbar_init(bar(B_UNITEMPTY + k), 1 + kSoftmaxWarps + 4);  // MMA + softmax + drain warps
@@ -700,9 +706,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
         if (lane == 0) mbar_arrive(bar(B_DSREADY));
       }
-      // ---- epilogue: this group's columns of dK = scale * acc or dV = acc (with
-      // two K/V slots the dQ drain warps write dK/dV instead)
-      if constexpr (L::kKVSlots == 1) {
+      // ---- epilogue: this group's columns of dK = scale * acc or dV = acc (or
+      // the dQ drain warps write dK/dV instead)
+      if constexpr (!kDrainEpi) {
         if (!wait_warp(bar(B_DKDVFULL), uc & 1, ctl, 0xA0000025u)) goto done;
         tc_fence_after();
         {
@@ -871,7 +877,85 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
         __syncwarp();
+        // with one K/V slot and the drain-side epilogue, the unit's last dO stage
+        // stages dK/dV and goes back to the producer after the epilogue
+        if (lane == 0 && (L::kKVSlots == 2 || !kDrainEpi || j + 1 < un.n_iters))
+          mbar_arrive(bar(B_EMPTYDO + s));
+      }
+      if constexpr (L::kKVSlots == 1 && kDrainEpi) {
+        // ---- epilogue: rows [32 quad, +32) of dK = scale * acc and dV = acc.  A key
+        // tile wholly inside the sequence is staged in this warp's quarter of the
+        // unit's last dO stage as 32-row x 64-column boxes (128-byte rows, 128-byte
+        // swizzle) and leaves through TMA tile stores (whole lines, and no per-row
+        // stores in the load/store pipe every warp's barrier operations use); a
+        // ragged tile stores per row and stops at the sequence end.
+        const uint32_t s = (it - 1) % kStages;
+        const uint32_t stage_off = L::kDO + s * L::kTile + quad * (L::kTile / 4);
+        const int key = un.n * BN + static_cast<int>(quad) * 32 + static_cast<int>(lane);
+        const bool tile_store = un.n * BN + BN <= un.si.sk;
+        if (!wait_warp(bar(B_DKDVFULL), uc & 1, ctl, 0xA0000035u)) goto done;
+        tc_fence_after();
+#pragma unroll 1
+        for (int t = 0; t < 2; ++t) {
+          const TensorArg& outp = t == 0 ? p.dk : p.dv;
+          const float mul = t == 0 ? p.scale : 1.0f;
+          if (t == 1 && tile_store) {  // the dK stores must have read the staging
+            if (lane == 0) bulk_wait_read_all();
+            __syncwarp();
+          }
+#pragma unroll 1
+          for (int c = 0; c < D / 32; ++c) {
+            uint32_t a[32];
+            tmem_ld32(tl + (t == 0 ? TM_DK : TM_DV) + c * 32, a);
+            tmem_wait_ld();
+            uint32_t o[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i)
+              o[i] = Pack<T>::two(__uint_as_float(a[2 * i]) * mul,
+                                  __uint_as_float(a[2 * i + 1]) * mul);
+            if (tile_store) {
+              // columns [32 c, 32 c + 32): 16-byte units 4 (c & 1) .. + 3 of box c / 2
+              const uint32_t row = stage_off + (c >> 1) * 4096 + lane * 128;
+#pragma unroll
+              for (int q = 0; q < 4; ++q)
+                *reinterpret_cast<uint4*>(smem + row + ((((c & 1) * 4 + q) ^ (lane & 7)) << 4)) =
+                    make_uint4(o[4 * q], o[4 * q + 1], o[4 * q + 2], o[4 * q + 3]);
+            } else if (key < un.si.sk) {
+              T* out_row = static_cast<T*>(const_cast<void*>(outp.ptr)) +
+                           (varlen ? 0 : un.b * outp.sb) +
+                           static_cast<int64_t>(un.si.k_start + key) * outp.ss +
+                           static_cast<int64_t>(un.g) * outp.sh + c * 32;
+#pragma unroll
+              for (int q = 0; q < 4; ++q)
+                if (c * 32 + 8 * q < p.head_dim)  // a padded head dimension stops early
+                  reinterpret_cast<uint4*>(out_row)[q] =
+                      make_uint4(o[4 * q], o[4 * q + 1], o[4 * q + 2], o[4 * q + 3]);
+            }
+          }
+          if (t == 1) {  // dK and dV have left TMEM: the next unit may restart them
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(B_DKDVFREE));
+          }
+          if (tile_store) {
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+#pragma unroll
+              for (int bx = 0; bx < D / 64; ++bx)
+                if (bx * 64 < p.head_dim)  // a padded head dimension stops early
+                  tma_store_4d(t == 0 ? &tmDK : &tmDV, sb + stage_off + bx * 4096, bx * 64,
+                               un.si.k_start + un.n * BN + static_cast<int>(quad) * 32, un.g,
+                               varlen ? 0 : un.b);
+              bulk_commit();
+            }
+          }
+        }
+        // the stores have read the staging: the stage goes back to the producer
+        if (lane == 0) bulk_wait_read_all();
+        __syncwarp();
         if (lane == 0) mbar_arrive(bar(B_EMPTYDO + s));
+        ++uc;
       }
       if constexpr (L::kKVSlots == 2) {
         // ---- epilogue: rows [32 quad, +32) of dK = scale * acc and dV = acc from
@@ -944,7 +1028,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 
 done:
-  if constexpr (L::kKVSlots == 2) {
+  if constexpr (kDrainEpi) {
     if (lane == 0) bulk_wait_all();  // no store may still read this CTA's shared memory
   }
   tc_fence_before();
