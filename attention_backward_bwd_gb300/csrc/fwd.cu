@@ -26,14 +26,15 @@
 // thread each), warps 4-7 softmax and epilogue (thread = query row = TMEM
 // lane).  S runs up to two tiles ahead of the softmax (three S buffers), so
 // the tensor pipe computes S of the next tile while the softmax warps work on
-// the current one.  (At D = 256 the same roles work on the chunk rings.)
+// the current one.  (At D = 192 and 256 the same roles work on the chunk rings.)
 //
 // TMEM columns (512 allocated): S buffers [0,128), [128,256), [256,384);
 // O [384, 384 + D).  Shared memory: 2 Q stages, 3 K stages, 2 V stages.
-// Head dimensions above 128 run on D = 256 tiles (extra columns zero): O takes
-// TMEM [256,512) next to two S buffers, the unit's Q tile (64 KiB) stays in
-// shared memory, and K and V stream through rings of 64-column chunks (six for
-// K, four for V), filled by the two producer threads in their consumers' order.
+// Head dimensions above 128 run on D = 192 tiles up to 192, D = 256 tiles above
+// (extra columns zero): O takes TMEM [256,256+D) next to two S buffers, the
+// unit's Q tile (48 or 64 KiB) stays in shared memory, and K and V stream
+// through rings of 64-column chunks (six for K; three or four, one tile, for V),
+// filled by the two producer threads in their consumers' order.
 #include <atomic>
 
 #include "common.cuh"
@@ -49,17 +50,19 @@ constexpr int kQSt = 2, kKSt = 3, kVSt = 2;
 constexpr uint32_t kFChunk = 128 * 128;  // one 64-column (128-byte) slice of a 128-row tile
 constexpr uint32_t kFTmemCols = 512;
 constexpr uint32_t TF_S = 0;
-// D = 256: K and V stream through rings of 64-column chunks (K: six slots, a
-// tile and a half; V: four slots, one tile, so a tile's chunk pairs never wrap)
-constexpr int kFKRing = 6, kFVRing = 4;
+// D = 192 and 256: K and V stream through rings of 64-column chunks (K: six
+// slots, two tiles resp. a tile and a half; V: one tile, three resp. four slots,
+// so a tile's chunk pairs never wrap)
+constexpr int kFKRing = 6, kFVRingMax = 4;
 
 // Per head-dimension layout: three S buffers and O at column 384 up to D = 128;
-// two S buffers and O at column 256 for the D = 256 tiles.
+// two S buffers and O at column 256 for the D = 192 and 256 tiles.
 template <int D>
 struct FCfg {
   static constexpr bool kWide = D > 128;
   static constexpr int kSBufs = kWide ? 2 : 3;
   static constexpr uint32_t kO = kWide ? 256 : 384;
+  static constexpr int kVRing = D == 192 ? 3 : 4;
 };
 constexpr float kRescaleLog2 = 8.f;  // P stays below 2^8 between rescales
 
@@ -74,24 +77,26 @@ enum FBar : uint32_t {
   F_OFULL = F_PVDONE + 3,       // the unit's last O += P V done
   F_FINAL,
   F_FINAL2,                     // the O += P V issuer's own drain before TMEM is released
-  F_RFULL,                      // D = 256: K ring slots, then V ring slots (released by SFULL / PVDONE)
-  F_COUNT = F_RFULL + kFKRing + kFVRing
+  F_RFULL,                      // D > 128: K ring slots, then V ring slots (released by SFULL / PVDONE)
+  F_COUNT = F_RFULL + kFKRing + kFVRingMax
 };
 
 template <int D>
 struct FSmem {
   static constexpr uint32_t kTile = (D / 64) * kFChunk;
   static constexpr uint32_t kQ = 0;
-  // up to D = 128: Q, K and V tile stages; D = 256: one Q tile, the K and V chunk rings
+  // up to D = 128: Q, K and V tile stages; above: one Q tile, the K and V chunk rings
   static constexpr uint32_t kK = kQ + (FCfg<D>::kWide ? 1 : kQSt) * kTile;
   static constexpr uint32_t kV = kK + (FCfg<D>::kWide ? kFKRing * kFChunk : kKSt * kTile);
-  static constexpr uint32_t kBar = kV + (FCfg<D>::kWide ? kFVRing * kFChunk : kVSt * kTile);
+  static constexpr uint32_t kBar =
+      kV + (FCfg<D>::kWide ? FCfg<D>::kVRing * kFChunk : kVSt * kTile);
   static constexpr uint32_t kTmemSlot = kBar + F_COUNT * 8;
   static constexpr uint32_t kAbort = kTmemSlot + 4;
   static constexpr uint32_t kTotal = kAbort + 4;
 };
 static_assert(FSmem<128>::kTotal <= 232448, "shared memory budget");
 static_assert(FSmem<256>::kTotal <= 232448, "shared memory budget (D = 256)");
+static_assert(FSmem<192>::kTotal <= 232448, "shared memory budget (D = 192)");
 
 struct FUnit {
   int m, h, b;
@@ -150,6 +155,7 @@ __global__ void __launch_bounds__(kFThreads, 1)
   constexpr bool kWide = FCfg<D>::kWide;
   constexpr int kSBufs = FCfg<D>::kSBufs;
   constexpr uint32_t TF_O = FCfg<D>::kO;
+  constexpr int kFVRing = FCfg<D>::kVRing;
   extern __shared__ __align__(1024) unsigned char smem[];
   if (p.input_bad != nullptr && *p.input_bad) return;
   const uint32_t sb = smem_u32(smem);
@@ -184,7 +190,7 @@ __global__ void __launch_bounds__(kFThreads, 1)
     mbar_init(bar(F_OFULL), 1);
     mbar_init(bar(F_FINAL), 1);
     mbar_init(bar(F_FINAL2), 1);
-    for (int r = 0; r < kFKRing + kFVRing; ++r) mbar_init(bar(F_RFULL + r), 1);
+    for (int r = 0; r < kFKRing + kFVRingMax; ++r) mbar_init(bar(F_RFULL + r), 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     fence_proxy_async_smem();
   }
@@ -199,9 +205,9 @@ __global__ void __launch_bounds__(kFThreads, 1)
 
   if (warp == 0 || warp == 3) {
     // ------------------------------------------------------------ TMA producers
-    // D = 256: warp 0 fills the chunk ring.  Up to D = 128: warp 0 loads Q and K,
-    // warp 3 loads V, so that a K load never waits behind the release of a V
-    // stage (which comes one tile later, after O += P V).
+    // D > 128: warps 0 and 3 fill the K and V chunk rings.  Up to D = 128:
+    // warp 0 loads Q and K, warp 3 loads V, so that a K load never waits behind
+    // the release of a V stage (which comes one tile later, after O += P V).
     if (lane == 0 && kWide) {
       const bool loads_v = warp == 3;
       prefetch_tmap(loads_v ? &tmV : &tmQ);
@@ -329,7 +335,7 @@ __global__ void __launch_bounds__(kFThreads, 1)
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0 && kWide) {
-      // D = 256: S = Q K^T from the unit's Q tile and the K ring
+      // D > 128: S = Q K^T from the unit's Q tile and the K ring
       constexpr uint32_t kIdS = idesc_f16(kIsBf16, 0, 0, FBM, FBN);  // Q, K both K-major
       uint32_t qc = 0, it = 0, q = 0;  // Q tiles, S tiles, K ring chunks consumed
       for (int u = blockIdx.x; u < num_units; u += gridDim.x) {
@@ -408,10 +414,12 @@ __global__ void __launch_bounds__(kFThreads, 1)
   } else if (warp == 2) {
     if (lane == 0) {
       // ---------------------------------------------------- O += P V issuer
-      // (D = 256: O in two N = 128 halves, V chunk pairs from the V ring)
+      // (D = 192 and 256: O in N = 128 parts over V chunk pairs from the V ring,
+      // the odd last chunk at D = 192 as an N = 64 part)
       constexpr uint32_t kIdPV =
           idesc_f16(kIsBf16, 0, 1, FBM, kWide ? 128 : D);  // P from TMEM, V MN-major
-      uint32_t it = 0, q = 0;  // P tiles; D = 256: V ring chunks consumed
+      constexpr uint32_t kIdPV64 = idesc_f16(kIsBf16, 0, 1, FBM, 64);
+      uint32_t it = 0, q = 0;  // P tiles; D > 128: V ring chunks consumed
       for (int u = blockIdx.x; u < num_units; u += gridDim.x) {
         const FUnit un = fwd_unit<kSeqMajor>(p, u, n_mt);
         if (!un.active || un.n_end == un.n_start) continue;
@@ -422,18 +430,21 @@ __global__ void __launch_bounds__(kFThreads, 1)
           if (!wait1(bar(F_PREADY + buf), (t / kSBufs) & 1, ctl, 0xA2000011u)) goto pv_exit;
           if (kWide) {
 #pragma unroll 1
-            for (int pr = 0; pr < D / 128; ++pr, q += 2) {
+            for (int pr = 0; pr < (D / 64 + 1) / 2; ++pr) {
+              const bool pair = 2 * pr + 1 < D / 64;
               const uint32_t r0 = kFKRing + q % kFVRing;
               if (!wait1(bar(F_RFULL + r0), (q / kFVRing) & 1, ctl, 0xA2000012u) ||
-                  !wait1(bar(F_RFULL + r0 + 1), ((q + 1) / kFVRing) & 1, ctl, 0xA2000012u))
+                  (pair &&
+                   !wait1(bar(F_RFULL + r0 + 1), ((q + 1) / kFVRing) & 1, ctl, 0xA2000012u)))
                 goto pv_exit;
               tc_fence_after();
               const uint32_t sV = sb + L::kV + (q % kFVRing) * kFChunk;
 #pragma unroll
               for (int kk = 0; kk < FBN / 16; ++kk)
                 mma_ts(tmem + TF_O + 128 * pr, tmem + TF_S + buf * 128 + kk * 8,
-                       sdesc_sw128(sV + kk * 2048, kFChunk, 1024), kIdPV,
+                       sdesc_sw128(sV + kk * 2048, kFChunk, 1024), pair ? kIdPV : kIdPV64,
                        (j > 0 || kk > 0) ? 1u : 0u);
+              q += pair ? 2 : 1;
             }
           } else {
             if (!wait1(bar(F_VFULL + vs), (t / kVSt) & 1, ctl, 0xA2000012u)) goto pv_exit;
@@ -655,13 +666,16 @@ cudaError_t launch_fwd_t(const FwdParams& p, int dtype, cudaStream_t stream) {
 
 template <bool kCap, bool kSeqMajor>
 cudaError_t launch_fwd_cap(const FwdParams& p, int dtype, cudaStream_t stream) {
-  const int dp = pad_head_dim(p.head_dim);
+  // tiles of 64, 128, 192 or 256 head-dim columns (the columns past D zero)
+  const int dp = p.head_dim <= 128 ? pad_head_dim(p.head_dim) : p.head_dim <= 192 ? 192 : 256;
   if (dtype == 1)
     return dp == 64    ? launch_fwd_t<__nv_bfloat16, 64, kCap, kSeqMajor>(p, dtype, stream)
            : dp == 128 ? launch_fwd_t<__nv_bfloat16, 128, kCap, kSeqMajor>(p, dtype, stream)
+           : dp == 192 ? launch_fwd_t<__nv_bfloat16, 192, kCap, kSeqMajor>(p, dtype, stream)
                        : launch_fwd_t<__nv_bfloat16, 256, kCap, kSeqMajor>(p, dtype, stream);
   return dp == 64    ? launch_fwd_t<__half, 64, kCap, kSeqMajor>(p, dtype, stream)
          : dp == 128 ? launch_fwd_t<__half, 128, kCap, kSeqMajor>(p, dtype, stream)
+         : dp == 192 ? launch_fwd_t<__half, 192, kCap, kSeqMajor>(p, dtype, stream)
                      : launch_fwd_t<__half, 256, kCap, kSeqMajor>(p, dtype, stream);
 }
 
