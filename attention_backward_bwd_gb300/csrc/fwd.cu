@@ -83,7 +83,8 @@ enum FBar : uint32_t {
 
 template <int D>
 struct FSmem {
-  static constexpr uint32_t kTile = (D / 64) * kFChunk;
+  // 64-column chunks of a tile row (D = 96: two, the second zero-filled past D)
+  static constexpr uint32_t kTile = ((D + 63) / 64) * kFChunk;
   static constexpr uint32_t kQ = 0;
   // up to D = 128: Q, K and V tile stages; above: one Q tile, the K and V chunk rings
   static constexpr uint32_t kK = kQ + (FCfg<D>::kWide ? 1 : kQSt) * kTile;
@@ -97,6 +98,7 @@ struct FSmem {
 static_assert(FSmem<128>::kTotal <= 232448, "shared memory budget");
 static_assert(FSmem<256>::kTotal <= 232448, "shared memory budget (D = 256)");
 static_assert(FSmem<192>::kTotal <= 232448, "shared memory budget (D = 192)");
+static_assert(FSmem<96>::kTotal == FSmem<128>::kTotal, "D = 96 uses the D = 128 layout");
 
 struct FUnit {
   int m, h, b;
@@ -156,6 +158,7 @@ __global__ void __launch_bounds__(kFThreads, 1)
   constexpr int kSBufs = FCfg<D>::kSBufs;
   constexpr uint32_t TF_O = FCfg<D>::kO;
   constexpr int kFVRing = FCfg<D>::kVRing;
+  constexpr int kDC = (D + 63) / 64;  // 64-column chunks of a tile row
   extern __shared__ __align__(1024) unsigned char smem[];
   if (p.input_bad != nullptr && *p.input_bad) return;
   const uint32_t sb = smem_u32(smem);
@@ -274,7 +277,7 @@ __global__ void __launch_bounds__(kFThreads, 1)
           if (use > 0 && !wait1(bar(F_QEMPTY + s), (use - 1) & 1, ctl, 0xA2000001u)) break;
           mbar_expect_tx(bar(F_QFULL + s), L::kTile);
 #pragma unroll
-          for (int c = 0; c < D / 64; ++c)
+          for (int c = 0; c < kDC; ++c)
             tma_load_4d(sb + L::kQ + s * L::kTile + c * kFChunk, &tmQ, bar(F_QFULL + s), c * 64,
                         un.si.q_start + un.m * FBM, un.h, bq);
           ++qc;
@@ -296,7 +299,7 @@ __global__ void __launch_bounds__(kFThreads, 1)
             }
             mbar_expect_tx(bar(F_VFULL + vs), L::kTile);
 #pragma unroll
-            for (int c = 0; c < D / 64; ++c)
+            for (int c = 0; c < kDC; ++c)
               tma_load_4d(sb + L::kV + vs * L::kTile + c * kFChunk, &tmV, bar(F_VFULL + vs),
                           c * 64, krow, hk, bq);
             ++vc;
@@ -314,7 +317,7 @@ __global__ void __launch_bounds__(kFThreads, 1)
           }
           mbar_expect_tx(bar(F_KFULL + ks), L::kTile);
 #pragma unroll
-          for (int c = 0; c < D / 64; ++c)
+          for (int c = 0; c < kDC; ++c)
             tma_load_4d(sb + L::kK + ks * L::kTile + c * kFChunk, &tmK, bar(F_KFULL + ks), c * 64,
                         krow, hk, bq);
           ++kc;
@@ -666,14 +669,20 @@ cudaError_t launch_fwd_t(const FwdParams& p, int dtype, cudaStream_t stream) {
 
 template <bool kCap, bool kSeqMajor>
 cudaError_t launch_fwd_cap(const FwdParams& p, int dtype, cudaStream_t stream) {
-  // tiles of 64, 128, 192 or 256 head-dim columns (the columns past D zero)
-  const int dp = p.head_dim <= 128 ? pad_head_dim(p.head_dim) : p.head_dim <= 192 ? 192 : 256;
+  // tiles of 64, 96, 128, 192 or 256 head-dim columns (the columns past D zero)
+  const int dp = p.head_dim <= 64    ? 64
+                 : p.head_dim <= 96  ? 96
+                 : p.head_dim <= 128 ? 128
+                 : p.head_dim <= 192 ? 192
+                                     : 256;
   if (dtype == 1)
     return dp == 64    ? launch_fwd_t<__nv_bfloat16, 64, kCap, kSeqMajor>(p, dtype, stream)
+           : dp == 96  ? launch_fwd_t<__nv_bfloat16, 96, kCap, kSeqMajor>(p, dtype, stream)
            : dp == 128 ? launch_fwd_t<__nv_bfloat16, 128, kCap, kSeqMajor>(p, dtype, stream)
            : dp == 192 ? launch_fwd_t<__nv_bfloat16, 192, kCap, kSeqMajor>(p, dtype, stream)
                        : launch_fwd_t<__nv_bfloat16, 256, kCap, kSeqMajor>(p, dtype, stream);
   return dp == 64    ? launch_fwd_t<__half, 64, kCap, kSeqMajor>(p, dtype, stream)
+         : dp == 96  ? launch_fwd_t<__half, 96, kCap, kSeqMajor>(p, dtype, stream)
          : dp == 128 ? launch_fwd_t<__half, 128, kCap, kSeqMajor>(p, dtype, stream)
          : dp == 192 ? launch_fwd_t<__half, 192, kCap, kSeqMajor>(p, dtype, stream)
                      : launch_fwd_t<__half, 256, kCap, kSeqMajor>(p, dtype, stream);

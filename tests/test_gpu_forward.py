@@ -48,7 +48,11 @@ CASES = [
     (1, 2, 1, 300, 500, 64, "bf16", False, (0, 0), 0.0),      # the aligned diagonal only
     (1, 4, 2, 600, 600, 128, "bf16", True, None, 5.0),        # logit cap
     (1, 2, 2, 400, 400, 128, "fp16", False, (64, 64), 3.0),   # cap with a band
-    (1, 4, 2, 300, 300, 96, "bf16", True, None, 0.0),         # padded head dim
+    (1, 4, 2, 300, 300, 96, "bf16", True, None, 0.0),         # D = 96 tiles
+    (1, 4, 2, 600, 600, 96, "bf16", True, (200, -1), 4.0),    # D = 96, window and cap
+    (2, 2, 2, 257, 257, 80, "fp16", False, None, 0.0),        # padded to the D = 96 tiles
+    (1, 4, 2, 520, 520, 192, "bf16", True, None, 0.0),        # D = 192 tiles
+    (1, 2, 2, 300, 300, 160, "fp16", False, (64, 64), 3.0),   # padded to D = 192, band + cap
     (1, 2, 2, 257, 257, 32, "fp16", False, None, 0.0),        # padded head dim (D = 64 kernel)
 ]
 
