@@ -49,6 +49,9 @@ CASES = [
     (5, 4, 4, 300, 300, 64, "fp16", False, 2),     # runs of 3 and 2 sequences
     (1, 16, 4, 513, 1000, 128, "bf16", True, 4),   # Sq < Sk, four kv-head chunks
     (3, 6, 3, 257, 129, 64, "bf16", True, 9),      # one kv head per chunk, Sq > Sk
+    (2, 4, 2, 300, 300, 96, "bf16", True, 0),      # D = 96 tiles
+    (1, 4, 2, 257, 257, 192, "bf16", True, 2),     # D = 192: two passes on three-chunk tiles
+    (2, 2, 1, 200, 200, 256, "fp16", False, 0),    # D = 256
 ]
 
 
