@@ -39,9 +39,10 @@ def _call(f, q, k, v, o, lse, do, dq, dk, dv, causal, deterministic, seqlen_q=No
              sk, int(deterministic), torch.cuda.current_stream().cuda_stream)
 
 
-@pytest.mark.parametrize("deterministic", [False, True])
-def test_noalloc_matches_attn_bwd_on_two_calls(deterministic):
-    w = synth.small("noalloc", 2, 4, 2, 300, 300, 128, "bf16", True, 123)
+@pytest.mark.parametrize("deterministic,d", [(False, 128), (True, 128), (False, 192), (True, 256)],
+                         ids=["d128", "d128-det", "d192", "d256-det"])
+def test_noalloc_matches_attn_bwd_on_two_calls(deterministic, d):
+    w = synth.small("noalloc", 2, 4, 2, 300, 300, d, "bf16", True, 123 + d)
     x = synth.make_inputs(w)
     q, k, v, do = (t.cuda() for t in (x.q, x.k, x.v, x.do))
     o, lse = ab.attn_fwd(q, k, v, causal=True)
