@@ -29,11 +29,13 @@ def _scramble_unused(x, used, rows_of, starts=None):
             x[sl] = (torch.randn(x[sl].shape, generator=g) * 3).to(x.dtype)
 
 
-@pytest.mark.parametrize("causal,det", [(True, False), (False, False), (True, True)])
-def test_seqused_padded(causal, det):
-    b, hq, hk, sq, sk, d = 3, 8, 2, 700, 700, 128
+@pytest.mark.parametrize("causal,det,d", [(True, False, 128), (False, False, 128), (True, True, 128),
+                                         (True, False, 96), (True, False, 192), (False, True, 256)],
+                         ids=["causal", "full", "causal-det", "d96", "d192", "d256-full-det"])
+def test_seqused_padded(causal, det, d):
+    b, hq, hk, sq, sk = 3, 8, 2, 700, 700
     uq, uk = [650, 0, 700], [600, 300, 129]
-    w = synth.small("used", b, hq, hk, sq, sk, d, "bf16", causal, 611)
+    w = synth.small("used", b, hq, hk, sq, sk, d, "bf16", causal, 611 + d)
     x = synth.make_inputs(w)
     for t, u in ((x.q, uq), (x.do, uq), (x.k, uk), (x.v, uk)):
         _scramble_unused(t, u, lambda _: t.shape[1])
