@@ -15,19 +15,20 @@ from attention_backward_bwd_gb300 import synth
 pytestmark = pytest.mark.gpu
 
 
-def _inputs(varlen, seed):
+def _inputs(varlen, seed, d=128):
     if varlen:
-        w = synth.Workload("graph_varlen", 0, 4, 2, 0, 0, 128, "bf16", True, seed, n_seqs=4,
+        w = synth.Workload("graph_varlen", 0, 4, 2, 0, 0, d, "bf16", True, seed, n_seqs=4,
                            len_lo=1, len_hi=600)
         return w, synth.make_inputs(w, lengths=[200, 0, 513, 128])
-    w = synth.small("graph", 2, 8, 2, 600, 600, 128, "bf16", True, seed)
+    w = synth.small("graph", 2, 8, 2, 600, 600, d, "bf16", True, seed)
     return w, synth.make_inputs(w)
 
 
-@pytest.mark.parametrize("varlen", [False, True])
-def test_attn_bwd_replays_in_a_cuda_graph(varlen):
-    w, x = _inputs(varlen, 21)
-    _, x2 = _inputs(varlen, 22)
+@pytest.mark.parametrize("varlen,d", [(False, 128), (True, 128), (False, 192), (True, 256)],
+                         ids=["padded", "varlen", "padded-d192", "varlen-d256"])
+def test_attn_bwd_replays_in_a_cuda_graph(varlen, d):
+    w, x = _inputs(varlen, 21, d)
+    _, x2 = _inputs(varlen, 22, d)
     dev = "cuda"
     q, k, v, do = (t.to(dev) for t in (x.q, x.k, x.v, x.do))
     kw = dict(causal=w.causal, deterministic=True)
