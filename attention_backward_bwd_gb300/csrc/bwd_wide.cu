@@ -89,7 +89,8 @@ struct WSmem {
   // V/dO interleaved); an N = 128 product reads a pair of chunks starting at
   // an even offset of its group as one operand, so both must sit in adjacent
   // slots: the ring is even (four chunks) or a multiple of three (three).
-  static constexpr int kRing = kPass == kPassDV ? (kNC == 4 ? 10 : 9) : 6;
+  // (Three chunks, pass dV: six slots measured 0.8 % faster than nine.)
+  static constexpr int kRing = kPass == kPassDV ? (kNC == 4 ? 10 : 6) : 6;
   static_assert(kRing % (kNC == 4 ? 2 : 3) == 0, "chunk pairs must not wrap the ring");
   static constexpr uint32_t kK = 0;
   static constexpr uint32_t kDS = kK + kNC * kWChunk;                         // pass dK/dQ
