@@ -59,9 +59,9 @@ constexpr uint32_t kWTmemCols = 512;
 enum WPass : int { kPassDV = 0, kPassDKDQ = 1 };
 
 enum WBar : uint32_t {
-  W_RFULL = 0,                 // ring slots (up to 10)
-  W_REMPTY = W_RFULL + 10,
-  W_KFULL = W_REMPTY + 10,     // the unit's K tile
+  W_RFULL = 0,                 // ring slots (6)
+  W_REMPTY = W_RFULL + 6,
+  W_KFULL = W_REMPTY + 6,      // the unit's K tile
   W_KEMPTY,
   W_STFULL,                    // 2 stages of LSE2 (+ Delta)
   W_STEMPTY = W_STFULL + 2,
@@ -89,9 +89,11 @@ struct WSmem {
   // V/dO interleaved); an N = 128 product reads a pair of chunks starting at
   // an even offset of its group as one operand, so both must sit in adjacent
   // slots: the ring is even (four chunks) or a multiple of three (three).
-  // (Three chunks, pass dV: six slots measured 0.8 % faster than nine.)
-  static constexpr int kRing = kPass == kPassDV ? (kNC == 4 ? 10 : 6) : 6;
+  // Six slots in both passes (pass dV measured 0.7 to 0.8 % faster with six
+  // than with ten at D = 256 or nine at D = 192).
+  static constexpr int kRing = 6;
   static_assert(kRing % (kNC == 4 ? 2 : 3) == 0, "chunk pairs must not wrap the ring");
+  static_assert(kRing == W_REMPTY - W_RFULL, "one full and one empty barrier per ring slot");
   static constexpr uint32_t kK = 0;
   static constexpr uint32_t kDS = kK + kNC * kWChunk;                         // pass dK/dQ
   static constexpr uint32_t kStage = kDS + (kPass == kPassDKDQ ? 2 * kWChunk : 0);
