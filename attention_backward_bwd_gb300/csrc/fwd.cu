@@ -50,10 +50,10 @@ constexpr int kQSt = 2, kKSt = 3, kVSt = 2;
 constexpr uint32_t kFChunk = 128 * 128;  // one 64-column (128-byte) slice of a 128-row tile
 constexpr uint32_t kFTmemCols = 512;
 constexpr uint32_t TF_S = 0;
-// D = 192 and 256: K and V stream through rings of 64-column chunks (K: six
-// slots, two tiles resp. a tile and a half; V: one tile, three resp. four slots,
-// so a tile's chunk pairs never wrap)
-constexpr int kFKRing = 6, kFVRingMax = 4;
+// D = 192 and 256: K and V stream through rings of 64-column chunks (K: four
+// resp. six slots, measured best of 4 and 6 at each width; V: one tile, three
+// resp. four slots, so a tile's chunk pairs never wrap)
+constexpr int kFKRingMax = 6, kFVRingMax = 4;
 
 // Per head-dimension layout: three S buffers and O at column 384 up to D = 128;
 // two S buffers and O at column 256 for the D = 192 and 256 tiles.
@@ -63,6 +63,7 @@ struct FCfg {
   static constexpr int kSBufs = kWide ? 2 : 3;
   static constexpr uint32_t kO = kWide ? 256 : 384;
   static constexpr int kVRing = D == 192 ? 3 : 4;
+  static constexpr int kKRing = D == 192 ? 4 : 6;
 };
 constexpr float kRescaleLog2 = 8.f;  // P stays below 2^8 between rescales
 
@@ -78,7 +79,7 @@ enum FBar : uint32_t {
   F_FINAL,
   F_FINAL2,                     // the O += P V issuer's own drain before TMEM is released
   F_RFULL,                      // D > 128: K ring slots, then V ring slots (released by SFULL / PVDONE)
-  F_COUNT = F_RFULL + kFKRing + kFVRingMax
+  F_COUNT = F_RFULL + kFKRingMax + kFVRingMax
 };
 
 template <int D>
@@ -88,7 +89,7 @@ struct FSmem {
   static constexpr uint32_t kQ = 0;
   // up to D = 128: Q, K and V tile stages; above: one Q tile, the K and V chunk rings
   static constexpr uint32_t kK = kQ + (FCfg<D>::kWide ? 1 : kQSt) * kTile;
-  static constexpr uint32_t kV = kK + (FCfg<D>::kWide ? kFKRing * kFChunk : kKSt * kTile);
+  static constexpr uint32_t kV = kK + (FCfg<D>::kWide ? FCfg<D>::kKRing * kFChunk : kKSt * kTile);
   static constexpr uint32_t kBar =
       kV + (FCfg<D>::kWide ? FCfg<D>::kVRing * kFChunk : kVSt * kTile);
   static constexpr uint32_t kTmemSlot = kBar + F_COUNT * 8;
@@ -158,6 +159,7 @@ __global__ void __launch_bounds__(kFThreads, 1)
   constexpr int kSBufs = FCfg<D>::kSBufs;
   constexpr uint32_t TF_O = FCfg<D>::kO;
   constexpr int kFVRing = FCfg<D>::kVRing;
+  constexpr int kFKRing = FCfg<D>::kKRing;
   constexpr int kDC = (D + 63) / 64;  // 64-column chunks of a tile row
   extern __shared__ __align__(1024) unsigned char smem[];
   if (p.input_bad != nullptr && *p.input_bad) return;
@@ -193,7 +195,7 @@ __global__ void __launch_bounds__(kFThreads, 1)
     mbar_init(bar(F_OFULL), 1);
     mbar_init(bar(F_FINAL), 1);
     mbar_init(bar(F_FINAL2), 1);
-    for (int r = 0; r < kFKRing + kFVRingMax; ++r) mbar_init(bar(F_RFULL + r), 1);
+    for (int r = 0; r < kFKRingMax + kFVRingMax; ++r) mbar_init(bar(F_RFULL + r), 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     fence_proxy_async_smem();
   }
@@ -218,7 +220,7 @@ __global__ void __launch_bounds__(kFThreads, 1)
       uint32_t qc = 0, q = 0;  // Q tiles and chunks (K or V) whose loads were issued
       const int ring = loads_v ? kFVRing : kFKRing;
       const uint32_t base = loads_v ? L::kV : L::kK;
-      const uint32_t fbar = loads_v ? F_RFULL + kFKRing : F_RFULL;
+      const uint32_t fbar = loads_v ? F_RFULL + kFKRingMax : F_RFULL;
       bool stop = false;
       for (int u = blockIdx.x; u < num_units && !stop; u += gridDim.x) {
         const FUnit un = fwd_unit<kSeqMajor>(p, u, n_mt);
@@ -435,7 +437,7 @@ __global__ void __launch_bounds__(kFThreads, 1)
 #pragma unroll 1
             for (int pr = 0; pr < (D / 64 + 1) / 2; ++pr) {
               const bool pair = 2 * pr + 1 < D / 64;
-              const uint32_t r0 = kFKRing + q % kFVRing;
+              const uint32_t r0 = kFKRingMax + q % kFVRing;
               if (!wait1(bar(F_RFULL + r0), (q / kFVRing) & 1, ctl, 0xA2000012u) ||
                   (pair &&
                    !wait1(bar(F_RFULL + r0 + 1), ((q + 1) / kFVRing) & 1, ctl, 0xA2000012u)))
